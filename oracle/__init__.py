@@ -1,0 +1,145 @@
+"""CPU fp64 oracle for the KDA core.
+
+TEST INFRASTRUCTURE ONLY.  The product path (the ``gated_delta_rule_gb300``
+package and its CUDA library) never imports, links or runs anything here; only
+``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg do.
+The oracle shares no code with the CUDA path; both only read the seeded inputs of
+``kda_inputs``.
+
+Contents:
+  * ``kda_oracle.cpp`` - the main oracle: the token-by-token recurrence in fp64,
+    OpenMP across independent (sequence, head) problems (built to
+    ``_kda_oracle.so`` by :func:`build`);
+  * ``kda_numpy``      - numpy restatements (three-step loop, explicit transition
+    matrix, chunked form, segment transition) used to pin the C++ oracle.
+
+Every function here takes the exact values of the tensors the GPU sees (bf16 or
+fp32, widened to fp64) and returns fp64 numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+from . import kda_numpy  # noqa: F401  (re-exported)
+
+_DIR = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_DIR, "kda_oracle.cpp")
+_LIB = os.path.join(_DIR, "_kda_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C++ oracle (g++ -O2 -fopenmp).  Returns the library path."""
+    with _lock:
+        fresh = os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)
+        if force or not fresh:
+            tmp = _LIB + f".{os.getpid()}.tmp"
+            subprocess.run(["g++", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c++17", _SRC,
+                            "-o", tmp], check=True)
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.kda_oracle_run.restype = ctypes.c_int
+        lib.kda_oracle_run.argtypes = [ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 6 + [
+            ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.kda_oracle_threads.restype = ctypes.c_int
+        lib.kda_oracle_threads.argtypes = [ctypes.c_int]
+        _lib = lib
+    return _lib
+
+
+def threads(nthreads: int = 0) -> int:
+    return int(_load().kda_oracle_threads(int(nthreads)))
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().cpu()
+        if not x.dtype.is_floating_point:
+            return np.ascontiguousarray(x.numpy().astype(np.float64))
+        x = x.double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def run_problems(row_start, row_count, q, k, v, g, beta, S0, scale, nthreads=0):
+    """Low-level entry: problem p runs rows [row_start[p], +row_count[p]) of the
+    row-major fp64 arrays q, k, g [rows, dk], v [rows, dv], beta [rows].
+    Returns (out [rows, dv], S_T [P, dk, dv], threads used)."""
+    lib = _load()
+    rs = np.ascontiguousarray(row_start, dtype=np.int64)
+    rc = np.ascontiguousarray(row_count, dtype=np.int64)
+    P = rs.shape[0]
+    dk, dv = q.shape[1], v.shape[1]
+    out = np.zeros((q.shape[0], dv))
+    ST = np.zeros((P, dk, dv))
+    S0c = None if S0 is None else np.ascontiguousarray(S0, dtype=np.float64).reshape(P, dk, dv)
+    nt = lib.kda_oracle_run(P, _ptr(rs), _ptr(rc), dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                            _ptr(beta), _ptr(S0c), float(scale), _ptr(out), _ptr(ST),
+                            int(nthreads))
+    if nt < 0:
+        raise ValueError(f"kda_oracle_run rejected its arguments ({nt})")
+    return out, ST, nt
+
+
+def prefill(q, k, v, g, beta, initial_state, scale, cu_seqlens=None, nthreads=0):
+    """Oracle of ``kda_chunk_fwd``.
+
+    q, k, g: [B, T, H, dk]; v: [B, T, H, dv]; beta: [B, T, H]; initial_state:
+    [N, H, dk, dv] or None; cu_seqlens: [N+1] offsets (then B == 1) or None (then
+    N == B and every batch row is one sequence).  Returns (out [B, T, H, dv],
+    final_state [N, H, dk, dv]) in fp64.
+    """
+    q, k, v, g, beta = (_f64(a) for a in (q, k, v, g, beta))
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    # head-major packing: [B, H, T, d] rows, so one problem's rows are contiguous
+    qp, kp, gp = (np.ascontiguousarray(a.transpose(0, 2, 1, 3)).reshape(B * H * T, dk)
+                  for a in (q, k, g))
+    vp = np.ascontiguousarray(v.transpose(0, 2, 1, 3)).reshape(B * H * T, dv)
+    bp = np.ascontiguousarray(beta.transpose(0, 2, 1)).reshape(B * H * T)
+    if cu_seqlens is None:
+        N = B
+        starts = [(b * H + h) * T for b in range(B) for h in range(H)]
+        counts = [T] * (B * H)
+    else:
+        cu = _f64(cu_seqlens).astype(np.int64)
+        if B != 1:
+            raise ValueError("varlen inputs must have B == 1")
+        N = cu.shape[0] - 1
+        starts = [h * T + int(cu[n]) for n in range(N) for h in range(H)]
+        counts = [int(cu[n + 1] - cu[n]) for n in range(N) for h in range(H)]
+    S0 = None if initial_state is None else _f64(initial_state).reshape(N * H, dk, dv)
+    out, ST, _ = run_problems(starts, counts, qp, kp, vp, gp, bp, S0, scale, nthreads)
+    out = out.reshape(B, H, T, dv).transpose(0, 2, 1, 3)
+    return np.ascontiguousarray(out), ST.reshape(N, H, dk, dv)
+
+
+def decode_step(state, q, k, v, g, beta, scale, nthreads=0):
+    """Oracle of ``kda_recurrent_step``: state [N, H, dk, dv]; q, k, g [N, H, dk];
+    v [N, H, dv]; beta [N, H].  Returns (out [N, H, dv], new_state) in fp64."""
+    q, k, v, g, beta, S = (_f64(a) for a in (q, k, v, g, beta, state))
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    P = N * H
+    out, ST, _ = run_problems(np.arange(P), np.ones(P), q.reshape(P, dk), k.reshape(P, dk),
+                              v.reshape(P, dv), g.reshape(P, dk), beta.reshape(P),
+                              S.reshape(P, dk, dv), scale, nthreads)
+    return out.reshape(N, H, dv), ST.reshape(N, H, dk, dv)
