@@ -1,0 +1,149 @@
+"""Python binding of libkda, the GB300 KDA core (C ABI in include/kda.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libkda.so``.  PyTorch supplies device memory and streams.  There is
+no fallback: if the library is missing, importing the binding's entry points
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB, build, up_to_date  # noqa: F401
+
+__all__ = ["kda_chunk_fwd", "kda_fused_recurrent_fwd", "kda_recurrent_step",
+           "kda_get_device_error", "KdaError", "load_library", "build", "STATUS"]
+
+STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
+          4: "KDA_ERR_DEVICE", 5: "KDA_ERR_TIMEOUT"}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
+
+EXPORTED = ["kda_chunk_fwd", "kda_fused_recurrent_fwd", "kda_recurrent_step",
+            "kda_get_device_error", "kda_status_string", "kda_last_error_message"]
+
+
+class KdaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+_lib = None
+_P = ctypes.POINTER(KdaTensor)
+
+
+def load_library(path: str | None = None):
+    """Load libkda.so (built in-tree by ``build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB
+    if not os.path.exists(path):
+        raise ImportError(f"libkda.so not built ({path}); run gated_delta_rule_gb300.build()")
+    lib = ctypes.CDLL(path)
+    fwd = [_P] * 6 + [ctypes.c_float, _P, _P, _P, ctypes.c_void_p]
+    for name in ("kda_chunk_fwd", "kda_fused_recurrent_fwd"):
+        f = getattr(lib, name)
+        f.restype, f.argtypes = ctypes.c_int, fwd
+    lib.kda_recurrent_step.restype = ctypes.c_int
+    lib.kda_recurrent_step.argtypes = [_P] * 6 + [ctypes.c_float, _P, ctypes.c_void_p]
+    lib.kda_get_device_error.restype = ctypes.c_int
+    lib.kda_get_device_error.argtypes = [ctypes.c_void_p]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_last_error_message.restype = ctypes.c_char_p
+    lib.kda_last_error_message.argtypes = []
+    _lib = lib
+    return lib
+
+
+def desc(t: torch.Tensor | None):
+    """kda_tensor descriptor of a torch tensor (no copy); None stays NULL."""
+    if t is None:
+        return None
+    if t.dim() > 4:
+        raise ValueError("at most 4 dimensions")
+    d = KdaTensor()
+    d.data = t.data_ptr() if t.numel() else None
+    d.dtype = DTYPES.get(t.dtype, -1)
+    d.ndim = t.dim()
+    for i, (s, st) in enumerate(zip(t.shape, t.stride())):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+def _ref(d):
+    return None if d is None else ctypes.byref(d)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream or None
+    return int(stream) or None
+
+
+def _check(lib, status: int):
+    if status != 0:
+        raise KdaError(status, lib.kda_last_error_message().decode())
+
+
+def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, scale=None, cu_seqlens=None, out=None,
+                  final_state=None, output_final_state=True, stream=None, _entry="kda_chunk_fwd"):
+    """Chunked KDA prefill.  Shapes as in include/kda.h; returns (out, final_state)."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    if scale is None:
+        scale = dk ** -0.5
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    ds = [desc(x) for x in (q, k, v, g, beta, initial_state, cu_seqlens, out, final_state)]
+    st = getattr(lib, _entry)(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), _ref(ds[4]),
+                              _ref(ds[5]), float(scale), _ref(ds[6]), _ref(ds[7]), _ref(ds[8]),
+                              _stream(stream))
+    _check(lib, st)
+    return out, final_state
+
+
+def kda_fused_recurrent_fwd(*args, **kw):
+    """Token-by-token KDA prefill with on-chip fp32 state; same contract as kda_chunk_fwd."""
+    kw["_entry"] = "kda_fused_recurrent_fwd"
+    return kda_chunk_fwd(*args, **kw)
+
+
+def kda_recurrent_step(state, q, k, v, g, beta, scale=None, out=None, stream=None):
+    """One decode step per (request, head); updates ``state`` in place, returns out."""
+    lib = load_library()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if scale is None:
+        scale = dk ** -0.5
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    ds = [desc(x) for x in (state, q, k, v, g, beta, out)]
+    st = lib.kda_recurrent_step(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), _ref(ds[4]),
+                                _ref(ds[5]), float(scale), _ref(ds[6]), _stream(stream))
+    _check(lib, st)
+    return out
+
+
+def kda_get_device_error(stream=None) -> int:
+    """Synchronise ``stream`` and raise KdaError if the device recorded an error."""
+    lib = load_library()
+    _check(lib, lib.kda_get_device_error(_stream(stream)))
+    return 0

@@ -1,0 +1,415 @@
+// C-ABI layer of libkda: argument validation, dispatch to the kernels, status
+// codes and the per-device error word.  Declarations and the contract of every
+// entry point are in include/kda.h.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+thread_local std::string g_msg;
+
+kda_status fail(kda_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_msg = buf;
+  return st;
+}
+
+// Device error word, one per device (a module-scope device variable is
+// instantiated on every device that loads the library).
+__device__ int g_device_error;
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices];
+std::mutex g_err_mu;
+
+kda_status device_error_ptr(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(KDA_ERR_UNSUPPORTED, "device %d", dev);
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error);
+    if (e != cudaSuccess)
+      return fail(KDA_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return KDA_OK;
+}
+
+size_t esize(int32_t dt) {
+  switch (dt) {
+    case KDA_DTYPE_F32:
+      return 4;
+    case KDA_DTYPE_BF16:
+      return 2;
+    case KDA_DTYPE_I32:
+      return 4;
+    default:
+      return 0;
+  }
+}
+
+const char* dtname(int32_t dt) {
+  switch (dt) {
+    case KDA_DTYPE_F32:
+      return "f32";
+    case KDA_DTYPE_BF16:
+      return "bf16";
+    case KDA_DTYPE_I32:
+      return "i32";
+    default:
+      return "?";
+  }
+}
+
+struct Extent {
+  uintptr_t lo = 0, hi = 0;  // [lo, hi); empty when lo == hi
+};
+
+Extent extent(const kda_tensor* t) {
+  Extent e;
+  if (!t || !t->data) return e;
+  int64_t last = 0;
+  for (int d = 0; d < t->ndim; ++d) {
+    if (t->shape[d] == 0) return e;
+    last += (t->shape[d] - 1) * t->stride[d];
+  }
+  const size_t es = esize(t->dtype);
+  e.lo = reinterpret_cast<uintptr_t>(t->data);
+  e.hi = e.lo + (uintptr_t)(last + 1) * es;
+  return e;
+}
+
+bool overlap(const kda_tensor* a, const kda_tensor* b) {
+  const Extent x = extent(a), y = extent(b);
+  if (x.lo == x.hi || y.lo == y.hi) return false;
+  return x.lo < y.hi && y.lo < x.hi;
+}
+
+// Checks a descriptor: rank, non-negative sizes and strides, innermost
+// contiguity and alignment (`align` bytes for the pointer and outer strides).
+kda_status check_desc(const kda_tensor* t, const char* name, int ndim, size_t align) {
+  if (!t) return fail(KDA_ERR_INVALID_ARG, "%s: descriptor is NULL", name);
+  if (t->ndim != ndim)
+    return fail(KDA_ERR_INVALID_ARG, "%s: expected %d dimensions, got %d", name, ndim, t->ndim);
+  const size_t es = esize(t->dtype);
+  if (!es) return fail(KDA_ERR_INVALID_ARG, "%s: unknown dtype %d", name, t->dtype);
+  int64_t numel = 1;
+  for (int d = 0; d < ndim; ++d) {
+    if (t->shape[d] < 0 || t->stride[d] < 0)
+      return fail(KDA_ERR_INVALID_ARG, "%s: negative size or stride in dim %d", name, d);
+    numel *= t->shape[d];
+  }
+  if (numel == 0) return KDA_OK;
+  if (!t->data) return fail(KDA_ERR_INVALID_ARG, "%s: data is NULL", name);
+  if (t->stride[ndim - 1] != 1 && t->shape[ndim - 1] > 1)
+    return fail(KDA_ERR_INVALID_ARG, "%s: innermost stride must be 1", name);
+  if (reinterpret_cast<uintptr_t>(t->data) % align)
+    return fail(KDA_ERR_INVALID_ARG, "%s: data pointer not %zu-byte aligned", name, align);
+  for (int d = 0; d + 1 < ndim; ++d)
+    if (t->shape[d] > 1 && ((size_t)t->stride[d] * es) % align)
+      return fail(KDA_ERR_INVALID_ARG, "%s: stride of dim %d is not a multiple of %zu bytes",
+                  name, d, align);
+  return KDA_OK;
+}
+
+kda_status check_shape(const kda_tensor* t, const char* name, int ndim, const int64_t* want,
+                       int32_t dtype) {
+  if (t->dtype != dtype)
+    return fail(KDA_ERR_INVALID_ARG, "%s: dtype %s, expected %s", name, dtname(t->dtype),
+                dtname(dtype));
+  for (int d = 0; d < ndim; ++d)
+    if (t->shape[d] != want[d])
+      return fail(KDA_ERR_INVALID_ARG, "%s: size %lld in dim %d, expected %lld", name,
+                  (long long)t->shape[d], d, (long long)want[d]);
+  return KDA_OK;
+}
+
+#define KDA_TRY(x)                \
+  do {                            \
+    kda_status st_ = (x);         \
+    if (st_ != KDA_OK) return st_; \
+  } while (0)
+
+kda_status check_head_dims(int64_t dk, int64_t dv) {
+  if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128))
+    return fail(KDA_ERR_UNSUPPORTED, "head dims d_k=%lld d_v=%lld; supported: 64, 128",
+                (long long)dk, (long long)dv);
+  return KDA_OK;
+}
+
+kda_status check_state(const kda_tensor* s, const char* name, int64_t N, int64_t H, int64_t dk,
+                       int64_t dv) {
+  KDA_TRY(check_desc(s, name, 4, 16));
+  const int64_t want[4] = {N, H, dk, dv};
+  KDA_TRY(check_shape(s, name, 4, want, KDA_DTYPE_F32));
+  if (N * H > 0 && s->stride[2] != dv)
+    return fail(KDA_ERR_INVALID_ARG, "%s: inner [d_k, d_v] block must be contiguous", name);
+  return KDA_OK;
+}
+
+kda::Act act(const kda_tensor* t) {
+  kda::Act a;
+  a.ptr = t->data;
+  if (t->ndim == 4) {
+    a.sb = t->stride[0];
+    a.st = t->stride[1];
+    a.sh = t->stride[2];
+  } else {  // [N, H, D]
+    a.sb = t->stride[0];
+    a.st = 0;
+    a.sh = t->stride[1];
+  }
+  return a;
+}
+
+kda_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+enum class PrefillPath { kChunked, kRecurrent };
+
+kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                   const kda_tensor* g, const kda_tensor* beta, const kda_tensor* s0,
+                   float scale, const kda_tensor* cu, kda_tensor* out, kda_tensor* sT,
+                   void* stream, PrefillPath path) {
+  g_msg.clear();
+  KDA_TRY(check_desc(q, "q", 4, 16));
+  const int32_t dt = q->dtype;
+  if (dt != KDA_DTYPE_BF16 && dt != KDA_DTYPE_F32)
+    return fail(KDA_ERR_INVALID_ARG, "q: dtype must be bf16 or f32");
+  const int64_t B = q->shape[0], T = q->shape[1], H = q->shape[2], dk = q->shape[3];
+  KDA_TRY(check_desc(v, "v", 4, 16));
+  const int64_t dv = v->shape[3];
+  KDA_TRY(check_head_dims(dk, dv));
+  const int64_t wq[4] = {B, T, H, dk}, wv[4] = {B, T, H, dv}, wb[3] = {B, T, H};
+  KDA_TRY(check_desc(k, "k", 4, 16));
+  KDA_TRY(check_shape(k, "k", 4, wq, dt));
+  KDA_TRY(check_shape(v, "v", 4, wv, dt));
+  KDA_TRY(check_desc(g, "g", 4, 16));
+  KDA_TRY(check_shape(g, "g", 4, wq, KDA_DTYPE_F32));
+  KDA_TRY(check_desc(beta, "beta", 3, 4));
+  KDA_TRY(check_shape(beta, "beta", 3, wb, KDA_DTYPE_F32));
+  KDA_TRY(check_desc(out, "out", 4, 16));
+  KDA_TRY(check_shape(out, "out", 4, wv, dt));
+  if (!isfinite(scale)) return fail(KDA_ERR_INVALID_ARG, "scale must be finite");
+  if (T > INT32_MAX || B > INT32_MAX || H > 65535)
+    return fail(KDA_ERR_UNSUPPORTED, "sizes too large (T, B < 2^31, H < 65536)");
+  int64_t N = B;
+  if (cu) {
+    KDA_TRY(check_desc(cu, "cu_seqlens", 1, 4));
+    if (cu->dtype != KDA_DTYPE_I32) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens: dtype must be i32");
+    if (cu->shape[0] < 1) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens: needs N+1 >= 1 entries");
+    if (B != 1) return fail(KDA_ERR_INVALID_ARG, "varlen (cu_seqlens) requires B == 1, got %lld",
+                            (long long)B);
+    N = cu->shape[0] - 1;
+  }
+  if (N * H > INT32_MAX / 8) return fail(KDA_ERR_UNSUPPORTED, "too many (sequence, head) pairs");
+  if (s0) KDA_TRY(check_state(s0, "initial_state", N, H, dk, dv));
+  if (sT) KDA_TRY(check_state(sT, "final_state", N, H, dk, dv));
+  // aliasing
+  const kda_tensor* ins[] = {q, k, v, g, beta, s0, cu};
+  const char* in_names[] = {"q", "k", "v", "g", "beta", "initial_state", "cu_seqlens"};
+  for (int i = 0; i < 7; ++i)
+    if (ins[i] && overlap(out, ins[i]))
+      return fail(KDA_ERR_INVALID_ARG, "out overlaps %s", in_names[i]);
+  if (sT) {
+    if (overlap(out, sT)) return fail(KDA_ERR_INVALID_ARG, "out overlaps final_state");
+    for (int i = 0; i < 5; ++i)
+      if (overlap(sT, ins[i])) return fail(KDA_ERR_INVALID_ARG, "final_state overlaps %s", in_names[i]);
+    if (cu && overlap(sT, cu)) return fail(KDA_ERR_INVALID_ARG, "final_state overlaps cu_seqlens");
+    if (s0 && overlap(sT, s0)) {
+      const bool same = s0->data == sT->data && s0->stride[0] == sT->stride[0] &&
+                        s0->stride[1] == sT->stride[1];
+      if (!same)
+        return fail(KDA_ERR_INVALID_ARG, "final_state partly overlaps initial_state");
+    }
+  }
+
+  kda::PrefillArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = act(q);
+  a.k = act(k);
+  a.v = act(v);
+  a.g = act(g);
+  a.beta = static_cast<const float*>(beta->data);
+  a.beta_sb = beta->stride[0];
+  a.beta_st = beta->stride[1];
+  a.beta_sh = beta->stride[2];
+  if (s0 && N * H > 0) {
+    a.s0 = static_cast<const float*>(s0->data);
+    a.s0_sn = s0->stride[0];
+    a.s0_sh = s0->stride[1];
+  }
+  if (sT && N * H > 0) {
+    a.sT = static_cast<float*>(sT->data);
+    a.sT_sn = sT->stride[0];
+    a.sT_sh = sT->stride[1];
+  }
+  a.out = out->data;
+  a.out_sb = out->stride[0];
+  a.out_st = out->stride[1];
+  a.out_sh = out->stride[2];
+  a.cu_seqlens = cu ? static_cast<const int32_t*>(cu->data) : nullptr;
+  a.B = (int)B;
+  a.T = (int)T;
+  a.H = (int)H;
+  a.N = (int)N;
+  a.dk = (int)dk;
+  a.dv = (int)dv;
+  a.bf16 = dt == KDA_DTYPE_BF16;
+  a.scale = scale;
+  if (N * H == 0) return KDA_OK;
+  if (!a.sT && T == 0) return KDA_OK;
+  KDA_TRY(device_error_ptr(&a.err));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (cu) {
+    e = kda::launch_check_seqlens(a.cu_seqlens, a.N, a.T, a.err, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cu_seqlens check launch");
+  }
+  if (path == PrefillPath::kChunked && a.bf16)
+    e = kda::launch_chunk_prefill_tc(a, st);
+  else
+    e = kda::launch_recurrent_prefill(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_chunk_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                         const kda_tensor* g, const kda_tensor* beta,
+                         const kda_tensor* initial_state, float scale,
+                         const kda_tensor* cu_seqlens, kda_tensor* out,
+                         kda_tensor* final_state, void* stream) {
+  return prefill(q, k, v, g, beta, initial_state, scale, cu_seqlens, out, final_state, stream,
+                 PrefillPath::kChunked);
+}
+
+kda_status kda_fused_recurrent_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                                   const kda_tensor* g, const kda_tensor* beta,
+                                   const kda_tensor* initial_state, float scale,
+                                   const kda_tensor* cu_seqlens, kda_tensor* out,
+                                   kda_tensor* final_state, void* stream) {
+  return prefill(q, k, v, g, beta, initial_state, scale, cu_seqlens, out, final_state, stream,
+                 PrefillPath::kRecurrent);
+}
+
+kda_status kda_recurrent_step(kda_tensor* state, const kda_tensor* q, const kda_tensor* k,
+                              const kda_tensor* v, const kda_tensor* g, const kda_tensor* beta,
+                              float scale, kda_tensor* out, void* stream) {
+  g_msg.clear();
+  KDA_TRY(check_desc(q, "q", 3, 16));
+  const int32_t dt = q->dtype;
+  if (dt != KDA_DTYPE_BF16 && dt != KDA_DTYPE_F32)
+    return fail(KDA_ERR_INVALID_ARG, "q: dtype must be bf16 or f32");
+  const int64_t N = q->shape[0], H = q->shape[1], dk = q->shape[2];
+  KDA_TRY(check_desc(v, "v", 3, 16));
+  const int64_t dv = v->shape[2];
+  KDA_TRY(check_head_dims(dk, dv));
+  const int64_t wq[3] = {N, H, dk}, wv[3] = {N, H, dv}, wb[2] = {N, H};
+  KDA_TRY(check_desc(k, "k", 3, 16));
+  KDA_TRY(check_shape(k, "k", 3, wq, dt));
+  KDA_TRY(check_shape(v, "v", 3, wv, dt));
+  KDA_TRY(check_desc(g, "g", 3, 16));
+  KDA_TRY(check_shape(g, "g", 3, wq, KDA_DTYPE_F32));
+  KDA_TRY(check_desc(beta, "beta", 2, 4));
+  KDA_TRY(check_shape(beta, "beta", 2, wb, KDA_DTYPE_F32));
+  KDA_TRY(check_desc(out, "out", 3, 16));
+  KDA_TRY(check_shape(out, "out", 3, wv, dt));
+  KDA_TRY(check_state(state, "state", N, H, dk, dv));
+  if (!isfinite(scale)) return fail(KDA_ERR_INVALID_ARG, "scale must be finite");
+  if (N * H > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "too many (request, head) pairs");
+  const kda_tensor* ins[] = {q, k, v, g, beta, state};
+  const char* names[] = {"q", "k", "v", "g", "beta", "state"};
+  for (int i = 0; i < 6; ++i)
+    if (overlap(out, ins[i])) return fail(KDA_ERR_INVALID_ARG, "out overlaps %s", names[i]);
+  for (int i = 0; i < 5; ++i)
+    if (overlap(state, ins[i])) return fail(KDA_ERR_INVALID_ARG, "state overlaps %s", names[i]);
+  if (N * H == 0) return KDA_OK;
+
+  kda::DecodeArgs a;
+  memset(&a, 0, sizeof(a));
+  a.state = static_cast<float*>(state->data);
+  a.s_sn = state->stride[0];
+  a.s_sh = state->stride[1];
+  a.q = act(q);
+  a.k = act(k);
+  a.v = act(v);
+  a.g = act(g);
+  a.beta = static_cast<const float*>(beta->data);
+  a.beta_sn = beta->stride[0];
+  a.beta_sh = beta->stride[1];
+  a.out = out->data;
+  a.out_sn = out->stride[0];
+  a.out_sh = out->stride[1];
+  a.N = (int)N;
+  a.H = (int)H;
+  a.dk = (int)dk;
+  a.dv = (int)dv;
+  a.bf16 = dt == KDA_DTYPE_BF16;
+  a.scale = scale;
+  cudaError_t e = kda::launch_decode(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return KDA_OK;
+}
+
+kda_status kda_get_device_error(void* stream) {
+  g_msg.clear();
+  int* p = nullptr;
+  KDA_TRY(device_error_ptr(&p));
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, p, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  if (word == 0) return KDA_OK;
+  const int zero = 0;
+  e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+  if (word & kda::kErrTimeout)
+    return fail(KDA_ERR_TIMEOUT, "a bounded device-side wait gave up (word 0x%x)", word);
+  return fail(KDA_ERR_DEVICE, "cu_seqlens must start at 0, never decrease and end at T (word 0x%x)",
+              word);
+}
+
+const char* kda_status_string(kda_status s) {
+  switch (s) {
+    case KDA_OK:
+      return "KDA_OK";
+    case KDA_ERR_INVALID_ARG:
+      return "KDA_ERR_INVALID_ARG";
+    case KDA_ERR_UNSUPPORTED:
+      return "KDA_ERR_UNSUPPORTED";
+    case KDA_ERR_CUDA:
+      return "KDA_ERR_CUDA";
+    case KDA_ERR_DEVICE:
+      return "KDA_ERR_DEVICE";
+    case KDA_ERR_TIMEOUT:
+      return "KDA_ERR_TIMEOUT";
+  }
+  return "KDA_ERR_UNKNOWN";
+}
+
+const char* kda_last_error_message(void) { return g_msg.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// Internal interface between the C-ABI layer (kda_api.cu) and the kernel files.
+// Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Device error word bits (or-ed by kernels, read by kda_get_device_error).
+enum : int {
+  kErrBadSeqlens = 1,  // cu_seqlens not starting at 0, decreasing or not ending at T
+  kErrTimeout = 2,     // a bounded wait gave up
+};
+
+// Strided view of a [B, T, H, D] (or [N, H, D]) activation; strides in elements.
+struct Act {
+  const void* ptr;
+  int64_t sb, st, sh;  // batch, time, head strides (innermost stride is 1)
+};
+
+struct PrefillArgs {
+  Act q, k, v, g;
+  const float* beta;
+  int64_t beta_sb, beta_st, beta_sh;
+  const float* s0;  // nullable; [N, H, dk, dv] with strides s_sn, s_sh (inner contiguous)
+  int64_t s0_sn, s0_sh;
+  float* sT;  // nullable
+  int64_t sT_sn, sT_sh;
+  void* out;
+  int64_t out_sb, out_st, out_sh;
+  const int32_t* cu_seqlens;  // nullable
+  int B, T, H, N, dk, dv;
+  int bf16;  // 1: q/k/v/out are bf16, 0: fp32
+  float scale;
+  int* err;  // device error word
+};
+
+struct DecodeArgs {
+  float* state;
+  int64_t s_sn, s_sh;
+  Act q, k, v, g;  // sb = request stride, sh = head stride (st unused)
+  const float* beta;
+  int64_t beta_sn, beta_sh;
+  void* out;
+  int64_t out_sn, out_sh;
+  int N, H, dk, dv;
+  int bf16;
+  float scale;
+};
+
+// SIMT kernels (kda_recurrent.cu)
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s);
+// cu_seqlens validation: sets kErrBadSeqlens in *err when the offsets are invalid.
+cudaError_t launch_check_seqlens(const int32_t* cu, int N, int T, int* err, cudaStream_t s);
+
+// Tensor-core chunked prefill (kda_prefill_tc.cu); bf16 inputs only.
+cudaError_t launch_chunk_prefill_tc(const PrefillArgs& a, cudaStream_t s);
+
+}  // namespace kda

@@ -1,0 +1,329 @@
+// SIMT kernels of the KDA core:
+//   * kda_decode_kernel     - one decode token per (request, head), state in place;
+//   * kda_recurrent_kernel  - token-by-token prefill with the state held in
+//                             registers (the fp32-input path, any sequence length);
+//   * kda_seqlens_kernel    - device-side validation of cu_seqlens.
+//
+// Both compute kernels run the single-step recurrence in the order of
+// "Kimi K3 核心算子拆解" (devpress.csdn.net) §2.3: decay every key-channel row by
+// alpha_i = exp(g_i), subtract beta k (k^T S), add beta k v^T, then read out
+// o = scale * S^T q ("Kimi K3 技术报告解读" (marsggbo.github.io) §3.2).  The
+// correction and the write are two fused multiply-adds per element,
+//   S' = fma(beta k_i, v_j, fma(-beta k_i, (k^T S)_j, S_ij)),
+// so a unit key with beta = 1 reproduces v exactly in that row.
+//
+// Thread layout (256 threads per (sequence|request, head)): a state row of d_v
+// fp32 values is covered by d_v/4 threads holding 4 consecutive columns
+// (one 16-byte vector each); 256/(d_v/4) rows are handled side by side and
+// each thread keeps d_k*(d_v/4)/256 rows in registers.  Column sums over the
+// key channels (k^T S and q^T S) are reduced through shared memory.  A warp
+// therefore loads and stores whole contiguous rows: 512 bytes per instruction
+// at d_v = 128.
+#include <cuda_bf16.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+  const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+  return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+
+template <typename T>
+__device__ __forceinline__ void store4(T* p, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, float4 v) {
+  *reinterpret_cast<float4*>(p) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+__device__ __forceinline__ void fma4(float4& acc, float s, const float4& x) {
+  acc.x = fmaf(s, x.x, acc.x);
+  acc.y = fmaf(s, x.y, acc.y);
+  acc.z = fmaf(s, x.z, acc.z);
+  acc.w = fmaf(s, x.w, acc.w);
+}
+
+// S' = fma(bk, v, fma(-bk, kS, S)) element-wise
+__device__ __forceinline__ float4 delta_write(float4 s, float bk, const float4& kS, const float4& v) {
+  s.x = fmaf(bk, v.x, fmaf(-bk, kS.x, s.x));
+  s.y = fmaf(bk, v.y, fmaf(-bk, kS.y, s.y));
+  s.z = fmaf(bk, v.z, fmaf(-bk, kS.z, s.z));
+  s.w = fmaf(bk, v.w, fmaf(-bk, kS.w, s.w));
+  return s;
+}
+
+template <int DK, int DV>
+struct Layout {
+  static constexpr int TPR = DV / 4;           // threads per state row
+  static constexpr int RPP = kThreads / TPR;   // rows side by side
+  static constexpr int R = DK / RPP;           // rows per thread
+  static_assert(R * RPP == DK, "layout");
+};
+
+// Sum over the RPP row groups of per-thread partial column sums.
+template <int DK, int DV>
+__device__ __forceinline__ float4 column_reduce(float4 part, float4 (*red)[DV / 4], int trow,
+                                               int col4) {
+  using L = Layout<DK, DV>;
+  red[trow][col4] = part;
+  __syncthreads();
+  float4 s = red[0][col4];
+#pragma unroll
+  for (int r = 1; r < L::RPP; ++r) {
+    const float4 x = red[r][col4];
+    s.x += x.x;
+    s.y += x.y;
+    s.z += x.z;
+    s.w += x.w;
+  }
+  return s;
+}
+
+// ---------------------------------------------------------------------------
+// decode: one CTA per (request, head); every state element read once, written once
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kThreads, 2) kda_decode_kernel(DecodeArgs a) {
+  using L = Layout<DK, DV>;
+  __shared__ float s_q[DK], s_k[DK], s_a[DK];
+  __shared__ float4 red0[L::RPP][DV / 4];
+  __shared__ float4 red1[L::RPP][DV / 4];
+  const int n = blockIdx.x / a.H;
+  const int h = blockIdx.x - n * a.H;
+  const int tid = threadIdx.x;
+  const int col4 = tid % L::TPR;
+  const int trow = tid / L::TPR;
+
+  float* S = a.state + n * a.s_sn + h * a.s_sh;
+  float4 s[L::R];
+#pragma unroll
+  for (int r = 0; r < L::R; ++r)
+    s[r] = __ldcs(reinterpret_cast<const float4*>(S + (trow + L::RPP * r) * DV + 4 * col4));
+
+  const T* qp = static_cast<const T*>(a.q.ptr) + n * a.q.sb + h * a.q.sh;
+  const T* kp = static_cast<const T*>(a.k.ptr) + n * a.k.sb + h * a.k.sh;
+  const float* gp = static_cast<const float*>(a.g.ptr) + n * a.g.sb + h * a.g.sh;
+  const T* vp = static_cast<const T*>(a.v.ptr) + n * a.v.sb + h * a.v.sh;
+  const float beta = __ldg(a.beta + n * a.beta_sn + h * a.beta_sh);
+  if (tid < DK) {
+    s_q[tid] = to_f(qp[tid]);
+    s_k[tid] = to_f(kp[tid]);
+    s_a[tid] = expf(__ldg(gp + tid));
+  }
+  const float4 v4 = load4<T>(vp + 4 * col4);
+  __syncthreads();
+
+  float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int r = 0; r < L::R; ++r) {
+    const int i = trow + L::RPP * r;
+    const float al = s_a[i];
+    s[r].x *= al;
+    s[r].y *= al;
+    s[r].z *= al;
+    s[r].w *= al;
+    fma4(part, s_k[i], s[r]);
+  }
+  const float4 kS = column_reduce<DK, DV>(part, red0, trow, col4);
+
+  float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int r = 0; r < L::R; ++r) {
+    const int i = trow + L::RPP * r;
+    s[r] = delta_write(s[r], beta * s_k[i], kS, v4);
+    __stcs(reinterpret_cast<float4*>(S + i * DV + 4 * col4), s[r]);
+    fma4(po, s_q[i], s[r]);
+  }
+  float4 o = column_reduce<DK, DV>(po, red1, trow, col4);
+  if (trow == 0) {
+    o.x *= a.scale;
+    o.y *= a.scale;
+    o.z *= a.scale;
+    o.w *= a.scale;
+    store4<T>(static_cast<T*>(a.out) + n * a.out_sn + h * a.out_sh + 4 * col4, o);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// token-by-token prefill: one CTA per (sequence, head), state in registers
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kThreads, 1) kda_recurrent_kernel(PrefillArgs a) {
+  using L = Layout<DK, DV>;
+  __shared__ float s_q[2][DK], s_k[2][DK], s_a[2][DK];
+  __shared__ float4 red0[L::RPP][DV / 4];
+  __shared__ float4 red1[L::RPP][DV / 4];
+  const int n = blockIdx.x / a.H;
+  const int h = blockIdx.x - n * a.H;
+  const int tid = threadIdx.x;
+  const int col4 = tid % L::TPR;
+  const int trow = tid / L::TPR;
+
+  // token range of this sequence: rows of batch b = n, or the cu_seqlens slice
+  int64_t b = n, t0 = 0, t1 = a.T;
+  if (a.cu_seqlens) {
+    b = 0;
+    t0 = min(max(__ldg(a.cu_seqlens + n), 0), a.T);
+    t1 = min(max(__ldg(a.cu_seqlens + n + 1), (int)t0), a.T);
+  }
+
+  float4 s[L::R];
+  if (a.s0) {
+    const float* S0 = a.s0 + n * a.s0_sn + h * a.s0_sh;
+#pragma unroll
+    for (int r = 0; r < L::R; ++r)
+      s[r] = *reinterpret_cast<const float4*>(S0 + (trow + L::RPP * r) * DV + 4 * col4);
+  } else {
+#pragma unroll
+    for (int r = 0; r < L::R; ++r) s[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+
+  const T* qb = static_cast<const T*>(a.q.ptr) + b * a.q.sb + h * a.q.sh;
+  const T* kb = static_cast<const T*>(a.k.ptr) + b * a.k.sb + h * a.k.sh;
+  const float* gb = static_cast<const float*>(a.g.ptr) + b * a.g.sb + h * a.g.sh;
+  const T* vb = static_cast<const T*>(a.v.ptr) + b * a.v.sb + h * a.v.sh;
+  const float* bb = a.beta + b * a.beta_sb + h * a.beta_sh;
+  T* ob = static_cast<T*>(a.out) + b * a.out_sb + h * a.out_sh;
+
+  // stage token t0 into buffer 0
+  float pq = 0.f, pk = 0.f, pa = 0.f;
+  if (t0 < t1 && tid < DK) {
+    pq = to_f(qb[t0 * a.q.st + tid]);
+    pk = to_f(kb[t0 * a.k.st + tid]);
+    pa = expf(__ldg(gb + t0 * a.g.st + tid));
+  }
+  for (int64_t t = t0; t < t1; ++t) {
+    const int buf = (int)((t - t0) & 1);
+    if (tid < DK) {
+      s_q[buf][tid] = pq;
+      s_k[buf][tid] = pk;
+      s_a[buf][tid] = pa;
+    }
+    const float4 v4 = load4<T>(vb + t * a.v.st + 4 * col4);
+    const float beta = __ldg(bb + t * a.beta_st);
+    if (t + 1 < t1 && tid < DK) {  // prefetch the next token while this one computes
+      pq = to_f(qb[(t + 1) * a.q.st + tid]);
+      pk = to_f(kb[(t + 1) * a.k.st + tid]);
+      pa = expf(__ldg(gb + (t + 1) * a.g.st + tid));
+    }
+    __syncthreads();
+    float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < L::R; ++r) {
+      const int i = trow + L::RPP * r;
+      const float al = s_a[buf][i];
+      s[r].x *= al;
+      s[r].y *= al;
+      s[r].z *= al;
+      s[r].w *= al;
+      fma4(part, s_k[buf][i], s[r]);
+    }
+    const float4 kS = column_reduce<DK, DV>(part, red0, trow, col4);
+    float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < L::R; ++r) {
+      const int i = trow + L::RPP * r;
+      s[r] = delta_write(s[r], beta * s_k[buf][i], kS, v4);
+      fma4(po, s_q[buf][i], s[r]);
+    }
+    float4 o = column_reduce<DK, DV>(po, red1, trow, col4);
+    if (trow == 0) {
+      o.x *= a.scale;
+      o.y *= a.scale;
+      o.z *= a.scale;
+      o.w *= a.scale;
+      store4<T>(ob + t * a.out_st + 4 * col4, o);
+    }
+    // red0/red1 are rewritten next token only after that token's first barrier,
+    // which every thread reaches after finishing its reads of this token.
+  }
+  if (a.sT) {
+    float* ST = a.sT + n * a.sT_sn + h * a.sT_sh;
+#pragma unroll
+    for (int r = 0; r < L::R; ++r)
+      *reinterpret_cast<float4*>(ST + (trow + L::RPP * r) * DV + 4 * col4) = s[r];
+  }
+}
+
+__global__ void kda_seqlens_kernel(const int32_t* cu, int N, int T, int* err) {
+  bool bad = false;
+  for (int i = threadIdx.x; i <= N; i += blockDim.x) {
+    const int c = cu[i];
+    if (i == 0 && c != 0) bad = true;
+    if (i == N && c != T) bad = true;
+    if (i > 0 && c < cu[i - 1]) bad = true;
+  }
+  if (bad) atomicOr(err, kErrBadSeqlens);
+}
+
+template <template <int, int, typename> class K, typename Args>
+cudaError_t dispatch(const Args& a, int dk, int dv, int bf16, dim3 grid, cudaStream_t st) {
+  void (*fn)(Args) = nullptr;
+#define KDA_CASE(DK_, DV_)                                                   \
+  if (dk == DK_ && dv == DV_)                                                \
+    fn = bf16 ? (void (*)(Args))K<DK_, DV_, __nv_bfloat16>::fn : K<DK_, DV_, float>::fn;
+  KDA_CASE(64, 64)
+  KDA_CASE(64, 128)
+  KDA_CASE(128, 64)
+  KDA_CASE(128, 128)
+#undef KDA_CASE
+  if (!fn) return cudaErrorInvalidValue;
+  fn<<<grid, kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DK, int DV, typename T>
+struct DecodeK {
+  static constexpr void (*fn)(DecodeArgs) = kda_decode_kernel<DK, DV, T>;
+};
+template <int DK, int DV, typename T>
+struct RecurrentK {
+  static constexpr void (*fn)(PrefillArgs) = kda_recurrent_kernel<DK, DV, T>;
+};
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  if ((int64_t)a.N * a.H == 0) return cudaSuccess;
+  return dispatch<DecodeK>(a, a.dk, a.dv, a.bf16, dim3((unsigned)(a.N * a.H)), s);
+}
+
+cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s) {
+  if ((int64_t)a.N * a.H == 0) return cudaSuccess;
+  return dispatch<RecurrentK>(a, a.dk, a.dv, a.bf16, dim3((unsigned)(a.N * a.H)), s);
+}
+
+cudaError_t launch_check_seqlens(const int32_t* cu, int N, int T, int* err, cudaStream_t s) {
+  kda_seqlens_kernel<<<1, 256, 0, s>>>(cu, N, T, err);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,165 @@
+/*
+ * libkda - Kimi Delta Attention (KDA) core for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (per sequence and head, state S in R^{d_k x d_v}, fp32):
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t                      (read-out after the update)
+ *
+ * Sources: "Kimi K3 核心算子拆解" (devpress.csdn.net) §2.2 (state update) and
+ * §2.3 (decay / rank-1 correction / write); "Kimi K3 技术报告解读"
+ * (marsggbo.github.io) §3.2 (read-out S_t^T q_t) and §3.5 (log-decay g bounded
+ * in (-5, 0)); chunked prefill: "尝试对Kimi KDA的数学推导&算子实现分析"
+ * (hjcheng0602.cn/blog/kdd) eqs. (9)-(66).
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are passed as kda_tensor descriptors: a DEVICE pointer, a dtype,
+ *    a rank and per-dimension sizes and strides counted in ELEMENTS.  The
+ *    caller owns every buffer; the library keeps no pointer after a call
+ *    returns.  The innermost dimension must be contiguous (stride 1) and every
+ *    data pointer and every outer stride (in bytes) a multiple of 16.
+ *  - g is the PER-TOKEN log-decay (alpha = exp(g)); its documented domain is
+ *    [-5, 0] and beta's is [0, 1].  Outside it results follow the definition
+ *    above but may lose precision.  q and k are expected L2-normalised by the
+ *    caller (the KDA layer does this before the core); the library does not
+ *    normalise them.
+ *  - Head dimensions d_k, d_v are each 64 or 128.
+ *  - q, k, v (and out) share one dtype: KDA_DTYPE_BF16 or KDA_DTYPE_F32.
+ *    g, beta and the states are always KDA_DTYPE_F32.  out has q's dtype,
+ *    rounded to nearest even from fp32 accumulators.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *    is the legacy default stream).  KDA_OK means "validated and enqueued".
+ *  - Errors the host can detect return KDA_ERR_INVALID_ARG or
+ *    KDA_ERR_UNSUPPORTED before anything is launched and set a thread-local
+ *    message (kda_last_error_message).  A failed launch returns KDA_ERR_CUDA.
+ *    Problems only the device can see (cu_seqlens not non-decreasing, not
+ *    starting at 0 or not ending at T) are recorded in a per-device error word
+ *    read by kda_get_device_error; outputs are then unspecified.  NaN inputs
+ *    propagate; nothing traps.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1, /* a descriptor, shape, dtype, stride, alias or value is invalid */
+  KDA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. d_k = 96) */
+  KDA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  KDA_ERR_DEVICE = 4,      /* the device reported bad cu_seqlens (kda_get_device_error) */
+  KDA_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (kda_get_device_error) */
+} kda_status;
+
+typedef enum kda_dtype {
+  KDA_DTYPE_F32 = 0,
+  KDA_DTYPE_BF16 = 1,
+  KDA_DTYPE_I32 = 2
+} kda_dtype;
+
+typedef struct kda_tensor {
+  void* data;        /* device pointer */
+  int32_t dtype;     /* kda_dtype */
+  int32_t ndim;      /* 1..4 */
+  int64_t shape[4];  /* sizes of the first ndim dimensions */
+  int64_t stride[4]; /* strides in elements; stride[ndim-1] must be 1 */
+} kda_tensor;
+
+/*
+ * kda_chunk_fwd - chunkwise-parallel prefill (forward) of the KDA core.
+ *
+ * Defined by the recurrence above, computed chunk by chunk as in
+ * "尝试对Kimi KDA的数学推导&算子实现分析" (hjcheng0602.cn/blog/kdd): in-chunk
+ * cumulative log-decay (eq. 9), strictly lower-triangular A / L (eqs. 22, 51),
+ * triangular solve for U (eq. 52), output (eq. 63), state passed between
+ * chunks (eqs. 64-66).
+ *
+ *   q, k          [B, T, H, d_k]  bf16 or f32
+ *   v             [B, T, H, d_v]  same dtype as q
+ *   g             [B, T, H, d_k]  f32, per-token log-decay
+ *   beta          [B, T, H]       f32
+ *   initial_state [N, H, d_k, d_v] f32, inner [d_k, d_v] contiguous; NULL = zeros
+ *   scale         finite float multiplying the read-out (usually 1/sqrt(d_k))
+ *   cu_seqlens    NULL: N = B and every batch row is one sequence of T tokens.
+ *                 Otherwise [N+1] int32 on the device, B must be 1, and
+ *                 sequence n is tokens [cu_seqlens[n], cu_seqlens[n+1]) of the
+ *                 packed batch; values must start at 0, never decrease and end
+ *                 at T (checked on the device).  No state crosses a boundary:
+ *                 each sequence's results equal those of the sequence alone.
+ *   out           [B, T, H, d_v]  q's dtype; written for every token
+ *   final_state   [N, H, d_k, d_v] f32 or NULL; may be the same tensor as
+ *                 initial_state (in place) but must not partly overlap it.
+ *   stream        cudaStream_t as void*
+ *
+ * out must not overlap any input.  Empty sequences are allowed (their final
+ * state is their initial state).  fp32 inputs run the recurrence itself in
+ * fp32 (error well under 1e-4); bf16 inputs run the chunked tensor-core path
+ * with fp32 accumulation and an fp32 state.
+ */
+kda_status kda_chunk_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                         const kda_tensor* g, const kda_tensor* beta,
+                         const kda_tensor* initial_state, float scale,
+                         const kda_tensor* cu_seqlens, kda_tensor* out,
+                         kda_tensor* final_state, void* stream);
+
+/*
+ * kda_fused_recurrent_fwd - the same operation and contract as kda_chunk_fwd,
+ * computed token by token with each (sequence, head) state held on chip in
+ * fp32 ("把注意力换成一块「会遗忘的内存」" (jokeuncle.github.io), section on
+ * the layer's two execution paths: short sequences use the fused recurrent
+ * kernel).  Meant for short sequences and as an independent device-side
+ * cross-check of the chunked path; kda_chunk_fwd uses it for fp32 inputs.
+ */
+kda_status kda_fused_recurrent_fwd(const kda_tensor* q, const kda_tensor* k,
+                                   const kda_tensor* v, const kda_tensor* g,
+                                   const kda_tensor* beta, const kda_tensor* initial_state,
+                                   float scale, const kda_tensor* cu_seqlens, kda_tensor* out,
+                                   kda_tensor* final_state, void* stream);
+
+/*
+ * kda_recurrent_step - one decode token per request, state updated in place.
+ *
+ * The single-step recurrence in the three steps of "Kimi K3 核心算子拆解"
+ * §2.3 (decay, rank-1 correction, write), fused so each state element is read
+ * once and written once.
+ *
+ *   state  [N, H, d_k, d_v] f32, inner [d_k, d_v] contiguous; read and
+ *          overwritten with S_t
+ *   q, k   [N, H, d_k]  bf16 or f32
+ *   v      [N, H, d_v]  same dtype as q
+ *   g      [N, H, d_k]  f32
+ *   beta   [N, H]       f32
+ *   out    [N, H, d_v]  q's dtype
+ *
+ * out must not overlap state or any input.  With beta = 1 and k a unit basis
+ * vector e_i the new row i of the state equals v exactly.
+ */
+kda_status kda_recurrent_step(kda_tensor* state, const kda_tensor* q, const kda_tensor* k,
+                              const kda_tensor* v, const kda_tensor* g,
+                              const kda_tensor* beta, float scale, kda_tensor* out,
+                              void* stream);
+
+/*
+ * kda_get_device_error - synchronises `stream`, then returns and clears the
+ * current device's error word: KDA_OK, KDA_ERR_DEVICE (bad cu_seqlens) or
+ * KDA_ERR_TIMEOUT; KDA_ERR_CUDA if the synchronisation itself failed.  The
+ * message of a non-OK result is available from kda_last_error_message().
+ */
+kda_status kda_get_device_error(void* stream);
+
+/* Static, human-readable name of a status code.  Never NULL. */
+const char* kda_status_string(kda_status status);
+
+/* Message of the last failed call on this host thread ("" if none).  Valid
+ * until the next call into the library from this thread. */
+const char* kda_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

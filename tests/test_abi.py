@@ -1,0 +1,136 @@
+"""The C-ABI library builds, loads and exports every entry point include/kda.h
+declares, and rejects invalid arguments on the host before touching the GPU
+(these calls never reach CUDA, so they run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_delta_rule_gb300 as kda
+from gated_delta_rule_gb300 import KdaTensor
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 1 << 40  # a 16-byte aligned address that is never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kda.build()
+    return kda.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(kda_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"kda_chunk_fwd", "kda_recurrent_step", "kda_get_device_error"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(kda.EXPORTED) >= set(names)
+
+
+def test_status_strings(lib):
+    for code, name in kda.STATUS.items():
+        assert lib.kda_status_string(code).decode() == name
+    assert lib.kda_status_string(99).decode() == "KDA_ERR_UNKNOWN"
+
+
+def T(shape, dtype=1, addr=FAKE, stride=None):
+    d = KdaTensor()
+    d.data = addr
+    d.dtype = dtype
+    d.ndim = len(shape)
+    if stride is None:
+        stride, acc = [], 1
+        for s in reversed(shape):
+            stride.insert(0, acc)
+            acc *= s
+    for i, (s, st) in enumerate(zip(shape, stride)):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+def prefill_args(B=1, Tn=64, H=2, dk=128, dv=128, dt=1):
+    base = FAKE
+    step = 1 << 30
+    return dict(q=T([B, Tn, H, dk], dt, base), k=T([B, Tn, H, dk], dt, base + step),
+                v=T([B, Tn, H, dv], dt, base + 2 * step), g=T([B, Tn, H, dk], 0, base + 3 * step),
+                beta=T([B, Tn, H], 0, base + 4 * step), s0=None, cu=None,
+                out=T([B, Tn, H, dv], dt, base + 5 * step), sT=None)
+
+
+def call_prefill(lib, a, scale=0.1):
+    r = lambda x: None if x is None else ctypes.byref(x)
+    st = lib.kda_chunk_fwd(r(a["q"]), r(a["k"]), r(a["v"]), r(a["g"]), r(a["beta"]), r(a["s0"]),
+                           scale, r(a["cu"]), r(a["out"]), r(a["sT"]), None)
+    return st, lib.kda_last_error_message().decode()
+
+
+@pytest.mark.parametrize("mutate,needle", [
+    (lambda a: a.update(q=None), "q: descriptor is NULL"),
+    (lambda a: a.update(k=T([1, 64, 2, 128], 0, FAKE + (1 << 30))), "k: dtype"),
+    (lambda a: a.update(v=T([1, 64, 2, 96], 1, FAKE + (2 << 30))), "head dims"),
+    (lambda a: a.update(g=T([1, 64, 2, 128], 1, FAKE + (3 << 30))), "g: dtype"),
+    (lambda a: a.update(beta=T([1, 64, 3], 0, FAKE + (4 << 30))), "beta: size"),
+    (lambda a: a.update(out=T([1, 64, 2, 128], 1, FAKE + 8)), "out: data pointer"),
+    (lambda a: a.update(out=T([1, 64, 2, 128], 1, FAKE + 16)), "out overlaps q"),
+    (lambda a: a.update(q=T([1, 64, 2, 128], 1, FAKE, stride=[64 * 256, 256, 129, 1])), "stride of dim 2"),
+    (lambda a: a.update(q=T([1, 64, 2, 128], 1, FAKE, stride=[64 * 256, 256, 128, 2])), "innermost"),
+    (lambda a: a.update(s0=T([1, 2, 128, 64], 0, FAKE + (6 << 30))), "initial_state: size"),
+    (lambda a: a.update(s0=T([1, 2, 128, 128], 0, FAKE + (6 << 30)),
+                        sT=T([1, 2, 128, 128], 0, FAKE + (6 << 30) + 4096)), "partly overlaps"),
+    (lambda a: a.update(prefill_args(B=2), cu=T([3], 2, FAKE + (7 << 30))), "requires B == 1"),
+    (lambda a: a.update(cu=T([3], 0, FAKE + (7 << 30))), "cu_seqlens: dtype"),
+])
+def test_prefill_rejects_invalid_arguments(lib, mutate, needle):
+    a = prefill_args()
+    mutate(a)
+    st, msg = call_prefill(lib, a)
+    assert st in (1, 2), (st, msg)
+    assert needle in msg, msg
+
+
+def test_prefill_rejects_nonfinite_scale(lib):
+    st, msg = call_prefill(lib, prefill_args(), scale=float("inf"))
+    assert st == 1 and "scale" in msg
+
+
+def test_prefill_empty_problem_is_a_no_op(lib):
+    a = prefill_args(B=0)
+    st, msg = call_prefill(lib, a)
+    assert st == 0, msg
+
+
+def test_decode_rejects_invalid_arguments(lib):
+    r = ctypes.byref
+    N, H = 4, 2
+    state = T([N, H, 128, 128], 0, FAKE)
+    q = T([N, H, 128], 1, FAKE + (1 << 30))
+    k = T([N, H, 128], 1, FAKE + (2 << 30))
+    v = T([N, H, 128], 1, FAKE + (3 << 30))
+    g = T([N, H, 128], 0, FAKE + (4 << 30))
+    beta = T([N, H], 0, FAKE + (5 << 30))
+    out = T([N, H, 128], 1, FAKE + 64)  # inside the state
+    st = lib.kda_recurrent_step(r(state), r(q), r(k), r(v), r(g), r(beta), 1.0, r(out), None)
+    assert st == 1 and "out overlaps state" in lib.kda_last_error_message().decode()
+    out = T([N, H, 128], 0, FAKE + (6 << 30))
+    st = lib.kda_recurrent_step(r(state), r(q), r(k), r(v), r(g), r(beta), 1.0, r(out), None)
+    assert st == 1 and "out: dtype" in lib.kda_last_error_message().decode()
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import importlib
+    m = importlib.import_module("gated_delta_rule_gb300")
+    saved = m._lib
+    m._lib = None
+    try:
+        with pytest.raises(ImportError):
+            m.load_library(str(tmp_path / "missing.so"))
+    finally:
+        m._lib = saved
