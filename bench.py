@@ -1,0 +1,445 @@
+"""Benchmark of the KDA core on one GB300 (or N replicas under torchrun).
+
+One step = one ``kda_chunk_fwd`` prefill of the workload B=2, H=16, T=4096,
+d_k=d_v=128 (bf16 q/k/v, fp32 g/beta/states, random initial state): the
+headline prefill tokens/s.  The same JSON line also carries the decode half
+of the metric (256 requests x 96 heads x 128 x 128, fp32 state in place, 64
+consecutive ``kda_recurrent_step`` calls) and the 96-head, 32768-token prefill.
+
+Timing: inputs are resident in HBM; every timed step is bracketed by CUDA
+events on the launching stream, and L2 is flushed (a 256 MiB write, outside
+the events) between prefill steps.  ``e2e`` repeats the prefill through the
+C ABI with the inputs in pinned host memory: host->device copies, the call
+and the device->host copy of out and the final state are inside the timed
+region.  ``--impl reference`` times the CPU oracle instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import kda_inputs as ki  # noqa: E402
+
+METRIC = "KDA prefill tokens/s & % bf16 TC roofline; decode steps/s & % HBM BW (1×GB300)"
+PREFILL_W = 1          # headline prefill workload
+K3_W = 2               # 96-head prefill, reported alongside
+DECODE_W = 3
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (per token-head, d = head dim): see the design doc
+
+def prefill_flops(token_heads, dk, dv, C=64):
+    return token_heads * (6 * dk * dv + 2 * C * (dk + dv))
+
+
+def prefill_bytes(token_heads, dk, dv, n_states_read, n_states_written, in_bytes=2):
+    per = in_bytes * (2 * dk + dv) + 4 * dk + 4 + in_bytes * dv
+    return token_heads * per + 4 * dk * dv * (n_states_read + n_states_written)
+
+
+def decode_bytes(NH, dk, dv, in_bytes=2):
+    return NH * (2 * 4 * dk * dv + in_bytes * (2 * dk + dv) + 4 * dk + 4 + in_bytes * dv)
+
+
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_delta_rule_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("source_sha") != source_sha():
+        return None
+    return d.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+
+def bench_prefill(kda, idx, steps, warmup, flush, stream):
+    w = ki.WORKLOADS[idx]
+    d = ki.workload_inputs(idx)
+    dev = torch.device("cuda")
+    t = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in d.items()}
+    B, T, H, dk = t["q"].shape
+    dv = t["v"].shape[-1]
+    N = B if t["cu_seqlens"] is None else t["cu_seqlens"].shape[0] - 1
+    out = torch.empty(B, T, H, dv, dtype=t["q"].dtype, device=dev)
+    sT = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
+
+    def step():
+        kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"],
+                          t["scale"], cu_seqlens=t["cu_seqlens"], out=out, final_state=sT,
+                          stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+            flush.zero_()
+    stream.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            step()
+            e1.record(stream)
+    stream.synchronize()
+    kda.kda_get_device_error(stream)
+    ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    th = B * T * H if t["cu_seqlens"] is None else T * H
+    n_read = N if t["initial_state"] is not None else 0
+    return dict(ms=ms, token_heads=th, tokens=B * T, dk=dk, dv=dv, H=H,
+                flops=prefill_flops(th, dk, dv),
+                bytes=prefill_bytes(th, dk, dv, n_read * H, N * H), d=d, t=t, out=out, sT=sT,
+                name=w["name"])
+
+
+def bench_prefill_e2e(kda, r, steps, warmup, stream):
+    """Same prefill through the C ABI from pinned host buffers (H2D + call + D2H timed)."""
+    d = r["d"]
+    host = {k: v.pin_memory() for k, v in d.items() if torch.is_tensor(v)}
+    dev = r["t"]
+    out_h = torch.empty(r["out"].shape, dtype=r["out"].dtype).pin_memory()
+    sT_h = torch.empty(r["sT"].shape, dtype=torch.float32).pin_memory()
+    names = [k for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens")
+             if host.get(k) is not None]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    d2h = out_h.numel() * out_h.element_size() + sT_h.numel() * 4
+
+    def step():
+        for k in names:
+            dev[k].copy_(host[k], non_blocking=True)
+        kda.kda_chunk_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
+                          dev.get("initial_state"), dev["scale"], cu_seqlens=dev.get("cu_seqlens"),
+                          out=r["out"], final_state=r["sT"], stream=stream)
+        out_h.copy_(r["out"], non_blocking=True)
+        sT_h.copy_(r["sT"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return dict(ms=ms, h2d=h2d, d2h=d2h)
+
+
+def bench_decode(kda, steps_total, warmup, stream):
+    w = ki.WORKLOADS[DECODE_W]
+    N, H, dk, dv = w["N"], w["H"], w["dk"], w["dv"]
+    seed = ki.SEED_BASE + DECODE_W
+    dev = torch.device("cuda")
+    S = ki.decode_state(N, H, dk, dv, seed=seed).to(dev)
+    n_in = w["steps"]
+    ins = []
+    for s in range(n_in):
+        x = ki.decode_inputs(N, H, dk, dv, "bf16", seed=seed, step=s)
+        ins.append({k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()})
+    out = torch.empty(N, H, dv, dtype=torch.bfloat16, device=dev)
+
+    def step(x):
+        kda.kda_recurrent_step(S, x["q"], x["k"], x["v"], x["g"], x["beta"], scale=x["scale"],
+                               out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(ins[i % n_in])
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps_total):
+            step(ins[i % n_in])
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps_total
+    return dict(ms=ms, NH=N * H, N=N, H=H, dk=dk, dv=dv, bytes=decode_bytes(N * H, dk, dv),
+                name=w["name"], steps=steps_total)
+
+
+def oracle_prefill_rate(idx, max_problems=None):
+    """CPU oracle on (a sample of) the workload: returns (tokens/s, threads, sample text)."""
+    import oracle
+    w = ki.WORKLOADS[idx]
+    heads = None
+    H = w["H"]
+    if max_problems is not None and max_problems < w.get("B", 1) * H:
+        heads = list(range(max(1, max_problems // w.get("B", 1))))
+    d = ki.workload_inputs(idx, heads=heads)
+    Hs = d["q"].shape[2]
+    B0 = d["q"].shape[0]
+    used = min(oracle.threads(), B0 * Hs if d["cu_seqlens"] is None else (d["cu_seqlens"].shape[0] - 1) * Hs)
+    t0 = time.perf_counter()
+    oracle.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], d["scale"],
+                   cu_seqlens=d["cu_seqlens"])
+    dt = time.perf_counter() - t0
+    B, T = d["q"].shape[0], d["q"].shape[1]
+    token_heads = B * T * Hs
+    tokens_per_s = token_heads / dt / H   # whole-token rate: every token has H heads
+    sample = f"{w['name']}: {B}x{T} tokens x {Hs} of {H} heads ({token_heads} token-heads), {dt:.2f} s"
+    return tokens_per_s, used, sample, dt
+
+
+# ---------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    rates, sample, threads = [], "", 1
+    import oracle
+    nprob = max(2, oracle.threads())
+    for _ in range(min(args.warmup, 1)):
+        oracle_prefill_rate(PREFILL_W, max_problems=nprob)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r, threads, sample, _ = oracle_prefill_rate(PREFILL_W, max_problems=nprob)
+        rates.append(r)
+    wall = time.perf_counter() - t0
+    w = ki.WORKLOADS[PREFILL_W]
+    val = statistics.median(rates)
+    tokens = w["B"] * w["T"]
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tokens / val, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w["name"], "B": w["B"], "T": w["T"], "H": w["H"],
+                       "d_k": w["dk"], "d_v": w["dv"], "parallelism": "none (CPU oracle)"},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-k3", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import gated_delta_rule_gb300 as kda
+    kda.build()
+    kda.load_library()
+    pk = peaks()
+    stream = torch.cuda.Stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with ClockSampler(local) as clk:
+        pre = bench_prefill(kda, PREFILL_W, args.steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+
+    ms = statistics.mean(pre["ms"])
+    ms = max_over_ranks(ms, world)
+    tokens_all = pre["tokens"] * world
+    value = tokens_all / (ms * 1e-3)
+    ach_gbs = pre["bytes"] / (ms * 1e-3) / 1e9
+    ach_tf = pre["flops"] / (ms * 1e-3) / 1e12
+    kname = "kda_chunk_prefill"
+    roof = {"bound": "hbm", "achieved": ach_gbs, "peak": pk["hbm"], "unit": "GB/s",
+            "frac": ach_gbs / pk["hbm"], "traffic": committed_traffic(kname),
+            "peak_source": pk["src"], "algorithmic_bytes_per_launch": pre["bytes"]}
+    tc = {"achieved": ach_tf, "peak": pk["bf16"], "unit": "TFLOP/s", "frac": ach_tf / pk["bf16"],
+          "algorithmic_flops_per_launch": pre["flops"]}
+    t_roof = max(pre["flops"] / (pk["bf16"] * 1e12), pre["bytes"] / (pk["hbm"] * 1e9))
+
+    e2e = bench_prefill_e2e(kda, pre, max(3, args.steps // 2), args.warmup, stream)
+    e2e_val = tokens_all / (max_over_ranks(e2e["ms"], world) * 1e-3)
+
+    extra = {}
+    with ClockSampler(local) as clk_dec:
+        dec = bench_decode(kda, 64, args.warmup, stream)
+    dms = max_over_ranks(dec["ms"], world)
+    d_gbs = dec["bytes"] / (dms * 1e-3) / 1e9
+    extra["decode"] = {
+        "workload": dec["name"], "ms_per_step": dms, "steps_timed": dec["steps"],
+        "steps_per_s": world * 1e3 / dms, "tokens_per_s": world * dec["N"] * 1e3 / dms,
+        "roofline": {"bound": "hbm", "achieved": d_gbs, "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": d_gbs / pk["hbm"], "traffic": committed_traffic("kda_decode"),
+                     "algorithmic_bytes_per_launch": dec["bytes"]},
+        "clocks": clk_dec.summary(), "gpu_launches": dec["steps"]}
+    del dec
+    if not args.no_k3:
+        k3 = bench_prefill(kda, K3_W, max(3, args.steps // 4), 3, flush, stream)
+        kms = max_over_ranks(statistics.mean(k3["ms"]), world)
+        extra["prefill_96heads"] = {
+            "workload": k3["name"], "ms_per_step": kms,
+            "tokens_per_s": world * k3["tokens"] / (kms * 1e-3),
+            "hbm_frac": k3["bytes"] / (kms * 1e-3) / 1e9 / pk["hbm"],
+            "tc_frac": k3["flops"] / (kms * 1e-3) / 1e12 / pk["bf16"],
+            "t_roof_over_t": max(k3["flops"] / (pk["bf16"] * 1e12),
+                                 k3["bytes"] / (pk["hbm"] * 1e9)) / (kms * 1e-3)}
+        del k3
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": pre["name"], "B": 2, "T": 4096, "H": pre["H"], "d_k": pre["dk"],
+                       "d_v": pre["dv"], "chunk": 64, "parallelism": f"replicas x{world}",
+                       "l2": "flushed (256 MiB write) between timed steps, outside the events"},
+            "roofline": roof, "tc_roofline": tc, "t_roof_over_t": t_roof / (ms * 1e-3),
+            "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": e2e["h2d"],
+                    "d2h_bytes_per_step": e2e["d2h"]},
+            "gpu_launches": args.steps, "clocks": clk.summary(), "wall_s_timed_region": wall}
+    line.update(extra)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r, threads, sample, _ = oracle_prefill_rate(PREFILL_W)
+        line["cpu_baseline"] = {"value": r, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
