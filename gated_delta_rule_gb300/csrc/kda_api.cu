@@ -10,7 +10,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/kda.h"
+#include "kda.h"
 #include "kda_internal.h"
 
 namespace {
