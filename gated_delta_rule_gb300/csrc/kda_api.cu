@@ -179,6 +179,8 @@ kda::Act act(const kda_tensor* t) {
   return a;
 }
 
+cudaMemPool_t g_pool[kMaxDevices];
+
 kda_status cuda_fail(cudaError_t e, const char* what) {
   return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
@@ -284,15 +286,57 @@ kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
     e = kda::launch_check_seqlens(a.cu_seqlens, a.N, a.T, a.err, st);
     if (e != cudaSuccess) return cuda_fail(e, "cu_seqlens check launch");
   }
-  if (path == PrefillPath::kChunked && a.bf16)
-    e = kda::launch_chunk_prefill_tc(a, st);
-  else
+  if (path == PrefillPath::kChunked && a.bf16) {
+    const size_t ws_bytes = kda::chunk_prefill_workspace_bytes(a);
+    void* ws = nullptr;
+    if (ws_bytes) {
+      e = kda::scratch_alloc(&ws, ws_bytes, st);
+      if (e != cudaSuccess) return cuda_fail(e, "chunk-record workspace allocation");
+    }
+    e = kda::launch_chunk_prefill_tc(a, ws, st);
+    const cudaError_t ef = ws ? kda::scratch_free(ws, st) : cudaSuccess;
+    if (e == cudaSuccess) e = ef;
+  } else {
     e = kda::launch_recurrent_prefill(a, st);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return KDA_OK;
 }
 
 }  // namespace
+
+namespace kda {
+
+// Per-device pool that keeps freed blocks for reuse (release threshold: never),
+// so repeated calls do not go back to the driver for their chunk records.
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    if (!g_pool[dev]) {
+      cudaMemPoolProps props;
+      memset(&props, 0, sizeof(props));
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      cudaMemPool_t pool;
+      e = cudaMemPoolCreate(&pool, &props);
+      if (e != cudaSuccess) return e;
+      uint64_t keep = ~0ull;
+      e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+      if (e != cudaSuccess) return e;
+      g_pool[dev] = pool;
+    }
+  }
+  return cudaMallocFromPoolAsync(p, bytes, g_pool[dev], s);
+}
+
+cudaError_t scratch_free(void* p, cudaStream_t s) { return cudaFreeAsync(p, s); }
+
+}  // namespace kda
 
 extern "C" {
 

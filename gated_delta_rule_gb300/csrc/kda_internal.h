@@ -55,7 +55,14 @@ cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s);
 // cu_seqlens validation: sets kErrBadSeqlens in *err when the offsets are invalid.
 cudaError_t launch_check_seqlens(const int32_t* cu, int N, int T, int* err, cudaStream_t s);
 
-// Tensor-core chunked prefill (kda_prefill_tc.cu); bf16 inputs only.
-cudaError_t launch_chunk_prefill_tc(const PrefillArgs& a, cudaStream_t s);
+// Tensor-core chunked prefill (kda_prefill_tc.cu); bf16 inputs only.  The
+// workspace (device memory, chunk_prefill_workspace_bytes(a) bytes, 1024-byte
+// aligned) holds the per-chunk records; it is only used by work enqueued on `s`.
+size_t chunk_prefill_workspace_bytes(const PrefillArgs& a);
+cudaError_t launch_chunk_prefill_tc(const PrefillArgs& a, void* workspace, cudaStream_t s);
+
+// Stream-ordered scratch memory from a per-device pool (kda_api.cu).
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s);
+cudaError_t scratch_free(void* p, cudaStream_t s);
 
 }  // namespace kda
