@@ -14,14 +14,14 @@ import torch
 
 from ._build import LIB, build, up_to_date  # noqa: F401
 
-__all__ = ["kda_chunk_fwd", "kda_fused_recurrent_fwd", "kda_recurrent_step",
+__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
            "kda_get_device_error", "KdaError", "load_library", "build", "STATUS"]
 
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
           4: "KDA_ERR_DEVICE", 5: "KDA_ERR_TIMEOUT"}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
 
-EXPORTED = ["kda_chunk_fwd", "kda_fused_recurrent_fwd", "kda_recurrent_step",
+EXPORTED = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
             "kda_get_device_error", "kda_status_string", "kda_last_error_message"]
 
 
@@ -51,7 +51,7 @@ def load_library(path: str | None = None):
         raise ImportError(f"libkda.so not built ({path}); run gated_delta_rule_gb300.build()")
     lib = ctypes.CDLL(path)
     fwd = [_P] * 6 + [ctypes.c_float, _P, _P, _P, ctypes.c_void_p]
-    for name in ("kda_chunk_fwd", "kda_fused_recurrent_fwd"):
+    for name in ("kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd"):
         f = getattr(lib, name)
         f.restype, f.argtypes = ctypes.c_int, fwd
     lib.kda_recurrent_step.restype = ctypes.c_int
@@ -123,6 +123,15 @@ def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, scale=None, cu_seqlens=N
 def kda_fused_recurrent_fwd(*args, **kw):
     """Token-by-token KDA prefill with on-chip fp32 state; same contract as kda_chunk_fwd."""
     kw["_entry"] = "kda_fused_recurrent_fwd"
+    return kda_chunk_fwd(*args, **kw)
+
+
+def kda_chunk_fwd_noalloc(*args, **kw):
+    """kda_chunk_fwd without any device allocation inside the library call: the
+    chunk records live in the library's fixed 64 MiB device workspace (see
+    include/kda.h).  Outputs not passed in are still allocated here, by torch,
+    before the call; pass ``out`` and ``final_state`` to avoid that too."""
+    kw["_entry"] = "kda_chunk_fwd_noalloc"
     return kda_chunk_fwd(*args, **kw)
 
 

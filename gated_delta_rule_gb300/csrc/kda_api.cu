@@ -185,7 +185,7 @@ kda_status cuda_fail(cudaError_t e, const char* what) {
   return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-enum class PrefillPath { kChunked, kRecurrent };
+enum class PrefillPath { kChunked, kRecurrent, kChunkedNoAlloc };
 
 kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
                    const kda_tensor* g, const kda_tensor* beta, const kda_tensor* s0,
@@ -279,9 +279,22 @@ kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
   a.scale = scale;
   if (N * H == 0) return KDA_OK;
   if (!a.sT && T == 0) return KDA_OK;
+  if (path == PrefillPath::kChunkedNoAlloc && a.bf16) {
+    const size_t need = kda::chunk_prefill_workspace_bytes(a);
+    if (need > kda::kNoallocWorkspaceBytes)
+      return fail(KDA_ERR_UNSUPPORTED,
+                  "this call needs %zu bytes of chunk-record scratch but the fixed workspace of "
+                  "kda_chunk_fwd_noalloc holds %zu; split the batch or use kda_chunk_fwd",
+                  need, (size_t)kda::kNoallocWorkspaceBytes);
+  }
   KDA_TRY(device_error_ptr(&a.err));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  void* fixed_ws = nullptr;
+  if (path == PrefillPath::kChunkedNoAlloc && a.bf16) {
+    e = kda::noalloc_workspace(&fixed_ws);
+    if (e != cudaSuccess) return cuda_fail(e, "fixed workspace address lookup");
+  }
   if (cu) {
     e = kda::launch_check_seqlens(a.cu_seqlens, a.N, a.T, a.err, st);
     if (e != cudaSuccess) return cuda_fail(e, "cu_seqlens check launch");
@@ -296,6 +309,8 @@ kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
     e = kda::launch_chunk_prefill_tc(a, ws, st);
     const cudaError_t ef = ws ? kda::scratch_free(ws, st) : cudaSuccess;
     if (e == cudaSuccess) e = ef;
+  } else if (path == PrefillPath::kChunkedNoAlloc && a.bf16) {
+    e = kda::launch_chunk_prefill_tc(a, fixed_ws, st);
   } else {
     e = kda::launch_recurrent_prefill(a, st);
   }
@@ -347,6 +362,15 @@ kda_status kda_chunk_fwd(const kda_tensor* q, const kda_tensor* k, const kda_ten
                          kda_tensor* final_state, void* stream) {
   return prefill(q, k, v, g, beta, initial_state, scale, cu_seqlens, out, final_state, stream,
                  PrefillPath::kChunked);
+}
+
+kda_status kda_chunk_fwd_noalloc(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                                 const kda_tensor* g, const kda_tensor* beta,
+                                 const kda_tensor* initial_state, float scale,
+                                 const kda_tensor* cu_seqlens, kda_tensor* out,
+                                 kda_tensor* final_state, void* stream) {
+  return prefill(q, k, v, g, beta, initial_state, scale, cu_seqlens, out, final_state, stream,
+                 PrefillPath::kChunkedNoAlloc);
 }
 
 kda_status kda_fused_recurrent_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,

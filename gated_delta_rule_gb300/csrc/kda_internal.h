@@ -61,6 +61,11 @@ cudaError_t launch_check_seqlens(const int32_t* cu, int N, int T, int* err, cuda
 size_t chunk_prefill_workspace_bytes(const PrefillArgs& a);
 cudaError_t launch_chunk_prefill_tc(const PrefillArgs& a, void* workspace, cudaStream_t s);
 
+// Size of the fixed device workspace behind kda_chunk_fwd_noalloc, and its
+// device address on the current device (kda_noalloc.cu; looked up once per device).
+constexpr size_t kNoallocWorkspaceBytes = size_t(64) << 20;
+cudaError_t noalloc_workspace(void** ptr);
+
 // Stream-ordered scratch memory from a per-device pool (kda_api.cu).
 cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s);
 cudaError_t scratch_free(void* p, cudaStream_t s);

@@ -121,6 +121,38 @@ kda_status kda_fused_recurrent_fwd(const kda_tensor* q, const kda_tensor* k,
                                    kda_tensor* final_state, void* stream);
 
 /*
+ * kda_chunk_fwd_noalloc - kda_chunk_fwd for callers that must not allocate.
+ *
+ * The pages have no counterpart for this entry point; it exists for callers
+ * that cannot call cudaMalloc or any allocating routine during a call: hosts
+ * whose device memory is fully pre-sized and owned by their own allocator, and
+ * code paths where allocation is not permitted.  It computes exactly what
+ * kda_chunk_fwd computes, with the same arguments, layouts and errors, but
+ * keeps the bf16 path's per-chunk records in a fixed 64 MiB device array
+ * built into the library instead of pool memory (fp32 inputs need no scratch).
+ *
+ *  - The array is allocated on every device that loads the library and stays
+ *    there until the process exits.
+ *  - Requests whose records would not fit return KDA_ERR_UNSUPPORTED before
+ *    anything is launched.  The records take 66560 bytes per (chunk, head)
+ *    at d_k = 128 and 41984 at d_k = 64, over B * ceil(T / 64) chunks (with
+ *    cu_seqlens: ceil(T / 64) + N, plus a small offset table), so at most
+ *    1008 (chunk, head) pairs at d_k = 128, e.g. B=1, H=15, T=4096.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - All calls share the one array.  Nothing in it has to start zeroed (every
+ *    byte a call reads is written earlier in the same call), but two calls
+ *    that run at the same time on the GPU, on any streams, overwrite each
+ *    other's records: order them, e.g. on one stream.
+ */
+kda_status kda_chunk_fwd_noalloc(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                                 const kda_tensor* g, const kda_tensor* beta,
+                                 const kda_tensor* initial_state, float scale,
+                                 const kda_tensor* cu_seqlens, kda_tensor* out,
+                                 kda_tensor* final_state, void* stream);
+
+/*
  * kda_recurrent_step - one decode token per request, state updated in place.
  *
  * The single-step recurrence in the three steps of "Kimi K3 核心算子拆解"

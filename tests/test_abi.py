@@ -134,3 +134,14 @@ def test_binding_fails_loudly_without_library(tmp_path):
             m.load_library(str(tmp_path / "missing.so"))
     finally:
         m._lib = saved
+
+
+def test_noalloc_rejects_requests_beyond_its_workspace(lib):
+    """kda_chunk_fwd_noalloc refuses, before touching the GPU, a call whose chunk
+    records would not fit its fixed workspace (1024 (chunk, head) pairs here)."""
+    r = lambda x: None if x is None else ctypes.byref(x)
+    a = prefill_args(B=1, Tn=4096, H=16)
+    st = lib.kda_chunk_fwd_noalloc(r(a["q"]), r(a["k"]), r(a["v"]), r(a["g"]), r(a["beta"]), None,
+                                   0.1, None, r(a["out"]), None, None)
+    msg = lib.kda_last_error_message().decode()
+    assert st == 2 and "fixed workspace" in msg, msg
