@@ -344,6 +344,31 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def ncu_case(which):
+    """Two untimed launches of one workload, for profiler captures."""
+    import gated_delta_rule_gb300 as kda
+    kda.build()
+    kda.load_library()
+    dev = torch.device("cuda")
+    if which.startswith("prefill"):
+        d = ki.workload_inputs(PREFILL_W if which == "prefill" else K3_W)
+        t = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in d.items()}
+        for _ in range(2):
+            kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"],
+                              t["scale"], cu_seqlens=t["cu_seqlens"])
+    else:
+        w = ki.WORKLOADS[DECODE_W]
+        N = 32 if which == "decode32" else w["N"]
+        S = ki.decode_state(N, w["H"], w["dk"], w["dv"], seed=1).to(dev)
+        x = ki.decode_inputs(N, w["H"], w["dk"], w["dv"], "bf16", seed=1, step=0)
+        x = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+        for _ in range(2):
+            kda.kda_recurrent_step(S, x["q"], x["k"], x["v"], x["g"], x["beta"], scale=x["scale"])
+    torch.cuda.synchronize()
+    kda.kda_get_device_error()
+    print(json.dumps({"ncu_case": which, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -352,7 +377,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-k3", action="store_true")
+    ap.add_argument("--ncu-case", choices=["prefill", "prefill96", "decode32", "decode"],
+                    help="run two untimed launches of one workload (for ncu captures) and exit")
     args = ap.parse_args()
+    if args.ncu_case:
+        ncu_case(args.ncu_case)
+        return
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -18,13 +18,15 @@
 //     two per SM.  It forms the in-chunk cumulative log-decay, the operand
 //     tiles, the Gram products (tcgen05), the triangular inverse (CUDA cores +
 //     warp-level tf32 MMA) and W (tcgen05), and writes one "chunk record" of
-//     ready-to-use swizzled bf16 tiles -- T B_beta, -W, [Q+ | A_Q],
-//     K e^{G_C - G} -- plus e^{G_C} to a workspace.
+//     ready-to-use swizzled bf16 tiles -- T B_beta, [-W ; Q+], A_Q,
+//     (K e^{G_C - G})^T -- plus e^{G_C} to a workspace.
 //   * kda_chunk_serial_kernel: one CTA per (sequence, head) keeps the fp32 state
-//     in TMEM and walks the chunks in order.  Each chunk's record arrives by one
-//     bulk copy (TMA engine) two chunks ahead, V by cp.async; the chunk then
-//     costs three tcgen05 products: [T_beta | -W] [V ; S], K_end^T U and
-//     [Q+ | A_Q] [S ; U].
+//     in TMEM and walks the chunks in order, with warp roles: a producer warp
+//     (record by bulk copy, V by cp.async, one chunk ahead), an MMA warp and
+//     four TMEM <-> memory warps.  Each chunk costs three tcgen05 products:
+//     [U ; Q+ S] = [T_beta | -W ; 0 | Q+] [V ; S], then S += K_end^T U on the
+//     state chain and O += A_Q U off it; the U/O accumulator is double-buffered
+//     in TMEM so the output epilogue overlaps the next chunk.
 //
 // Exponents are only ever formed as differences that stay inside a 16-token
 // sub-block or decay toward the later token, so nothing overflows for
@@ -60,11 +62,11 @@ __host__ __device__ constexpr int align1k(int x) { return (x + 1023) & ~1023; }
 // as they sit in shared memory, so one bulk copy moves the whole record.
 template <int DK>
 struct Rec {
-  static constexpr int T2 = 0;                        // T Diag(beta): 64 x 64, K-major
-  static constexpr int AW = T2 + 64 * 64 * 2;         // -W: 64 x DK, K-major
-  static constexpr int OQ = AW + 64 * DK * 2;         // [Q+ | A_Q]: 64 x (DK + 64), K-major
-  static constexpr int KE = OQ + 64 * (DK + 64) * 2;  // K e^{G_C - G}: [64 tokens][DK], MN-major
-  static constexpr int P = KE + 64 * DK * 2;          // e^{G_C}: DK fp32
+  static constexpr int T2 = 0;                      // T Diag(beta): 64 x 64, K-major
+  static constexpr int WQ = T2 + 64 * 64 * 2;       // [-W ; Q+]: 128 x DK, K-major
+  static constexpr int AQ = WQ + 128 * DK * 2;      // A_Q: 64 x 64, K-major
+  static constexpr int KE = AQ + 64 * 64 * 2;       // (K e^{G_C - G})^T: DK x 64, K-major
+  static constexpr int P = KE + 64 * DK * 2;        // e^{G_C}: DK fp32
   static constexpr int kBytes = align1k(P + DK * 4);
 };
 
@@ -101,16 +103,19 @@ struct PrepSmem {
 
 template <int DK, int DV>
 struct SerialSmem {
-  static constexpr int REC = 0;  // two record buffers
-  static constexpr int VT = REC + 2 * Rec<DK>::kBytes;  // two V chunks, [64][DV] MN-major
-  static constexpr int SB = VT + 2 * 64 * DV * 2;       // bf16 S, [DK][DV] MN-major
-  static constexpr int UB = SB + DK * DV * 2;           // bf16 U, [64][DV] MN-major
-  static constexpr int MBAR = UB + 64 * DV * 2;         // mma, rec0, rec1
-  static constexpr int TSLOT = MBAR + 24;
+  // a record buffer holds [T2 | zero tile | rest of the record]: the zero tile is
+  // the lower half of T2's M = 128 window
+  static constexpr int kRecBuf = align1k(Rec<DK>::kBytes + 64 * 64 * 2);
+  static constexpr int REC = 0;                          // two record buffers
+  static constexpr int VT = REC + 2 * kRecBuf;           // two V chunks [64][DV] MN-major (U reuses)
+  static constexpr int SB = VT + 2 * 64 * DV * 2;        // bf16 S, [DK][DV] MN-major
+  static constexpr int OSTG = SB + DK * DV * 2;          // output staging: 2 warps x 32 rows x 144 B
+  static constexpr int MBAR = OSTG + 2 * 32 * 144;       // mma_a, mma_s, rec0/1, free0/1, orel0/1
+  static constexpr int TSLOT = MBAR + 64;
   static constexpr int FLAG = TSLOT + 4;
   static constexpr int kAlloc = FLAG + 4 + 1024;
   static_assert(kAlloc <= 232448, "shared memory budget");
-  static constexpr uint32_t kTmemCols = 2 * DV <= 128 ? 128 : 256;  // U/O and S
+  static constexpr uint32_t kTmemCols = 3 * DV <= 256 ? 256 : 512;  // U/O x2 and S
 };
 
 struct Split {
@@ -391,6 +396,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
           const uint4 u = pack8(x);
           st_shared_v4(addr, u.x, u.y, u.z, u.w);
         };
+        // K_end^T is stored K-major ([channel][token]): this thread's 8 x TPP block,
+        // packed in token pairs, is written once after the token loop
+        uint32_t ket[8][TPP / 2];
+        float ke_even[8];
 #pragma unroll
         for (int i = 0; i < TPP; ++i) {
           const int t = part * TPP + i;
@@ -415,14 +424,19 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
           st8(sbase + L::X + sw128(64 + t, col, 128), x);
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] *= fbl[e];
-          *reinterpret_cast<uint4*>(rec + R::OQ + sw128(t, col, 64)) = pack8(x);
+          *reinterpret_cast<uint4*>(rec + R::WQ + sw128(64 + t, col, 128)) = pack8(x);
           // column versions: own block k e^{-G}; later blocks k e^{en - G} (x f2, f3); and K_end
           float y[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) y[e] = ((e & 1) ? bf_hi(kw[e >> 1]) : bf_lo(kw[e >> 1])) * ia[e];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = y[e] * hk[e];
-          *reinterpret_cast<uint4*>(rec + R::KE + sw128(t, col, 64)) = pack8(x);
+          for (int e = 0; e < 8; ++e) {
+            const float ke = y[e] * hk[e];
+            if (i & 1)
+              ket[e][i >> 1] = pack_bf16(ke_even[e], ke);
+            else
+              ke_even[e] = ke;
+          }
 #pragma unroll
           for (int J = 0; J < 4; ++J) {
             if (J < blk) continue;
@@ -436,6 +450,14 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
               st8(addr, x);
             }
           }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          unsigned char* dst = rec + R::KE + sw128(col + e, part * TPP, DK);
+          if constexpr (TPP == 8)
+            *reinterpret_cast<uint4*>(dst) = make_uint4(ket[e][0], ket[e][1], ket[e][2], ket[e][3]);
+          else
+            *reinterpret_cast<uint2*>(dst) = make_uint2(ket[e][0], ket[e][1]);
         }
       }
       fence_async_smem();
@@ -488,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
                   float x[8];
 #pragma unroll
                   for (int e = 0; e < 8; ++e) x[e] = (j0 + 8 * u + e <= i) ? v[8 * u + e] : 0.f;
-                  *reinterpret_cast<uint4*>(rec + R::OQ + sw128(i, DK + j0 + 8 * u, 64)) =
+                  *reinterpret_cast<uint4*>(rec + R::AQ + sw128(i, j0 + 8 * u, 64)) =
                       make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
                                  pack_bf16(x[6], x[7]));
                 }
@@ -498,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
         }
         if (tid >= 64) {  // A_Q columns past this row's sub-block are zero
           for (int j0 = 16 * (myblk + 1); j0 < 64; j0 += 8)
-            *reinterpret_cast<uint4*>(rec + R::OQ + sw128(i, DK + j0, 64)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(rec + R::AQ + sw128(i, j0, 64)) = make_uint4(0, 0, 0, 0);
         }
       }
       __syncthreads();
@@ -605,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
           tmem_ld32(tmem + lane_base + c0, v);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint4*>(rec + R::AW + sw128(tid, c0 + 8 * u, 64)) =
+            *reinterpret_cast<uint4*>(rec + R::WQ + sw128(tid, c0 + 8 * u, 128)) =
                 make_uint4(pack_bf16(-v[8 * u], -v[8 * u + 1]), pack_bf16(-v[8 * u + 2], -v[8 * u + 3]),
                            pack_bf16(-v[8 * u + 4], -v[8 * u + 5]), pack_bf16(-v[8 * u + 6], -v[8 * u + 7]));
         }
@@ -625,9 +647,25 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
 }
 
 // ---------------------------------------------------------------------------
-// serial: one (sequence, head) per CTA, fp32 state in TMEM
+// serial: one (sequence, head) per CTA, fp32 state in TMEM.
+// Warps 0-3 move data between TMEM and shared / global memory, warp 4 issues the
+// tensor-core products, warp 5 loads chunk records (bulk copy) and V (cp.async);
+// both kinds of copy complete on the record buffer's mbarrier.  Hand-offs:
+//   bar 1 (160): bf16 copy of the state entering the chunk is in shared memory
+//   bar 2 (160): the TMEM state is decayed and U is in shared memory
+//   mbarriers  : MMA completion (a: U / Q+S, s: state), records (plus V)
+//                landed, a buffer's chunk finished (output ready, buffers
+//                free), and orel[b]: warps 2-3 have read the output of buffer
+//                b's chunk out of TMEM (64 arrivals), so the chunk two later may
+//                write it.  (Per buffer, and an mbarrier rather than a named
+//                barrier: warps 2-3 may arrive for the next chunk before the MMA
+//                warp has waited for this one.)  Every mbarrier here is waited
+//                on by a role that the barrier's next phase depends on, so no
+//                waiter can fall two phases behind.
+constexpr int kSerialThreads = 192;
+
 template <int DK, int DV>
-__global__ void __launch_bounds__(kThreads, 1) kda_chunk_serial_kernel(PrefillArgs a, Split sp) {
+__global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(PrefillArgs a, Split sp) {
   using L = SerialSmem<DK, DV>;
   using R = Rec<DK>;
   extern __shared__ unsigned char smem_raw[];
@@ -635,11 +673,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_serial_kernel(PrefillAr
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   volatile int* sFlag = reinterpret_cast<volatile int*>(smem + L::FLAG);
-  const uint32_t mbar_rec0 = sbase + L::MBAR + 8;
+  const uint32_t mbar_a = sbase + L::MBAR, mbar_s = mbar_a + 8;
+  const uint32_t mbar_rec0 = mbar_a + 16;   // record (+ V) of buffer b landed
+  const uint32_t mbar_free0 = mbar_a + 32;  // buffer b's chunk has finished its last product
+  const uint32_t mbar_orel0 = mbar_a + 48;  // buffer b's output has been read out of TMEM
+  constexpr int kT2 = 64 * 64 * 2;  // T2 tile bytes; the rest of a record lands after the zero tile
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  const int lane = tid & 31;
+  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
   const int n = blockIdx.x / a.H;
   const int h = blockIdx.x - n * a.H;
   const Range rg = seq_range(a, n);
@@ -650,22 +693,38 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_serial_kernel(PrefillAr
   __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + rg.brow * a.out_sb + rg.tok0 * a.out_st + h * a.out_sh;
 
   if (tid == 0) {
-    mbar_init(sbase + L::MBAR, 1);
-    mbar_init(mbar_rec0, 1);
-    mbar_init(mbar_rec0 + 8, 1);
+    mbar_init(mbar_a, 1);
+    mbar_init(mbar_s, 1);
+    mbar_init(mbar_rec0, 33);  // producer lane 0's expect_tx arrival + 32 cp.async arrivals
+    mbar_init(mbar_rec0 + 8, 33);
+    mbar_init(mbar_free0, 1);
+    mbar_init(mbar_free0 + 8, 1);
+    mbar_init(mbar_orel0, 64);  // every thread of warps 2-3
+    mbar_init(mbar_orel0 + 8, 64);
     fence_mbar_init();
     *sFlag = 0;
+  }
+  for (int i = tid; i < 2 * kT2 / 16; i += kSerialThreads) {  // zero tiles below each T2 buffer
+    const int b = i / (kT2 / 16), o = i % (kT2 / 16);
+    st_shared_v4(sbase + L::REC + b * L::kRecBuf + kT2 + 16 * o, 0u, 0u, 0u, 0u);
   }
   if (warp == 0) tmem_alloc(sbase + L::TSLOT, L::kTmemCols);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::TSLOT);
-  const uint32_t tX = tmem;       // U / O (DV cols)
-  const uint32_t tS = tmem + DV;  // fp32 state (DV cols)
-  Ctx ctx{sbase + L::MBAR, 0u, sFlag, a.err};
+  const uint32_t tS = tmem + 2 * DV;  // fp32 state (DV cols); U/O buffers at 0 and DV
+  auto tX = [&](int b) { return tmem + (uint32_t)(b * DV); };
+  // bounded wait; after any timeout every later wait returns at once so all roles finish
+  auto wait = [&](uint32_t mbar, uint32_t parity) {
+    if (!*sFlag && !mbar_wait(mbar, parity)) {
+      atomicOr(a.err, kErrTimeout);
+      *sFlag = 1;
+    }
+    fence_after_sync();
+  };
 
-  if (tid < DK) {  // lane c holds state row c
+  if (tid < DK) {  // lane c holds state row c: TMEM <- S0, shared <- bf16(S0)
     const float* s0 = a.s0 ? a.s0 + n * a.s0_sn + h * a.s0_sh + (int64_t)tid * DV : nullptr;
 #pragma unroll
     for (int c0 = 0; c0 < DV; c0 += 32) {
@@ -686,160 +745,203 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_serial_kernel(PrefillAr
                      pack_bf16(v[8 * u + 6], v[8 * u + 7]));
     }
   }
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
 
-  // record by one bulk copy, V chunk by cp.async (zero rows past the sequence end)
-  auto issue = [&](int ci) {
-    const int b = ci & 1;
-    if (tid == 0) {
-      mbar_arrive_expect_tx(mbar_rec0 + 8 * b, R::kBytes);
-      bulk_g2s(sbase + L::REC + b * R::kBytes, sp.rec + (rec0 + (int64_t)ci * a.H) * R::kBytes, R::kBytes,
-               mbar_rec0 + 8 * b);
-    }
-    const int lc = min(kC, rg.len - ci * kC);
-    constexpr int kVec = DV / 8;
-#pragma unroll
-    for (int it = 0; it < (64 * kVec) / kThreads; ++it) {
-      const int idx = it * kThreads + tid;
-      const int t = idx / kVec, cv = idx % kVec;
-      const bool ok = t < lc;
-      const __nv_bfloat16* src = ok ? vg + ((int64_t)ci * kC + t) * a.v.st + 8 * cv : vg;
-      cp_async16(sbase + L::VT + b * 64 * DV * 2 + sw128(t, 8 * cv, 64), src, ok ? 16u : 0u);
-    }
-    cp_async_commit();
-  };
-  if (nch > 0) issue(0);
-  if (nch > 1) issue(1);
-
-  for (int ci = 0; ci < nch; ++ci) {
-    const int b = ci & 1;
-    const int lc = min(kC, rg.len - ci * kC);
-    const uint32_t rec = sbase + L::REC + b * R::kBytes;
-    const uint32_t vt = sbase + L::VT + b * 64 * DV * 2;
-    if (!mbar_wait(mbar_rec0 + 8 * b, (ci >> 1) & 1)) {
-      atomicOr(a.err, kErrTimeout);
-      *sFlag = 1;
-    }
-    if (ci + 1 < nch) cp_async_wait_1(); else cp_async_wait_all();
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    if (*sFlag) break;
-
-    // ---- U = T_beta V - W S (accumulated in TMEM) ----
-    if (tid == 0) {
-      fence_after_sync();
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tX, desc_kmajor(rec + R::T2, 64, ks), desc_mnmajor(vt, 64, ks),
-                 idesc_bf16(128, DV, false, true), ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < DK / 16; ++ks)
-        mma_bf16(tX, desc_kmajor(rec + R::AW, 64, ks), desc_mnmajor(sbase + L::SB, DK, ks),
-                 idesc_bf16(128, DV, false, true), 1u);
-      mma_commit(ctx.mbar);
-    }
-    // meanwhile: S <- Diag(e^{G_C}) S in TMEM (rows are key channels)
-    if (tid < DK) {
-      const float pc = reinterpret_cast<const float*>(smem + L::REC + b * R::kBytes + R::P)[tid];
-#pragma unroll
-      for (int c0 = 0; c0 < DV; c0 += 32) {
-        float v[32];
-        tmem_ld32(tS + lane_base + c0, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= pc;
-        tmem_st32(tS + lane_base + c0, v);
+  if (warp == 5) {
+    // ======================= producer warp =======================
+    for (int ci = 0; ci < nch; ++ci) {
+      const int b = ci & 1;
+      if (ci >= 2) wait(mbar_free0 + 8 * b, (uint32_t)(((ci - 2) >> 1) & 1));  // chunk ci - 2 is done
+      const uint32_t dst = sbase + L::REC + b * L::kRecBuf;
+      const uint32_t mb = mbar_rec0 + 8 * b;
+      if (lane == 0) {
+        const unsigned char* src = sp.rec + (rec0 + (int64_t)ci * a.H) * R::kBytes;
+        mbar_arrive_expect_tx(mb, R::kBytes);
+        bulk_g2s(dst, src, kT2, mb);
+        bulk_g2s(dst + 2 * kT2, src + kT2, R::kBytes - kT2, mb);
       }
-    }
-    wait_mma(ctx);
-
-    // ---- U -> bf16 (MN-major [j][n]) ----
-    if (tid < 64) {
-#pragma unroll
-      for (int c0 = 0; c0 < DV; c0 += 32) {
-        float v[32];
-        tmem_ld32(tX + lane_base + c0, v);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          st_shared_v4(sbase + L::UB + sw128(tid, c0 + 8 * u, 64), pack_bf16(v[8 * u], v[8 * u + 1]),
-                       pack_bf16(v[8 * u + 2], v[8 * u + 3]), pack_bf16(v[8 * u + 4], v[8 * u + 5]),
-                       pack_bf16(v[8 * u + 6], v[8 * u + 7]));
+      const int lc = min(kC, rg.len - ci * kC);
+      constexpr int kVec = DV / 8;
+#pragma unroll 4
+      for (int idx = lane; idx < 64 * kVec; idx += 32) {
+        const int t = idx / kVec, cv = idx % kVec;
+        const bool ok = t < lc;
+        const __nv_bfloat16* src = ok ? vg + ((int64_t)ci * kC + t) * a.v.st + 8 * cv : vg;
+        cp_async16(sbase + L::VT + b * 64 * DV * 2 + sw128(t, 8 * cv, 64), src, ok ? 16u : 0u);
       }
+      cp_async_mbar_arrive(mb);
     }
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-
-    // ---- S += K_end^T U ;  O = [Q+ | A_Q] [S ; U] ----
-    if (tid == 0) {
-      fence_after_sync();
+    cp_async_wait_all();
+  } else if (warp == 4) {
+    // ======================= MMA warp =======================
+    for (int ci = 0; ci < nch; ++ci) {
+      const int b = ci & 1;
+      const uint32_t rec = sbase + L::REC + b * L::kRecBuf;  // T2 at +0, zero tile, then the rest
+      const uint32_t rWQ = rec + 2 * kT2 + (R::WQ - kT2);
+      const uint32_t rAQ = rec + 2 * kT2 + (R::AQ - kT2);
+      const uint32_t rKE = rec + 2 * kT2 + (R::KE - kT2);
+      const uint32_t vt = sbase + L::VT + b * 64 * DV * 2;
+      wait(mbar_rec0 + 8 * b, (ci >> 1) & 1);
+      bar_sync(1, 160);
+      // U/O buffer b was last used by chunk ci - 2: its output must have been read out
+      if (ci >= 2) wait(mbar_orel0 + 8 * b, (uint32_t)(((ci - 2) >> 1) & 1));
+      // [U ; Q+ S] = [T_beta | -W ; 0 | Q+] [V ; S]
+      if (lane == 0) {
+        fence_after_sync();
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tS, desc_mnmajor(rec + R::KE, 64, ks), desc_mnmajor(sbase + L::UB, 64, ks),
-                 idesc_bf16(128, DV, true, true), 1u);
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tX(b), desc_kmajor(rec, 64, ks), desc_mnmajor(vt, 64, ks),
+                   idesc_bf16(128, DV, false, true), ks > 0);
 #pragma unroll
-      for (int ks = 0; ks < DK / 16 + 4; ++ks) {
-        const int pnl = ks >> 2;
-        const uint64_t ad = desc_sw128(rec + R::OQ + (uint32_t)(pnl * 64 * 128) - 64 * 128 + (ks & 3) * 32, 16, 1024);
-        const uint64_t bd = ks < DK / 16 ? desc_mnmajor(sbase + L::SB, DK, ks)
-                                         : desc_mnmajor(sbase + L::UB, 64, ks - DK / 16);
-        mma_bf16(tX, ad, bd, idesc_bf16(128, DV, false, true), ks > 0);
+        for (int ks = 0; ks < DK / 16; ++ks)
+          mma_bf16(tX(b), desc_kmajor(rWQ, 128, ks), desc_mnmajor(sbase + L::SB, DK, ks),
+                   idesc_bf16(128, DV, false, true), 1u);
+        mma_commit(mbar_a);
       }
-      mma_commit(ctx.mbar);
+      __syncwarp();
+      bar_sync(2, 160);
+      // S += K_end^T U  (the state chain), then O += A_Q U (rows 64..127 of buffer b)
+      if (lane == 0) {
+        fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tS, desc_kmajor(rKE, DK, ks), desc_mnmajor(vt, 64, ks),
+                   idesc_bf16(128, DV, false, true), 1u);
+        mma_commit(mbar_s);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tX(b), desc_kmajor(rAQ - 64 * 128, 64, ks), desc_mnmajor(vt, 64, ks),
+                   idesc_bf16(128, DV, false, true), 1u);
+        mma_commit(mbar_free0 + 8 * b);  // chunk ci's output is ready; its buffers are free
+      }
+      __syncwarp();
     }
-    wait_mma(ctx);
-
-    // ---- outputs (lanes 64..127) and the bf16 copy of the new state ----
-    if (warp >= 2) {
-      const int t = tid - 64;
-      __nv_bfloat16* orow = og + ((int64_t)ci * kC + t) * a.out_st;
+  } else {
+    // ======================= TMEM <-> memory warps =======================
+    // rows 64..127 of chunk pc's U/O buffer -> out (warps 2-3).  The values are
+    // read from TMEM first and the buffer is released at once (orel, when
+    // `release`); each warp then turns its 32 rows around through a small
+    // shared staging area so that every store instruction writes four whole
+    // 128-byte lines.
+    auto store_out = [&](int pc, bool release) {
+      const int lc = min(kC, rg.len - pc * kC);
+      // 144-byte staging rows: consecutive rows start on different banks
+      const uint32_t stage = sbase + L::OSTG + (warp - 2) * 32 * 144;
+      uint32_t r[DV / 32][32];
 #pragma unroll
-      for (int c0 = 0; c0 < DV; c0 += 32) {
-        float v[32];
-        tmem_ld32(tX + lane_base + c0, v);
-        if (t < lc) {
+      for (int q = 0; q < DV / 32; ++q) tmem_ld32_async(tX(pc & 1) + lane_base + 32 * q, r[q]);
+      tmem_wait_ld();
+      if (release) {
+        fence_before_sync();
+        mbar_arrive(mbar_orel0 + 8 * (pc & 1));
+      }
+      const int row0 = 32 * (warp - 2);  // this warp's first token row in the chunk
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 w;
-            w.x = pack_bf16(a.scale * v[8 * u], a.scale * v[8 * u + 1]);
-            w.y = pack_bf16(a.scale * v[8 * u + 2], a.scale * v[8 * u + 3]);
-            w.z = pack_bf16(a.scale * v[8 * u + 4], a.scale * v[8 * u + 5]);
-            w.w = pack_bf16(a.scale * v[8 * u + 6], a.scale * v[8 * u + 7]);
-            *reinterpret_cast<uint4*>(orow + c0 + 8 * u) = w;
-          }
+      for (int half = 0; half < DV / 64; ++half) {
+        __syncwarp();  // the previous half has been read back
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float* f = reinterpret_cast<const float*>(r[2 * half + (u >> 2)]) + 8 * (u & 3);
+          st_shared_v4(stage + lane * 144 + 16 * u, pack_bf16(a.scale * f[0], a.scale * f[1]),
+                       pack_bf16(a.scale * f[2], a.scale * f[3]), pack_bf16(a.scale * f[4], a.scale * f[5]),
+                       pack_bf16(a.scale * f[6], a.scale * f[7]));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int rr = 4 * it + (lane >> 3), ch = lane & 7;
+          uint4 w;
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                       : "r"(stage + rr * 144 + 16 * ch));
+          const int t = row0 + rr;
+          if (t < lc)
+            *reinterpret_cast<uint4*>(og + ((int64_t)pc * kC + t) * a.out_st + 64 * half + 8 * ch) = w;
         }
       }
+    };
+    for (int ci = 0; ci < nch; ++ci) {
+      const int b = ci & 1;
+      const uint32_t rec = sbase + L::REC + b * L::kRecBuf;
+      const uint32_t vt = sbase + L::VT + b * 64 * DV * 2;
+      // (1) bf16 copy of the state entering this chunk (read once from TMEM, kept in registers)
+      uint32_t r[DV / 32][32];
+      if (ci > 0) wait(mbar_s, (uint32_t)((ci - 1) & 1));
+      if (tid < DK) {
+#pragma unroll
+        for (int q = 0; q < DV / 32; ++q) tmem_ld32_async(tS + lane_base + 32 * q, r[q]);
+        tmem_wait_ld();
+        if (ci > 0) {
+#pragma unroll
+          for (int q = 0; q < DV / 32; ++q)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              st_shared_v4(sbase + L::SB + sw128(tid, 32 * q + 8 * u, DK),
+                           pack_bf16(__uint_as_float(r[q][8 * u]), __uint_as_float(r[q][8 * u + 1])),
+                           pack_bf16(__uint_as_float(r[q][8 * u + 2]), __uint_as_float(r[q][8 * u + 3])),
+                           pack_bf16(__uint_as_float(r[q][8 * u + 4]), __uint_as_float(r[q][8 * u + 5])),
+                           pack_bf16(__uint_as_float(r[q][8 * u + 6]), __uint_as_float(r[q][8 * u + 7])));
+        }
+      }
+      fence_async_smem();
+      bar_arrive(1, 160);
+      // (2) decay the TMEM state by e^{G_C} of this chunk (overlaps the first product)
+      wait(mbar_rec0 + 8 * b, (ci >> 1) & 1);
+      if (tid < DK) {
+        const float pc = reinterpret_cast<const float*>(smem + (rec - sbase) + 2 * kT2 + (R::P - kT2))[tid];
+#pragma unroll
+        for (int q = 0; q < DV / 32; ++q) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[q][i] = __float_as_uint(__uint_as_float(r[q][i]) * pc);
+          tmem_st32_async(tS + lane_base + 32 * q, r[q]);
+        }
+        tmem_wait_st();
+      }
+      // (3) warps 0-1: U -> bf16 (MN-major [j][n]) into the consumed V buffer
+      if (warp < 2) {
+        wait(mbar_a, (uint32_t)(ci & 1));
+#pragma unroll
+        for (int q = 0; q < DV / 32; ++q) tmem_ld32_async(tX(b) + lane_base + 32 * q, r[q]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < DV / 32; ++q)
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            st_shared_v4(vt + sw128(tid, 32 * q + 8 * u, 64),
+                         pack_bf16(__uint_as_float(r[q][8 * u]), __uint_as_float(r[q][8 * u + 1])),
+                         pack_bf16(__uint_as_float(r[q][8 * u + 2]), __uint_as_float(r[q][8 * u + 3])),
+                         pack_bf16(__uint_as_float(r[q][8 * u + 4]), __uint_as_float(r[q][8 * u + 5])),
+                         pack_bf16(__uint_as_float(r[q][8 * u + 6]), __uint_as_float(r[q][8 * u + 7])));
+        fence_async_smem();
+      }
+      fence_before_sync();
+      bar_arrive(2, 160);
+      // (4) warps 2-3: output of the previous chunk, then release its U/O buffer
+      if (warp >= 2 && ci > 0) {
+        wait(mbar_free0 + 8 * ((ci - 1) & 1), (uint32_t)(((ci - 1) >> 1) & 1));
+        store_out(ci - 1, true);
+      }
     }
-    if (tid < DK) {
+    // last output and the final state
+    if (nch > 0) {
+      wait(mbar_s, (uint32_t)((nch - 1) & 1));
+      if (warp >= 2) {
+        wait(mbar_free0 + 8 * ((nch - 1) & 1), (uint32_t)(((nch - 1) >> 1) & 1));
+        store_out(nch - 1, false);
+      }
+    }
+    if (a.sT && tid < DK) {
+      float* dst = a.sT + n * a.sT_sn + h * a.sT_sh + (int64_t)tid * DV;
 #pragma unroll
       for (int c0 = 0; c0 < DV; c0 += 32) {
         float v[32];
         tmem_ld32(tS + lane_base + c0, v);
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          st_shared_v4(sbase + L::SB + sw128(tid, c0 + 8 * u, DK), pack_bf16(v[8 * u], v[8 * u + 1]),
-                       pack_bf16(v[8 * u + 2], v[8 * u + 3]), pack_bf16(v[8 * u + 4], v[8 * u + 5]),
-                       pack_bf16(v[8 * u + 6], v[8 * u + 7]));
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(dst + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
       }
-    }
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    if (*sFlag) break;
-    // this chunk's record and V buffers are free: fetch chunk ci + 2 into them
-    if (ci + 2 < nch) issue(ci + 2);
-  }
-
-  // ---- final state ----
-  cp_async_wait_all();
-  if (a.sT && tid < DK) {
-    float* dst = a.sT + n * a.sT_sn + h * a.sT_sh + (int64_t)tid * DV;
-#pragma unroll
-    for (int c0 = 0; c0 < DV; c0 += 32) {
-      float v[32];
-      tmem_ld32(tS + lane_base + c0, v);
-#pragma unroll
-      for (int i = 0; i < 32; i += 4)
-        *reinterpret_cast<float4*>(dst + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
     }
   }
   fence_before_sync();
@@ -922,7 +1024,7 @@ cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
   auto ser = kda_chunk_serial_kernel<DK, DV>;
   e = cudaFuncSetAttribute(ser, cudaFuncAttributeMaxDynamicSharedMemorySize, SerialSmem<DK, DV>::kAlloc);
   if (e != cudaSuccess) return e;
-  ser<<<dim3((unsigned)(a.N * a.H)), kThreads, SerialSmem<DK, DV>::kAlloc, s>>>(a, sp);
+  ser<<<dim3((unsigned)(a.N * a.H)), kSerialThreads, SerialSmem<DK, DV>::kAlloc, s>>>(a, sp);
   return cudaGetLastError();
 }
 
