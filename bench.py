@@ -18,6 +18,7 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import math
@@ -41,6 +42,7 @@ PREFILL_W = 1          # headline prefill workload
 K3_W = 2               # 96-head prefill, reported alongside
 DECODE_W = 3
 L2_FLUSH_BYTES = 256 << 20
+SLEEP_CYCLES = 200_000  # about 0.1 ms at 2 GHz, spent before each timed step
 
 
 def peaks():
@@ -65,6 +67,20 @@ def prefill_bytes(token_heads, dk, dv, n_states_read, n_states_written, in_bytes
     return token_heads * per + 4 * dk * dv * (n_states_read + n_states_written)
 
 
+def prefill_kernel_bytes(token_heads, dk, dv, n_states_read, n_states_written, in_bytes=2):
+    """The same algorithmic bytes split by the kernel that moves them: the chunk
+    prep kernel reads q, k, g, beta; the serial kernel reads v and the initial
+    states and writes out and the final states."""
+    return {"kda_chunk_prep_kernel": token_heads * (in_bytes * 2 * dk + 4 * dk + 4),
+            "kda_chunk_serial_kernel": token_heads * 2 * in_bytes * dv
+            + 4 * dk * dv * (n_states_read + n_states_written)}
+
+
+# kernels of one kda_chunk_fwd call (bf16), in launch order
+CHUNK_KERNELS = ["kda_chunk_prep_kernel", "kda_chunk_serial_kernel"]
+CHUNK_KERNELS_VARLEN = ["kda_seqlens_kernel", "kda_chunk_offsets_kernel"] + CHUNK_KERNELS
+
+
 def decode_bytes(NH, dk, dv, in_bytes=2):
     return NH * (2 * 4 * dk * dv + in_bytes * (2 * dk + dv) + 4 * dk + 4 + in_bytes * dv)
 
@@ -72,23 +88,84 @@ def decode_bytes(NH, dk, dv, in_bytes=2):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    """SM clock and throttle reasons while the timed loop runs.
+
+    Polls NVML (the counters nvidia-smi reports) from a thread about once per
+    millisecond, so that even a timed region of a few milliseconds has samples;
+    falls back to ``nvidia-smi -lms 200`` where libnvidia-ml cannot be loaded.
+    Reads only; changes no setting."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # nvmlClocksEventReasons bits (nvml.h)
+    BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown"}
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.nvml = None
         self.lines = []
+        self.sm = []
+        self.mx = None
+        self.reasons = set()
+        self.source = None
+
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        ok = False
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.index).uuid)
+            ok = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+        except (AttributeError, RuntimeError):
+            ok = False
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(h)) != 0:
+            lib.nvmlShutdown()
+            return None
+        v = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(v)) == 0:  # NVML_CLOCK_SM
+            self.mx = float(v.value)
+        try:
+            reasons = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons
+
+    def _poll(self):
+        import ctypes
+        lib, h, get_reasons = self.nvml
+        v, r = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(v)) == 0:
+                self.sm.append(float(v.value))
+            if get_reasons(h, ctypes.byref(r)) == 0:
+                for bit, name in self.BITS.items():
+                    if r.value & bit:
+                        self.reasons.add(name)
+            self.stop.wait(0.001)
 
     def __enter__(self):
+        self.stop = threading.Event()
+        try:
+            self.nvml = self._nvml_open()
+        except OSError:
+            self.nvml = None
+        if self.nvml:
+            self.source = "nvml, ~1 ms polling"
+            self.t = threading.Thread(target=self._poll, daemon=True)
+            self.t.start()
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi -lms 200"
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except OSError:
@@ -100,6 +177,10 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        self.stop.set()
+        if self.nvml:
+            self.t.join(timeout=5)
+            self.nvml[0].nvmlShutdown()
         if self.proc:
             self.proc.terminate()
             try:
@@ -108,7 +189,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons = list(self.sm), self.mx, set(self.reasons)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -123,9 +204,10 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0,
+                    "source": self.source}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": self.source}
 
 
 def dist_setup(gpus):
@@ -149,6 +231,13 @@ def barrier(world):
         dist.barrier()
 
 
+def whole_job_rate(units_per_rank, ms_slowest, world):
+    """Units per second of the whole job: every rank processes `units_per_rank`
+    (weak scaling, independent replicas) and the job takes as long as the
+    slowest rank."""
+    return units_per_rank * world / (ms_slowest * 1e-3)
+
+
 def max_over_ranks(x, world):
     if world == 1:
         return x
@@ -159,29 +248,38 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
-def source_sha():
+# source files each kernel is compiled from (their hash dates a traffic record)
+KERNEL_SOURCES = {
+    "kda_chunk_prep_kernel": ["kda_prefill_tc.cu", "kda_sm100.cuh", "kda_internal.h"],
+    "kda_chunk_serial_kernel": ["kda_prefill_tc.cu", "kda_sm100.cuh", "kda_internal.h"],
+    "kda_decode_kernel": ["kda_recurrent.cu", "kda_internal.h"],
+}
+
+
+def source_sha(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def committed_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    """DRAM bytes (read + write) per launch from the committed ncu summary
+    (profiles/traffic.json), if it was taken on the kernel's current sources;
+    else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
+    if not os.path.exists(p) or kernel not in KERNEL_SOURCES:
         return None
     d = json.load(open(p)).get(kernel)
-    if not d or d.get("source_sha") != source_sha():
+    if not d or d.get("source_sha") != source_sha(kernel):
         return None
     return d.get("bytes_per_launch")
 
 
 # ---------------------------------------------------------------------------
 
-def bench_prefill(kda, idx, steps, warmup, flush, stream):
+def bench_prefill(kda, idx, steps, warmup, flush, stream, clk=None, world=1):
     w = ki.WORKLOADS[idx]
     d = ki.workload_inputs(idx)
     dev = torch.device("cuda")
@@ -202,23 +300,61 @@ def bench_prefill(kda, idx, steps, warmup, flush, stream):
             step()
             flush.zero_()
     stream.synchronize()
+    names = CHUNK_KERNELS if t["cu_seqlens"] is None else CHUNK_KERNELS_VARLEN
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
-    with torch.cuda.stream(stream):
-        for e0, e1 in evs:
-            flush.zero_()
-            e0.record(stream)
-            step()
-            e1.record(stream)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+           for _ in range(steps)]
+    for e in [x for row in kev for x in row]:
+        e.record(stream)  # creates the CUDA handles before the timed loop
     stream.synchronize()
+    launches = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with (clk or contextlib.nullcontext()), torch.cuda.stream(stream):
+        for (e0, e1), ke in zip(evs, kev):
+            flush.zero_()
+            # keep the GPU busy while the host enqueues the step, so no host-side
+            # gap falls between the events
+            torch.cuda._sleep(SLEEP_CYCLES)
+            e0.record(stream)
+            kda.kda_set_launch_events(ke)
+            step()
+            launches += kda.kda_last_launch_count()
+            e1.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
     kda.kda_get_device_error(stream)
     ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    if launches != steps * len(names):
+        raise RuntimeError(f"expected {len(names)} kernels per step, counted {launches / steps}")
+    kernel_ms = {n: statistics.mean(ke[i].elapsed_time(ke[i + 1]) for ke in kev)
+                 for i, n in enumerate(names)}
     th = B * T * H if t["cu_seqlens"] is None else T * H
     n_read = N if t["initial_state"] is not None else 0
     return dict(ms=ms, token_heads=th, tokens=B * T, dk=dk, dv=dv, H=H,
                 flops=prefill_flops(th, dk, dv),
-                bytes=prefill_bytes(th, dk, dv, n_read * H, N * H), d=d, t=t, out=out, sT=sT,
+                bytes=prefill_bytes(th, dk, dv, n_read * H, N * H),
+                kernel_bytes=prefill_kernel_bytes(th, dk, dv, n_read * H, N * H),
+                kernel_ms=kernel_ms, launches=launches, wall=wall, d=d, t=t, out=out, sT=sT,
                 name=w["name"])
+
+
+def kernel_roofline(r, pk, world):
+    """Roofline of the kernel that takes the most device time per step."""
+    timed = {n: ms for n, ms in r["kernel_ms"].items() if n in r["kernel_bytes"]}
+    name = max(timed, key=timed.get)
+    ms = max_over_ranks(timed[name], world)
+    gbs = r["kernel_bytes"][name] / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": name, "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
+            "frac": gbs / pk["hbm"], "traffic": committed_traffic(name),
+            "peak_source": pk["src"] + " (burst copy)",
+            "algorithmic_bytes_per_launch": r["kernel_bytes"][name],
+            "launch_ms": ms,
+            "kernel_ms": {n: max_over_ranks(v, world) for n, v in r["kernel_ms"].items()}}
 
 
 def bench_prefill_e2e(kda, r, steps, warmup, stream):
@@ -256,7 +392,7 @@ def bench_prefill_e2e(kda, r, steps, warmup, stream):
     return dict(ms=ms, h2d=h2d, d2h=d2h)
 
 
-def bench_decode(kda, steps_total, warmup, stream):
+def bench_decode(kda, steps_total, warmup, stream, clk=None):
     w = ki.WORKLOADS[DECODE_W]
     N, H, dk, dv = w["N"], w["H"], w["dk"], w["dv"]
     seed = ki.SEED_BASE + DECODE_W
@@ -278,15 +414,18 @@ def bench_decode(kda, steps_total, warmup, stream):
             step(ins[i % n_in])
     stream.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
+    launches = 0
+    with (clk or contextlib.nullcontext()), torch.cuda.stream(stream):
+        torch.cuda._sleep(SLEEP_CYCLES)
         e0.record(stream)
         for i in range(steps_total):
             step(ins[i % n_in])
+            launches += kda.kda_last_launch_count()
         e1.record(stream)
-    stream.synchronize()
+        stream.synchronize()
     ms = e0.elapsed_time(e1) / steps_total
     return dict(ms=ms, NH=N * H, N=N, H=H, dk=dk, dv=dv, bytes=decode_bytes(N * H, dk, dv),
-                name=w["name"], steps=steps_total)
+                name=w["name"], steps=steps_total, launches=launches)
 
 
 def oracle_prefill_rate(idx, max_problems=None):
@@ -397,25 +536,20 @@ def main():
     stream = torch.cuda.Stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
 
-    barrier(world)
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    with ClockSampler(local) as clk:
-        pre = bench_prefill(kda, PREFILL_W, args.steps, args.warmup, flush, stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    wall = time.perf_counter() - wall0
+    clk = ClockSampler(local)
+    pre = bench_prefill(kda, PREFILL_W, args.steps, args.warmup, flush, stream, clk, world)
+    wall = pre["wall"]
 
     ms = statistics.mean(pre["ms"])
     ms = max_over_ranks(ms, world)
     tokens_all = pre["tokens"] * world
-    value = tokens_all / (ms * 1e-3)
+    value = whole_job_rate(pre["tokens"], ms, world)
     ach_gbs = pre["bytes"] / (ms * 1e-3) / 1e9
     ach_tf = pre["flops"] / (ms * 1e-3) / 1e12
-    kname = "kda_chunk_prefill"
-    roof = {"bound": "hbm", "achieved": ach_gbs, "peak": pk["hbm"], "unit": "GB/s",
-            "frac": ach_gbs / pk["hbm"], "traffic": committed_traffic(kname),
-            "peak_source": pk["src"], "algorithmic_bytes_per_launch": pre["bytes"]}
+    roof = kernel_roofline(pre, pk, world)
+    path_roof = {"bound": "hbm", "achieved": ach_gbs, "peak": pk["hbm"], "unit": "GB/s",
+                 "frac": ach_gbs / pk["hbm"], "algorithmic_bytes_per_step": pre["bytes"],
+                 "note": "whole step (all kernels of one kda_chunk_fwd call)"}
     tc = {"achieved": ach_tf, "peak": pk["bf16"], "unit": "TFLOP/s", "frac": ach_tf / pk["bf16"],
           "algorithmic_flops_per_launch": pre["flops"]}
     t_roof = max(pre["flops"] / (pk["bf16"] * 1e12), pre["bytes"] / (pk["hbm"] * 1e9))
@@ -424,28 +558,34 @@ def main():
     e2e_val = tokens_all / (max_over_ranks(e2e["ms"], world) * 1e-3)
 
     extra = {}
-    with ClockSampler(local) as clk_dec:
-        dec = bench_decode(kda, 64, args.warmup, stream)
+    clk_dec = ClockSampler(local)
+    dec = bench_decode(kda, 64, args.warmup, stream, clk_dec)
     dms = max_over_ranks(dec["ms"], world)
     d_gbs = dec["bytes"] / (dms * 1e-3) / 1e9
     extra["decode"] = {
         "workload": dec["name"], "ms_per_step": dms, "steps_timed": dec["steps"],
         "steps_per_s": world * 1e3 / dms, "tokens_per_s": world * dec["N"] * 1e3 / dms,
-        "roofline": {"bound": "hbm", "achieved": d_gbs, "peak": pk["hbm"], "unit": "GB/s",
-                     "frac": d_gbs / pk["hbm"], "traffic": committed_traffic("kda_decode"),
+        "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": d_gbs,
+                     "peak": pk["hbm"], "unit": "GB/s", "frac": d_gbs / pk["hbm"],
+                     "traffic": committed_traffic("kda_decode_kernel"),
                      "algorithmic_bytes_per_launch": dec["bytes"]},
-        "clocks": clk_dec.summary(), "gpu_launches": dec["steps"]}
+        "clocks": clk_dec.summary(), "gpu_launches": dec["launches"]}
     del dec
     if not args.no_k3:
-        k3 = bench_prefill(kda, K3_W, max(3, args.steps // 4), 3, flush, stream)
+        clk_k3 = ClockSampler(local)
+        k3 = bench_prefill(kda, K3_W, max(3, args.steps // 4), 3, flush, stream, clk_k3, world)
         kms = max_over_ranks(statistics.mean(k3["ms"]), world)
         extra["prefill_96heads"] = {
             "workload": k3["name"], "ms_per_step": kms,
+            "kernel_ms": {n: max_over_ranks(v, world) for n, v in k3["kernel_ms"].items()},
+            "kernel_hbm_frac": {n: k3["kernel_bytes"][n] / (k3["kernel_ms"][n] * 1e-3) / 1e9 / pk["hbm"]
+                                for n in k3["kernel_bytes"]},
             "tokens_per_s": world * k3["tokens"] / (kms * 1e-3),
             "hbm_frac": k3["bytes"] / (kms * 1e-3) / 1e9 / pk["hbm"],
             "tc_frac": k3["flops"] / (kms * 1e-3) / 1e12 / pk["bf16"],
             "t_roof_over_t": max(k3["flops"] / (pk["bf16"] * 1e12),
-                                 k3["bytes"] / (pk["hbm"] * 1e9)) / (kms * 1e-3)}
+                                 k3["bytes"] / (pk["hbm"] * 1e9)) / (kms * 1e-3),
+            "clocks": clk_k3.summary(), "gpu_launches": k3["launches"]}
         del k3
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -455,10 +595,11 @@ def main():
             "config": {"workload": pre["name"], "B": 2, "T": 4096, "H": pre["H"], "d_k": pre["dk"],
                        "d_v": pre["dv"], "chunk": 64, "parallelism": f"replicas x{world}",
                        "l2": "flushed (256 MiB write) between timed steps, outside the events"},
-            "roofline": roof, "tc_roofline": tc, "t_roof_over_t": t_roof / (ms * 1e-3),
+            "roofline": roof, "path_roofline": path_roof, "tc_roofline": tc,
+            "t_roof_over_t": t_roof / (ms * 1e-3),
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": e2e["h2d"],
                     "d2h_bytes_per_step": e2e["d2h"]},
-            "gpu_launches": args.steps, "clocks": clk.summary(), "wall_s_timed_region": wall}
+            "gpu_launches": pre["launches"], "clocks": clk.summary(), "wall_s_timed_region": wall}
     line.update(extra)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r, threads, sample, _ = oracle_prefill_rate(PREFILL_W)

@@ -15,14 +15,16 @@ import torch
 from ._build import LIB, build, up_to_date  # noqa: F401
 
 __all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
-           "kda_get_device_error", "KdaError", "load_library", "build", "STATUS"]
+           "kda_get_device_error", "kda_set_launch_events", "kda_last_launch_count", "KdaError",
+           "load_library", "build", "STATUS"]
 
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
           4: "KDA_ERR_DEVICE", 5: "KDA_ERR_TIMEOUT"}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
 
 EXPORTED = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
-            "kda_get_device_error", "kda_status_string", "kda_last_error_message"]
+            "kda_get_device_error", "kda_status_string", "kda_last_error_message",
+            "kda_set_launch_events", "kda_last_launch_count"]
 
 
 class KdaTensor(ctypes.Structure):
@@ -62,6 +64,10 @@ def load_library(path: str | None = None):
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_last_error_message.restype = ctypes.c_char_p
     lib.kda_last_error_message.argtypes = []
+    lib.kda_set_launch_events.restype = ctypes.c_int
+    lib.kda_set_launch_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+    lib.kda_last_launch_count.restype = ctypes.c_int
+    lib.kda_last_launch_count.argtypes = []
     _lib = lib
     return lib
 
@@ -156,3 +162,26 @@ def kda_get_device_error(stream=None) -> int:
     lib = load_library()
     _check(lib, lib.kda_get_device_error(_stream(stream)))
     return 0
+
+
+_armed = None  # keeps the handle array alive until the armed call has returned
+
+
+def kda_set_launch_events(events) -> None:
+    """Arm this thread's next compute call to record ``events[0]`` before its first
+    kernel and ``events[i]`` after its i-th (``torch.cuda.Event(enable_timing=True)``
+    objects that have been recorded once, so that their CUDA handles exist).  An
+    empty list or None disarms."""
+    global _armed
+    lib = load_library()
+    events = list(events or [])
+    handles = [e.cuda_event for e in events]
+    if any(h == 0 for h in handles):
+        raise ValueError("record each event once before arming it (its handle is created lazily)")
+    _armed = (ctypes.c_void_p * max(1, len(handles)))(*handles)
+    _check(lib, lib.kda_set_launch_events(_armed if handles else None, len(handles)))
+
+
+def kda_last_launch_count() -> int:
+    """Kernels enqueued by this thread's last compute call."""
+    return load_library().kda_last_launch_count()

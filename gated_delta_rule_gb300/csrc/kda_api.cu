@@ -17,6 +17,30 @@ namespace {
 
 thread_local std::string g_msg;
 
+// Launch accounting of the calling thread (kda_set_launch_events,
+// kda_last_launch_count).  `ev` is armed for one compute call.
+struct LaunchLog {
+  void* const* ev = nullptr;
+  int cap = 0;
+  int used = 0;
+  int launches = 0;
+  cudaError_t pending = cudaSuccess;  // a failed record of events[0]
+};
+thread_local LaunchLog g_launch;
+
+// Scope of one compute call: resets the count, and disarms the events at exit.
+struct LaunchScope {
+  LaunchScope() {
+    g_launch.launches = 0;
+    g_launch.used = 0;
+    g_launch.pending = cudaSuccess;
+  }
+  ~LaunchScope() {
+    g_launch.ev = nullptr;
+    g_launch.cap = 0;
+  }
+};
+
 kda_status fail(kda_status st, const char* fmt, ...) {
   char buf[512];
   va_list ap;
@@ -322,6 +346,37 @@ kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
 
 namespace kda {
 
+void launch_begin(cudaStream_t s) {
+  if (g_launch.ev && g_launch.used == 0 && g_launch.cap > 0) {
+    const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(g_launch.ev[0]), s);
+    if (e == cudaSuccess) {
+      g_launch.used = 1;
+    } else {  // reported by launch_end, not by the kernel's own launch check
+      cudaGetLastError();
+      g_launch.pending = e;
+      g_launch.ev = nullptr;
+    }
+  }
+}
+
+cudaError_t launch_end(cudaStream_t s) {
+  ++g_launch.launches;
+  if (g_launch.pending != cudaSuccess) {
+    const cudaError_t e = g_launch.pending;
+    g_launch.pending = cudaSuccess;
+    return e;
+  }
+  if (!g_launch.ev || g_launch.used == 0 || g_launch.used >= g_launch.cap) return cudaSuccess;
+  cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(g_launch.ev[g_launch.used]), s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // not sticky; the kernel's own launch check has already passed
+    g_launch.ev = nullptr;
+    return e;
+  }
+  ++g_launch.used;
+  return cudaSuccess;
+}
+
 // Per-device pool that keeps freed blocks for reuse (release threshold: never),
 // so repeated calls do not go back to the driver for their chunk records.
 cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s) {
@@ -360,6 +415,7 @@ kda_status kda_chunk_fwd(const kda_tensor* q, const kda_tensor* k, const kda_ten
                          const kda_tensor* initial_state, float scale,
                          const kda_tensor* cu_seqlens, kda_tensor* out,
                          kda_tensor* final_state, void* stream) {
+  LaunchScope scope;
   return prefill(q, k, v, g, beta, initial_state, scale, cu_seqlens, out, final_state, stream,
                  PrefillPath::kChunked);
 }
@@ -369,6 +425,7 @@ kda_status kda_chunk_fwd_noalloc(const kda_tensor* q, const kda_tensor* k, const
                                  const kda_tensor* initial_state, float scale,
                                  const kda_tensor* cu_seqlens, kda_tensor* out,
                                  kda_tensor* final_state, void* stream) {
+  LaunchScope scope;
   return prefill(q, k, v, g, beta, initial_state, scale, cu_seqlens, out, final_state, stream,
                  PrefillPath::kChunkedNoAlloc);
 }
@@ -378,6 +435,7 @@ kda_status kda_fused_recurrent_fwd(const kda_tensor* q, const kda_tensor* k, con
                                    const kda_tensor* initial_state, float scale,
                                    const kda_tensor* cu_seqlens, kda_tensor* out,
                                    kda_tensor* final_state, void* stream) {
+  LaunchScope scope;
   return prefill(q, k, v, g, beta, initial_state, scale, cu_seqlens, out, final_state, stream,
                  PrefillPath::kRecurrent);
 }
@@ -385,6 +443,7 @@ kda_status kda_fused_recurrent_fwd(const kda_tensor* q, const kda_tensor* k, con
 kda_status kda_recurrent_step(kda_tensor* state, const kda_tensor* q, const kda_tensor* k,
                               const kda_tensor* v, const kda_tensor* g, const kda_tensor* beta,
                               float scale, kda_tensor* out, void* stream) {
+  LaunchScope scope;
   g_msg.clear();
   KDA_TRY(check_desc(q, "q", 3, 16));
   const int32_t dt = q->dtype;
@@ -479,5 +538,16 @@ const char* kda_status_string(kda_status s) {
 }
 
 const char* kda_last_error_message(void) { return g_msg.c_str(); }
+
+kda_status kda_set_launch_events(void* const* events, int count) {
+  g_msg.clear();
+  if (count < 0 || (!events && count > 0))
+    return fail(KDA_ERR_INVALID_ARG, "launch events: %d handles at %p", count, (const void*)events);
+  g_launch.ev = count > 0 ? events : nullptr;
+  g_launch.cap = count;
+  return KDA_OK;
+}
+
+int kda_last_launch_count(void) { return g_launch.launches; }
 
 }  // extern "C"

@@ -66,6 +66,12 @@ cudaError_t launch_chunk_prefill_tc(const PrefillArgs& a, void* workspace, cudaS
 constexpr size_t kNoallocWorkspaceBytes = size_t(64) << 20;
 cudaError_t noalloc_workspace(void** ptr);
 
+// Launch accounting (kda_api.cu): every kernel launch is bracketed by
+// launch_begin (before) and launch_end (after its own launch check succeeded).
+// launch_end returns the error of recording an armed event, if any.
+void launch_begin(cudaStream_t s);
+cudaError_t launch_end(cudaStream_t s);
+
 // Stream-ordered scratch memory from a per-device pool (kda_api.cu).
 cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s);
 cudaError_t scratch_free(void* p, cudaStream_t s);

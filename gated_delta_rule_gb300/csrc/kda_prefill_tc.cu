@@ -1012,20 +1012,29 @@ cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
   sp.rec = static_cast<unsigned char*>(ws) + off_bytes;
   sp.total = (int)total;
   sp.nck = (int)(((int64_t)a.T + kC - 1) / kC);
+  cudaError_t e;
   if (a.cu_seqlens) {
+    launch_begin(s);
     kda_chunk_offsets_kernel<<<1, 256, 0, s>>>(a, sp.total, static_cast<int*>(ws));
+    if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   }
   auto prep = kda_chunk_prep_kernel<DK>;
-  cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, PrepSmem<DK>::kAlloc);
+  e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, PrepSmem<DK>::kAlloc);
   if (e != cudaSuccess) return e;
-  const int64_t items = total * a.H;
-  const int grid = (int)(items < 2 * sm_count() ? items : 2 * sm_count());
-  if (grid > 0) prep<<<grid, kThreads, PrepSmem<DK>::kAlloc, s>>>(a, sp);
   auto ser = kda_chunk_serial_kernel<DK, DV>;
   e = cudaFuncSetAttribute(ser, cudaFuncAttributeMaxDynamicSharedMemorySize, SerialSmem<DK, DV>::kAlloc);
   if (e != cudaSuccess) return e;
+  const int64_t items = total * a.H;
+  const int grid = (int)(items < 2 * sm_count() ? items : 2 * sm_count());
+  if (grid > 0) {
+    launch_begin(s);
+    prep<<<grid, kThreads, PrepSmem<DK>::kAlloc, s>>>(a, sp);
+    if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
+  }
+  launch_begin(s);
   ser<<<dim3((unsigned)(a.N * a.H)), kSerialThreads, SerialSmem<DK, DV>::kAlloc, s>>>(a, sp);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_end(s);
 }
 
 }  // namespace

@@ -296,8 +296,10 @@ cudaError_t dispatch(const Args& a, int dk, int dv, int bf16, dim3 grid, cudaStr
   KDA_CASE(128, 128)
 #undef KDA_CASE
   if (!fn) return cudaErrorInvalidValue;
+  launch_begin(st);
   fn<<<grid, kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  return e != cudaSuccess ? e : launch_end(st);
 }
 
 template <int DK, int DV, typename T>
@@ -322,8 +324,10 @@ cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_check_seqlens(const int32_t* cu, int N, int T, int* err, cudaStream_t s) {
+  launch_begin(s);
   kda_seqlens_kernel<<<1, 256, 0, s>>>(cu, N, T, err);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  return e != cudaSuccess ? e : launch_end(s);
 }
 
 }  // namespace kda

@@ -190,6 +190,29 @@ const char* kda_status_string(kda_status status);
  * until the next call into the library from this thread. */
 const char* kda_last_error_message(void);
 
+/*
+ * Launch accounting, a measurement aid with no counterpart on the pages.
+ *
+ * kda_set_launch_events arms the calling host thread's next compute call
+ * (kda_chunk_fwd, kda_chunk_fwd_noalloc, kda_fused_recurrent_fwd or
+ * kda_recurrent_step), and that call only.  It records events[0] on its stream
+ * just before its first kernel and events[i] just after its i-th kernel, as far
+ * as `count` reaches.  The elapsed time between consecutive events is then the
+ * device time of one kernel.
+ *   events  array of `count` cudaEvent_t handles (as void*), created by the
+ *           caller on the device of the call's stream; owned by the caller and
+ *           needed only until the armed call returns.  NULL (with count 0)
+ *           disarms.
+ * Returns KDA_ERR_INVALID_ARG when count < 0, or events is NULL while
+ * count > 0.  An event the runtime cannot record makes the armed call return
+ * KDA_ERR_CUDA; the kernels it had enqueued by then stay enqueued.
+ */
+kda_status kda_set_launch_events(void* const* events, int count);
+
+/* Number of kernels the calling thread's last compute call enqueued (0 when it
+ * returned before launching any). */
+int kda_last_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

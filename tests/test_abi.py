@@ -145,3 +145,16 @@ def test_noalloc_rejects_requests_beyond_its_workspace(lib):
                                    0.1, None, r(a["out"]), None, None)
     msg = lib.kda_last_error_message().decode()
     assert st == 2 and "fixed workspace" in msg, msg
+
+
+def test_launch_events_argument_checks(lib):
+    assert lib.kda_set_launch_events(None, -1) == 1
+    assert lib.kda_set_launch_events(None, 3) == 1
+    assert lib.kda_set_launch_events(None, 0) == 0  # disarm
+
+
+def test_failed_call_reports_no_launches(lib):
+    """A call rejected on the host enqueues nothing, and says so."""
+    assert lib.kda_recurrent_step(None, None, None, None, None, None, ctypes.c_float(1.0), None,
+                                  None) == 1
+    assert lib.kda_last_launch_count() == 0
