@@ -19,7 +19,8 @@
 //     tiles, the Gram products (tcgen05), the triangular inverse (CUDA cores +
 //     warp-level tf32 MMA) and W (tcgen05), and writes one "chunk record" of
 //     ready-to-use swizzled bf16 tiles -- T B_beta, [-W ; Q+], A_Q,
-//     (K e^{G_C - G})^T -- plus e^{G_C} to a workspace.
+//     K e^{G_C - G} -- plus e^{G_C} to a workspace.  Tiles that come out of
+//     TMEM or the solve are staged in shared memory and leave by bulk copy.
 //   * kda_chunk_serial_kernel: one CTA per (sequence, head) keeps the fp32 state
 //     in TMEM and walks the chunks in order, with warp roles: a producer warp
 //     (record by bulk copy, V by cp.async, one chunk ahead), an MMA warp and
@@ -53,7 +54,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kC = 64;
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // prep kernel
 constexpr float kLog2e = 1.4426950408889634f;
 
 __host__ __device__ constexpr int align1k(int x) { return (x + 1023) & ~1023; }
@@ -65,7 +66,7 @@ struct Rec {
   static constexpr int T2 = 0;                      // T Diag(beta): 64 x 64, K-major
   static constexpr int WQ = T2 + 64 * 64 * 2;       // [-W ; Q+]: 128 x DK, K-major
   static constexpr int AQ = WQ + 128 * DK * 2;      // A_Q: 64 x 64, K-major
-  static constexpr int KE = AQ + 64 * 64 * 2;       // (K e^{G_C - G})^T: DK x 64, K-major
+  static constexpr int KE = AQ + 64 * 64 * 2;       // K e^{G_C - G}: 64 x DK, MN-major (A of S += K_end^T U)
   static constexpr int P = KE + 64 * DK * 2;        // e^{G_C}: DK fp32
   static constexpr int kBytes = align1k(P + DK * 4);
 };
@@ -74,26 +75,36 @@ struct Rec {
 __host__ __device__ constexpr int yrows(int I) { return 16 * (I + 1); }
 __host__ __device__ constexpr int yoff_rows(int I) { return 8 * I * (I + 1); }  // rows before version I
 
+// Decay-factor table of the prep kernel: entry (a, b), a < b <= 4, holds
+// 2^(bnd[b] - bnd[a]) per channel, bnd[x] being the cumulative log2-decay before
+// sub-block x (bnd[4]: at the chunk end).
+__host__ __device__ constexpr int ft_index(int a, int b) { return a * (9 - a) / 2 + (b - a - 1); }
+
 template <int DK>
 struct PrepSmem {
+  static constexpr int kParts = kThreads / (DK / 8);   // token parts of the build
+  // region shared by the Gram operands and, after the Gram product, the solve
   static constexpr int X = 0;                          // 128 rows [K; Q] x DK, K-major
   static constexpr int Y = X + 128 * DK * 2;           // versions 0..3, 160 rows x DK, K-major
   static constexpr int kGram = Y + 160 * DK * 2;
-  static constexpr int kLd = 68;  // fp32 row stride of L (16-byte rows, conflict-free tf32 loads)
+  static constexpr int CARRY = 0;                      // scan partials [part][DK] fp32 (before X is built)
+  static_assert(kParts * DK * 4 <= 128 * DK * 2, "scan partials fit below Y");
+  static constexpr int kLd = 68;  // fp32 row stride of L
   static constexpr int kTd = 72;  // fp32 row stride of T
-  static constexpr int kRd = 56;  // fp32 row stride of the block-row workspace
+  static constexpr int kRd = 40;  // fp32 row stride of the product scratch
   static constexpr int SL = 0;
   static constexpr int ST = SL + 64 * kLd * 4;
-  static constexpr int SR = ST + 64 * kTd * 4;
-  static constexpr int T2 = align1k(SR + 16 * kRd * 4);  // 64 x 64 bf16 (+ an 8K window)
+  static constexpr int SR = ST + 64 * kTd * 4;         // 32 x kRd
+  static constexpr int T2 = align1k(SR + 32 * kRd * 4);  // 64 x 64 bf16 (+ an 8K window)
+  static constexpr int AQS = T2 + 64 * 64 * 2;  // A_Q staging: the window below T2, whose
+                                                // product rows are never read
   static constexpr int kSolve = T2 + 2 * 64 * 64 * 2;
   static constexpr int kG = kGram > kSolve ? kGram : kSolve;
   static constexpr int KP = align1k(kG);  // K+ : [64 tokens][DK], MN-major
   static constexpr int BETA = KP + 64 * DK * 2;
-  static constexpr int BND = BETA + 64 * 4;  // 5 x DK fp32 (log2 units)
-  static constexpr int kParts = kThreads / (DK / 8);
-  static constexpr int CARRY = BND + 5 * DK * 4;
-  static constexpr int MBAR = CARRY + kParts * DK * 4;
+  static constexpr int BND = BETA + 64 * 4;   // 5 x DK fp32 (log2 units)
+  static constexpr int FT = BND + 5 * DK * 4; // 10 x DK fp32 decay factors
+  static constexpr int MBAR = FT + 10 * DK * 4;
   static constexpr int TSLOT = MBAR + 8;
   static constexpr int FLAG = TSLOT + 4;
   static constexpr int kAlloc = FLAG + 4 + 1024;
@@ -195,14 +206,39 @@ __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 
 
 
 // ---------------------------------------------------------------------------
-// prep: one chunk of one head per iteration; persistent CTAs
+// C (16 x 8 tile) = sum over k in [k0, k1) of A[row][k] B[k][col] on one warp
+// (m16n8k8, tf32 inputs, fp32 accumulation).  A and B are fp32 in shared memory,
+// A's tile starting at `A` with row stride lda, B's at `B` with row stride ldb.
+__device__ __forceinline__ void warp_tile_tf32(float (&acc)[4], const float* A, int lda, const float* B,
+                                               int ldb, int k0, int k1, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  for (int k = k0; k < k1; k += 8) {
+    const uint32_t af[4] = {to_tf32(A[g * lda + k + t]), to_tf32(A[(g + 8) * lda + k + t]),
+                            to_tf32(A[g * lda + k + t + 4]), to_tf32(A[(g + 8) * lda + k + t + 4])};
+    const uint32_t bf[2] = {to_tf32(B[(k + t) * ldb + g]), to_tf32(B[(k + t + 4) * ldb + g])};
+    mma_tf32(acc, af, bf);
+  }
+}
+
+// Store a 16 x 8 accumulator tile (times `sign`) at C (row stride ldc).
+__device__ __forceinline__ void warp_tile_store(const float (&acc)[4], float* C, int ldc, float sign, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  C[g * ldc + 2 * t] = sign * acc[0];
+  C[g * ldc + 2 * t + 1] = sign * acc[1];
+  C[(g + 8) * ldc + 2 * t] = sign * acc[2];
+  C[(g + 8) * ldc + 2 * t + 1] = sign * acc[3];
+}
+
+// ---------------------------------------------------------------------------
+// prep: one chunk of one head per iteration; persistent CTAs of 8 warps, two per SM
 template <int DK>
 __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs a, Split sp) {
   using L = PrepSmem<DK>;
   using R = Rec<DK>;
   constexpr int OCT = DK / 8;            // channel octets
   constexpr int NPART = kThreads / OCT;  // token parts in the build
-  constexpr int TPP = 64 / NPART;        // tokens per part (8 or 4)
+  constexpr int TPP = 64 / NPART;        // tokens per part (4 or 2)
+  constexpr int PPB = 16 / TPP;          // parts per 16-token sub-block
   static_assert(16 % TPP == 0, "a part lies inside one 16-token sub-block");
 
   extern __shared__ unsigned char smem_raw[];
@@ -214,13 +250,14 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
   float* sR = reinterpret_cast<float*>(smem + L::SR);
   float* sBeta = reinterpret_cast<float*>(smem + L::BETA);
   float* sBnd = reinterpret_cast<float*>(smem + L::BND);
+  float* sFt = reinterpret_cast<float*>(smem + L::FT);
   float* sCarry = reinterpret_cast<float*>(smem + L::CARRY);
   volatile int* sFlag = reinterpret_cast<volatile int*>(smem + L::FLAG);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quarter
 
   if (tid == 0) {
     mbar_init(sbase + L::MBAR, 1);
@@ -236,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
 
   const int oct = tid % OCT;
   const int part = tid / OCT;
-  const int blk = (part * TPP) >> 4;  // this part's 16-token sub-block
+  const int blk = part / PPB;  // this part's 16-token sub-block
   const int nitems = sp.total * a.H;
   const int nseq_chunks = sp.off ? __ldg(sp.off + a.N) : sp.total;
 
@@ -304,6 +341,23 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
     const float* bb = a.beta + it.brow * a.beta_sb + it.h * a.beta_sh;
     rbeta = (it.valid && tid < it.lc) ? __ldg(bb + (it.row0 + tid) * a.beta_st) : 0.f;
   };
+  auto pack8 = [](const float* x) {
+    return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+  };
+  auto st8 = [&](uint32_t addr, const float* x) {
+    const uint4 u = pack8(x);
+    st_shared_v4(addr, u.x, u.y, u.z, u.w);
+  };
+  // 8 consecutive fp32 of shared memory (16-byte aligned)
+  auto ld8 = [](const float* p, float* x) {
+    const float4 u = reinterpret_cast<const float4*>(p)[0], v = reinterpret_cast<const float4*>(p)[1];
+    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w; x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
+  };
+  auto bf16x8 = [](const uint4& w, float* x) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = (e & 1) ? bf_hi(u[e >> 1]) : bf_lo(u[e >> 1]);
+  };
 
   Item cur = item(blockIdx.x);
   load_kq(cur);
@@ -313,8 +367,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
     const Item nxt = item(w + gridDim.x);
     if (cur.valid) {
       unsigned char* rec = sp.rec + cur.rec * R::kBytes;
+      const int col = 8 * oct;
 
-      // ================= scan: G (log2 units) for 8 channels x TPP tokens =================
+      // ================= scan: G (log2 units), 8 channels x TPP tokens per thread =================
       float G[TPP][8];
       {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -328,136 +383,122 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
             G[i][e] = acc[e];
           }
         }
-        float4* cw = reinterpret_cast<float4*>(sCarry + part * DK + 8 * oct);
+        float4* cw = reinterpret_cast<float4*>(sCarry + part * DK + col);
         cw[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         cw[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
         if (tid < 64) sBeta[tid] = rbeta;
       }
       __syncthreads();
-      {
-        float off[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int q = 0; q < part; ++q) {
-          const float4* cr = reinterpret_cast<const float4*>(sCarry + q * DK + 8 * oct);
-          const float4 x0 = cr[0], x1 = cr[1];
-          off[0] += x0.x; off[1] += x0.y; off[2] += x0.z; off[3] += x0.w;
-          off[4] += x1.x; off[5] += x1.y; off[6] += x1.z; off[7] += x1.w;
+      // one thread per channel: exclusive prefix over the parts, the sub-block
+      // boundaries, e^{G_C} (record) and the decay-factor table
+      if (tid < DK) {
+        const int c = tid;
+        float v[NPART];
+#pragma unroll
+        for (int p = 0; p < NPART; ++p) v[p] = sCarry[p * DK + c];
+        float run = 0.f, bnd[5];
+#pragma unroll
+        for (int p = 0; p < NPART; ++p) {
+          if (p % PPB == 0) bnd[p / PPB] = run;
+          sCarry[p * DK + c] = run;
+          run += v[p];
         }
+        bnd[4] = run;
+#pragma unroll
+        for (int x = 0; x < 5; ++x) sBnd[x * DK + c] = bnd[x];
+        reinterpret_cast<float*>(rec + R::P)[c] = exp2f(run);
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+#pragma unroll
+          for (int y = x + 1; y <= 4; ++y) sFt[ft_index(x, y) * DK + c] = ex2(bnd[y] - bnd[x]);
+      }
+      __syncthreads();
+      {
+        // G relative to the start of this thread's sub-block
+        float off[8], b0[8];
+        ld8(sCarry + part * DK + col, off);
+        ld8(sBnd + blk * DK + col, b0);
 #pragma unroll
         for (int i = 0; i < TPP; ++i)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) G[i][e] += off[e];
-        if (part == 0) {
-          float4* b0 = reinterpret_cast<float4*>(sBnd + 8 * oct);
-          b0[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-          b0[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        if (((part + 1) * TPP) % 16 == 0) {  // this part ends a sub-block: publish its boundary
-          const int kb = ((part + 1) * TPP) >> 4;
-          float4* bw = reinterpret_cast<float4*>(sBnd + kb * DK + 8 * oct);
-          bw[0] = make_float4(G[TPP - 1][0], G[TPP - 1][1], G[TPP - 1][2], G[TPP - 1][3]);
-          bw[1] = make_float4(G[TPP - 1][4], G[TPP - 1][5], G[TPP - 1][6], G[TPP - 1][7]);
-          if (kb == 4) {  // the chunk's state decay e^{G_C}
-            float4* pw = reinterpret_cast<float4*>(rec + R::P + 32 * oct);
-            pw[0] = make_float4(exp2f(G[TPP - 1][0]), exp2f(G[TPP - 1][1]), exp2f(G[TPP - 1][2]),
-                                exp2f(G[TPP - 1][3]));
-            pw[1] = make_float4(exp2f(G[TPP - 1][4]), exp2f(G[TPP - 1][5]), exp2f(G[TPP - 1][6]),
-                                exp2f(G[TPP - 1][7]));
-          }
-        }
+          for (int e = 0; e < 8; ++e) G[i][e] += off[e] - b0[e];
       }
+      // the previous item's bulk copies must have read their staging tiles (which
+      // the build overwrites); the scan partials share memory with X
+      if (tid == 0) bulk_wait_read0();
       __syncthreads();
 
       // ================= build: operand tiles =================
+      // Rows use the reference G at the start of sub-block blk: X = k e^{G - bnd[blk]},
+      // and K+ = X 2^{bnd[blk]}.  Column version J >= blk uses the reference at the
+      // start of sub-block J: k e^{bnd[J] - G}.  K_end = k e^{G_C - G}.
       {
-        // per-channel factors of sub-block blk (log2 units): bl = G before the
-        // block, en = G at its end, pe = G at the chunk end.  fbl = 2^bl,
-        // hI = 2^(en - bl), hk = hI 2^(pe - en), f2 / f3 = 2^(G at the start of
-        // block blk+2 / blk+3 - en).
-        float fbl[8], hI[8], hk[8], f2[8], f3[8];
+        float fbl[8];
+        if (blk > 0) {
+          ld8(sFt + ft_index(0, blk) * DK + col, fbl);
+        } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int c = 8 * oct + e;
-          const float bl = sBnd[blk * DK + c];
-          const float en = sBnd[(blk + 1) * DK + c];
-          fbl[e] = ex2(bl);
-          hI[e] = ex2(en - bl);
-          hk[e] = hI[e] * ex2(sBnd[4 * DK + c] - en);
-          f2[e] = blk + 2 <= 3 ? ex2(sBnd[min(blk + 2, 4) * DK + c] - en) : 0.f;
-          f3[e] = blk + 3 <= 3 ? ex2(sBnd[min(blk + 3, 4) * DK + c] - en) : 0.f;
-#pragma unroll
-          for (int i = 0; i < TPP; ++i) G[i][e] -= bl;  // G now relative to the block start
+          for (int e = 0; e < 8; ++e) fbl[e] = 1.f;
         }
-        const int col = 8 * oct;
-        auto pack8 = [&](const float* x) {
-          return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-                            pack_bf16(x[6], x[7]));
-        };
-        auto st8 = [&](uint32_t addr, const float* x) {
-          const uint4 u = pack8(x);
-          st_shared_v4(addr, u.x, u.y, u.z, u.w);
-        };
-        // K_end^T is stored K-major ([channel][token]): this thread's 8 x TPP block,
-        // packed in token pairs, is written once after the token loop
-        uint32_t ket[8][TPP / 2];
-        float ke_even[8];
+        // q rows: Gram rows 64.. and Q+ (record)
 #pragma unroll
         for (int i = 0; i < TPP; ++i) {
           const int t = part * TPP + i;
-          const uint32_t kw[4] = {rk[i].x, rk[i].y, rk[i].z, rk[i].w};
-          const uint32_t qw[4] = {rq[i].x, rq[i].y, rq[i].z, rq[i].w};
-          float av[8], ia[8], x[8];
+          float x[8];
+          bf16x8(rq[i], x);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            av[e] = ex2(G[i][e]);
-            ia[e] = ex2(-G[i][e]);
-          }
-          // Gram rows (block-local) and K+ = K e^{G}
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = ((e & 1) ? bf_hi(kw[e >> 1]) : bf_lo(kw[e >> 1])) * av[e];
-          st8(sbase + L::X + sw128(t, col, 128), x);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] *= fbl[e];
-          st8(sbase + L::KP + sw128(t, col, 64), x);
-          // Gram rows of q and Q+ = Q e^{G} (record)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = ((e & 1) ? bf_hi(qw[e >> 1]) : bf_lo(qw[e >> 1])) * av[e];
+          for (int e = 0; e < 8; ++e) x[e] *= ex2(G[i][e]);
           st8(sbase + L::X + sw128(64 + t, col, 128), x);
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] *= fbl[e];
           *reinterpret_cast<uint4*>(rec + R::WQ + sw128(64 + t, col, 128)) = pack8(x);
-          // column versions: own block k e^{-G}; later blocks k e^{en - G} (x f2, f3); and K_end
-          float y[8];
+        }
+        // k rows and K+; y = k e^{bnd[blk] - G} is kept for the column versions and K_end
+        float y[TPP][8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = ((e & 1) ? bf_hi(kw[e >> 1]) : bf_lo(kw[e >> 1])) * ia[e];
+        for (int i = 0; i < TPP; ++i) {
+          const int t = part * TPP + i;
+          float kv[8], x[8];
+          bf16x8(rk[i], kv);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float ke = y[e] * hk[e];
-            if (i & 1)
-              ket[e][i >> 1] = pack_bf16(ke_even[e], ke);
-            else
-              ke_even[e] = ke;
+          for (int e = 0; e < 8; ++e) x[e] = kv[e] * ex2(G[i][e]);
+          st8(sbase + L::X + sw128(t, col, 128), x);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] *= fbl[e];
+          st8(sbase + L::KP + sw128(t, col, 64), x);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[i][e] = kv[e] * ex2(-G[i][e]);
+        }
+        // column version J >= blk: y 2^{bnd[J] - bnd[blk]}
+#pragma unroll
+        for (int J = 0; J < 4; ++J) {
+          if (J < blk) continue;
+          float f[8];
+          if (J > blk) {
+            ld8(sFt + ft_index(blk, J) * DK + col, f);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = 1.f;
           }
 #pragma unroll
-          for (int J = 0; J < 4; ++J) {
-            if (J < blk) continue;
-            const uint32_t addr = sbase + L::Y + yoff_rows(J) * DK * 2 + sw128(t, col, yrows(J));
-            if (J == blk) {
-              st8(addr, y);
-            } else {
+          for (int i = 0; i < TPP; ++i) {
+            float x[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                x[e] = y[e] * hI[e] * (J == blk + 1 ? 1.f : (J == blk + 2 ? f2[e] : f3[e]));
-              st8(addr, x);
-            }
+            for (int e = 0; e < 8; ++e) x[e] = y[i][e] * f[e];
+            st8(sbase + L::Y + yoff_rows(J) * DK * 2 + sw128(part * TPP + i, col, yrows(J)), x);
           }
         }
+        // K_end = y 2^{bnd[4] - bnd[blk]} (record, token rows)
+        {
+          float f[8];
+          ld8(sFt + ft_index(blk, 4) * DK + col, f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          unsigned char* dst = rec + R::KE + sw128(col + e, part * TPP, DK);
-          if constexpr (TPP == 8)
-            *reinterpret_cast<uint4*>(dst) = make_uint4(ket[e][0], ket[e][1], ket[e][2], ket[e][3]);
-          else
-            *reinterpret_cast<uint2*>(dst) = make_uint2(ket[e][0], ket[e][1]);
+          for (int i = 0; i < TPP; ++i) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = y[i][e] * f[e];
+            *reinterpret_cast<uint4*>(rec + R::KE + sw128(part * TPP + i, col, 64)) = pack8(x);
+          }
         }
       }
       fence_async_smem();
@@ -480,128 +521,115 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
       load_kq(nxt);
       wait_mma(ctx);
 
-      // ---- Gram epilogue: lane i < 64 -> row i of L (fp32); lane 64 + i -> row i of A_Q ----
+      // ---- Gram epilogue: TMEM lane r < 64 -> row r of L (fp32); lane 64 + r -> row r of A_Q ----
+      // Warp w reads lane quarter w & 3 and the column version b of one of its two
+      // row blocks (warps 4-7 take the second).
       {
-        const int i = tid & 63;
+        const int quarter = warp & 3;
+        const int i = (32 * quarter + lane) & 63;
         const int myblk = i >> 4;
-        const int b0 = (warp & 1) * 2;  // this warp's lanes fall in row blocks b0, b0 + 1
+        const int b = (quarter & 1) * 2 + (warp >> 2);
+        for (int pc = 0; pc <= b; ++pc) {  // 16-column pieces of version b
+          float v[16];
+          tmem_ld16(tmem + lane_base + yoff_rows(b) + 16 * pc, v);
+          if (myblk == b) {
+            const int j0 = 16 * pc;
+            if (quarter < 2) {
+              const float bi = sBeta[i];
 #pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          const int b = b0 + bb;
-          for (int pc = 0; pc <= b; ++pc) {  // 16-column pieces of version b
-            float v[16];
-            tmem_ld16(tmem + lane_base + yoff_rows(b) + 16 * pc, v);
-            if (myblk == b) {
-              const int j0 = 16 * pc;
-              if (tid < 64) {
-                const float bi = sBeta[i];
+              for (int u = 0; u < 4; ++u) {
+                float4 f;
+                f.x = (j0 + 4 * u + 0 < i) ? bi * v[4 * u + 0] : 0.f;
+                f.y = (j0 + 4 * u + 1 < i) ? bi * v[4 * u + 1] : 0.f;
+                f.z = (j0 + 4 * u + 2 < i) ? bi * v[4 * u + 2] : 0.f;
+                f.w = (j0 + 4 * u + 3 < i) ? bi * v[4 * u + 3] : 0.f;
+                *reinterpret_cast<float4*>(sL + i * L::kLd + j0 + 4 * u) = f;
+              }
+            } else {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  float4 f;
-                  f.x = (j0 + 4 * u + 0 < i) ? bi * v[4 * u + 0] : 0.f;
-                  f.y = (j0 + 4 * u + 1 < i) ? bi * v[4 * u + 1] : 0.f;
-                  f.z = (j0 + 4 * u + 2 < i) ? bi * v[4 * u + 2] : 0.f;
-                  f.w = (j0 + 4 * u + 3 < i) ? bi * v[4 * u + 3] : 0.f;
-                  *reinterpret_cast<float4*>(sL + i * L::kLd + j0 + 4 * u) = f;
-                }
-              } else {
+              for (int u = 0; u < 2; ++u) {
+                float x[8];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                  float x[8];
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) x[e] = (j0 + 8 * u + e <= i) ? v[8 * u + e] : 0.f;
-                  *reinterpret_cast<uint4*>(rec + R::AQ + sw128(i, j0 + 8 * u, 64)) =
-                      make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-                                 pack_bf16(x[6], x[7]));
-                }
+                for (int e = 0; e < 8; ++e) x[e] = (j0 + 8 * u + e <= i) ? v[8 * u + e] : 0.f;
+                st8(sbase + L::AQS + sw128(i, j0 + 8 * u, 64), x);
               }
             }
           }
         }
-        if (tid >= 64) {  // A_Q columns past this row's sub-block are zero
+        if (quarter >= 2 && myblk == b) {  // A_Q columns past this row's sub-block are zero
           for (int j0 = 16 * (myblk + 1); j0 < 64; j0 += 8)
-            *reinterpret_cast<uint4*>(rec + R::AQ + sw128(i, j0, 64)) = make_uint4(0, 0, 0, 0);
+            st_shared_v4(sbase + L::AQS + sw128(i, j0, 64), 0u, 0u, 0u, 0u);
         }
+        fence_async_smem();
       }
       __syncthreads();
+      if (tid == 0) bulk_s2g(rec + R::AQ, sbase + L::AQS, 64 * 64 * 2);
 
       // ================= T = (I + L)^-1 (fp32) =================
-      if (tid < 64) {  // diagonal 16 x 16 blocks, one column per thread
+      if (tid < 64) {  // diagonal 16 x 16 blocks by substitution, one column per thread
         const int I = tid >> 4, cc = tid & 15;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-          float s = (r == cc) ? 1.f : 0.f;
+          float s0 = (r == cc) ? 1.f : 0.f, s1 = 0.f;
           if (r > cc) {
 #pragma unroll
-            for (int m = 0; m < r; ++m) s -= sL[(16 * I + r) * L::kLd + 16 * I + m] * x[m];
+            for (int m = 0; m < r; m += 2) {
+              s0 -= sL[(16 * I + r) * L::kLd + 16 * I + m] * x[m];
+              if (m + 1 < r) s1 -= sL[(16 * I + r) * L::kLd + 16 * I + m + 1] * x[m + 1];
+            }
           }
-          x[r] = (r >= cc) ? s : 0.f;
+          x[r] = (r >= cc) ? s0 + s1 : 0.f;
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) sT[(16 * I + r) * L::kTd + 16 * I + cc] = x[r];
       }
       __syncthreads();
-      // block rows I = 1..3 on the warp-level tensor cores (tf32, fp32 accumulate):
-      //   R = L[I, 0:16I] T[0:16I, 0:16I] ;  T[I, 0:16I] = -T_II R
-      // Each warp owns whole 8-column tiles, so R stays within the warp.
-      {
-        const int gq = lane >> 2, tq = lane & 3;
-#pragma unroll
-        for (int I = 1; I < 4; ++I) {
-          for (int nt = warp; nt < 2 * I; nt += 4) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int ks = 2 * (nt >> 1); ks < 2 * I; ++ks) {
-              const int k0 = 8 * ks;
-              const float* l0 = sL + (16 * I + gq) * L::kLd + k0 + tq;
-              const float* l1 = l0 + 8 * L::kLd;
-              const uint32_t af[4] = {to_tf32(l0[0]), to_tf32(l1[0]), to_tf32(l0[4]), to_tf32(l1[4])};
-              const uint32_t bf[2] = {to_tf32(sT[(k0 + tq) * L::kTd + 8 * nt + gq]),
-                                      to_tf32(sT[(k0 + tq + 4) * L::kTd + 8 * nt + gq])};
-              mma_tf32(acc, af, bf);
-            }
-            sR[gq * L::kRd + 8 * nt + 2 * tq] = acc[0];
-            sR[gq * L::kRd + 8 * nt + 2 * tq + 1] = acc[1];
-            sR[(gq + 8) * L::kRd + 8 * nt + 2 * tq] = acc[2];
-            sR[(gq + 8) * L::kRd + 8 * nt + 2 * tq + 1] = acc[3];
-            __syncwarp();
-            float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-              const int k0 = 8 * ks;
-              const float* t0 = sT + (16 * I + gq) * L::kTd + 16 * I + k0 + tq;
-              const float* t1 = t0 + 8 * L::kTd;
-              const uint32_t af[4] = {to_tf32(t0[0]), to_tf32(t1[0]), to_tf32(t0[4]), to_tf32(t1[4])};
-              const uint32_t bf[2] = {to_tf32(sR[(k0 + tq) * L::kRd + 8 * nt + gq]),
-                                      to_tf32(sR[(k0 + tq + 4) * L::kRd + 8 * nt + gq])};
-              mma_tf32(acc2, af, bf);
-            }
-            float* d0 = sT + (16 * I + gq) * L::kTd + 8 * nt + 2 * tq;
-            float* d1 = d0 + 8 * L::kTd;
-            d0[0] = -acc2[0];
-            d0[1] = -acc2[1];
-            d1[0] = -acc2[2];
-            d1[1] = -acc2[3];
-          }
-          __syncthreads();
-        }
+      // Off-diagonal blocks by doubling, on the warp-level tensor cores (tf32):
+      //   16 -> 32:  T[2p+1, 2p] = -D_{2p+1} (L[2p+1, 2p] D_{2p})        (p = 0, 1)
+      //   32 -> 64:  T[B, A] = -T_BB (L_BA T_AA),  A = rows 0-31, B = rows 32-63
+      // Blocks of T above the diagonal are never read (they hold stale values).
+      if (warp < 4) {  // R_p = L[2p+1, 2p] D_{2p}: 16 x 16, two column tiles each
+        const int p = warp >> 1, nt = warp & 1;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        warp_tile_tf32(acc, sL + (32 * p + 16) * L::kLd + 32 * p, L::kLd, sT + (32 * p) * L::kTd + 32 * p + 8 * nt,
+                       L::kTd, 0, 16, lane);
+        warp_tile_store(acc, sR + (16 * p) * L::kRd + 8 * nt, L::kRd, 1.f, lane);
       }
-      // T_beta = T Diag(beta) -> bf16 K-major [i][j], into shared memory and the record
+      __syncthreads();
+      if (warp < 4) {  // T[2p+1, 2p] = -D_{2p+1} R_p
+        const int p = warp >> 1, nt = warp & 1;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        warp_tile_tf32(acc, sT + (32 * p + 16) * L::kTd + 32 * p + 16, L::kTd, sR + (16 * p) * L::kRd + 8 * nt,
+                       L::kRd, 0, 16, lane);
+        warp_tile_store(acc, sT + (32 * p + 16) * L::kTd + 32 * p + 8 * nt, L::kTd, -1.f, lane);
+      }
+      __syncthreads();
+      {  // X = L_BA T_AA (32 x 32): warp -> row tile mt, column tile nt; T_AA is block lower triangular
+        const int mt = warp >> 2, nt = warp & 3;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        warp_tile_tf32(acc, sL + (32 + 16 * mt) * L::kLd, L::kLd, sT + 8 * nt, L::kTd, nt >= 2 ? 16 : 0, 32, lane);
+        warp_tile_store(acc, sR + (16 * mt) * L::kRd + 8 * nt, L::kRd, 1.f, lane);
+      }
+      __syncthreads();
+      {  // T_BA = -T_BB X: T_BB is block lower triangular
+        const int mt = warp >> 2, nt = warp & 3;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        warp_tile_tf32(acc, sT + (32 + 16 * mt) * L::kTd + 32, L::kTd, sR + 8 * nt, L::kRd, 0, 16 * (mt + 1), lane);
+        warp_tile_store(acc, sT + (32 + 16 * mt) * L::kTd + 8 * nt, L::kTd, -1.f, lane);
+      }
+      __syncthreads();
+      // T_beta = T Diag(beta) -> bf16 K-major [i][j] in shared memory (and the record, by bulk copy)
       {
-        const int i = tid >> 1, j0 = 32 * (tid & 1);
+        const int i = tid >> 2, j0 = 16 * (tid & 3);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint32_t wv[4];
+        for (int u = 0; u < 2; ++u) {
+          float tv[8], bv[8], x[8];
+          ld8(sT + i * L::kTd + j0 + 8 * u, tv);
+          ld8(sBeta + j0 + 8 * u, bv);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int ja = j0 + 8 * u + 2 * e, jb = ja + 1;
-            const float xa = (ja <= i) ? sT[i * L::kTd + ja] * sBeta[ja] : 0.f;
-            const float xb = (jb <= i) ? sT[i * L::kTd + jb] * sBeta[jb] : 0.f;
-            wv[e] = pack_bf16(xa, xb);
-          }
-          const uint32_t off = sw128(i, j0 + 8 * u, 64);
-          st_shared_v4(sbase + L::T2 + off, wv[0], wv[1], wv[2], wv[3]);
-          *reinterpret_cast<uint4*>(rec + R::T2 + off) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          for (int e = 0; e < 8; ++e) x[e] = (j0 + 8 * u + e <= i) ? tv[e] * bv[e] : 0.f;
+          st8(sbase + L::T2 + sw128(i, j0 + 8 * u, 64), x);
         }
       }
       fence_async_smem();
@@ -616,24 +644,38 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
           mma_bf16(tmem, desc_kmajor(sbase + L::T2, 64, ks), desc_mnmajor(sbase + L::KP, 64, ks),
                    idesc_bf16(128, DK, false, true), ks > 0);
         mma_commit(ctx.mbar);
+        bulk_s2g(rec + R::T2, sbase + L::T2, 64 * 64 * 2);
       }
       load_g(nxt);
       wait_mma(ctx);
-      // ---- -W -> record (bf16 K-major rows 0..63) ----
-      if (tid < 64) {
+      // ---- -W (bf16, rows 0..63 of the [-W ; Q+] tile) staged over K+ (free once W is
+      // done), then one bulk copy per 64-column panel.  Lane quarters 0-1; warps 4-5
+      // take the upper columns. ----
+      if ((warp & 3) < 2) {
+        const int r = 32 * (warp & 3) + lane;
+        const int c_lo = (warp >> 2) * (DK / 2);
 #pragma unroll
-        for (int c0 = 0; c0 < DK; c0 += 32) {
+        for (int c0 = c_lo; c0 < c_lo + DK / 2; c0 += 32) {
           float v[32];
           tmem_ld32(tmem + lane_base + c0, v);
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint4*>(rec + R::WQ + sw128(tid, c0 + 8 * u, 128)) =
-                make_uint4(pack_bf16(-v[8 * u], -v[8 * u + 1]), pack_bf16(-v[8 * u + 2], -v[8 * u + 3]),
-                           pack_bf16(-v[8 * u + 4], -v[8 * u + 5]), pack_bf16(-v[8 * u + 6], -v[8 * u + 7]));
+          for (int u = 0; u < 4; ++u) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = -v[8 * u + e];
+            st8(sbase + L::KP + sw128(r, c0 + 8 * u, 64), x);
+          }
         }
+        fence_async_smem();
       }
       fence_before_sync();
       __syncthreads();
+      if (tid == 0) {
+#pragma unroll
+        for (int pn = 0; pn < DK / 64; ++pn)  // panel pn: 64 rows x 128 B, at pn * 128 rows in the record
+          bulk_s2g(rec + R::WQ + pn * 128 * 128, sbase + L::KP + pn * 64 * 128, 64 * 128);
+        bulk_commit();
+      }
       if (*sFlag) break;
     } else {
       load_kq(nxt);
@@ -641,6 +683,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
     }
     cur = nxt;
   }
+  if (tid == 0) bulk_wait0();  // this CTA's record writes are complete
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, L::kTmemCols);
@@ -807,8 +850,8 @@ __global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(Pre
         fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tS, desc_kmajor(rKE, DK, ks), desc_mnmajor(vt, 64, ks),
-                   idesc_bf16(128, DV, false, true), 1u);
+          mma_bf16(tS, desc_mnmajor(rKE, 64, ks), desc_mnmajor(vt, 64, ks),
+                   idesc_bf16(128, DV, true, true), 1u);
         mma_commit(mbar_s);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
