@@ -690,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
 }
 
 // ---------------------------------------------------------------------------
-// serial: one (sequence, head) per CTA, fp32 state in TMEM.
+// serial: one (sequence, head, value-column slice) per CTA, fp32 state in TMEM.
 // Warps 0-3 move data between TMEM and shared / global memory, warp 4 issues the
 // tensor-core products, warp 5 loads chunk records (bulk copy) and V (cp.async);
 // both kinds of copy complete on the record buffer's mbarrier.  Hand-offs:
@@ -726,14 +726,22 @@ __global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(Pre
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-  const int n = blockIdx.x / a.H;
-  const int h = blockIdx.x - n * a.H;
+  // CTA -> (sequence n, head h, column slice sl): the state's columns evolve
+  // independently, so a CTA may own DV of the head's a.dv value columns
+  const int nsl = a.dv / DV;
+  const int sl = blockIdx.x % nsl;
+  const int nh = blockIdx.x / nsl;
+  const int n = nh / a.H;
+  const int h = nh - n * a.H;
+  const int v0 = sl * DV;  // first value column of this CTA
   const Range rg = seq_range(a, n);
   const int nch = min(num_chunks(sp, n), (rg.len + kC - 1) / kC);
   const int64_t rec0 = (int64_t)first_chunk(sp, n) * a.H + h;  // record of chunk ci: rec0 + ci * H
 
-  const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(a.v.ptr) + rg.brow * a.v.sb + rg.tok0 * a.v.st + h * a.v.sh;
-  __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + rg.brow * a.out_sb + rg.tok0 * a.out_st + h * a.out_sh;
+  const __nv_bfloat16* vg =
+      static_cast<const __nv_bfloat16*>(a.v.ptr) + rg.brow * a.v.sb + rg.tok0 * a.v.st + h * a.v.sh + v0;
+  __nv_bfloat16* og =
+      static_cast<__nv_bfloat16*>(a.out) + rg.brow * a.out_sb + rg.tok0 * a.out_st + h * a.out_sh + v0;
 
   if (tid == 0) {
     mbar_init(mbar_a, 1);
@@ -768,7 +776,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(Pre
   };
 
   if (tid < DK) {  // lane c holds state row c: TMEM <- S0, shared <- bf16(S0)
-    const float* s0 = a.s0 ? a.s0 + n * a.s0_sn + h * a.s0_sh + (int64_t)tid * DV : nullptr;
+    const float* s0 = a.s0 ? a.s0 + n * a.s0_sn + h * a.s0_sh + (int64_t)tid * a.dv + v0 : nullptr;
 #pragma unroll
     for (int c0 = 0; c0 < DV; c0 += 32) {
       float v[32];
@@ -976,7 +984,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(Pre
       }
     }
     if (a.sT && tid < DK) {
-      float* dst = a.sT + n * a.sT_sn + h * a.sT_sh + (int64_t)tid * DV;
+      float* dst = a.sT + n * a.sT_sn + h * a.sT_sh + (int64_t)tid * a.dv + v0;
 #pragma unroll
       for (int c0 = 0; c0 < DV; c0 += 32) {
         float v[32];
@@ -1064,8 +1072,14 @@ cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
   auto prep = kda_chunk_prep_kernel<DK>;
   e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, PrepSmem<DK>::kAlloc);
   if (e != cudaSuccess) return e;
-  auto ser = kda_chunk_serial_kernel<DK, DV>;
-  e = cudaFuncSetAttribute(ser, cudaFuncAttributeMaxDynamicSharedMemorySize, SerialSmem<DK, DV>::kAlloc);
+  // Few chains (sequence-heads): split d_v = 128 into two 64-column CTAs so more SMs
+  // carry the serial loop.  Each slice CTA reads the whole chunk record.
+  constexpr int DVS = DV == 128 ? 64 : DV;
+  const bool split = DVS != DV && (int64_t)a.N * a.H * (DV / DVS) <= sm_count();
+  auto ser = split ? kda_chunk_serial_kernel<DK, DVS> : kda_chunk_serial_kernel<DK, DV>;
+  const int ser_smem = split ? SerialSmem<DK, DVS>::kAlloc : SerialSmem<DK, DV>::kAlloc;
+  const unsigned ser_grid = (unsigned)(a.N * a.H * (split ? DV / DVS : 1));
+  e = cudaFuncSetAttribute(ser, cudaFuncAttributeMaxDynamicSharedMemorySize, ser_smem);
   if (e != cudaSuccess) return e;
   const int64_t items = total * a.H;
   const int grid = (int)(items < 2 * sm_count() ? items : 2 * sm_count());
@@ -1075,7 +1089,7 @@ cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   }
   launch_begin(s);
-  ser<<<dim3((unsigned)(a.N * a.H)), kSerialThreads, SerialSmem<DK, DV>::kAlloc, s>>>(a, sp);
+  ser<<<dim3(ser_grid), kSerialThreads, ser_smem, s>>>(a, sp);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_end(s);
 }
