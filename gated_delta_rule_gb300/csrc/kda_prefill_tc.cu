@@ -835,16 +835,21 @@ __global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(Pre
       const uint32_t rKE = rec + 2 * kT2 + (R::KE - kT2);
       const uint32_t vt = sbase + L::VT + b * 64 * DV * 2;
       wait(mbar_rec0 + 8 * b, (ci >> 1) & 1);
-      bar_sync(1, 160);
       // U/O buffer b was last used by chunk ci - 2: its output must have been read out
       if (ci >= 2) wait(mbar_orel0 + 8 * b, (uint32_t)(((ci - 2) >> 1) & 1));
-      // [U ; Q+ S] = [T_beta | -W ; 0 | Q+] [V ; S]
+      // [U ; Q+ S] = [T_beta | -W ; 0 | Q+] [V ; S]; the V half needs no state, so it
+      // is issued before the state's bf16 copy is ready
       if (lane == 0) {
         fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           mma_bf16(tX(b), desc_kmajor(rec, 64, ks), desc_mnmajor(vt, 64, ks),
                    idesc_bf16(128, DV, false, true), ks > 0);
+      }
+      __syncwarp();
+      bar_sync(1, 160);
+      if (lane == 0) {
+        fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < DK / 16; ++ks)
           mma_bf16(tX(b), desc_kmajor(rWQ, 128, ks), desc_mnmajor(sbase + L::SB, DK, ks),
