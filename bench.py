@@ -40,6 +40,7 @@ import kda_inputs as ki  # noqa: E402
 METRIC = "KDA prefill tokens/s & % bf16 TC roofline; decode steps/s & % HBM BW (1×GB300)"
 PREFILL_W = 1          # headline prefill workload
 K3_W = 2               # 96-head prefill, reported alongside
+VARLEN_W = 4           # 1M-token varlen prefill (16 sequences), reported alongside
 DECODE_W = 3
 L2_FLUSH_BYTES = 256 << 20
 SLEEP_CYCLES = 200_000  # about 0.1 ms at 2 GHz, spent before each timed step
@@ -76,9 +77,16 @@ def prefill_kernel_bytes(token_heads, dk, dv, n_states_read, n_states_written, i
             + 4 * dk * dv * (n_states_read + n_states_written)}
 
 
-# kernels of one kda_chunk_fwd call (bf16), in launch order
-CHUNK_KERNELS = ["kda_chunk_prep_kernel", "kda_chunk_serial_kernel"]
-CHUNK_KERNELS_VARLEN = ["kda_seqlens_kernel", "kda_chunk_offsets_kernel"] + CHUNK_KERNELS
+def chunk_kernels(varlen, count):
+    """Kernels of one bf16 kda_chunk_fwd call, in launch order, from how many it
+    launched: [cu_seqlens check, chunk offsets,] prep, serial pass 0[, segment
+    combine][, serial pass 1] (the last two only when some sequence is longer
+    than one 512-chunk segment)."""
+    head = ["kda_seqlens_kernel", "kda_chunk_offsets_kernel"] if varlen else []
+    rest = count - len(head)
+    tail = {2: [], 3: ["kda_chunk_serial_kernel_pass1"],
+            4: ["kda_segment_combine_kernel", "kda_chunk_serial_kernel_pass1"]}[rest]
+    return head + ["kda_chunk_prep_kernel", "kda_chunk_serial_kernel"] + tail
 
 
 def decode_bytes(NH, dk, dv, in_bytes=2):
@@ -300,7 +308,9 @@ def bench_prefill(kda, idx, steps, warmup, flush, stream, clk=None, world=1):
             step()
             flush.zero_()
     stream.synchronize()
-    names = CHUNK_KERNELS if t["cu_seqlens"] is None else CHUNK_KERNELS_VARLEN
+    step()
+    stream.synchronize()
+    names = chunk_kernels(t["cu_seqlens"] is not None, kda.kda_last_launch_count())
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
@@ -331,8 +341,9 @@ def bench_prefill(kda, idx, steps, warmup, flush, stream, clk=None, world=1):
     ms = [e0.elapsed_time(e1) for e0, e1 in evs]
     if launches != steps * len(names):
         raise RuntimeError(f"expected {len(names)} kernels per step, counted {launches / steps}")
-    kernel_ms = {n: statistics.mean(ke[i].elapsed_time(ke[i + 1]) for ke in kev)
-                 for i, n in enumerate(names)}
+    kernel_ms = {}
+    for i, n in enumerate(names):
+        kernel_ms[n] = kernel_ms.get(n, 0.0) + statistics.mean(ke[i].elapsed_time(ke[i + 1]) for ke in kev)
     th = B * T * H if t["cu_seqlens"] is None else T * H
     n_read = N if t["initial_state"] is not None else 0
     return dict(ms=ms, token_heads=th, tokens=B * T, dk=dk, dv=dv, H=H,
@@ -516,6 +527,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-k3", action="store_true")
+    ap.add_argument("--no-varlen", action="store_true")
     ap.add_argument("--ncu-case", choices=["prefill", "prefill96", "decode32", "decode"],
                     help="run two untimed launches of one workload (for ncu captures) and exit")
     args = ap.parse_args()
@@ -587,6 +599,18 @@ def main():
                                  k3["bytes"] / (pk["hbm"] * 1e9)) / (kms * 1e-3),
             "clocks": clk_k3.summary(), "gpu_launches": k3["launches"]}
         del k3
+
+    if not args.no_varlen:
+        clk_vl = ClockSampler(local)
+        vl = bench_prefill(kda, VARLEN_W, 3, 3, flush, stream, clk_vl, world)
+        vms = max_over_ranks(statistics.mean(vl["ms"]), world)
+        extra["prefill_varlen_1M"] = {
+            "workload": vl["name"], "ms_per_step": vms,
+            "kernel_ms": {n: max_over_ranks(v, world) for n, v in vl["kernel_ms"].items()},
+            "tokens_per_s": world * vl["tokens"] / (vms * 1e-3),
+            "hbm_frac": vl["bytes"] / (vms * 1e-3) / 1e9 / pk["hbm"],
+            "clocks": clk_vl.summary(), "gpu_launches": vl["launches"]}
+        del vl
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,

@@ -161,6 +161,43 @@ __device__ __forceinline__ int num_chunks(const Split& sp, int n) {
   return sp.off ? __ldg(sp.off + n + 1) - __ldg(sp.off + n) : sp.nck;
 }
 
+// Segment split of long sequences.  A sequence of more than kSegChunks chunks is
+// cut into segments of kSegChunks chunks counted from its start (so the cut
+// depends on the sequence alone).  Segment 0 runs from the initial state.  Each
+// later ("tail") segment s first runs from zero on the augmented state
+// [S~ | M], which starts as [0 | I] with values [V | 0]: M then equals the
+// product of the chunk transitions Diag(e^{G_C}) - K_end^T W over the segment
+// and S~ the segment's result from a zero state.  The states entering the tail
+// segments follow in order, S_in(s + 1) = M_s S_in(s) + S~_s, and a second
+// pass reruns the tail segments from them, writing their outputs.
+constexpr int kSegChunks = 512;
+
+struct Seg {
+  float* tr;        // [tail unit][H][DK][dv + DK] fp32: (S~ | M) of each tail segment
+  float* sin;       // [tail unit][H][DK][dv] fp32: state entering each tail segment
+  const int* soff;  // tail segments before sequence n ([N + 1]); null for fixed length
+  int ntail;        // tail units allocated
+  int tps;          // tail segments per sequence (fixed length)
+};
+
+__host__ __device__ __forceinline__ int num_segments(int nc) {
+  return nc > kSegChunks ? (nc + kSegChunks - 1) / kSegChunks : 1;
+}
+__device__ __forceinline__ int tail_first(const Seg& sg, int n) { return sg.soff ? __ldg(sg.soff + n) : n * sg.tps; }
+__device__ __forceinline__ int tail_count(const Seg& sg, int N) {
+  return sg.soff ? min(__ldg(sg.soff + N), sg.ntail) : N * sg.tps;
+}
+// sequence of tail unit u (u < tail_count)
+__device__ __forceinline__ int tail_seq(const Seg& sg, int N, int u) {
+  if (!sg.soff) return u / sg.tps;
+  int lo = 0, hi = N - 1;  // largest n with soff[n] <= u
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(sg.soff + mid) <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 struct Ctx {
   uint32_t mbar;
   uint32_t phase;
@@ -707,8 +744,98 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
 //                waiter can fall two phases behind.
 constexpr int kSerialThreads = 192;
 
+// What one serial CTA computes: DV columns of one (sequence, head) state over the
+// chunk range [c0, c1) of the sequence.
+struct Unit {
+  int n, h;
+  int c0, c1;
+  int kind;            // 0: value columns (outputs); 1: tail pass 1, S~ columns; 2: tail pass 1, M columns
+  int col;             // first value column (kinds 0 and 1)
+  int m0;              // first M column (kind 2)
+  const float* init;   // initial state rows, row stride init_ld; null = zero (kinds 0, 1)
+  int64_t init_ld;
+  float* fin;          // where the final state rows go (row stride fin_ld), or null
+  int64_t fin_ld;
+  int fin_cols;        // columns of fin to write
+};
+
+// CTA -> unit.  pass 0: first the units of every sequence's first segment (value
+// column slices), then, per tail unit and head, slices of the DV + DK augmented
+// columns; pass 1: per tail unit and head, value column slices.  Returns false for
+// CTAs past the tail units in use.
 template <int DK, int DV>
-__global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(PrefillArgs a, Split sp) {
+__device__ __forceinline__ bool serial_unit(const PrefillArgs& a, const Split& sp, const Seg& sg, int pass, int bid,
+                                            Unit& u) {
+  const int nsl = a.dv / DV;  // value column slices per (sequence, head)
+  const int nfirst = a.N * a.H * nsl;
+  if (pass == 0 && bid < nfirst) {
+    const int sl = bid % nsl, nh = bid / nsl;
+    u.n = nh / a.H;
+    u.h = nh - u.n * a.H;
+    const Range rg = seq_range(a, u.n);
+    const int nc = min(num_chunks(sp, u.n), (rg.len + kC - 1) / kC);
+    u.c0 = 0;
+    u.c1 = min(nc, kSegChunks);
+    u.kind = 0;
+    u.col = sl * DV;
+    u.m0 = 0;
+    u.init = a.s0 ? a.s0 + u.n * a.s0_sn + u.h * a.s0_sh + u.col : nullptr;
+    u.init_ld = a.dv;
+    u.fin_ld = a.dv;
+    u.fin_cols = DV;
+    if (num_segments(nc) == 1) {
+      u.fin = a.sT ? a.sT + u.n * a.sT_sn + u.h * a.sT_sh + u.col : nullptr;
+    } else {
+      const int t = tail_first(sg, u.n);
+      u.fin = t < tail_count(sg, a.N) ? sg.sin + ((int64_t)t * a.H + u.h) * DK * a.dv + u.col : nullptr;
+    }
+    return true;
+  }
+  const int t = pass == 0 ? bid - nfirst : bid;
+  const int nx = pass == 0 ? (a.dv + DK + DV - 1) / DV : nsl;  // column slices of a tail unit
+  const int xs = t % nx, uh = t / nx;
+  u.h = uh % a.H;
+  const int ut = uh / a.H;
+  if (ut >= tail_count(sg, a.N)) return false;
+  u.n = tail_seq(sg, a.N, ut);
+  const Range rg = seq_range(a, u.n);
+  const int nc = min(num_chunks(sp, u.n), (rg.len + kC - 1) / kC);
+  const int sgi = ut - tail_first(sg, u.n) + 1;  // segment index (>= 1)
+  u.c0 = sgi * kSegChunks;
+  u.c1 = min(nc, u.c0 + kSegChunks);
+  u.m0 = 0;
+  if (pass == 0) {
+    const int x0 = xs * DV;
+    u.fin = sg.tr + ((int64_t)ut * a.H + u.h) * DK * (a.dv + DK) + x0;
+    u.fin_ld = a.dv + DK;
+    u.fin_cols = min(DV, a.dv + DK - x0);
+    u.init = nullptr;
+    u.init_ld = 0;
+    if (x0 < a.dv) {
+      u.kind = 1;
+      u.col = x0;
+    } else {
+      u.kind = 2;
+      u.col = 0;
+      u.m0 = x0 - a.dv;
+    }
+  } else {
+    u.kind = 0;
+    u.col = xs * DV;
+    u.init = sg.sin + ((int64_t)ut * a.H + u.h) * DK * a.dv + u.col;
+    u.init_ld = a.dv;
+    u.fin = (sgi == num_segments(nc) - 1 && a.sT) ? a.sT + u.n * a.sT_sn + u.h * a.sT_sh + u.col : nullptr;
+    u.fin_ld = a.dv;
+    u.fin_cols = DV;
+  }
+  return true;
+}
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(kSerialThreads, 1)
+    kda_chunk_serial_kernel(PrefillArgs a, Split sp, Seg sg, int pass) {
+  Unit un;
+  if (!serial_unit<DK, DV>(a, sp, sg, pass, blockIdx.x, un)) return;  // CTA-uniform
   using L = SerialSmem<DK, DV>;
   using R = Rec<DK>;
   extern __shared__ unsigned char smem_raw[];
@@ -726,22 +853,21 @@ __global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(Pre
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-  // CTA -> (sequence n, head h, column slice sl): the state's columns evolve
-  // independently, so a CTA may own DV of the head's a.dv value columns
-  const int nsl = a.dv / DV;
-  const int sl = blockIdx.x % nsl;
-  const int nh = blockIdx.x / nsl;
-  const int n = nh / a.H;
-  const int h = nh - n * a.H;
-  const int v0 = sl * DV;  // first value column of this CTA
+  // The state's columns evolve independently, so a CTA owns DV columns of one
+  // (sequence, head) state over a range of its chunks.
+  const int n = un.n, h = un.h;
   const Range rg = seq_range(a, n);
-  const int nch = min(num_chunks(sp, n), (rg.len + kC - 1) / kC);
-  const int64_t rec0 = (int64_t)first_chunk(sp, n) * a.H + h;  // record of chunk ci: rec0 + ci * H
+  const int c0 = un.c0;         // chunk ci of this CTA is chunk c0 + ci of the sequence
+  const int nch = un.c1 - un.c0;
+  const bool vzero = un.kind == 2;  // M columns: no values
+  const bool outs = un.kind == 0;
+  // record of the sequence's chunk c: rec0 + c * H
+  const int64_t rec0 = (int64_t)first_chunk(sp, n) * a.H + h;
 
   const __nv_bfloat16* vg =
-      static_cast<const __nv_bfloat16*>(a.v.ptr) + rg.brow * a.v.sb + rg.tok0 * a.v.st + h * a.v.sh + v0;
+      static_cast<const __nv_bfloat16*>(a.v.ptr) + rg.brow * a.v.sb + rg.tok0 * a.v.st + h * a.v.sh + un.col;
   __nv_bfloat16* og =
-      static_cast<__nv_bfloat16*>(a.out) + rg.brow * a.out_sb + rg.tok0 * a.out_st + h * a.out_sh + v0;
+      static_cast<__nv_bfloat16*>(a.out) + rg.brow * a.out_sb + rg.tok0 * a.out_st + h * a.out_sh + un.col;
 
   if (tid == 0) {
     mbar_init(mbar_a, 1);
@@ -775,23 +901,28 @@ __global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(Pre
     fence_after_sync();
   };
 
-  if (tid < DK) {  // lane c holds state row c: TMEM <- S0, shared <- bf16(S0)
-    const float* s0 = a.s0 ? a.s0 + n * a.s0_sn + h * a.s0_sh + (int64_t)tid * a.dv + v0 : nullptr;
+  if (tid < DK) {  // lane c holds state row c: TMEM <- initial state, shared <- its bf16 copy
+    const float* s0 = un.init ? un.init + (int64_t)tid * un.init_ld : nullptr;
 #pragma unroll
-    for (int c0 = 0; c0 < DV; c0 += 32) {
+    for (int cb = 0; cb < DV; cb += 32) {
       float v[32];
+      if (un.kind == 2) {  // identity columns m0 .. m0 + DV - 1 of M (zero past DK)
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + c0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[i] = x.x;
-        v[i + 1] = x.y;
-        v[i + 2] = x.z;
-        v[i + 3] = x.w;
+        for (int i = 0; i < 32; ++i) v[i] = (tid == un.m0 + cb + i) ? 1.f : 0.f;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + cb + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[i] = x.x;
+          v[i + 1] = x.y;
+          v[i + 2] = x.z;
+          v[i + 3] = x.w;
+        }
       }
-      tmem_st32(tS + lane_base + c0, v);
+      tmem_st32(tS + lane_base + cb, v);
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        st_shared_v4(sbase + L::SB + sw128(tid, c0 + 8 * u, DK), pack_bf16(v[8 * u], v[8 * u + 1]),
+        st_shared_v4(sbase + L::SB + sw128(tid, cb + 8 * u, DK), pack_bf16(v[8 * u], v[8 * u + 1]),
                      pack_bf16(v[8 * u + 2], v[8 * u + 3]), pack_bf16(v[8 * u + 4], v[8 * u + 5]),
                      pack_bf16(v[8 * u + 6], v[8 * u + 7]));
     }
@@ -808,18 +939,18 @@ __global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(Pre
       const uint32_t dst = sbase + L::REC + b * L::kRecBuf;
       const uint32_t mb = mbar_rec0 + 8 * b;
       if (lane == 0) {
-        const unsigned char* src = sp.rec + (rec0 + (int64_t)ci * a.H) * R::kBytes;
+        const unsigned char* src = sp.rec + (rec0 + (int64_t)(c0 + ci) * a.H) * R::kBytes;
         mbar_arrive_expect_tx(mb, R::kBytes);
         bulk_g2s(dst, src, kT2, mb);
         bulk_g2s(dst + 2 * kT2, src + kT2, R::kBytes - kT2, mb);
       }
-      const int lc = min(kC, rg.len - ci * kC);
+      const int lc = vzero ? 0 : min(kC, rg.len - (c0 + ci) * kC);  // no values: zero fill
       constexpr int kVec = DV / 8;
 #pragma unroll 4
       for (int idx = lane; idx < 64 * kVec; idx += 32) {
         const int t = idx / kVec, cv = idx % kVec;
         const bool ok = t < lc;
-        const __nv_bfloat16* src = ok ? vg + ((int64_t)ci * kC + t) * a.v.st + 8 * cv : vg;
+        const __nv_bfloat16* src = ok ? vg + ((int64_t)(c0 + ci) * kC + t) * a.v.st + 8 * cv : vg;
         cp_async16(sbase + L::VT + b * 64 * DV * 2 + sw128(t, 8 * cv, 64), src, ok ? 16u : 0u);
       }
       cp_async_mbar_arrive(mb);
@@ -882,7 +1013,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(Pre
     // shared staging area so that every store instruction writes four whole
     // 128-byte lines.
     auto store_out = [&](int pc, bool release) {
-      const int lc = min(kC, rg.len - pc * kC);
+      const int lc = min(kC, rg.len - (c0 + pc) * kC);
       // 144-byte staging rows: consecutive rows start on different banks
       const uint32_t stage = sbase + L::OSTG + (warp - 2) * 32 * 144;
       uint32_t r[DV / 32][32];
@@ -914,7 +1045,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(Pre
                        : "r"(stage + rr * 144 + 16 * ch));
           const int t = row0 + rr;
           if (t < lc)
-            *reinterpret_cast<uint4*>(og + ((int64_t)pc * kC + t) * a.out_st + 64 * half + 8 * ch) = w;
+            *reinterpret_cast<uint4*>(og + ((int64_t)(c0 + pc) * kC + t) * a.out_st + 64 * half + 8 * ch) = w;
         }
       }
     };
@@ -977,26 +1108,33 @@ __global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(Pre
       // (4) warps 2-3: output of the previous chunk, then release its U/O buffer
       if (warp >= 2 && ci > 0) {
         wait(mbar_free0 + 8 * ((ci - 1) & 1), (uint32_t)(((ci - 1) >> 1) & 1));
-        store_out(ci - 1, true);
+        if (outs) {
+          store_out(ci - 1, true);
+        } else {  // no outputs: release the buffer at once
+          fence_before_sync();
+          mbar_arrive(mbar_orel0 + 8 * ((ci - 1) & 1));
+        }
       }
     }
     // last output and the final state
     if (nch > 0) {
       wait(mbar_s, (uint32_t)((nch - 1) & 1));
-      if (warp >= 2) {
+      if (warp >= 2 && outs) {
         wait(mbar_free0 + 8 * ((nch - 1) & 1), (uint32_t)(((nch - 1) >> 1) & 1));
         store_out(nch - 1, false);
       }
     }
-    if (a.sT && tid < DK) {
-      float* dst = a.sT + n * a.sT_sn + h * a.sT_sh + (int64_t)tid * a.dv + v0;
+    if (un.fin && tid < DK) {
+      float* dst = un.fin + (int64_t)tid * un.fin_ld;
 #pragma unroll
-      for (int c0 = 0; c0 < DV; c0 += 32) {
+      for (int cb = 0; cb < DV; cb += 32) {
         float v[32];
-        tmem_ld32(tS + lane_base + c0, v);
+        tmem_ld32(tS + lane_base + cb, v);
+        if (cb < un.fin_cols) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(dst + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + cb + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
       }
     }
   }
@@ -1007,36 +1145,125 @@ __global__ void __launch_bounds__(kSerialThreads, 1) kda_chunk_serial_kernel(Pre
 
 // ---------------------------------------------------------------------------
 // chunk offsets of each sequence (varlen): off[n] = sum_{m < n} ceil(len_m / 64),
-// capped at `total` so no record index can fall outside the workspace
-__global__ void kda_chunk_offsets_kernel(PrefillArgs a, int total, int* off) {
-  __shared__ int part[256];
+// capped at `total` so no record index can fall outside the workspace; and, when
+// soff is given, tail-segment offsets soff[n] = sum_{m < n} (segments_m - 1),
+// capped at `ntail`
+__global__ void kda_chunk_offsets_kernel(PrefillArgs a, int total, int* off, int* soff, int ntail) {
+  __shared__ int part[256], spart[256];
   const int N = a.N;
   const int per = (N + 255) / 256;
   const int n0 = threadIdx.x * per;
-  int s = 0;
-  for (int i = 0; i < per; ++i) {
-    const int n = n0 + i;
-    if (n < N) s += (seq_range(a, n).len + kC - 1) / kC;
-  }
-  part[threadIdx.x] = s;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int i = 0; i < 256; ++i) {
-      const int x = part[i];
-      part[i] = run;
-      run += x;
-    }
-    off[N] = min(run, total);
-  }
-  __syncthreads();
-  int run = part[threadIdx.x];
+  int s = 0, ss = 0;
   for (int i = 0; i < per; ++i) {
     const int n = n0 + i;
     if (n < N) {
-      off[n] = min(run, total);
-      run += (seq_range(a, n).len + kC - 1) / kC;
+      const int nc = (seq_range(a, n).len + kC - 1) / kC;
+      s += nc;
+      ss += num_segments(nc) - 1;
     }
+  }
+  part[threadIdx.x] = s;
+  spart[threadIdx.x] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0, srun = 0;
+    for (int i = 0; i < 256; ++i) {
+      const int x = part[i], y = spart[i];
+      part[i] = run;
+      spart[i] = srun;
+      run += x;
+      srun += y;
+    }
+    off[N] = min(run, total);
+    if (soff) soff[N] = min(srun, ntail);
+  }
+  __syncthreads();
+  int run = part[threadIdx.x], srun = spart[threadIdx.x];
+  for (int i = 0; i < per; ++i) {
+    const int n = n0 + i;
+    if (n < N) {
+      const int nc = (seq_range(a, n).len + kC - 1) / kC;
+      off[n] = min(run, total);
+      if (soff) soff[n] = min(srun, ntail);
+      run += nc;
+      srun += num_segments(nc) - 1;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// States entering the tail segments: S_in(s + 1) = M_s S_in(s) + S~_s, in fp32,
+// in order over the segments of each (sequence, head).  S_in(1) is segment 0's
+// final state (serial pass 0).  One CTA per (sequence, head, 32 value columns).
+constexpr int kCombineThreads = 256;
+template <int DK>
+struct CombineSmem {
+  static constexpr int kMd = DK + 4;  // fp32 row stride of M
+  static constexpr int kBytes = (DK * kMd + DK * 32) * 4;
+};
+
+template <int DK>
+__global__ void __launch_bounds__(kCombineThreads) kda_segment_combine_kernel(PrefillArgs a, Split sp, Seg sg) {
+  constexpr int RPT = DK / 32;  // rows per thread: 8 threads x 4 columns cover 32 columns
+  using CS = CombineSmem<DK>;
+  extern __shared__ float csm[];
+  float* Ms = csm;                 // M: [DK][kMd]
+  float* Ss = csm + DK * CS::kMd;  // state block: [DK][32]
+  const int ncb = a.dv / 32;
+  const int cb = blockIdx.x % ncb, nh = blockIdx.x / ncb;
+  const int n = nh / a.H, h = nh - (nh / a.H) * a.H;
+  const Range rg = seq_range(a, n);
+  const int nc = min(num_chunks(sp, n), (rg.len + kC - 1) / kC);
+  const int ns = num_segments(nc);
+  if (ns < 3) return;
+  const int t0 = tail_first(sg, n);
+  if (t0 + ns - 2 >= tail_count(sg, a.N)) return;
+  const int tid = threadIdx.x;
+  const int r0 = RPT * (tid >> 3), cq = 4 * (tid & 7);
+  const int64_t ldt = a.dv + DK;
+  const float* sin0 = sg.sin + ((int64_t)t0 * a.H + h) * DK * a.dv + 32 * cb;
+  for (int i = tid; i < DK * 8; i += kCombineThreads) {
+    const int r = i >> 3, c = 4 * (i & 7);
+    *reinterpret_cast<float4*>(Ss + r * 32 + c) = *reinterpret_cast<const float4*>(sin0 + (int64_t)r * a.dv + c);
+  }
+  for (int sgi = 2; sgi < ns; ++sgi) {
+    // (S~ | M) of segment sgi - 1
+    const float* tr = sg.tr + ((int64_t)(t0 + sgi - 2) * a.H + h) * DK * ldt;
+    for (int i = tid; i < DK * DK / 4; i += kCombineThreads) {
+      const int r = i / (DK / 4), k = 4 * (i % (DK / 4));
+      *reinterpret_cast<float4*>(Ms + r * CS::kMd + k) = *reinterpret_cast<const float4*>(tr + r * ldt + a.dv + k);
+    }
+    __syncthreads();
+    float acc[RPT][4];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const float4 x = *reinterpret_cast<const float4*>(tr + (int64_t)(r0 + i) * ldt + 32 * cb + cq);
+      acc[i][0] = x.x;
+      acc[i][1] = x.y;
+      acc[i][2] = x.z;
+      acc[i][3] = x.w;
+    }
+#pragma unroll 4
+    for (int k = 0; k < DK; ++k) {
+      const float4 b = *reinterpret_cast<const float4*>(Ss + k * 32 + cq);
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const float m = Ms[(r0 + i) * CS::kMd + k];
+        acc[i][0] = fmaf(m, b.x, acc[i][0]);
+        acc[i][1] = fmaf(m, b.y, acc[i][1]);
+        acc[i][2] = fmaf(m, b.z, acc[i][2]);
+        acc[i][3] = fmaf(m, b.w, acc[i][3]);
+      }
+    }
+    __syncthreads();
+    float* dst = sg.sin + ((int64_t)(t0 + sgi - 1) * a.H + h) * DK * a.dv + 32 * cb;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const float4 x = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      *reinterpret_cast<float4*>(Ss + (r0 + i) * 32 + cq) = x;
+      *reinterpret_cast<float4*>(dst + (int64_t)(r0 + i) * a.dv + cq) = x;
+    }
+    __syncthreads();
   }
 }
 
@@ -1059,19 +1286,55 @@ int64_t split_total_chunks(const PrefillArgs& a) {
   return a.cu_seqlens ? nck + a.N : nck * a.N;
 }
 
+// Workspace plan: [chunk offsets | tail-segment offsets | records | (S~ | M) | S_in]
+struct Plan {
+  int64_t off_bytes, soff_bytes, rec_bytes, tr_bytes, sin_bytes;
+  int ntail, tps;
+  int64_t total() const { return off_bytes + soff_bytes + rec_bytes + tr_bytes + sin_bytes; }
+};
+
+Plan plan(const PrefillArgs& a) {
+  Plan p{};
+  const int64_t total = split_total_chunks(a);
+  const int64_t nck = ((int64_t)a.T + kC - 1) / kC;
+  p.off_bytes = a.cu_seqlens ? (((int64_t)(a.N + 1) * 4 + 1023) & ~int64_t(1023)) : 0;
+  p.rec_bytes = total * a.H * (a.dk == 128 ? Rec<128>::kBytes : Rec<64>::kBytes);
+  if (a.cu_seqlens) {
+    // sum over sequences of (segments - 1) <= (sum of chunks) / kSegChunks
+    p.ntail = (int)(total / kSegChunks);
+    p.tps = 0;
+    p.soff_bytes = p.ntail ? (((int64_t)(a.N + 1) * 4 + 1023) & ~int64_t(1023)) : 0;
+  } else {
+    p.tps = num_segments((int)nck) - 1;
+    p.ntail = a.N * p.tps;
+    p.soff_bytes = 0;
+  }
+  p.tr_bytes = (int64_t)p.ntail * a.H * a.dk * (a.dv + a.dk) * 4;
+  p.sin_bytes = (int64_t)p.ntail * a.H * a.dk * a.dv * 4;
+  return p;
+}
+
 template <int DK, int DV>
 cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
-  const int64_t total = split_total_chunks(a);
-  const int64_t off_bytes = a.cu_seqlens ? (((int64_t)(a.N + 1) * 4 + 1023) & ~int64_t(1023)) : 0;
+  const Plan pl = plan(a);
+  unsigned char* base = static_cast<unsigned char*>(ws);
   Split sp;
-  sp.off = a.cu_seqlens ? static_cast<const int*>(ws) : nullptr;
-  sp.rec = static_cast<unsigned char*>(ws) + off_bytes;
-  sp.total = (int)total;
+  sp.off = a.cu_seqlens ? reinterpret_cast<const int*>(base) : nullptr;
+  sp.rec = base + pl.off_bytes + pl.soff_bytes;
+  sp.total = (int)split_total_chunks(a);
   sp.nck = (int)(((int64_t)a.T + kC - 1) / kC);
+  Seg sg;
+  sg.soff = pl.soff_bytes ? reinterpret_cast<const int*>(base + pl.off_bytes) : nullptr;
+  sg.tr = reinterpret_cast<float*>(sp.rec + pl.rec_bytes);
+  sg.sin = reinterpret_cast<float*>(sp.rec + pl.rec_bytes + pl.tr_bytes);
+  sg.ntail = pl.ntail;
+  sg.tps = pl.tps;
   cudaError_t e;
   if (a.cu_seqlens) {
     launch_begin(s);
-    kda_chunk_offsets_kernel<<<1, 256, 0, s>>>(a, sp.total, static_cast<int*>(ws));
+    kda_chunk_offsets_kernel<<<1, 256, 0, s>>>(a, sp.total, reinterpret_cast<int*>(base),
+                                               sg.soff ? reinterpret_cast<int*>(base + pl.off_bytes) : nullptr,
+                                               pl.ntail);
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   }
   auto prep = kda_chunk_prep_kernel<DK>;
@@ -1081,32 +1344,44 @@ cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
   // carry the serial loop.  Each slice CTA reads the whole chunk record.
   constexpr int DVS = DV == 128 ? 64 : DV;
   const bool split = DVS != DV && (int64_t)a.N * a.H * (DV / DVS) <= sm_count();
+  const int W = split ? DVS : DV;  // columns per serial CTA
   auto ser = split ? kda_chunk_serial_kernel<DK, DVS> : kda_chunk_serial_kernel<DK, DV>;
   const int ser_smem = split ? SerialSmem<DK, DVS>::kAlloc : SerialSmem<DK, DV>::kAlloc;
-  const unsigned ser_grid = (unsigned)(a.N * a.H * (split ? DV / DVS : 1));
   e = cudaFuncSetAttribute(ser, cudaFuncAttributeMaxDynamicSharedMemorySize, ser_smem);
   if (e != cudaSuccess) return e;
-  const int64_t items = total * a.H;
+  const int64_t items = (int64_t)sp.total * a.H;
   const int grid = (int)(items < 2 * sm_count() ? items : 2 * sm_count());
   if (grid > 0) {
     launch_begin(s);
     prep<<<grid, kThreads, PrepSmem<DK>::kAlloc, s>>>(a, sp);
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   }
+  // pass 0: every sequence's first segment, and the tail segments' (S~ | M)
+  const int64_t nfirst = (int64_t)a.N * a.H * (DV / W);
+  const int64_t ntail_ctas = (int64_t)pl.ntail * a.H * ((DV + DK + W - 1) / W);
   launch_begin(s);
-  ser<<<dim3(ser_grid), kSerialThreads, ser_smem, s>>>(a, sp);
+  ser<<<dim3((unsigned)(nfirst + ntail_ctas)), kSerialThreads, ser_smem, s>>>(a, sp, sg, 0);
+  if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
+  if (pl.ntail == 0) return cudaSuccess;
+  // states entering the tail segments (only sequences of three or more segments need it)
+  if (a.cu_seqlens ? pl.ntail >= 2 : pl.tps >= 2) {
+    auto comb = kda_segment_combine_kernel<DK>;
+    e = cudaFuncSetAttribute(comb, cudaFuncAttributeMaxDynamicSharedMemorySize, CombineSmem<DK>::kBytes);
+    if (e != cudaSuccess) return e;
+    launch_begin(s);
+    comb<<<dim3((unsigned)((int64_t)a.N * a.H * (DV / 32))), kCombineThreads, CombineSmem<DK>::kBytes, s>>>(a, sp, sg);
+    if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
+  }
+  // pass 1: the tail segments from their input states, with outputs
+  launch_begin(s);
+  ser<<<dim3((unsigned)((int64_t)pl.ntail * a.H * (DV / W))), kSerialThreads, ser_smem, s>>>(a, sp, sg, 1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_end(s);
 }
 
 }  // namespace
 
-size_t chunk_prefill_workspace_bytes(const PrefillArgs& a) {
-  const int64_t total = split_total_chunks(a);
-  const int64_t off_bytes = a.cu_seqlens ? (((int64_t)(a.N + 1) * 4 + 1023) & ~int64_t(1023)) : 0;
-  const int64_t rb = a.dk == 128 ? rec_bytes<128>() : rec_bytes<64>();
-  return (size_t)(off_bytes + total * a.H * rb);
-}
+size_t chunk_prefill_workspace_bytes(const PrefillArgs& a) { return (size_t)plan(a).total(); }
 
 cudaError_t launch_chunk_prefill_tc(const PrefillArgs& a, void* workspace, cudaStream_t s) {
   if (!a.bf16) return cudaErrorInvalidValue;

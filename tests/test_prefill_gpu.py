@@ -175,3 +175,40 @@ def test_workload4_sampled_sequences(kda):
         assert max_abs(out[:, a:b][:, :, heads], o_ref) <= 2e-2, n
         assert rel_fro(sT[n:n + 1, heads], s_ref) <= 1e-2, n
     assert torch.isfinite(sT).all()
+
+
+# ---- segment split: sequences longer than 512 chunks (32768 tokens) ----
+
+SEG = 512 * 64  # tokens per segment
+
+
+@pytest.mark.parametrize("B,T,H", [(1, SEG + 100, 2),          # two segments, the second of 2 chunks
+                                   (2, 3 * SEG + 200, 1)])     # four segments per sequence
+def test_segment_split_matches_oracle(kda, B, T, H):
+    d = ki.prefill_inputs(B, T, H, 128, 128, "bf16", seed=40 + B, s0=True)
+    check_prefill(kda.kda_chunk_fwd, d, label=f"segments B{B} T{T}")
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 128), (128, 64), (64, 64)])
+def test_segment_split_head_dims(kda, dk, dv):
+    d = ki.prefill_inputs(1, 2 * SEG + 64 * 7 + 5, 1, dk, dv, "bf16", seed=43, s0=True)
+    check_prefill(kda.kda_chunk_fwd, d, label=f"segments {dk}x{dv}")
+
+
+def test_segment_split_varlen_bit_exact(kda):
+    """Packed long and short sequences: each matches the oracle, and equals the same
+    sequence run alone bit for bit (segments are cut from each sequence start)."""
+    lens = [100, SEG + 6000, 0, 2 * SEG + 4000, SEG + 200]
+    cu = ki.cu_seqlens_from_lengths(lens)
+    d = ki.prefill_inputs(1, int(cu[-1]), 1, 128, 128, "bf16", seed=44, s0=True, n_states=len(lens))
+    d["cu_seqlens"] = torch.from_numpy(cu)
+    check_prefill(kda.kda_chunk_fwd, d, label="segments varlen")
+    t = to_dev(d)
+    out, sT = kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"], t["scale"],
+                                cu_seqlens=t["cu_seqlens"])
+    for n in (1, 3, 4):
+        a, b = int(cu[n]), int(cu[n + 1])
+        sl = lambda x: x[:, a:b].contiguous()
+        o1, s1 = kda.kda_chunk_fwd(sl(t["q"]), sl(t["k"]), sl(t["v"]), sl(t["g"]), sl(t["beta"]),
+                                   t["initial_state"][n:n + 1].contiguous(), t["scale"])
+        assert torch.equal(out[:, a:b], o1) and torch.equal(sT[n:n + 1], s1), n
