@@ -137,7 +137,10 @@ kda_status kda_fused_recurrent_fwd(const kda_tensor* q, const kda_tensor* k,
  *    anything is launched.  The records take 66560 bytes per (chunk, head)
  *    at d_k = 128 and 41984 at d_k = 64, over B * ceil(T / 64) chunks (with
  *    cu_seqlens: ceil(T / 64) + N, plus a small offset table), so at most
- *    1008 (chunk, head) pairs at d_k = 128, e.g. B=1, H=15, T=4096.
+ *    1008 (chunk, head) pairs at d_k = 128, e.g. B=1, H=15, T=4096.  A
+ *    sequence longer than 512 chunks (32768 tokens) also needs, per head and
+ *    per 512-chunk segment after its first, d_k * (2 d_v + d_k) * 4 bytes
+ *    (192 KiB at d_k = d_v = 128) of segment states.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any stream
  *    capture.
