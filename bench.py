@@ -439,6 +439,42 @@ def bench_decode(kda, steps_total, warmup, stream, clk=None):
                 name=w["name"], steps=steps_total, launches=launches)
 
 
+def bench_multi_step(kda, n_tok, warmup, stream, clk=None, iters=20):
+    """kda_recurrent_multi_step on the decode batch (256 requests x 96 heads), n_tok
+    tokens per request, all accepted: the state is read and written once per call."""
+    w = ki.WORKLOADS[DECODE_W]
+    N, H, dk, dv = w["N"], w["H"], w["dk"], w["dv"]
+    seed = ki.SEED_BASE + DECODE_W
+    dev = torch.device("cuda")
+    S = ki.decode_state(N, H, dk, dv, seed=seed).to(dev)
+    d = ki.prefill_inputs(N, n_tok, H, dk, dv, "bf16", seed=seed + 100)
+    t = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in d.items()}
+    out = torch.empty(N, n_tok, H, dv, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        kda.kda_recurrent_multi_step(S, t["q"], t["k"], t["v"], t["g"], t["beta"], scale=t["scale"],
+                                     out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    with (clk or contextlib.nullcontext()), torch.cuda.stream(stream):
+        torch.cuda._sleep(SLEEP_CYCLES)
+        e0.record(stream)
+        for _ in range(iters):
+            step()
+            launches += kda.kda_last_launch_count()
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    per_tok = 2 * (2 * dk + dv) + 4 * dk + 4 + 2 * dv
+    nbytes = N * H * (8 * dk * dv + n_tok * per_tok)
+    return dict(ms=ms, N=N, H=H, n=n_tok, bytes=nbytes, launches=launches, iters=iters)
+
+
 def oracle_prefill_rate(idx, max_problems=None):
     """CPU oracle on (a sample of) the workload: returns (tokens/s, threads, sample text)."""
     import oracle
@@ -583,6 +619,18 @@ def main():
                      "algorithmic_bytes_per_launch": dec["bytes"]},
         "clocks": clk_dec.summary(), "gpu_launches": dec["launches"]}
     del dec
+    clk_ms = ClockSampler(local)
+    ms4 = bench_multi_step(kda, 4, args.warmup, stream, clk_ms)
+    m_ms = max_over_ranks(ms4["ms"], world)
+    m_gbs = ms4["bytes"] / (m_ms * 1e-3) / 1e9
+    extra["decode_multi_token"] = {
+        "workload": f"kda_multi_step_N{ms4['N']}_H{ms4['H']}_n{ms4['n']}_d128", "ms_per_call": m_ms,
+        "tokens_per_s": world * ms4["N"] * ms4["n"] * 1e3 / m_ms,
+        "roofline": {"bound": "hbm", "kernel": "kda_recurrent_kernel", "achieved": m_gbs,
+                     "peak": pk["hbm"], "unit": "GB/s", "frac": m_gbs / pk["hbm"],
+                     "algorithmic_bytes_per_launch": ms4["bytes"]},
+        "clocks": clk_ms.summary(), "gpu_launches": ms4["launches"]}
+    del ms4
     if not args.no_k3:
         clk_k3 = ClockSampler(local)
         k3 = bench_prefill(kda, K3_W, max(3, args.steps // 4), 3, flush, stream, clk_k3, world)

@@ -15,6 +15,7 @@ import torch
 from ._build import LIB, build, up_to_date  # noqa: F401
 
 __all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
+           "kda_recurrent_multi_step",
            "kda_get_device_error", "kda_set_launch_events", "kda_last_launch_count", "KdaError",
            "load_library", "build", "STATUS"]
 
@@ -23,6 +24,7 @@ STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "K
 DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
 
 EXPORTED = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
+            "kda_recurrent_multi_step",
             "kda_get_device_error", "kda_status_string", "kda_last_error_message",
             "kda_set_launch_events", "kda_last_launch_count"]
 
@@ -58,6 +60,8 @@ def load_library(path: str | None = None):
         f.restype, f.argtypes = ctypes.c_int, fwd
     lib.kda_recurrent_step.restype = ctypes.c_int
     lib.kda_recurrent_step.argtypes = [_P] * 6 + [ctypes.c_float, _P, ctypes.c_void_p]
+    lib.kda_recurrent_multi_step.restype = ctypes.c_int
+    lib.kda_recurrent_multi_step.argtypes = [_P] * 6 + [ctypes.c_float, _P, _P, ctypes.c_void_p]
     lib.kda_get_device_error.restype = ctypes.c_int
     lib.kda_get_device_error.argtypes = [ctypes.c_void_p]
     lib.kda_status_string.restype = ctypes.c_char_p
@@ -153,6 +157,28 @@ def kda_recurrent_step(state, q, k, v, g, beta, scale=None, out=None, stream=Non
     ds = [desc(x) for x in (state, q, k, v, g, beta, out)]
     st = lib.kda_recurrent_step(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), _ref(ds[4]),
                                 _ref(ds[5]), float(scale), _ref(ds[6]), _stream(stream))
+    _check(lib, st)
+    return out
+
+
+def kda_recurrent_multi_step(state, q, k, v, g, beta, scale=None, num_accepted=None, out=None,
+                             stream=None):
+    """n decode tokens per request: q, k, g [N, n, H, d_k], v [N, n, H, d_v], beta
+    [N, n, H].  Keeps the state after the first ``num_accepted[i]`` tokens (int32
+    [N] on the device; None = all n), written once in place.  With ``q=None`` no
+    outputs are made (a commit); otherwise returns out [N, n, H, d_v]."""
+    lib = load_library()
+    N, n, H, dk = k.shape
+    dv = v.shape[-1]
+    if scale is None:
+        scale = dk ** -0.5
+    if q is not None and out is None:
+        out = torch.empty((N, n, H, dv), dtype=k.dtype, device=k.device)
+    if q is None:
+        out = None
+    ds = [desc(x) for x in (state, q, k, v, g, beta, num_accepted, out)]
+    st = lib.kda_recurrent_multi_step(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), _ref(ds[4]),
+                                      _ref(ds[5]), float(scale), _ref(ds[6]), _ref(ds[7]), _stream(stream))
     _check(lib, st)
     return out
 

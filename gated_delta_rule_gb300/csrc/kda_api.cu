@@ -500,6 +500,93 @@ kda_status kda_recurrent_step(kda_tensor* state, const kda_tensor* q, const kda_
   return KDA_OK;
 }
 
+kda_status kda_recurrent_multi_step(kda_tensor* state, const kda_tensor* q, const kda_tensor* k,
+                                    const kda_tensor* v, const kda_tensor* g, const kda_tensor* beta,
+                                    float scale, const kda_tensor* num_accepted, kda_tensor* out,
+                                    void* stream) {
+  LaunchScope scope;
+  g_msg.clear();
+  KDA_TRY(check_desc(k, "k", 4, 16));
+  const int32_t dt = k->dtype;
+  if (dt != KDA_DTYPE_BF16 && dt != KDA_DTYPE_F32)
+    return fail(KDA_ERR_INVALID_ARG, "k: dtype must be bf16 or f32");
+  const int64_t N = k->shape[0], n = k->shape[1], H = k->shape[2], dk = k->shape[3];
+  KDA_TRY(check_desc(v, "v", 4, 16));
+  const int64_t dv = v->shape[3];
+  KDA_TRY(check_head_dims(dk, dv));
+  const int64_t wq[4] = {N, n, H, dk}, wv[4] = {N, n, H, dv}, wb[3] = {N, n, H};
+  KDA_TRY(check_shape(v, "v", 4, wv, dt));
+  KDA_TRY(check_desc(g, "g", 4, 16));
+  KDA_TRY(check_shape(g, "g", 4, wq, KDA_DTYPE_F32));
+  KDA_TRY(check_desc(beta, "beta", 3, 4));
+  KDA_TRY(check_shape(beta, "beta", 3, wb, KDA_DTYPE_F32));
+  if ((q == nullptr) != (out == nullptr))
+    return fail(KDA_ERR_INVALID_ARG, "q and out must both be given or both be NULL");
+  if (q) {
+    KDA_TRY(check_desc(q, "q", 4, 16));
+    KDA_TRY(check_shape(q, "q", 4, wq, dt));
+    KDA_TRY(check_desc(out, "out", 4, 16));
+    KDA_TRY(check_shape(out, "out", 4, wv, dt));
+  }
+  KDA_TRY(check_state(state, "state", N, H, dk, dv));
+  if (num_accepted) {
+    KDA_TRY(check_desc(num_accepted, "num_accepted", 1, 4));
+    if (num_accepted->dtype != KDA_DTYPE_I32)
+      return fail(KDA_ERR_INVALID_ARG, "num_accepted: dtype must be i32");
+    if (num_accepted->shape[0] != N)
+      return fail(KDA_ERR_INVALID_ARG, "num_accepted: %lld entries, expected %lld",
+                  (long long)num_accepted->shape[0], (long long)N);
+  }
+  if (!isfinite(scale)) return fail(KDA_ERR_INVALID_ARG, "scale must be finite");
+  if (n > INT32_MAX || N > INT32_MAX || H > 65535 || N * H > INT32_MAX / 8)
+    return fail(KDA_ERR_UNSUPPORTED, "sizes too large");
+  const kda_tensor* ins[] = {q, k, v, g, beta, num_accepted};
+  const char* names[] = {"q", "k", "v", "g", "beta", "num_accepted"};
+  for (int i = 0; i < 6; ++i) {
+    if (!ins[i]) continue;
+    if (overlap(state, ins[i])) return fail(KDA_ERR_INVALID_ARG, "state overlaps %s", names[i]);
+    if (out && overlap(out, ins[i])) return fail(KDA_ERR_INVALID_ARG, "out overlaps %s", names[i]);
+  }
+  if (out && overlap(out, state)) return fail(KDA_ERR_INVALID_ARG, "out overlaps state");
+  if (N * H == 0 || n == 0) return KDA_OK;
+
+  kda::PrefillArgs a;
+  memset(&a, 0, sizeof(a));
+  if (q) a.q = act(q);
+  a.k = act(k);
+  a.v = act(v);
+  a.g = act(g);
+  a.beta = static_cast<const float*>(beta->data);
+  a.beta_sb = beta->stride[0];
+  a.beta_st = beta->stride[1];
+  a.beta_sh = beta->stride[2];
+  a.s0 = static_cast<const float*>(state->data);
+  a.s0_sn = state->stride[0];
+  a.s0_sh = state->stride[1];
+  a.sT = static_cast<float*>(state->data);
+  a.sT_sn = state->stride[0];
+  a.sT_sh = state->stride[1];
+  if (out) {
+    a.out = out->data;
+    a.out_sb = out->stride[0];
+    a.out_st = out->stride[1];
+    a.out_sh = out->stride[2];
+  }
+  a.accepted = num_accepted ? static_cast<const int32_t*>(num_accepted->data) : nullptr;
+  a.B = (int)N;
+  a.T = (int)n;
+  a.H = (int)H;
+  a.N = (int)N;
+  a.dk = (int)dk;
+  a.dv = (int)dv;
+  a.bf16 = dt == KDA_DTYPE_BF16;
+  a.scale = scale;
+  KDA_TRY(device_error_ptr(&a.err));
+  cudaError_t e = kda::launch_recurrent_prefill(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "multi-step decode launch");
+  return KDA_OK;
+}
+
 kda_status kda_get_device_error(void* stream) {
   g_msg.clear();
   int* p = nullptr;

@@ -27,9 +27,13 @@ struct PrefillArgs {
   int64_t s0_sn, s0_sh;
   float* sT;  // nullable
   int64_t sT_sn, sT_sh;
-  void* out;
+  void* out;  // nullable for the recurrent kernel (no outputs)
   int64_t out_sb, out_st, out_sh;
   const int32_t* cu_seqlens;  // nullable
+  // nullable (recurrent kernel only): per-sequence count of tokens whose state
+  // update is kept; the final state is the state after that many tokens (clamped
+  // to [0, length]) and is not written when the count is 0
+  const int32_t* accepted;
   int B, T, H, N, dk, dv;
   int bf16;  // 1: q/k/v/out are bf16, 0: fp32
   float scale;

@@ -609,14 +609,16 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
           float s0 = (r == cc) ? 1.f : 0.f, s1 = 0.f;
-          if (r > cc) {
+          const float4* lr = reinterpret_cast<const float4*>(sL + (16 * I + r) * L::kLd + 16 * I);
 #pragma unroll
-            for (int m = 0; m < r; m += 2) {
-              s0 -= sL[(16 * I + r) * L::kLd + 16 * I + m] * x[m];
-              if (m + 1 < r) s1 -= sL[(16 * I + r) * L::kLd + 16 * I + m + 1] * x[m + 1];
-            }
+          for (int m4 = 0; m4 < r; m4 += 4) {  // L[r][m] for m < r (entries at m >= r are zero)
+            const float4 l = lr[m4 >> 2];
+            s0 -= l.x * x[m4];
+            if (m4 + 1 < r) s1 -= l.y * x[m4 + 1];
+            if (m4 + 2 < r) s0 -= l.z * x[m4 + 2];
+            if (m4 + 3 < r) s1 -= l.w * x[m4 + 3];
           }
-          x[r] = (r >= cc) ? s0 + s1 : 0.f;
+          x[r] = (r > cc) ? s0 + s1 : ((r == cc) ? 1.f : 0.f);
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) sT[(16 * I + r) * L::kTd + 16 * I + cc] = x[r];

@@ -1,7 +1,9 @@
 // SIMT kernels of the KDA core:
 //   * kda_decode_kernel     - one decode token per (request, head), state in place;
 //   * kda_recurrent_kernel  - token-by-token prefill with the state held in
-//                             registers (the fp32-input path, any sequence length);
+//                             registers (the fp32-input path, any sequence length),
+//                             also the multi-token decode step (requests as
+//                             sequences, the state kept after an accepted count);
 //   * kda_seqlens_kernel    - device-side validation of cu_seqlens.
 //
 // Both compute kernels run the single-step recurrence in the order of
@@ -12,13 +14,13 @@
 //   S' = fma(beta k_i, v_j, fma(-beta k_i, (k^T S)_j, S_ij)),
 // so a unit key with beta = 1 reproduces v exactly in that row.
 //
-// Thread layout (256 threads per (sequence|request, head)): a state row of d_v
-// fp32 values is covered by d_v/4 threads holding 4 consecutive columns
-// (one 16-byte vector each); 256/(d_v/4) rows are handled side by side and
-// each thread keeps d_k*(d_v/4)/256 rows in registers.  Column sums over the
-// key channels (k^T S and q^T S) are reduced through shared memory.  A warp
-// therefore loads and stores whole contiguous rows: 512 bytes per instruction
-// at d_v = 128.
+// Thread layout (256 threads per (sequence|request, head, 64 value columns)): a
+// 64-column state row slice is covered by 16 threads holding 4 consecutive
+// columns (one 16-byte vector each); 16 rows are handled side by side and each
+// thread keeps d_k/16 rows in registers.  Column sums over the key channels
+// (k^T S and q^T S) are reduced through shared memory in the same order in both
+// compute kernels.  A warp loads and stores two 256-byte row slices per
+// instruction.
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -90,7 +92,8 @@ struct Layout {
   static_assert(R * RPP == DK, "layout");
 };
 
-// Sum over the RPP row groups of per-thread partial column sums.
+// Sum over the RPP row groups of per-thread partial column sums (the same order
+// in both compute kernels, so a token gives the same bits whichever kernel runs it).
 template <int DK, int DV>
 __device__ __forceinline__ float4 column_reduce(float4 part, float4 (*red)[DV / 4], int trow,
                                                int col4) {
@@ -112,27 +115,31 @@ __device__ __forceinline__ float4 column_reduce(float4 part, float4 (*red)[DV / 
 // ---------------------------------------------------------------------------
 // decode: one CTA per (request, head); every state element read once, written once
 template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(kThreads, 2) kda_decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) kda_decode_kernel(DecodeArgs a) {
   using L = Layout<DK, DV>;
   __shared__ float s_q[DK], s_k[DK], s_a[DK];
   __shared__ float4 red0[L::RPP][DV / 4];
   __shared__ float4 red1[L::RPP][DV / 4];
-  const int n = blockIdx.x / a.H;
-  const int h = blockIdx.x - n * a.H;
+  const int nsl = a.dv / DV;                 // CTAs per (request, head): DV columns each
+  const int col0 = (blockIdx.x % nsl) * DV;
+  const int nh = blockIdx.x / nsl;
+  const int n = nh / a.H;
+  const int h = nh - n * a.H;
+  const int64_t ld = a.dv;                   // state row stride
   const int tid = threadIdx.x;
   const int col4 = tid % L::TPR;
   const int trow = tid / L::TPR;
 
-  float* S = a.state + n * a.s_sn + h * a.s_sh;
+  float* S = a.state + n * a.s_sn + h * a.s_sh + col0;
   float4 s[L::R];
 #pragma unroll
   for (int r = 0; r < L::R; ++r)
-    s[r] = __ldcs(reinterpret_cast<const float4*>(S + (trow + L::RPP * r) * DV + 4 * col4));
+    s[r] = __ldcs(reinterpret_cast<const float4*>(S + (trow + L::RPP * r) * ld + 4 * col4));
 
   const T* qp = static_cast<const T*>(a.q.ptr) + n * a.q.sb + h * a.q.sh;
   const T* kp = static_cast<const T*>(a.k.ptr) + n * a.k.sb + h * a.k.sh;
   const float* gp = static_cast<const float*>(a.g.ptr) + n * a.g.sb + h * a.g.sh;
-  const T* vp = static_cast<const T*>(a.v.ptr) + n * a.v.sb + h * a.v.sh;
+  const T* vp = static_cast<const T*>(a.v.ptr) + n * a.v.sb + h * a.v.sh + col0;
   const float beta = __ldg(a.beta + n * a.beta_sn + h * a.beta_sh);
   if (tid < DK) {
     s_q[tid] = to_f(qp[tid]);
@@ -160,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_decode_kernel(DecodeArgs a) {
   for (int r = 0; r < L::R; ++r) {
     const int i = trow + L::RPP * r;
     s[r] = delta_write(s[r], beta * s_k[i], kS, v4);
-    __stcs(reinterpret_cast<float4*>(S + i * DV + 4 * col4), s[r]);
+    __stcs(reinterpret_cast<float4*>(S + i * ld + 4 * col4), s[r]);
     fma4(po, s_q[i], s[r]);
   }
   float4 o = column_reduce<DK, DV>(po, red1, trow, col4);
@@ -169,20 +176,26 @@ __global__ void __launch_bounds__(kThreads, 2) kda_decode_kernel(DecodeArgs a) {
     o.y *= a.scale;
     o.z *= a.scale;
     o.w *= a.scale;
-    store4<T>(static_cast<T*>(a.out) + n * a.out_sn + h * a.out_sh + 4 * col4, o);
+    store4<T>(static_cast<T*>(a.out) + n * a.out_sn + h * a.out_sh + col0 + 4 * col4, o);
   }
 }
 
 // ---------------------------------------------------------------------------
-// token-by-token prefill: one CTA per (sequence, head), state in registers
+// token-by-token prefill: one CTA per (sequence, head, DV value columns), state in
+// registers.  The state's columns evolve independently, so a (sequence, head)
+// may be spread over a.dv / DV CTAs.
 template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(kThreads, 1) kda_recurrent_kernel(PrefillArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) kda_recurrent_kernel(PrefillArgs a) {
   using L = Layout<DK, DV>;
   __shared__ float s_q[2][DK], s_k[2][DK], s_a[2][DK];
   __shared__ float4 red0[L::RPP][DV / 4];
   __shared__ float4 red1[L::RPP][DV / 4];
-  const int n = blockIdx.x / a.H;
-  const int h = blockIdx.x - n * a.H;
+  const int nsl = a.dv / DV;
+  const int col0 = (blockIdx.x % nsl) * DV;  // first value column of this CTA
+  const int nh = blockIdx.x / nsl;
+  const int n = nh / a.H;
+  const int h = nh - n * a.H;
+  const int64_t ld = a.dv;                   // state row stride
   const int tid = threadIdx.x;
   const int col4 = tid % L::TPR;
   const int trow = tid / L::TPR;
@@ -197,28 +210,38 @@ __global__ void __launch_bounds__(kThreads, 1) kda_recurrent_kernel(PrefillArgs 
 
   float4 s[L::R];
   if (a.s0) {
-    const float* S0 = a.s0 + n * a.s0_sn + h * a.s0_sh;
+    const float* S0 = a.s0 + n * a.s0_sn + h * a.s0_sh + col0;
 #pragma unroll
-    for (int r = 0; r < L::R; ++r)
-      s[r] = *reinterpret_cast<const float4*>(S0 + (trow + L::RPP * r) * DV + 4 * col4);
+    for (int r = 0; r < L::R; ++r)  // streaming: each state element is read once
+      s[r] = __ldcs(reinterpret_cast<const float4*>(S0 + (trow + L::RPP * r) * ld + 4 * col4));
   } else {
 #pragma unroll
     for (int r = 0; r < L::R; ++r) s[r] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
-  const T* qb = static_cast<const T*>(a.q.ptr) + b * a.q.sb + h * a.q.sh;
+  // tokens whose update is kept (the rest still produce outputs)
+  const int64_t keep = a.accepted ? min(max((int64_t)__ldg(a.accepted + n), (int64_t)0), t1 - t0) : t1 - t0;
+  if (!a.out) t1 = t0 + keep;  // nothing to read out past the kept tokens
+  const bool has_q = a.q.ptr != nullptr;
+
+  const T* qb = has_q ? static_cast<const T*>(a.q.ptr) + b * a.q.sb + h * a.q.sh : nullptr;
   const T* kb = static_cast<const T*>(a.k.ptr) + b * a.k.sb + h * a.k.sh;
   const float* gb = static_cast<const float*>(a.g.ptr) + b * a.g.sb + h * a.g.sh;
-  const T* vb = static_cast<const T*>(a.v.ptr) + b * a.v.sb + h * a.v.sh;
+  const T* vb = static_cast<const T*>(a.v.ptr) + b * a.v.sb + h * a.v.sh + col0;
   const float* bb = a.beta + b * a.beta_sb + h * a.beta_sh;
-  T* ob = static_cast<T*>(a.out) + b * a.out_sb + h * a.out_sh;
+  T* ob = a.out ? static_cast<T*>(a.out) + b * a.out_sb + h * a.out_sh + col0 : nullptr;
 
   // stage token t0 into buffer 0
-  float pq = 0.f, pk = 0.f, pa = 0.f;
-  if (t0 < t1 && tid < DK) {
-    pq = to_f(qb[t0 * a.q.st + tid]);
-    pk = to_f(kb[t0 * a.k.st + tid]);
-    pa = expf(__ldg(gb + t0 * a.g.st + tid));
+  float pq = 0.f, pk = 0.f, pa = 0.f, pb = 0.f;
+  float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (t0 < t1) {
+    if (tid < DK) {
+      pq = has_q ? to_f(qb[t0 * a.q.st + tid]) : 0.f;
+      pk = to_f(kb[t0 * a.k.st + tid]);
+      pa = expf(__ldg(gb + t0 * a.g.st + tid));
+    }
+    pv = load4<T>(vb + t0 * a.v.st + 4 * col4);
+    pb = __ldg(bb + t0 * a.beta_st);
   }
   for (int64_t t = t0; t < t1; ++t) {
     const int buf = (int)((t - t0) & 1);
@@ -227,12 +250,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_recurrent_kernel(PrefillArgs 
       s_k[buf][tid] = pk;
       s_a[buf][tid] = pa;
     }
-    const float4 v4 = load4<T>(vb + t * a.v.st + 4 * col4);
-    const float beta = __ldg(bb + t * a.beta_st);
-    if (t + 1 < t1 && tid < DK) {  // prefetch the next token while this one computes
-      pq = to_f(qb[(t + 1) * a.q.st + tid]);
-      pk = to_f(kb[(t + 1) * a.k.st + tid]);
-      pa = expf(__ldg(gb + (t + 1) * a.g.st + tid));
+    const float4 v4 = pv;
+    const float beta = pb;
+    if (t + 1 < t1) {  // prefetch the next token while this one computes
+      if (tid < DK) {
+        pq = has_q ? to_f(qb[(t + 1) * a.q.st + tid]) : 0.f;
+        pk = to_f(kb[(t + 1) * a.k.st + tid]);
+        pa = expf(__ldg(gb + (t + 1) * a.g.st + tid));
+      }
+      pv = load4<T>(vb + (t + 1) * a.v.st + 4 * col4);
+      pb = __ldg(bb + (t + 1) * a.beta_st);
     }
     __syncthreads();
     float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -254,22 +281,28 @@ __global__ void __launch_bounds__(kThreads, 1) kda_recurrent_kernel(PrefillArgs 
       s[r] = delta_write(s[r], beta * s_k[buf][i], kS, v4);
       fma4(po, s_q[buf][i], s[r]);
     }
-    float4 o = column_reduce<DK, DV>(po, red1, trow, col4);
-    if (trow == 0) {
-      o.x *= a.scale;
-      o.y *= a.scale;
-      o.z *= a.scale;
-      o.w *= a.scale;
-      store4<T>(ob + t * a.out_st + 4 * col4, o);
+    if (a.accepted && a.sT && t == t0 + keep - 1) {  // the kept state: written once
+      float* ST = a.sT + n * a.sT_sn + h * a.sT_sh + col0;
+#pragma unroll
+      for (int r = 0; r < L::R; ++r) __stcs(reinterpret_cast<float4*>(ST + (trow + L::RPP * r) * ld + 4 * col4), s[r]);
+    }
+    if (a.out) {
+      float4 o = column_reduce<DK, DV>(po, red1, trow, col4);
+      if (trow == 0) {
+        o.x *= a.scale;
+        o.y *= a.scale;
+        o.z *= a.scale;
+        o.w *= a.scale;
+        store4<T>(ob + t * a.out_st + 4 * col4, o);
+      }
     }
     // red0/red1 are rewritten next token only after that token's first barrier,
     // which every thread reaches after finishing its reads of this token.
   }
-  if (a.sT) {
-    float* ST = a.sT + n * a.sT_sn + h * a.sT_sh;
+  if (a.sT && !a.accepted) {
+    float* ST = a.sT + n * a.sT_sn + h * a.sT_sh + col0;
 #pragma unroll
-    for (int r = 0; r < L::R; ++r)
-      *reinterpret_cast<float4*>(ST + (trow + L::RPP * r) * DV + 4 * col4) = s[r];
+    for (int r = 0; r < L::R; ++r) __stcs(reinterpret_cast<float4*>(ST + (trow + L::RPP * r) * ld + 4 * col4), s[r]);
   }
 }
 
@@ -306,21 +339,28 @@ template <int DK, int DV, typename T>
 struct DecodeK {
   static constexpr void (*fn)(DecodeArgs) = kda_decode_kernel<DK, DV, T>;
 };
-template <int DK, int DV, typename T>
-struct RecurrentK {
-  static constexpr void (*fn)(PrefillArgs) = kda_recurrent_kernel<DK, DV, T>;
-};
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   if ((int64_t)a.N * a.H == 0) return cudaSuccess;
-  return dispatch<DecodeK>(a, a.dk, a.dv, a.bf16, dim3((unsigned)(a.N * a.H)), s);
+  // 64 value columns per CTA, the layout of the recurrent kernel, so that a
+  // multi-token call and the same tokens one step at a time round identically
+  return dispatch<DecodeK>(a, a.dk, 64, a.bf16, dim3((unsigned)(a.N * a.H * (a.dv / 64))), s);
 }
 
 cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s) {
   if ((int64_t)a.N * a.H == 0) return cudaSuccess;
-  return dispatch<RecurrentK>(a, a.dk, a.dv, a.bf16, dim3((unsigned)(a.N * a.H)), s);
+  // 64 value columns per CTA (three CTAs per SM): for d_v = 128 a (sequence, head)
+  // spreads over two CTAs, which keeps more state traffic in flight
+  void (*fn)(PrefillArgs) = nullptr;
+  if (a.dk == 128) fn = a.bf16 ? kda_recurrent_kernel<128, 64, __nv_bfloat16> : kda_recurrent_kernel<128, 64, float>;
+  if (a.dk == 64) fn = a.bf16 ? kda_recurrent_kernel<64, 64, __nv_bfloat16> : kda_recurrent_kernel<64, 64, float>;
+  if (!fn || (a.dv != 64 && a.dv != 128)) return cudaErrorInvalidValue;
+  launch_begin(s);
+  fn<<<dim3((unsigned)(a.N * a.H * (a.dv / 64))), kThreads, 0, s>>>(a);
+  const cudaError_t e = cudaGetLastError();
+  return e != cudaSuccess ? e : launch_end(s);
 }
 
 cudaError_t launch_check_seqlens(const int32_t* cu, int N, int T, int* err, cudaStream_t s) {

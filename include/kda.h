@@ -179,6 +179,45 @@ kda_status kda_recurrent_step(kda_tensor* state, const kda_tensor* q, const kda_
                               void* stream);
 
 /*
+ * kda_recurrent_multi_step - n decode tokens per request in one call, with the
+ * state read once and written back once (multi-token and speculative decoding).
+ *
+ * For every request and head it runs the recurrence above over tokens
+ * 0 .. n-1 in order ("Kimi K3 核心算子拆解" (devpress.csdn.net) §2.3 for the
+ * single step).  "Kimi K3 技术报告解读" (marsggbo.github.io) §9, on
+ * speculative decoding with KDA, keeps only the draft tokens' inputs and
+ * rebuilds the accepted tokens' state on chip by replaying them, verification
+ * and write-back in one kernel; this call is that kernel: pass the previous
+ * step's accepted tokens followed by the new drafts, with num_accepted = the
+ * number of replayed tokens.  Token j's output uses the
+ * state after tokens 0 .. j.  The state written back is the state after the
+ * first num_accepted[request] tokens: a draft that was verified with outputs
+ * (num_accepted = 0, nothing written) is committed by a second call without
+ * outputs that replays the accepted tokens.
+ *
+ *   state        [N, H, d_k, d_v] f32, inner [d_k, d_v] contiguous; in/out
+ *   q            [N, n, H, d_k] bf16 or f32, or NULL together with out
+ *   k            [N, n, H, d_k]  same dtype as q
+ *   v            [N, n, H, d_v]  same dtype as q
+ *   g            [N, n, H, d_k]  f32, per-token log-decay
+ *   beta         [N, n, H]       f32
+ *   scale        finite float multiplying the read-out
+ *   num_accepted [N] int32 on the device, or NULL (= n for every request);
+ *                values are clamped to [0, n]; 0 leaves the state untouched
+ *   out          [N, n, H, d_v]  k's dtype, or NULL (no outputs: only the
+ *                accepted tokens are processed)
+ *   stream       cudaStream_t as void*
+ *
+ * Errors as for kda_recurrent_step; q and out must both be given or both be
+ * NULL.  n = 0 is a no-op.  Tokens are processed one after another inside the
+ * kernel, so n is meant to be small (draft lengths of a few tokens); any n works.
+ */
+kda_status kda_recurrent_multi_step(kda_tensor* state, const kda_tensor* q, const kda_tensor* k,
+                                    const kda_tensor* v, const kda_tensor* g, const kda_tensor* beta,
+                                    float scale, const kda_tensor* num_accepted, kda_tensor* out,
+                                    void* stream);
+
+/*
  * kda_get_device_error - synchronises `stream`, then returns and clears the
  * current device's error word: KDA_OK, KDA_ERR_DEVICE (bad cu_seqlens) or
  * KDA_ERR_TIMEOUT; KDA_ERR_CUDA if the synchronisation itself failed.  The

@@ -143,3 +143,35 @@ def decode_step(state, q, k, v, g, beta, scale, nthreads=0):
                               v.reshape(P, dv), g.reshape(P, dk), beta.reshape(P),
                               S.reshape(P, dk, dv), scale, nthreads)
     return out.reshape(N, H, dv), ST.reshape(N, H, dk, dv)
+
+
+def multi_step(state, q, k, v, g, beta, scale, num_accepted=None, nthreads=0):
+    """Oracle of ``kda_recurrent_multi_step``: state [N, H, dk, dv]; q (or None), k, g
+    [N, n, H, dk]; v [N, n, H, dv]; beta [N, n, H]; num_accepted [N] or None (= n).
+
+    The n tokens of a request run the recurrence in order, token j's output read
+    from the state after tokens 0..j ("Kimi K3 核心算子拆解" (devpress.csdn.net)
+    §2.3, one step per token); the state kept is the one after the first
+    clamp(num_accepted, 0, n) tokens, the replay of accepted draft tokens of
+    "Kimi K3 技术报告解读" (marsggbo.github.io) §9.  Returns (out [N, n, H, dv] or
+    None when q is None, kept state [N, H, dk, dv]) in fp64.
+    """
+    k, v, g, beta, S = (_f64(a) for a in (k, v, g, beta, state))
+    N, n, H, dk = k.shape
+    dv = v.shape[3]
+    if num_accepted is None:
+        acc = np.full(N, n, dtype=np.int64)
+    else:
+        acc = np.clip(_f64(num_accepted).astype(np.int64).reshape(N), 0, n)
+    out = None
+    if q is not None:
+        out, _ = prefill(q, k, v, g, beta, S, scale, nthreads=nthreads)
+    kp, gp = (np.ascontiguousarray(a.transpose(0, 2, 1, 3)).reshape(N * H * n, dk) for a in (k, g))
+    vp = np.ascontiguousarray(v.transpose(0, 2, 1, 3)).reshape(N * H * n, dv)
+    bp = np.ascontiguousarray(beta.transpose(0, 2, 1)).reshape(N * H * n)
+    starts = [(i * H + h) * n for i in range(N) for h in range(H)]
+    counts = [int(acc[i]) for i in range(N) for h in range(H)]
+    # the kept state only: the read-outs of this run (q = k here) are discarded
+    _, ST, _ = run_problems(starts, counts, kp, kp, vp, gp, bp, S.reshape(N * H, dk, dv), scale,
+                            nthreads)
+    return out, ST.reshape(N, H, dk, dv)

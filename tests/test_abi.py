@@ -158,3 +158,26 @@ def test_failed_call_reports_no_launches(lib):
     assert lib.kda_recurrent_step(None, None, None, None, None, None, ctypes.c_float(1.0), None,
                                   None) == 1
     assert lib.kda_last_launch_count() == 0
+
+
+def test_multi_step_requires_q_and_out_together(lib):
+    import torch
+    r = lambda x: ctypes.byref(x)
+    N, n, H, dk = 2, 3, 1, 64
+    k = KdaTensor(); k.data = FAKE; k.dtype = 1; k.ndim = 4
+    for i, (sh, st) in enumerate(zip((N, n, H, dk), (n * H * dk, H * dk, dk, 1))):
+        k.shape[i] = sh
+        k.stride[i] = st
+    v, g, q = KdaTensor.from_buffer_copy(k), KdaTensor.from_buffer_copy(k), KdaTensor.from_buffer_copy(k)
+    g.dtype = 0
+    beta = KdaTensor(); beta.data = FAKE; beta.dtype = 0; beta.ndim = 3
+    for i, (sh, st) in enumerate(zip((N, n, H), (n * H, H, 1))):
+        beta.shape[i] = sh
+        beta.stride[i] = st
+    S = KdaTensor(); S.data = FAKE; S.dtype = 0; S.ndim = 4
+    for i, (sh, st) in enumerate(zip((N, H, dk, dk), (H * dk * dk, dk * dk, dk, 1))):
+        S.shape[i] = sh
+        S.stride[i] = st
+    st = lib.kda_recurrent_multi_step(r(S), r(q), r(k), r(v), r(g), r(beta), ctypes.c_float(1.0), None,
+                                      None, None)
+    assert st == 1 and b"both" in lib.kda_last_error_message()

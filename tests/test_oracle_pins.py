@@ -231,6 +231,41 @@ def test_decode_step_is_one_token_prefill():
     assert np.array_equal(o, o2[:, 0]) and np.array_equal(S1, S2)
 
 
+def test_multi_step_matches_numpy_token_loop():
+    """Multi-token decode: every request's outputs are those of the numpy three-step
+    loop over its n tokens, and the kept state is that loop stopped after the
+    accepted count (clamped to [0, n])."""
+    import kda_inputs as ki
+    N, n, H, dk, dv = 5, 4, 2, 16, 8
+    S = ki.decode_state(N, H, dk, dv, seed=6).double().numpy()
+    d = ki.prefill_inputs(N, n, H, dk, dv, "bf16", seed=6)
+    acc = np.array([0, 1, 4, 7, -2])
+    out, Sk = oracle.multi_step(S, d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], acc)
+    f = lambda x: np.asarray(x.double() if hasattr(x, "double") else x, dtype=np.float64)
+    q, k, v, g, beta = map(f, (d["q"], d["k"], d["v"], d["g"], d["beta"]))
+    for i in range(N):
+        a = min(max(int(acc[i]), 0), n)
+        for h in range(H):
+            o_ref, _ = kn.recurrence_three_step(q[i, :, h], k[i, :, h], v[i, :, h], g[i, :, h],
+                                                beta[i, :, h], S[i, h], d["scale"])
+            _, s_ref = kn.recurrence_three_step(q[i, :a, h], k[i, :a, h], v[i, :a, h], g[i, :a, h],
+                                                beta[i, :a, h], S[i, h], d["scale"])
+            assert np.allclose(out[i, :, h], o_ref, rtol=0, atol=1e-12)
+            assert np.allclose(Sk[i, h], s_ref, rtol=0, atol=1e-12)
+    assert np.array_equal(Sk[0], S[0])  # nothing accepted: the state is untouched
+
+
+def test_multi_step_outputs_do_not_depend_on_acceptance():
+    import kda_inputs as ki
+    S = ki.decode_state(2, 1, 8, 8, seed=7).double().numpy()
+    d = ki.prefill_inputs(2, 3, 1, 8, 8, "f32", seed=7)
+    o1, _ = oracle.multi_step(S, d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, np.array([0, 0]))
+    o2, S2 = oracle.multi_step(S, d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, None)
+    assert np.array_equal(o1, o2)
+    _, S3 = oracle.multi_step(S, None, d["k"], d["v"], d["g"], d["beta"], 1.0, np.array([3, 3]))
+    assert np.array_equal(S2, S3)
+
+
 # ---------------------------------------------------------------------------
 # planted mistakes: each broken copy of the loop must fail at least one pin
 
