@@ -287,9 +287,11 @@ def committed_traffic(kernel):
 
 # ---------------------------------------------------------------------------
 
-def bench_prefill(kda, idx, steps, warmup, flush, stream, clk=None, world=1):
+def bench_prefill(kda, idx, steps, warmup, flush, stream, clk=None, world=1, gated=False):
     w = ki.WORKLOADS[idx]
     d = ki.workload_inputs(idx)
+    if gated:  # decay logits + per-head scale instead of the fp32 log-decay
+        d = ki.gate_logits(d, seed=ki.SEED_BASE + idx)
     dev = torch.device("cuda")
     t = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in d.items()}
     B, T, H, dk = t["q"].shape
@@ -299,9 +301,14 @@ def bench_prefill(kda, idx, steps, warmup, flush, stream, clk=None, world=1):
     sT = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
 
     def step():
-        kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"],
-                          t["scale"], cu_seqlens=t["cu_seqlens"], out=out, final_state=sT,
-                          stream=stream)
+        if gated:
+            kda.kda_chunk_fwd_gated(t["q"], t["k"], t["v"], t["z"], t["gate_scale"], t["beta"],
+                                    t["initial_state"], t["scale"], cu_seqlens=t["cu_seqlens"], out=out,
+                                    final_state=sT, stream=stream)
+        else:
+            kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"],
+                              t["scale"], cu_seqlens=t["cu_seqlens"], out=out, final_state=sT,
+                              stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -346,9 +353,10 @@ def bench_prefill(kda, idx, steps, warmup, flush, stream, clk=None, world=1):
         kernel_ms[n] = kernel_ms.get(n, 0.0) + statistics.mean(ke[i].elapsed_time(ke[i + 1]) for ke in kev)
     th = B * T * H if t["cu_seqlens"] is None else T * H
     n_read = N if t["initial_state"] is not None else 0
+    g_saving = th * 2 * dk if gated else 0  # bf16 logits instead of fp32 log-decay
     return dict(ms=ms, token_heads=th, tokens=B * T, dk=dk, dv=dv, H=H,
                 flops=prefill_flops(th, dk, dv),
-                bytes=prefill_bytes(th, dk, dv, n_read * H, N * H),
+                bytes=prefill_bytes(th, dk, dv, n_read * H, N * H) - g_saving,
                 kernel_bytes=prefill_kernel_bytes(th, dk, dv, n_read * H, N * H),
                 kernel_ms=kernel_ms, launches=launches, wall=wall, d=d, t=t, out=out, sT=sT,
                 name=w["name"])
@@ -648,6 +656,14 @@ def main():
             "clocks": clk_k3.summary(), "gpu_launches": k3["launches"]}
         del k3
 
+    gp = bench_prefill(kda, PREFILL_W, args.steps, 3, flush, stream, None, world, gated=True)
+    gms = max_over_ranks(statistics.mean(gp["ms"]), world)
+    extra["prefill_gated"] = {
+        "workload": gp["name"] + "_gate_logits", "ms_per_step": gms,
+        "kernel_ms": {n: max_over_ranks(v, world) for n, v in gp["kernel_ms"].items()},
+        "tokens_per_s": world * gp["tokens"] / (gms * 1e-3),
+        "hbm_frac": gp["bytes"] / (gms * 1e-3) / 1e9 / pk["hbm"], "gpu_launches": gp["launches"]}
+    del gp
     if not args.no_varlen:
         clk_vl = ClockSampler(local)
         vl = bench_prefill(kda, VARLEN_W, 3, 3, flush, stream, clk_vl, world)

@@ -15,7 +15,7 @@ import torch
 from ._build import LIB, build, up_to_date  # noqa: F401
 
 __all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
-           "kda_recurrent_multi_step",
+           "kda_recurrent_multi_step", "kda_chunk_fwd_gated",
            "kda_get_device_error", "kda_set_launch_events", "kda_last_launch_count", "KdaError",
            "load_library", "build", "STATUS"]
 
@@ -24,7 +24,7 @@ STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "K
 DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
 
 EXPORTED = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
-            "kda_recurrent_multi_step",
+            "kda_recurrent_multi_step", "kda_chunk_fwd_gated",
             "kda_get_device_error", "kda_status_string", "kda_last_error_message",
             "kda_set_launch_events", "kda_last_launch_count"]
 
@@ -60,6 +60,8 @@ def load_library(path: str | None = None):
         f.restype, f.argtypes = ctypes.c_int, fwd
     lib.kda_recurrent_step.restype = ctypes.c_int
     lib.kda_recurrent_step.argtypes = [_P] * 6 + [ctypes.c_float, _P, ctypes.c_void_p]
+    lib.kda_chunk_fwd_gated.restype = ctypes.c_int
+    lib.kda_chunk_fwd_gated.argtypes = [_P] * 7 + [ctypes.c_float, _P, _P, _P, ctypes.c_void_p]
     lib.kda_recurrent_multi_step.restype = ctypes.c_int
     lib.kda_recurrent_multi_step.argtypes = [_P] * 6 + [ctypes.c_float, _P, _P, ctypes.c_void_p]
     lib.kda_get_device_error.restype = ctypes.c_int
@@ -126,6 +128,29 @@ def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, scale=None, cu_seqlens=N
     st = getattr(lib, _entry)(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), _ref(ds[4]),
                               _ref(ds[5]), float(scale), _ref(ds[6]), _ref(ds[7]), _ref(ds[8]),
                               _stream(stream))
+    _check(lib, st)
+    return out, final_state
+
+
+def kda_chunk_fwd_gated(q, k, v, gate, gate_scale, beta, initial_state=None, scale=None,
+                        cu_seqlens=None, out=None, final_state=None, output_final_state=True,
+                        stream=None):
+    """Chunked prefill with the log-decay formed in the kernel: g = -5 sigmoid(A_h z),
+    ``gate`` = z [B, T, H, dk] in q's dtype, ``gate_scale`` = A [H] fp32 (device).
+    Returns (out, final_state)."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    if scale is None:
+        scale = dk ** -0.5
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    ds = [desc(x) for x in (q, k, v, gate, gate_scale, beta, initial_state, cu_seqlens, out, final_state)]
+    st = lib.kda_chunk_fwd_gated(*[_ref(x) for x in ds[:7]], float(scale), _ref(ds[7]), _ref(ds[8]),
+                                 _ref(ds[9]), _stream(stream))
     _check(lib, st)
     return out, final_state
 

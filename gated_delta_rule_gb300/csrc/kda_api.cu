@@ -214,7 +214,7 @@ enum class PrefillPath { kChunked, kRecurrent, kChunkedNoAlloc };
 kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
                    const kda_tensor* g, const kda_tensor* beta, const kda_tensor* s0,
                    float scale, const kda_tensor* cu, kda_tensor* out, kda_tensor* sT,
-                   void* stream, PrefillPath path) {
+                   void* stream, PrefillPath path, const kda_tensor* gate_scale = nullptr) {
   g_msg.clear();
   KDA_TRY(check_desc(q, "q", 4, 16));
   const int32_t dt = q->dtype;
@@ -228,8 +228,14 @@ kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
   KDA_TRY(check_desc(k, "k", 4, 16));
   KDA_TRY(check_shape(k, "k", 4, wq, dt));
   KDA_TRY(check_shape(v, "v", 4, wv, dt));
-  KDA_TRY(check_desc(g, "g", 4, 16));
-  KDA_TRY(check_shape(g, "g", 4, wq, KDA_DTYPE_F32));
+  const bool gated = gate_scale != nullptr;
+  KDA_TRY(check_desc(g, gated ? "gate" : "g", 4, 16));
+  KDA_TRY(check_shape(g, gated ? "gate" : "g", 4, wq, gated ? dt : KDA_DTYPE_F32));
+  if (gated) {
+    KDA_TRY(check_desc(gate_scale, "gate_scale", 1, 4));
+    const int64_t wh[1] = {H};
+    KDA_TRY(check_shape(gate_scale, "gate_scale", 1, wh, KDA_DTYPE_F32));
+  }
   KDA_TRY(check_desc(beta, "beta", 3, 4));
   KDA_TRY(check_shape(beta, "beta", 3, wb, KDA_DTYPE_F32));
   KDA_TRY(check_desc(out, "out", 4, 16));
@@ -250,11 +256,13 @@ kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
   if (s0) KDA_TRY(check_state(s0, "initial_state", N, H, dk, dv));
   if (sT) KDA_TRY(check_state(sT, "final_state", N, H, dk, dv));
   // aliasing
-  const kda_tensor* ins[] = {q, k, v, g, beta, s0, cu};
-  const char* in_names[] = {"q", "k", "v", "g", "beta", "initial_state", "cu_seqlens"};
-  for (int i = 0; i < 7; ++i)
+  const kda_tensor* ins[] = {q, k, v, g, beta, s0, cu, gate_scale};
+  const char* in_names[] = {"q", "k", "v", "g", "beta", "initial_state", "cu_seqlens", "gate_scale"};
+  for (int i = 0; i < 8; ++i)
     if (ins[i] && overlap(out, ins[i]))
       return fail(KDA_ERR_INVALID_ARG, "out overlaps %s", in_names[i]);
+  if (sT && gate_scale && overlap(sT, gate_scale))
+    return fail(KDA_ERR_INVALID_ARG, "final_state overlaps gate_scale");
   if (sT) {
     if (overlap(out, sT)) return fail(KDA_ERR_INVALID_ARG, "out overlaps final_state");
     for (int i = 0; i < 5; ++i)
@@ -301,6 +309,8 @@ kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
   a.dv = (int)dv;
   a.bf16 = dt == KDA_DTYPE_BF16;
   a.scale = scale;
+  a.gate = gated ? 1 : 0;
+  a.gate_scale = gated ? static_cast<const float*>(gate_scale->data) : nullptr;
   if (N * H == 0) return KDA_OK;
   if (!a.sT && T == 0) return KDA_OK;
   if (path == PrefillPath::kChunkedNoAlloc && a.bf16) {
@@ -418,6 +428,20 @@ kda_status kda_chunk_fwd(const kda_tensor* q, const kda_tensor* k, const kda_ten
   LaunchScope scope;
   return prefill(q, k, v, g, beta, initial_state, scale, cu_seqlens, out, final_state, stream,
                  PrefillPath::kChunked);
+}
+
+kda_status kda_chunk_fwd_gated(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                               const kda_tensor* gate, const kda_tensor* gate_scale,
+                               const kda_tensor* beta, const kda_tensor* initial_state, float scale,
+                               const kda_tensor* cu_seqlens, kda_tensor* out,
+                               kda_tensor* final_state, void* stream) {
+  LaunchScope scope;
+  if (!gate_scale) {
+    g_msg.clear();
+    return fail(KDA_ERR_INVALID_ARG, "gate_scale: descriptor is NULL");
+  }
+  return prefill(q, k, v, gate, beta, initial_state, scale, cu_seqlens, out, final_state, stream,
+                 PrefillPath::kChunked, gate_scale);
 }
 
 kda_status kda_chunk_fwd_noalloc(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,

@@ -34,6 +34,10 @@ struct PrefillArgs {
   // update is kept; the final state is the state after that many tokens (clamped
   // to [0, length]) and is not written when the count is 0
   const int32_t* accepted;
+  // gate: 0 = g holds the per-token log-decay (fp32); 1 = g holds decay logits z
+  // in the q/k/v dtype and the log-decay is -5 sigmoid(gate_scale[h] z)
+  int gate;
+  const float* gate_scale;  // [H] (gate == 1)
   int B, T, H, N, dk, dv;
   int bf16;  // 1: q/k/v/out are bf16, 0: fp32
   float scale;

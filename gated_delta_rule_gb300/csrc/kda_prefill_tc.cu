@@ -223,6 +223,13 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 1/x on the special-function unit (relative error ~2^-23; 1/inf = 0).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t to_tf32(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -268,7 +275,7 @@ __device__ __forceinline__ void warp_tile_store(const float (&acc)[4], float* C,
 
 // ---------------------------------------------------------------------------
 // prep: one chunk of one head per iteration; persistent CTAs of 8 warps, two per SM
-template <int DK>
+template <int DK, bool GATE>
 __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs a, Split sp) {
   using L = PrepSmem<DK>;
   using R = Rec<DK>;
@@ -350,8 +357,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
   };
 
   uint4 rk[TPP], rq[TPP];
-  float4 rg[TPP][2];
+  float4 rg[TPP][2];  // log-decay (fp32), or
+  uint4 rz[TPP];      // decay logits (bf16) with the gate
   float rbeta = 0.f;
+  float gsc = 0.f;    // gate scale of the current head
   auto load_kq = [&](const Item& it) {
     const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(a.k.ptr) + it.brow * a.k.sb + it.h * a.k.sh;
     const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q.ptr) + it.brow * a.q.sb + it.h * a.q.sh;
@@ -365,18 +374,30 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
     }
   };
   auto load_g = [&](const Item& it) {
-    const float* gb = static_cast<const float*>(a.g.ptr) + it.brow * a.g.sb + it.h * a.g.sh;
+    if constexpr (GATE) {
+      const __nv_bfloat16* zb = static_cast<const __nv_bfloat16*>(a.g.ptr) + it.brow * a.g.sb + it.h * a.g.sh;
 #pragma unroll
-    for (int i = 0; i < TPP; ++i) {
-      const int t = part * TPP + i;
-      const bool ok = it.valid && t < it.lc;
-      const int64_t row = it.row0 + t;
-      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      rg[i][0] = ok ? __ldg(reinterpret_cast<const float4*>(gb + row * a.g.st) + 2 * oct) : z;
-      rg[i][1] = ok ? __ldg(reinterpret_cast<const float4*>(gb + row * a.g.st) + 2 * oct + 1) : z;
+      for (int i = 0; i < TPP; ++i) {
+        const int t = part * TPP + i;
+        const bool ok = it.valid && t < it.lc;
+        const int64_t row = it.row0 + t;
+        rz[i] = ok ? __ldg(reinterpret_cast<const uint4*>(zb + row * a.g.st) + oct) : make_uint4(0, 0, 0, 0);
+      }
+    } else {
+      const float* gb = static_cast<const float*>(a.g.ptr) + it.brow * a.g.sb + it.h * a.g.sh;
+#pragma unroll
+      for (int i = 0; i < TPP; ++i) {
+        const int t = part * TPP + i;
+        const bool ok = it.valid && t < it.lc;
+        const int64_t row = it.row0 + t;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        rg[i][0] = ok ? __ldg(reinterpret_cast<const float4*>(gb + row * a.g.st) + 2 * oct) : z;
+        rg[i][1] = ok ? __ldg(reinterpret_cast<const float4*>(gb + row * a.g.st) + 2 * oct + 1) : z;
+      }
     }
     const float* bb = a.beta + it.brow * a.beta_sb + it.h * a.beta_sh;
     rbeta = (it.valid && tid < it.lc) ? __ldg(bb + (it.row0 + tid) * a.beta_st) : 0.f;
+    if constexpr (GATE) gsc = it.valid ? __ldg(a.gate_scale + it.h) : 0.f;
   };
   auto pack8 = [](const float* x) {
     return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
@@ -412,8 +433,20 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < TPP; ++i) {
-          const float gv[8] = {rg[i][0].x, rg[i][0].y, rg[i][0].z, rg[i][0].w,
-                               rg[i][1].x, rg[i][1].y, rg[i][1].z, rg[i][1].w};
+          float gv[8];
+          if constexpr (GATE) {
+            // g = -5 sigmoid(A_h z) = -5 / (1 + 2^(-A_h z log2 e)); an infinite
+            // power gives a zero reciprocal, so g -> -0 for very negative A_h z.
+            // Tokens past the chunk's end (padding) keep g = 0.
+            float zf[8];
+            bf16x8(rz[i], zf);
+            const bool real = part * TPP + i < cur.lc;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) gv[e] = real ? -5.f * rcp_approx(1.f + ex2(-kLog2e * gsc * zf[e])) : 0.f;
+          } else {
+            gv[0] = rg[i][0].x; gv[1] = rg[i][0].y; gv[2] = rg[i][0].z; gv[3] = rg[i][0].w;
+            gv[4] = rg[i][1].x; gv[5] = rg[i][1].y; gv[6] = rg[i][1].z; gv[7] = rg[i][1].w;
+          }
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             acc[e] = fmaf(gv[e], kLog2e, acc[e]);
@@ -1339,7 +1372,7 @@ cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
                                                pl.ntail);
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   }
-  auto prep = kda_chunk_prep_kernel<DK>;
+  auto prep = a.gate ? kda_chunk_prep_kernel<DK, true> : kda_chunk_prep_kernel<DK, false>;
   e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, PrepSmem<DK>::kAlloc);
   if (e != cudaSuccess) return e;
   // Few chains (sequence-heads): split d_v = 128 into two 64-column CTAs so more SMs

@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 3) kda_decode_kernel(DecodeArgs a) {
 // token-by-token prefill: one CTA per (sequence, head, DV value columns), state in
 // registers.  The state's columns evolve independently, so a (sequence, head)
 // may be spread over a.dv / DV CTAs.
-template <int DK, int DV, typename T>
+template <int DK, int DV, typename T, bool GATE>
 __global__ void __launch_bounds__(kThreads, 3) kda_recurrent_kernel(PrefillArgs a) {
   using L = Layout<DK, DV>;
   __shared__ float s_q[2][DK], s_k[2][DK], s_a[2][DK];
@@ -226,7 +226,15 @@ __global__ void __launch_bounds__(kThreads, 3) kda_recurrent_kernel(PrefillArgs 
 
   const T* qb = has_q ? static_cast<const T*>(a.q.ptr) + b * a.q.sb + h * a.q.sh : nullptr;
   const T* kb = static_cast<const T*>(a.k.ptr) + b * a.k.sb + h * a.k.sh;
+  // per-token decay factors alpha = e^g: g given (fp32), or g = -5 sigmoid(A_h z)
+  // from decay logits z in the input dtype
   const float* gb = static_cast<const float*>(a.g.ptr) + b * a.g.sb + h * a.g.sh;
+  const T* zb = static_cast<const T*>(a.g.ptr) + b * a.g.sb + h * a.g.sh;
+  const float gsc = GATE ? __ldg(a.gate_scale + h) : 0.f;
+  auto alpha = [&](int64_t t) {
+    if constexpr (GATE) return expf(-5.f / (1.f + expf(-gsc * to_f(zb[t * a.g.st + tid]))));
+    else return expf(__ldg(gb + t * a.g.st + tid));
+  };
   const T* vb = static_cast<const T*>(a.v.ptr) + b * a.v.sb + h * a.v.sh + col0;
   const float* bb = a.beta + b * a.beta_sb + h * a.beta_sh;
   T* ob = a.out ? static_cast<T*>(a.out) + b * a.out_sb + h * a.out_sh + col0 : nullptr;
@@ -238,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 3) kda_recurrent_kernel(PrefillArgs 
     if (tid < DK) {
       pq = has_q ? to_f(qb[t0 * a.q.st + tid]) : 0.f;
       pk = to_f(kb[t0 * a.k.st + tid]);
-      pa = expf(__ldg(gb + t0 * a.g.st + tid));
+      pa = alpha(t0);
     }
     pv = load4<T>(vb + t0 * a.v.st + 4 * col4);
     pb = __ldg(bb + t0 * a.beta_st);
@@ -256,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 3) kda_recurrent_kernel(PrefillArgs 
       if (tid < DK) {
         pq = has_q ? to_f(qb[(t + 1) * a.q.st + tid]) : 0.f;
         pk = to_f(kb[(t + 1) * a.k.st + tid]);
-        pa = expf(__ldg(gb + (t + 1) * a.g.st + tid));
+        pa = alpha(t + 1);
       }
       pv = load4<T>(vb + (t + 1) * a.v.st + 4 * col4);
       pb = __ldg(bb + (t + 1) * a.beta_st);
@@ -354,8 +362,10 @@ cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s) {
   // 64 value columns per CTA (three CTAs per SM): for d_v = 128 a (sequence, head)
   // spreads over two CTAs, which keeps more state traffic in flight
   void (*fn)(PrefillArgs) = nullptr;
-  if (a.dk == 128) fn = a.bf16 ? kda_recurrent_kernel<128, 64, __nv_bfloat16> : kda_recurrent_kernel<128, 64, float>;
-  if (a.dk == 64) fn = a.bf16 ? kda_recurrent_kernel<64, 64, __nv_bfloat16> : kda_recurrent_kernel<64, 64, float>;
+#define KDA_REC(DK_, G_) (a.bf16 ? kda_recurrent_kernel<DK_, 64, __nv_bfloat16, G_> : kda_recurrent_kernel<DK_, 64, float, G_>)
+  if (a.dk == 128) fn = a.gate ? KDA_REC(128, true) : KDA_REC(128, false);
+  if (a.dk == 64) fn = a.gate ? KDA_REC(64, true) : KDA_REC(64, false);
+#undef KDA_REC
   if (!fn || (a.dv != 64 && a.dv != 128)) return cudaErrorInvalidValue;
   launch_begin(s);
   fn<<<dim3((unsigned)(a.N * a.H * (a.dv / 64))), kThreads, 0, s>>>(a);

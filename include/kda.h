@@ -179,6 +179,28 @@ kda_status kda_recurrent_step(kda_tensor* state, const kda_tensor* q, const kda_
                               void* stream);
 
 /*
+ * kda_chunk_fwd_gated - kda_chunk_fwd with the log-decay formed in the kernel
+ * from decay logits: g = -5 * sigmoid(gate_scale[h] * gate).
+ *
+ * "Kimi K3 技术报告解读" (marsggbo.github.io) §3.5 replaces the negative
+ * softplus decay map by a scaled sigmoid of the decay logit z with a learnable
+ * per-head scale A_h, so that every step keeps alpha > e^-5; the formula itself
+ * is not legible in the page text, and this call takes the reading that keeps
+ * that bound for any A_h: g = -5 sigmoid(A_h z).  "Kimi K3 四个核心模块的公式与
+ * 真实张量流" (gentlecold.top) §1.5 names the fused-gate chunked kernel.  The
+ * logits travel in the input dtype (bf16: 2 bytes per channel instead of 4).
+ *
+ *   gate        [B, T, H, d_k]  same dtype as q: decay logits z
+ *   gate_scale  [H] f32 on the device: A_h
+ *   all other arguments, shapes, errors and guarantees as for kda_chunk_fwd.
+ */
+kda_status kda_chunk_fwd_gated(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                               const kda_tensor* gate, const kda_tensor* gate_scale,
+                               const kda_tensor* beta, const kda_tensor* initial_state, float scale,
+                               const kda_tensor* cu_seqlens, kda_tensor* out,
+                               kda_tensor* final_state, void* stream);
+
+/*
  * kda_recurrent_multi_step - n decode tokens per request in one call, with the
  * state read once and written back once (multi-token and speculative decoding).
  *

@@ -34,6 +34,7 @@ import torch
 SEED_BASE = 20260
 
 Q, K, V, GATE, BETA, S0, LENGTHS = 1, 2, 3, 4, 5, 6, 7
+GATE_SCALE = 8
 
 # The five workloads: sizes and distributions as the KDA pages describe them
 # (96 heads x 128 head dim from "Kimi K3 四个核心模块的公式与真实张量流" §0-§1,
@@ -149,6 +150,25 @@ def prefill_inputs(B: int, T: int, H: int, dk: int, dv: int, dtype: str = "bf16"
     return dict(q=q.view(B, T, Hs, dk), k=k.view(B, T, Hs, dk), v=v.view(B, T, Hs, dv),
                 g=g.view(B, T, Hs, dk), beta=beta.view(B, T, Hs), initial_state=S,
                 scale=float(scale if scale is not None else 1.0 / math.sqrt(dk)))
+
+
+def gate_logits(d: dict, *, seed: int, heads=None) -> dict:
+    """Decay logits for the fused-gate prefill, added to the inputs ``d`` of
+    :func:`prefill_inputs`: ``z`` [B, T, H', dk] ~ N(0, 1) in q's dtype (the same
+    draws that ``d["g"]`` was formed from) and ``gate_scale`` [H'] fp32, one
+    draw per head from U(0.5, 2).  Random numbers only."""
+    B, T, Hs, dk = d["q"].shape
+    H_all = heads if heads is not None else list(range(Hs))
+    rows = B * T
+    z = torch.empty((rows, Hs, dk), dtype=d["q"].dtype)
+    A = torch.empty((Hs,), dtype=torch.float32)
+    for j, h in enumerate(H_all):
+        z[:, j] = torch.from_numpy(_normal((seed, GATE, h), (rows, dk))).to(d["q"].dtype)
+        A[j] = float(_rng(seed, GATE_SCALE, h).uniform(0.5, 2.0))
+    out = dict(d)
+    out["z"] = z.view(B, T, Hs, dk)
+    out["gate_scale"] = A
+    return out
 
 
 def decode_state(N: int, H: int, dk: int, dv: int, *, seed: int, heads=None) -> torch.Tensor:

@@ -175,3 +175,15 @@ def multi_step(state, q, k, v, g, beta, scale, num_accepted=None, nthreads=0):
     _, ST, _ = run_problems(starts, counts, kp, kp, vp, gp, bp, S.reshape(N * H, dk, dv), scale,
                             nthreads)
     return out, ST.reshape(N, H, dk, dv)
+
+
+def gate_log_decay(z, gate_scale):
+    """Log-decay of the fused-gate prefill: g = -5 sigmoid(A_h z) in fp64, z
+    [..., H, dk], A [H] ("Kimi K3 技术报告解读" (marsggbo.github.io) §3.5: a scaled
+    sigmoid of the decay logit with a learnable per-head scale, keeping every
+    per-step decay factor above e^-5; the formula's reading is that bound's)."""
+    z = _f64(z)
+    A = _f64(gate_scale).reshape(-1)
+    x = z * A[:, None]
+    with np.errstate(over="ignore"):  # exp(-x) = inf for very negative x gives g = -0
+        return -5.0 / (1.0 + np.exp(-x))

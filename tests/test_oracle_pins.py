@@ -231,6 +231,22 @@ def test_decode_step_is_one_token_prefill():
     assert np.array_equal(o, o2[:, 0]) and np.array_equal(S1, S2)
 
 
+def test_gate_closed_forms():
+    """g = -5 sigmoid(A z): -2.5 at z = 0, -5 and 0 in the limits, g(-z) = -5 - g(z),
+    strictly inside (-5, 0) for finite A z, and A scales the logit, not the output."""
+    z = np.array([[[[0.0, 1e6, -1e6, 1.3, -1.3, 0.2]]]])
+    A = np.array([1.0])
+    g = oracle.gate_log_decay(z, A)[0, 0, 0]
+    assert g[0] == -2.5 and g[1] == -5.0 and g[2] == 0.0
+    assert math.isclose(g[3] + g[4], -5.0, abs_tol=1e-15)
+    assert -5.0 < g[5] < 0.0
+    assert math.isclose(g[3], -5.0 / (1.0 + math.exp(-1.3)), rel_tol=1e-15)
+    g2 = oracle.gate_log_decay(z, np.array([2.0]))[0, 0, 0]
+    assert math.isclose(g2[5], oracle.gate_log_decay(2 * z, A)[0, 0, 0][5], rel_tol=1e-15)
+    zz = np.zeros((1, 1, 2, 3))
+    assert np.all(oracle.gate_log_decay(zz, np.array([0.5, 3.0])) == -2.5)
+
+
 def test_multi_step_matches_numpy_token_loop():
     """Multi-token decode: every request's outputs are those of the numpy three-step
     loop over its n tokens, and the kept state is that loop stopped after the
