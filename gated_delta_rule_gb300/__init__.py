@@ -15,7 +15,7 @@ import torch
 from ._build import LIB, build, up_to_date  # noqa: F401
 
 __all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
-           "kda_recurrent_multi_step", "kda_chunk_fwd_gated",
+           "kda_recurrent_multi_step", "kda_chunk_fwd_gated", "kda_chunk_fwd_checkpointed",
            "kda_get_device_error", "kda_set_launch_events", "kda_last_launch_count", "KdaError",
            "load_library", "build", "STATUS"]
 
@@ -24,7 +24,7 @@ STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "K
 DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
 
 EXPORTED = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
-            "kda_recurrent_multi_step", "kda_chunk_fwd_gated",
+            "kda_recurrent_multi_step", "kda_chunk_fwd_gated", "kda_chunk_fwd_checkpointed",
             "kda_get_device_error", "kda_status_string", "kda_last_error_message",
             "kda_set_launch_events", "kda_last_launch_count"]
 
@@ -60,6 +60,9 @@ def load_library(path: str | None = None):
         f.restype, f.argtypes = ctypes.c_int, fwd
     lib.kda_recurrent_step.restype = ctypes.c_int
     lib.kda_recurrent_step.argtypes = [_P] * 6 + [ctypes.c_float, _P, ctypes.c_void_p]
+    lib.kda_chunk_fwd_checkpointed.restype = ctypes.c_int
+    lib.kda_chunk_fwd_checkpointed.argtypes = [_P] * 6 + [ctypes.c_float, _P, ctypes.c_int64, _P, _P, _P,
+                                                   ctypes.c_void_p]
     lib.kda_chunk_fwd_gated.restype = ctypes.c_int
     lib.kda_chunk_fwd_gated.argtypes = [_P] * 7 + [ctypes.c_float, _P, _P, _P, ctypes.c_void_p]
     lib.kda_recurrent_multi_step.restype = ctypes.c_int
@@ -153,6 +156,34 @@ def kda_chunk_fwd_gated(q, k, v, gate, gate_scale, beta, initial_state=None, sca
                                  _ref(ds[9]), _stream(stream))
     _check(lib, st)
     return out, final_state
+
+
+def kda_chunk_fwd_checkpointed(q, k, v, g, beta, initial_state=None, scale=None, cu_seqlens=None,
+                               checkpoint_tokens=512, checkpoints=None, num_checkpoints=None, out=None,
+                               final_state=None, output_final_state=True, stream=None):
+    """kda_chunk_fwd plus the state after every ``checkpoint_tokens`` tokens of each
+    sequence.  ``checkpoints`` [N * C, H, dk, dv] fp32 (allocated with C =
+    ``num_checkpoints``, default T // checkpoint_tokens, when None); row n * C + j
+    is checkpoint j of sequence n.  Returns (out, final_state, checkpoints)."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    if scale is None:
+        scale = dk ** -0.5
+    if checkpoints is None:
+        C = T // checkpoint_tokens if num_checkpoints is None else int(num_checkpoints)
+        checkpoints = torch.zeros((N * C, H, dk, dv), dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    ds = [desc(x) for x in (q, k, v, g, beta, initial_state, cu_seqlens, checkpoints, out, final_state)]
+    st = lib.kda_chunk_fwd_checkpointed(*[_ref(x) for x in ds[:6]], float(scale), _ref(ds[6]),
+                                        int(checkpoint_tokens), _ref(ds[7]), _ref(ds[8]), _ref(ds[9]),
+                                        _stream(stream))
+    _check(lib, st)
+    return out, final_state, checkpoints
 
 
 def kda_fused_recurrent_fwd(*args, **kw):

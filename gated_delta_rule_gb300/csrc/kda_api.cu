@@ -214,7 +214,8 @@ enum class PrefillPath { kChunked, kRecurrent, kChunkedNoAlloc };
 kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
                    const kda_tensor* g, const kda_tensor* beta, const kda_tensor* s0,
                    float scale, const kda_tensor* cu, kda_tensor* out, kda_tensor* sT,
-                   void* stream, PrefillPath path, const kda_tensor* gate_scale = nullptr) {
+                   void* stream, PrefillPath path, const kda_tensor* gate_scale = nullptr,
+                   kda_tensor* ckpt = nullptr, int64_t ck_tokens = 0) {
   g_msg.clear();
   KDA_TRY(check_desc(q, "q", 4, 16));
   const int32_t dt = q->dtype;
@@ -263,6 +264,30 @@ kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
       return fail(KDA_ERR_INVALID_ARG, "out overlaps %s", in_names[i]);
   if (sT && gate_scale && overlap(sT, gate_scale))
     return fail(KDA_ERR_INVALID_ARG, "final_state overlaps gate_scale");
+  int64_t ck_count = 0;
+  if (ckpt) {
+    if (ck_tokens <= 0 || ck_tokens % 64 != 0 || ck_tokens > INT32_MAX)
+      return fail(KDA_ERR_INVALID_ARG, "checkpoint_tokens must be a positive multiple of 64, got %lld",
+                  (long long)ck_tokens);
+    KDA_TRY(check_desc(ckpt, "checkpoints", 4, 16));
+    if (ckpt->dtype != KDA_DTYPE_F32) return fail(KDA_ERR_INVALID_ARG, "checkpoints: dtype must be f32");
+    if (N > 0 && ckpt->shape[0] % N != 0)
+      return fail(KDA_ERR_INVALID_ARG, "checkpoints: %lld rows is not a multiple of N = %lld",
+                  (long long)ckpt->shape[0], (long long)N);
+    ck_count = N > 0 ? ckpt->shape[0] / N : 0;
+    if (ckpt->shape[1] != H || ckpt->shape[2] != dk || ckpt->shape[3] != dv)
+      return fail(KDA_ERR_INVALID_ARG, "checkpoints: expected [N * C, %lld, %lld, %lld]", (long long)H,
+                  (long long)dk, (long long)dv);
+    if (ckpt->stride[2] != dv)
+      return fail(KDA_ERR_INVALID_ARG, "checkpoints: inner [d_k, d_v] block must be contiguous");
+    if (ck_count > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "too many checkpoints");
+    const kda_tensor* others[] = {q, k, v, g, beta, s0, cu, gate_scale, out, sT};
+    const char* onames[] = {"q", "k", "v", "g", "beta", "initial_state", "cu_seqlens", "gate_scale", "out",
+                            "final_state"};
+    for (int i = 0; i < 10; ++i)
+      if (others[i] && overlap(ckpt, others[i]))
+        return fail(KDA_ERR_INVALID_ARG, "checkpoints overlaps %s", onames[i]);
+  }
   if (sT) {
     if (overlap(out, sT)) return fail(KDA_ERR_INVALID_ARG, "out overlaps final_state");
     for (int i = 0; i < 5; ++i)
@@ -311,6 +336,13 @@ kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
   a.scale = scale;
   a.gate = gated ? 1 : 0;
   a.gate_scale = gated ? static_cast<const float*>(gate_scale->data) : nullptr;
+  if (ckpt && ck_count > 0 && H > 0) {
+    a.ckpt = static_cast<float*>(ckpt->data);
+    a.ck_sr = ckpt->stride[0];
+    a.ck_sh = ckpt->stride[1];
+    a.ck_count = (int)ck_count;
+    a.ck_tokens = (int)ck_tokens;
+  }
   if (N * H == 0) return KDA_OK;
   if (!a.sT && T == 0) return KDA_OK;
   if (path == PrefillPath::kChunkedNoAlloc && a.bf16) {
@@ -442,6 +474,21 @@ kda_status kda_chunk_fwd_gated(const kda_tensor* q, const kda_tensor* k, const k
   }
   return prefill(q, k, v, gate, beta, initial_state, scale, cu_seqlens, out, final_state, stream,
                  PrefillPath::kChunked, gate_scale);
+}
+
+kda_status kda_chunk_fwd_checkpointed(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                                      const kda_tensor* g, const kda_tensor* beta,
+                                      const kda_tensor* initial_state, float scale,
+                                      const kda_tensor* cu_seqlens, int64_t checkpoint_tokens,
+                                      kda_tensor* checkpoints, kda_tensor* out, kda_tensor* final_state,
+                                      void* stream) {
+  LaunchScope scope;
+  if (!checkpoints) {
+    g_msg.clear();
+    return fail(KDA_ERR_INVALID_ARG, "checkpoints: descriptor is NULL");
+  }
+  return prefill(q, k, v, g, beta, initial_state, scale, cu_seqlens, out, final_state, stream,
+                 PrefillPath::kChunked, nullptr, checkpoints, checkpoint_tokens);
 }
 
 kda_status kda_chunk_fwd_noalloc(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,

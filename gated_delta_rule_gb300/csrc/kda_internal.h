@@ -38,6 +38,12 @@ struct PrefillArgs {
   // in the q/k/v dtype and the log-decay is -5 sigmoid(gate_scale[h] z)
   int gate;
   const float* gate_scale;  // [H] (gate == 1)
+  // nullable: state checkpoints [N * ck_count, H, dk, dv] fp32 (inner block
+  // contiguous); checkpoint j of sequence n (row n * ck_count + j) is the state
+  // after (j + 1) * ck_tokens tokens of that sequence, written when j < ck_count
+  float* ckpt;
+  int64_t ck_sr, ck_sh;  // row (n * ck_count + j) and head strides
+  int ck_count, ck_tokens;
   int B, T, H, N, dk, dv;
   int bf16;  // 1: q/k/v/out are bf16, 0: fp32
   float scale;

@@ -1095,6 +1095,19 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
 #pragma unroll
         for (int q = 0; q < DV / 32; ++q) tmem_ld32_async(tS + lane_base + 32 * q, r[q]);
         tmem_wait_ld();
+        // prefix-cache checkpoint: the state after (c0 + ci) * 64 tokens of the sequence
+        const int tok = (c0 + ci) * kC;
+        if (a.ckpt && outs && tok > 0 && tok % a.ck_tokens == 0 && tok / a.ck_tokens <= a.ck_count) {
+          float* dst = a.ckpt + ((int64_t)n * a.ck_count + tok / a.ck_tokens - 1) * a.ck_sr + h * a.ck_sh +
+                       (int64_t)tid * a.dv + un.col;
+#pragma unroll
+          for (int q = 0; q < DV / 32; ++q)
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(dst + 32 * q + i) =
+                  make_float4(__uint_as_float(r[q][i]), __uint_as_float(r[q][i + 1]), __uint_as_float(r[q][i + 2]),
+                              __uint_as_float(r[q][i + 3]));
+        }
         if (ci > 0) {
 #pragma unroll
           for (int q = 0; q < DV / 32; ++q)
@@ -1159,16 +1172,28 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
         store_out(nch - 1, false);
       }
     }
-    if (un.fin && tid < DK) {
-      float* dst = un.fin + (int64_t)tid * un.fin_ld;
+    // a checkpoint that falls on the sequence's end is the state after the last chunk
+    const int end_tok = un.c1 * kC;
+    const bool end_ck = a.ckpt && outs && nch > 0 && rg.len == end_tok && end_tok % a.ck_tokens == 0 &&
+                        end_tok / a.ck_tokens <= a.ck_count;
+    if ((un.fin || end_ck) && tid < DK) {
+      float* dst = un.fin ? un.fin + (int64_t)tid * un.fin_ld : nullptr;
+      float* cdst = end_ck ? a.ckpt + ((int64_t)n * a.ck_count + end_tok / a.ck_tokens - 1) * a.ck_sr +
+                                 h * a.ck_sh + (int64_t)tid * a.dv + un.col
+                           : nullptr;
 #pragma unroll
       for (int cb = 0; cb < DV; cb += 32) {
         float v[32];
         tmem_ld32(tS + lane_base + cb, v);
-        if (cb < un.fin_cols) {
+        if (dst && cb < un.fin_cols) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4*>(dst + cb + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
+        if (cdst) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(cdst + cb + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
         }
       }
     }

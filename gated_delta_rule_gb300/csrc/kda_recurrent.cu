@@ -289,6 +289,12 @@ __global__ void __launch_bounds__(kThreads, 3) kda_recurrent_kernel(PrefillArgs 
       s[r] = delta_write(s[r], beta * s_k[buf][i], kS, v4);
       fma4(po, s_q[buf][i], s[r]);
     }
+    if (a.ckpt && ((t - t0 + 1) % a.ck_tokens) == 0 && (t - t0 + 1) / a.ck_tokens <= a.ck_count) {
+      // prefix-cache checkpoint: the state after (t - t0 + 1) tokens of the sequence
+      float* C = a.ckpt + ((int64_t)n * a.ck_count + (t - t0 + 1) / a.ck_tokens - 1) * a.ck_sr + h * a.ck_sh + col0;
+#pragma unroll
+      for (int r = 0; r < L::R; ++r) *reinterpret_cast<float4*>(C + (trow + L::RPP * r) * ld + 4 * col4) = s[r];
+    }
     if (a.accepted && a.sT && t == t0 + keep - 1) {  // the kept state: written once
       float* ST = a.sT + n * a.sT_sn + h * a.sT_sh + col0;
 #pragma unroll

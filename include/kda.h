@@ -179,6 +179,34 @@ kda_status kda_recurrent_step(kda_tensor* state, const kda_tensor* q, const kda_
                               void* stream);
 
 /*
+ * kda_chunk_fwd_checkpointed - kda_chunk_fwd that also writes the state at
+ * regular token boundaries of every sequence (prefix-cache checkpoints).
+ *
+ * "Kimi K3 技术报告解读" (marsggbo.github.io) §9: prefixes are matched on
+ * 512-token hash blocks and the KDA state is checkpointed only at sparse block
+ * boundaries; a hit restores the nearest checkpoint and continues the prefill
+ * from there.  Checkpoint j of sequence n is the state after the first
+ * (j + 1) * checkpoint_tokens tokens of that sequence, exactly the state the
+ * chunked recurrence holds there, so a prefill resumed from it (initial_state =
+ * the checkpoint, inputs = the rest of the sequence) continues the original
+ * run; without the segment split (sequences of at most 32768 tokens) the resumed
+ * outputs and final state are bit-identical.
+ *
+ *   checkpoint_tokens  positive multiple of 64 (the chunk length)
+ *   checkpoints        [N * C, H, d_k, d_v] f32, inner [d_k, d_v] contiguous:
+ *                      row n * C + j holds checkpoint j of sequence n, for
+ *                      j < min(C, length_n / checkpoint_tokens); other rows
+ *                      are left as they are
+ *   all other arguments, shapes, errors and guarantees as for kda_chunk_fwd.
+ */
+kda_status kda_chunk_fwd_checkpointed(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                                      const kda_tensor* g, const kda_tensor* beta,
+                                      const kda_tensor* initial_state, float scale,
+                                      const kda_tensor* cu_seqlens, int64_t checkpoint_tokens,
+                                      kda_tensor* checkpoints, kda_tensor* out, kda_tensor* final_state,
+                                      void* stream);
+
+/*
  * kda_chunk_fwd_gated - kda_chunk_fwd with the log-decay formed in the kernel
  * from decay logits: g = -5 * sigmoid(gate_scale[h] * gate).
  *

@@ -187,3 +187,34 @@ def gate_log_decay(z, gate_scale):
     x = z * A[:, None]
     with np.errstate(over="ignore"):  # exp(-x) = inf for very negative x gives g = -0
         return -5.0 / (1.0 + np.exp(-x))
+
+
+def prefill_checkpoints(q, k, v, g, beta, initial_state, scale, checkpoint_tokens, num_checkpoints,
+                        cu_seqlens=None, nthreads=0):
+    """Oracle of the checkpoints of ``kda_chunk_fwd_checkpointed``: [N * C, H, dk, dv]
+    fp64 with row n * C + j = the state after the first (j + 1) * checkpoint_tokens
+    tokens of sequence n (the prefix-cache checkpoints of "Kimi K3 技术报告解读"
+    (marsggbo.github.io) §9), NaN where the sequence is shorter.  The recurrence
+    runs from checkpoint to checkpoint, carrying the state."""
+    q, k, v, g, beta = (_f64(a) for a in (q, k, v, g, beta))
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    C, ck = int(num_checkpoints), int(checkpoint_tokens)
+    if cu_seqlens is None:
+        N = B
+        spans = [(b, 0, T) for b in range(B)]
+    else:
+        cu = _f64(cu_seqlens).astype(np.int64)
+        N = cu.shape[0] - 1
+        spans = [(0, int(cu[n]), int(cu[n + 1])) for n in range(N)]
+    S0 = None if initial_state is None else _f64(initial_state).reshape(N, H, dk, dv)
+    res = np.full((N * C, H, dk, dv), np.nan)
+    for n, (b, t0, t1) in enumerate(spans):
+        S = np.zeros((H, dk, dv)) if S0 is None else S0[n].copy()
+        for j in range(min(C, (t1 - t0) // ck)):
+            a, e = t0 + j * ck, t0 + (j + 1) * ck
+            _, S = prefill(q[b:b + 1, a:e], k[b:b + 1, a:e], v[b:b + 1, a:e], g[b:b + 1, a:e],
+                           beta[b:b + 1, a:e], S[None], scale, nthreads=nthreads)
+            S = S[0]
+            res[n * C + j] = S
+    return res

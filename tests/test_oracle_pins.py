@@ -247,6 +247,26 @@ def test_gate_closed_forms():
     assert np.all(oracle.gate_log_decay(zz, np.array([0.5, 3.0])) == -2.5)
 
 
+def test_checkpoints_match_numpy_token_loop():
+    """Checkpoint j is the numpy loop's state after (j + 1) * ck tokens; rows past a
+    sequence's end are NaN."""
+    import kda_inputs as ki
+    d = ki.prefill_inputs(2, 17, 2, 8, 4, "bf16", seed=8, s0=True)
+    ck, C = 5, 4
+    res = oracle.prefill_checkpoints(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"],
+                                     d["scale"], ck, C)
+    f = lambda x: np.asarray(x.double(), dtype=np.float64)
+    q, k, v, g, beta, S0 = map(f, (d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"]))
+    for b in range(2):
+        for h in range(2):
+            for j in range(3):
+                n_tok = (j + 1) * ck
+                _, s_ref = kn.recurrence_three_step(q[b, :n_tok, h], k[b, :n_tok, h], v[b, :n_tok, h],
+                                                    g[b, :n_tok, h], beta[b, :n_tok, h], S0[b, h], d["scale"])
+                assert np.allclose(res[b * C + j, h], s_ref, rtol=0, atol=1e-12)
+            assert np.isnan(res[b * C + 3]).all()  # 17 tokens hold three checkpoints of 5
+
+
 def test_multi_step_matches_numpy_token_loop():
     """Multi-token decode: every request's outputs are those of the numpy three-step
     loop over its n tokens, and the kept state is that loop stopped after the
