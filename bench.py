@@ -483,6 +483,45 @@ def bench_multi_step(kda, n_tok, warmup, stream, clk=None, iters=20):
     return dict(ms=ms, N=N, H=H, n=n_tok, bytes=nbytes, launches=launches, iters=iters)
 
 
+def bench_decode_fused(kda, steps_total, warmup, stream, clk=None):
+    """kda_decode_step_fused on the decode batch: short convolutions, SiLU, L2 norm,
+    the step, RMSNorm and the output gate per token."""
+    w = ki.WORKLOADS[DECODE_W]
+    N, H, dk, dv = w["N"], w["H"], w["dk"], w["dv"]
+    seed = ki.SEED_BASE + DECODE_W
+    dev = torch.device("cuda")
+    S = ki.decode_state(N, H, dk, dv, seed=seed).to(dev)
+    x = {k: v.to(dev) for k, v in ki.fused_decode_extras(N, H, dk, dv, "bf16", seed=seed).items()}
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v)
+         for k, v in ki.decode_inputs(N, H, dk, dv, "bf16", seed=seed, step=0).items()}
+    out = torch.empty(N, H, dv, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        kda.kda_decode_step_fused(S, x["conv_q"], x["conv_k"], x["conv_v"], d["q"], d["k"], d["v"], x["w_q"],
+                                  x["w_k"], x["w_v"], d["g"], d["beta"], x["out_gate"], x["norm_weight"],
+                                  scale=d["scale"], eps=1e-6, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    with (clk or contextlib.nullcontext()), torch.cuda.stream(stream):
+        torch.cuda._sleep(SLEEP_CYCLES)
+        e0.record(stream)
+        for _ in range(steps_total):
+            step()
+            launches += kda.kda_last_launch_count()
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps_total
+    # state read + write, raw q/k/v, g, beta, gate logits, out, three cache slots read
+    # and written per q/k/v channel
+    per_head = 8 * dk * dv + 2 * (2 * dk + dv) + 4 * dk + 4 + 2 * dv + 2 * dv + 6 * 2 * (2 * dk + dv)
+    return dict(ms=ms, N=N, H=H, bytes=N * H * per_head, launches=launches, steps=steps_total)
+
+
 def oracle_prefill_rate(idx, max_problems=None):
     """CPU oracle on (a sample of) the workload: returns (tokens/s, threads, sample text)."""
     import oracle
@@ -627,6 +666,16 @@ def main():
                      "algorithmic_bytes_per_launch": dec["bytes"]},
         "clocks": clk_dec.summary(), "gpu_launches": dec["launches"]}
     del dec
+    fz = bench_decode_fused(kda, 64, args.warmup, stream)
+    f_ms = max_over_ranks(fz["ms"], world)
+    f_gbs = fz["bytes"] / (f_ms * 1e-3) / 1e9
+    extra["decode_fused"] = {
+        "workload": f"kda_decode_fused_N{fz['N']}_H{fz['H']}_d128", "ms_per_step": f_ms,
+        "steps_per_s": world * 1e3 / f_ms,
+        "roofline": {"bound": "hbm", "kernel": "kda_decode_fused_kernel", "achieved": f_gbs, "peak": pk["hbm"],
+                     "unit": "GB/s", "frac": f_gbs / pk["hbm"], "algorithmic_bytes_per_launch": fz["bytes"]},
+        "gpu_launches": fz["launches"]}
+    del fz
     clk_ms = ClockSampler(local)
     ms4 = bench_multi_step(kda, 4, args.warmup, stream, clk_ms)
     m_ms = max_over_ranks(ms4["ms"], world)

@@ -16,6 +16,7 @@ from ._build import LIB, build, up_to_date  # noqa: F401
 
 __all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
            "kda_recurrent_multi_step", "kda_chunk_fwd_gated", "kda_chunk_fwd_checkpointed",
+           "kda_decode_step_fused",
            "kda_get_device_error", "kda_set_launch_events", "kda_last_launch_count", "KdaError",
            "load_library", "build", "STATUS"]
 
@@ -25,6 +26,7 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
 
 EXPORTED = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
             "kda_recurrent_multi_step", "kda_chunk_fwd_gated", "kda_chunk_fwd_checkpointed",
+            "kda_decode_step_fused",
             "kda_get_device_error", "kda_status_string", "kda_last_error_message",
             "kda_set_launch_events", "kda_last_launch_count"]
 
@@ -60,6 +62,8 @@ def load_library(path: str | None = None):
         f.restype, f.argtypes = ctypes.c_int, fwd
     lib.kda_recurrent_step.restype = ctypes.c_int
     lib.kda_recurrent_step.argtypes = [_P] * 6 + [ctypes.c_float, _P, ctypes.c_void_p]
+    lib.kda_decode_step_fused.restype = ctypes.c_int
+    lib.kda_decode_step_fused.argtypes = [_P] * 14 + [ctypes.c_float, ctypes.c_float, _P, ctypes.c_void_p]
     lib.kda_chunk_fwd_checkpointed.restype = ctypes.c_int
     lib.kda_chunk_fwd_checkpointed.argtypes = [_P] * 6 + [ctypes.c_float, _P, ctypes.c_int64, _P, _P, _P,
                                                    ctypes.c_void_p]
@@ -235,6 +239,26 @@ def kda_recurrent_multi_step(state, q, k, v, g, beta, scale=None, num_accepted=N
     ds = [desc(x) for x in (state, q, k, v, g, beta, num_accepted, out)]
     st = lib.kda_recurrent_multi_step(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), _ref(ds[4]),
                                       _ref(ds[5]), float(scale), _ref(ds[6]), _ref(ds[7]), _stream(stream))
+    _check(lib, st)
+    return out
+
+
+def kda_decode_step_fused(state, conv_q, conv_k, conv_v, q, k, v, w_q, w_k, w_v, g, beta, out_gate,
+                          norm_weight=None, scale=None, eps=1e-6, out=None, stream=None):
+    """Decode step with the layer's front end (short convolutions over the caches,
+    SiLU, L2 norm of q and k) and back end (RMSNorm, sigmoid output gate).  The
+    state and the three conv caches are updated in place; returns out [N, H, dv]."""
+    lib = load_library()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if scale is None:
+        scale = dk ** -0.5
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    ds = [desc(x) for x in (state, conv_q, conv_k, conv_v, q, k, v, w_q, w_k, w_v, g, beta, out_gate,
+                            norm_weight, out)]
+    st = lib.kda_decode_step_fused(*[_ref(x) for x in ds[:14]], float(scale), float(eps), _ref(ds[14]),
+                                   _stream(stream))
     _check(lib, st)
     return out
 

@@ -571,6 +571,111 @@ kda_status kda_recurrent_step(kda_tensor* state, const kda_tensor* q, const kda_
   return KDA_OK;
 }
 
+kda_status kda_decode_step_fused(kda_tensor* state, kda_tensor* conv_q, kda_tensor* conv_k,
+                                 kda_tensor* conv_v, const kda_tensor* q, const kda_tensor* k,
+                                 const kda_tensor* v, const kda_tensor* w_q, const kda_tensor* w_k,
+                                 const kda_tensor* w_v, const kda_tensor* g, const kda_tensor* beta,
+                                 const kda_tensor* out_gate, const kda_tensor* norm_weight, float scale,
+                                 float eps, kda_tensor* out, void* stream) {
+  LaunchScope scope;
+  g_msg.clear();
+  KDA_TRY(check_desc(q, "q", 3, 16));
+  const int32_t dt = q->dtype;
+  if (dt != KDA_DTYPE_BF16 && dt != KDA_DTYPE_F32)
+    return fail(KDA_ERR_INVALID_ARG, "q: dtype must be bf16 or f32");
+  const int64_t N = q->shape[0], H = q->shape[1], dk = q->shape[2];
+  KDA_TRY(check_desc(v, "v", 3, 16));
+  const int64_t dv = v->shape[2];
+  KDA_TRY(check_head_dims(dk, dv));
+  const int64_t wq3[3] = {N, H, dk}, wv3[3] = {N, H, dv}, wb[2] = {N, H};
+  KDA_TRY(check_desc(k, "k", 3, 16));
+  KDA_TRY(check_shape(k, "k", 3, wq3, dt));
+  KDA_TRY(check_shape(v, "v", 3, wv3, dt));
+  KDA_TRY(check_desc(g, "g", 3, 16));
+  KDA_TRY(check_shape(g, "g", 3, wq3, KDA_DTYPE_F32));
+  KDA_TRY(check_desc(beta, "beta", 2, 4));
+  KDA_TRY(check_shape(beta, "beta", 2, wb, KDA_DTYPE_F32));
+  KDA_TRY(check_desc(out_gate, "out_gate", 3, 16));
+  KDA_TRY(check_shape(out_gate, "out_gate", 3, wv3, dt));
+  KDA_TRY(check_desc(out, "out", 3, 16));
+  KDA_TRY(check_shape(out, "out", 3, wv3, dt));
+  KDA_TRY(check_state(state, "state", N, H, dk, dv));
+  const int64_t cqk[4] = {N, 3, H, dk}, cvs[4] = {N, 3, H, dv};
+  KDA_TRY(check_desc(conv_q, "conv_q", 4, 2));
+  KDA_TRY(check_shape(conv_q, "conv_q", 4, cqk, dt));
+  KDA_TRY(check_desc(conv_k, "conv_k", 4, 2));
+  KDA_TRY(check_shape(conv_k, "conv_k", 4, cqk, dt));
+  KDA_TRY(check_desc(conv_v, "conv_v", 4, 2));
+  KDA_TRY(check_shape(conv_v, "conv_v", 4, cvs, dt));
+  const kda_tensor* ws[3] = {w_q, w_k, w_v};
+  const char* wn[3] = {"w_q", "w_k", "w_v"};
+  for (int i = 0; i < 3; ++i) {
+    const int64_t d = i < 2 ? dk : dv;
+    const int64_t shp[3] = {H, d, 4};
+    KDA_TRY(check_desc(ws[i], wn[i], 3, 16));
+    KDA_TRY(check_shape(ws[i], wn[i], 3, shp, KDA_DTYPE_F32));
+    if (ws[i]->stride[1] != 4 || ws[i]->stride[0] != 4 * d)
+      return fail(KDA_ERR_INVALID_ARG, "%s: must be contiguous [H, d, 4]", wn[i]);
+  }
+  if (norm_weight) {
+    const int64_t shp[1] = {dv};
+    KDA_TRY(check_desc(norm_weight, "norm_weight", 1, 16));
+    KDA_TRY(check_shape(norm_weight, "norm_weight", 1, shp, KDA_DTYPE_F32));
+  }
+  if (!isfinite(scale)) return fail(KDA_ERR_INVALID_ARG, "scale must be finite");
+  if (!isfinite(eps) || eps < 0.f) return fail(KDA_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (N * H > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "too many (request, head) pairs");
+  const kda_tensor* ins[] = {q, k, v, g, beta, out_gate, w_q, w_k, w_v, norm_weight};
+  const char* names[] = {"q", "k", "v", "g", "beta", "out_gate", "w_q", "w_k", "w_v", "norm_weight"};
+  kda_tensor* outs[] = {state, conv_q, conv_k, conv_v, out};
+  const char* onames[] = {"state", "conv_q", "conv_k", "conv_v", "out"};
+  for (int o = 0; o < 5; ++o) {
+    for (int i = 0; i < 10; ++i)
+      if (ins[i] && overlap(outs[o], ins[i])) return fail(KDA_ERR_INVALID_ARG, "%s overlaps %s", onames[o], names[i]);
+    for (int p = o + 1; p < 5; ++p)
+      if (overlap(outs[o], outs[p])) return fail(KDA_ERR_INVALID_ARG, "%s overlaps %s", onames[o], onames[p]);
+  }
+  if (N * H == 0) return KDA_OK;
+
+  kda::FusedDecodeArgs fa;
+  memset(&fa, 0, sizeof(fa));
+  kda::DecodeArgs& a = fa.d;
+  a.state = static_cast<float*>(state->data);
+  a.s_sn = state->stride[0];
+  a.s_sh = state->stride[1];
+  a.q = act(q);
+  a.k = act(k);
+  a.v = act(v);
+  a.g = act(g);
+  a.beta = static_cast<const float*>(beta->data);
+  a.beta_sn = beta->stride[0];
+  a.beta_sh = beta->stride[1];
+  a.out = out->data;
+  a.out_sn = out->stride[0];
+  a.out_sh = out->stride[1];
+  a.N = (int)N;
+  a.H = (int)H;
+  a.dk = (int)dk;
+  a.dv = (int)dv;
+  a.bf16 = dt == KDA_DTYPE_BF16;
+  a.scale = scale;
+  fa.cq = conv_q->data;
+  fa.ck = conv_k->data;
+  fa.cv = conv_v->data;
+  fa.cq_sn = conv_q->stride[0]; fa.cq_ss = conv_q->stride[1]; fa.cq_sh = conv_q->stride[2];
+  fa.ck_sn = conv_k->stride[0]; fa.ck_ss = conv_k->stride[1]; fa.ck_sh = conv_k->stride[2];
+  fa.cv_sn = conv_v->stride[0]; fa.cv_ss = conv_v->stride[1]; fa.cv_sh = conv_v->stride[2];
+  fa.wq = static_cast<const float*>(w_q->data);
+  fa.wk = static_cast<const float*>(w_k->data);
+  fa.wv = static_cast<const float*>(w_v->data);
+  fa.gate = act(out_gate);
+  fa.norm_w = norm_weight ? static_cast<const float*>(norm_weight->data) : nullptr;
+  fa.eps = eps;
+  cudaError_t e = kda::launch_decode_fused(fa, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fused decode launch");
+  return KDA_OK;
+}
+
 kda_status kda_recurrent_multi_step(kda_tensor* state, const kda_tensor* q, const kda_tensor* k,
                                     const kda_tensor* v, const kda_tensor* g, const kda_tensor* beta,
                                     float scale, const kda_tensor* num_accepted, kda_tensor* out,

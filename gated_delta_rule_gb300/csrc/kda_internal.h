@@ -63,7 +63,26 @@ struct DecodeArgs {
   float scale;
 };
 
+// Decode step with the layer's front and back ends (kda_recurrent.cu):
+// short causal convolutions of q, k, v over cached raw inputs, SiLU, L2 norm of
+// q and k, the step, then head RMSNorm and a sigmoid output gate.
+struct FusedDecodeArgs {
+  DecodeArgs d;  // q, k, v hold the raw (pre-convolution) inputs; out gets the gated output
+  // conv caches [N, 3, H, dim] in the q/k/v dtype: the last three raw inputs, oldest first
+  void* cq;
+  void* ck;
+  void* cv;
+  int64_t cq_sn, cq_ss, cq_sh, ck_sn, ck_ss, ck_sh, cv_sn, cv_ss, cv_sh;
+  const float* wq;  // conv weights [H, dim, 4] fp32, contiguous; [..., 3] multiplies the current input
+  const float* wk;
+  const float* wv;
+  Act gate;                 // output-gate logits [N, H, dv] (sb = request stride, sh = head stride)
+  const float* norm_w;      // [dv] fp32 or null
+  float eps;                // RMSNorm epsilon
+};
+
 // SIMT kernels (kda_recurrent.cu)
+cudaError_t launch_decode_fused(const FusedDecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s);
 // cu_seqlens validation: sets kErrBadSeqlens in *err when the offsets are invalid.

@@ -181,6 +181,130 @@ __global__ void __launch_bounds__(kThreads, 3) kda_decode_kernel(DecodeArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// fused decode: front end (short convolutions, SiLU, L2 norm of q and k), the
+// decode step, back end (head RMSNorm, sigmoid output gate).  One CTA per
+// (request, head) with all d_v columns, since the RMS norm spans them.
+
+// Sum of one value per thread over the first `nthr` threads (a multiple of 32),
+// returned to every thread.  `buf` holds kThreads / 32 floats; two barriers.
+__device__ __forceinline__ float block_sum(float x, float* buf, int nthr) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  if (lane == 0) buf[warp] = x;
+  __syncthreads();
+  float s = 0.f;
+  for (int w = 0; w < nthr / 32; ++w) s += buf[w];
+  __syncthreads();
+  return s;
+}
+
+// conv (width 4, causal, depthwise) of channel c, then SiLU; the cache slots
+// move down by one and the raw input enters the newest slot.
+template <typename T>
+__device__ __forceinline__ float conv_silu_update(T* cache, int64_t slot_stride, const T* x, const float* w) {
+  const float c0 = to_f(cache[0]), c1 = to_f(cache[slot_stride]), c2 = to_f(cache[2 * slot_stride]);
+  const T raw = *x;
+  const float4 wv = __ldg(reinterpret_cast<const float4*>(w));
+  const float y = wv.x * c0 + wv.y * c1 + wv.z * c2 + wv.w * to_f(raw);
+  cache[0] = cache[slot_stride];
+  cache[slot_stride] = cache[2 * slot_stride];
+  cache[2 * slot_stride] = raw;
+  return y / (1.f + expf(-y));
+}
+
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kThreads, 2) kda_decode_fused_kernel(FusedDecodeArgs fa) {
+  using L = Layout<DK, DV>;
+  const DecodeArgs& a = fa.d;
+  __shared__ float s_q[DK], s_k[DK], s_a[DK], s_v[DV], s_buf[kThreads / 32];
+  __shared__ float4 red0[L::RPP][DV / 4];
+  __shared__ float4 red1[L::RPP][DV / 4];
+  const int n = blockIdx.x / a.H;
+  const int h = blockIdx.x - n * a.H;
+  const int tid = threadIdx.x;
+  const int col4 = tid % L::TPR;
+  const int trow = tid / L::TPR;
+
+  float* S = a.state + n * a.s_sn + h * a.s_sh;
+  float4 s[L::R];
+#pragma unroll
+  for (int r = 0; r < L::R; ++r)  // issued first: the front end runs while the state arrives
+    s[r] = __ldcs(reinterpret_cast<const float4*>(S + (trow + L::RPP * r) * DV + 4 * col4));
+
+  // ---- front end ----
+  float qa = 0.f, ka = 0.f;
+  if (tid < DK) {
+    T* cq = static_cast<T*>(fa.cq) + n * fa.cq_sn + h * fa.cq_sh + tid;
+    T* ck = static_cast<T*>(fa.ck) + n * fa.ck_sn + h * fa.ck_sh + tid;
+    qa = conv_silu_update<T>(cq, fa.cq_ss, static_cast<const T*>(a.q.ptr) + n * a.q.sb + h * a.q.sh + tid,
+                             fa.wq + ((int64_t)h * DK + tid) * 4);
+    ka = conv_silu_update<T>(ck, fa.ck_ss, static_cast<const T*>(a.k.ptr) + n * a.k.sb + h * a.k.sh + tid,
+                             fa.wk + ((int64_t)h * DK + tid) * 4);
+    s_a[tid] = expf(__ldg(static_cast<const float*>(a.g.ptr) + n * a.g.sb + h * a.g.sh + tid));
+  }
+  if (tid < DV) {
+    T* cv = static_cast<T*>(fa.cv) + n * fa.cv_sn + h * fa.cv_sh + tid;
+    s_v[tid] = conv_silu_update<T>(cv, fa.cv_ss, static_cast<const T*>(a.v.ptr) + n * a.v.sb + h * a.v.sh + tid,
+                                   fa.wv + ((int64_t)h * DV + tid) * 4);
+  }
+  const float nq = sqrtf(block_sum(qa * qa, s_buf, DK));
+  const float nk = sqrtf(block_sum(ka * ka, s_buf, DK));
+  if (tid < DK) {
+    s_q[tid] = qa / fmaxf(nq, 1e-6f);
+    s_k[tid] = ka / fmaxf(nk, 1e-6f);
+  }
+  const float beta = __ldg(a.beta + n * a.beta_sn + h * a.beta_sh);
+  __syncthreads();
+  const float4 v4 = *reinterpret_cast<const float4*>(s_v + 4 * col4);
+
+  // ---- the decode step ----
+  float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int r = 0; r < L::R; ++r) {
+    const int i = trow + L::RPP * r;
+    const float al = s_a[i];
+    s[r].x *= al;
+    s[r].y *= al;
+    s[r].z *= al;
+    s[r].w *= al;
+    fma4(part, s_k[i], s[r]);
+  }
+  const float4 kS = column_reduce<DK, DV>(part, red0, trow, col4);
+  float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int r = 0; r < L::R; ++r) {
+    const int i = trow + L::RPP * r;
+    s[r] = delta_write(s[r], beta * s_k[i], kS, v4);
+    __stcs(reinterpret_cast<float4*>(S + i * DV + 4 * col4), s[r]);
+    fma4(po, s_q[i], s[r]);
+  }
+  float4 o = column_reduce<DK, DV>(po, red1, trow, col4);
+
+  // ---- back end: the threads of row group 0 hold the d_v outputs ----
+  if (trow == 0) {
+    o.x *= a.scale;
+    o.y *= a.scale;
+    o.z *= a.scale;
+    o.w *= a.scale;
+    float ss = o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
+    // row group 0 is lanes 0 .. TPR-1 of warp 0: only those take part
+    constexpr unsigned kMask = L::TPR >= 32 ? 0xffffffffu : ((1u << L::TPR) - 1u);
+#pragma unroll
+    for (int off = L::TPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(kMask, ss, off, L::TPR);
+    const float inv = rsqrtf(ss / DV + fa.eps);
+    const float4 gl = load4<T>(static_cast<const T*>(fa.gate.ptr) + n * fa.gate.sb + h * fa.gate.sh + 4 * col4);
+    const float4 wn = fa.norm_w ? __ldg(reinterpret_cast<const float4*>(fa.norm_w + 4 * col4))
+                                : make_float4(1.f, 1.f, 1.f, 1.f);
+    o.x = o.x * inv * wn.x / (1.f + expf(-gl.x));
+    o.y = o.y * inv * wn.y / (1.f + expf(-gl.y));
+    o.z = o.z * inv * wn.z / (1.f + expf(-gl.z));
+    o.w = o.w * inv * wn.w / (1.f + expf(-gl.w));
+    store4<T>(static_cast<T*>(a.out) + n * a.out_sn + h * a.out_sh + 4 * col4, o);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // token-by-token prefill: one CTA per (sequence, head, DV value columns), state in
 // registers.  The state's columns evolve independently, so a (sequence, head)
 // may be spread over a.dv / DV CTAs.
@@ -375,6 +499,25 @@ cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s) {
   if (!fn || (a.dv != 64 && a.dv != 128)) return cudaErrorInvalidValue;
   launch_begin(s);
   fn<<<dim3((unsigned)(a.N * a.H * (a.dv / 64))), kThreads, 0, s>>>(a);
+  const cudaError_t e = cudaGetLastError();
+  return e != cudaSuccess ? e : launch_end(s);
+}
+
+cudaError_t launch_decode_fused(const FusedDecodeArgs& fa, cudaStream_t s) {
+  const DecodeArgs& a = fa.d;
+  if ((int64_t)a.N * a.H == 0) return cudaSuccess;
+  void (*fn)(FusedDecodeArgs) = nullptr;
+#define KDA_FCASE(DK_, DV_)                                                                     \
+  if (a.dk == DK_ && a.dv == DV_)                                                               \
+    fn = a.bf16 ? kda_decode_fused_kernel<DK_, DV_, __nv_bfloat16> : kda_decode_fused_kernel<DK_, DV_, float>;
+  KDA_FCASE(64, 64)
+  KDA_FCASE(64, 128)
+  KDA_FCASE(128, 64)
+  KDA_FCASE(128, 128)
+#undef KDA_FCASE
+  if (!fn) return cudaErrorInvalidValue;
+  launch_begin(s);
+  fn<<<dim3((unsigned)(a.N * a.H)), kThreads, 0, s>>>(fa);
   const cudaError_t e = cudaGetLastError();
   return e != cudaSuccess ? e : launch_end(s);
 }

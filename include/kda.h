@@ -229,6 +229,42 @@ kda_status kda_chunk_fwd_gated(const kda_tensor* q, const kda_tensor* k, const k
                                kda_tensor* final_state, void* stream);
 
 /*
+ * kda_decode_step_fused - one decode token per (request, head) with the KDA
+ * layer's front and back ends fused around kda_recurrent_step.
+ *
+ * Front ("Kimi K3 四个核心模块的公式与真实张量流" (gentlecold.top) §1.2; "Kimi K3
+ * 核心算子拆解" (devpress.csdn.net) §2.6): each of q, k, v passes a causal
+ * depthwise convolution of width 4 over its three cached raw inputs and the new
+ * one, then SiLU; q and k are L2-normalised (x / max(||x||, 1e-6)).  The caches
+ * then drop their oldest input and take the new raw one.  Core: the decode step
+ * on the processed q, k, v.  Back ("把注意力换成一块「会遗忘的内存」"
+ * (jokeuncle.github.io), the sigmoid output gate of the layer's norm; devpress
+ * §2.5): out = o / sqrt(mean(o^2) + eps) * norm_weight * sigmoid(out_gate), o the
+ * step's read-out (scale * S^T q) over the head's d_v values.
+ *
+ *   state            [N, H, d_k, d_v] f32, inner block contiguous; in/out
+ *   conv_q, conv_k   [N, 3, H, d_k] in q's dtype; conv_v [N, 3, H, d_v]: the last
+ *                    three raw inputs, oldest first; in/out
+ *   q, k             [N, H, d_k] raw (pre-convolution) inputs, bf16 or f32
+ *   v                [N, H, d_v] raw, q's dtype
+ *   w_q, w_k         [H, d_k, 4] f32 contiguous; w_v [H, d_v, 4]: convolution
+ *                    weights, [..., 3] multiplying the new input
+ *   g                [N, H, d_k] f32 log-decay; beta [N, H] f32
+ *   out_gate         [N, H, d_v] q's dtype: output-gate logits
+ *   norm_weight      [d_v] f32, or NULL (all ones)
+ *   scale, eps       finite; eps >= 0
+ *   out              [N, H, d_v] q's dtype
+ *
+ * Errors as for kda_recurrent_step; no output may overlap another tensor.
+ */
+kda_status kda_decode_step_fused(kda_tensor* state, kda_tensor* conv_q, kda_tensor* conv_k,
+                                 kda_tensor* conv_v, const kda_tensor* q, const kda_tensor* k,
+                                 const kda_tensor* v, const kda_tensor* w_q, const kda_tensor* w_k,
+                                 const kda_tensor* w_v, const kda_tensor* g, const kda_tensor* beta,
+                                 const kda_tensor* out_gate, const kda_tensor* norm_weight, float scale,
+                                 float eps, kda_tensor* out, void* stream);
+
+/*
  * kda_recurrent_multi_step - n decode tokens per request in one call, with the
  * state read once and written back once (multi-token and speculative decoding).
  *

@@ -35,6 +35,7 @@ SEED_BASE = 20260
 
 Q, K, V, GATE, BETA, S0, LENGTHS = 1, 2, 3, 4, 5, 6, 7
 GATE_SCALE = 8
+CONV_W, CONV_CACHE, OUT_GATE, NORM_W = 9, 10, 11, 12
 
 # The five workloads: sizes and distributions as the KDA pages describe them
 # (96 heads x 128 head dim from "Kimi K3 四个核心模块的公式与真实张量流" §0-§1,
@@ -169,6 +170,24 @@ def gate_logits(d: dict, *, seed: int, heads=None) -> dict:
     out["z"] = z.view(B, T, Hs, dk)
     out["gate_scale"] = A
     return out
+
+
+def fused_decode_extras(N: int, H: int, dk: int, dv: int, dtype: str = "bf16", *, seed: int,
+                        step: int = 0) -> dict:
+    """Synthetic tensors of the fused decode step: convolution weights w_q, w_k
+    [H, dk, 4], w_v [H, dv, 4] ~ N(0, 0.5^2) fp32; conv caches conv_q, conv_k [N, 3,
+    H, dk], conv_v [N, 3, H, dv] ~ N(0, 1) in ``dtype``; output-gate logits out_gate
+    [N, H, dv] ~ N(0, 1) in ``dtype`` (fresh per step); norm_weight [dv] ~ U(0.5,
+    1.5).  Random numbers only."""
+    tdt = torch_dtype(dtype)
+    f = lambda key, shape: torch.from_numpy(_normal((seed,) + key, shape))
+    return dict(
+        w_q=0.5 * f((CONV_W, 0), (H, dk, 4)), w_k=0.5 * f((CONV_W, 1), (H, dk, 4)),
+        w_v=0.5 * f((CONV_W, 2), (H, dv, 4)),
+        conv_q=f((CONV_CACHE, 0), (N, 3, H, dk)).to(tdt), conv_k=f((CONV_CACHE, 1), (N, 3, H, dk)).to(tdt),
+        conv_v=f((CONV_CACHE, 2), (N, 3, H, dv)).to(tdt),
+        out_gate=f((OUT_GATE, step), (N, H, dv)).to(tdt),
+        norm_weight=torch.from_numpy(_rng(seed, NORM_W).uniform(0.5, 1.5, dv).astype(np.float32)))
 
 
 def decode_state(N: int, H: int, dk: int, dv: int, *, seed: int, heads=None) -> torch.Tensor:

@@ -218,3 +218,42 @@ def prefill_checkpoints(q, k, v, g, beta, initial_state, scale, checkpoint_token
             S = S[0]
             res[n * C + j] = S
     return res
+
+
+def decode_fused(state, conv_q, conv_k, conv_v, q, k, v, w_q, w_k, w_v, g, beta, out_gate,
+                 norm_weight, scale, eps, l2_eps=1e-6, nthreads=0):
+    """Oracle of ``kda_decode_step_fused``: one decode token with the layer's front
+    and back ends, in fp64.
+
+    Front ("Kimi K3 四个核心模块的公式与真实张量流" (gentlecold.top) §1.2; "Kimi K3
+    核心算子拆解" (devpress.csdn.net) §2.6): each of q, k, v goes through a causal
+    depthwise convolution of width 4 over its last three raw inputs (conv_* [N, 3, H,
+    d], oldest first) and itself, weights w_* [H, d, 4] (w[..., 3] on the current
+    input), then SiLU; q and k are L2-normalised (x / max(||x||, l2_eps)).  Core: the
+    decode step.  Back ("把注意力换成一块「会遗忘的内存」" (jokeuncle.github.io), the
+    output gate; devpress §2.5): y = o / sqrt(mean(o^2) + eps) * norm_weight *
+    sigmoid(out_gate).  Returns (y [N, H, dv], new state, new conv_q, conv_k, conv_v).
+    """
+    S = _f64(state)
+    cq, ck, cv = (_f64(a) for a in (conv_q, conv_k, conv_v))
+    xq, xk, xv = (_f64(a) for a in (q, k, v))
+    wq, wk, wv = (_f64(a) for a in (w_q, w_k, w_v))
+
+    def conv_silu(cache, x, w):
+        y = (w[None, :, :, 0] * cache[:, 0] + w[None, :, :, 1] * cache[:, 1] +
+             w[None, :, :, 2] * cache[:, 2] + w[None, :, :, 3] * x)
+        return y / (1.0 + np.exp(-y))
+
+    def l2n(x):
+        n = np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
+        return x / np.maximum(n, l2_eps)
+
+    qa = l2n(conv_silu(cq, xq, wq))
+    ka = l2n(conv_silu(ck, xk, wk))
+    va = conv_silu(cv, xv, wv)
+    o, S1 = decode_step(S, qa, ka, va, g, beta, scale, nthreads)
+    gate = _f64(out_gate)
+    wn = np.ones(o.shape[-1]) if norm_weight is None else _f64(norm_weight)
+    y = o / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps) * wn / (1.0 + np.exp(-gate))
+    shift = lambda c, x: np.concatenate([c[:, 1:], x[:, None]], axis=1)
+    return y, S1, shift(cq, xq), shift(ck, xk), shift(cv, xv)

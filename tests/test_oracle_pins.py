@@ -267,6 +267,47 @@ def test_checkpoints_match_numpy_token_loop():
             assert np.isnan(res[b * C + 3]).all()  # 17 tokens hold three checkpoints of 5
 
 
+def test_decode_fused_special_cases():
+    """Fused decode front/back ends: an identity convolution (weight only on the
+    current input) with inputs whose SiLU is known; q, k come out unit-length; the
+    cache shifts by one; a zero gate logit halves, and the RMS norm makes the output
+    of a constant vector equal to the norm weight."""
+    rng = np.random.default_rng(3)
+    N, H, dk, dv = 2, 2, 4, 3
+    S = rng.standard_normal((N, H, dk, dv))
+    cq, ck = rng.standard_normal((N, 3, H, dk)), rng.standard_normal((N, 3, H, dk))
+    cv = rng.standard_normal((N, 3, H, dv))
+    q, k, v = rng.standard_normal((N, H, dk)), rng.standard_normal((N, H, dk)), rng.standard_normal((N, H, dv))
+    w_id_k = np.zeros((H, dk, 4)); w_id_k[..., 3] = 1.0
+    w_id_v = np.zeros((H, dv, 4)); w_id_v[..., 3] = 1.0
+    g = -rng.uniform(0, 5, (N, H, dk)); beta = rng.uniform(0, 1, (N, H))
+    gate = np.zeros((N, H, dv)); wn = rng.uniform(0.5, 2, dv)
+    y, S1, nq, nk, nv = oracle.decode_fused(S, cq, ck, cv, q, k, v, w_id_k, w_id_k, w_id_v, g, beta,
+                                            gate, wn, 0.5, 0.0)
+    silu = lambda x: x / (1 + np.exp(-x))
+    qa, ka = silu(q), silu(k)
+    qa /= np.linalg.norm(qa, axis=-1, keepdims=True)
+    ka /= np.linalg.norm(ka, axis=-1, keepdims=True)
+    for n in range(N):
+        for h in range(H):
+            o, s_ref = kn.recurrence_three_step(qa[n, h][None], ka[n, h][None], silu(v[n, h])[None],
+                                                g[n, h][None], beta[n, h][None], S[n, h], 0.5)
+            assert np.allclose(S1[n, h], s_ref, rtol=0, atol=1e-12)
+            o = o[0]
+            assert np.allclose(y[n, h], o / np.sqrt(np.mean(o * o)) * wn * 0.5, rtol=1e-12, atol=0)
+    assert np.array_equal(nq[:, :2], cq[:, 1:]) and np.array_equal(nq[:, 2], q)
+    assert np.array_equal(nv[:, 2], v)
+    # a convolution that only sees the oldest cached input
+    w_old = np.zeros((H, dk, 4)); w_old[..., 0] = 2.0
+    y2, S2, *_ = oracle.decode_fused(S, cq, ck, cv, q, k, v, w_old, w_old, np.concatenate(
+        [np.zeros((H, dv, 3)), np.ones((H, dv, 1))], -1), g, beta, gate, None, 0.5, 0.0)
+    qa2 = silu(2.0 * cq[:, 0]); qa2 /= np.linalg.norm(qa2, axis=-1, keepdims=True)
+    ka2 = silu(2.0 * ck[:, 0]); ka2 /= np.linalg.norm(ka2, axis=-1, keepdims=True)
+    _, s2 = kn.recurrence_three_step(qa2[0, 0][None], ka2[0, 0][None], silu(v[0, 0])[None], g[0, 0][None],
+                                     beta[0, 0][None], S[0, 0], 0.5)
+    assert np.allclose(S2[0, 0], s2, rtol=0, atol=1e-12)
+
+
 def test_multi_step_matches_numpy_token_loop():
     """Multi-token decode: every request's outputs are those of the numpy three-step
     loop over its n tokens, and the kept state is that loop stopped after the
