@@ -36,8 +36,9 @@
 //   * Gram blocks use, for output rows in sub-block I, the reference G at the
 //     start of sub-block I: rows K_i e^{G_i - G_{16I-1}} (<= 1) and columns
 //     K_j e^{G_{16I-1} - G_j} (<= 1 for earlier sub-blocks, < e^80 inside I).
-//     The column operand exists in 4 versions (16, 32, 48, 64 rows); product I
-//     covers all 128 rows [K; Q] and only its row block I is kept.
+//     The column operand exists in 4 versions (16, 32, 48, 64 rows), stacked as
+//     one 160-row operand; one product covers all 128 rows [K; Q] against all
+//     versions, and row block I keeps only version I's columns.
 //   * K+ = K e^{G}, Q+ = Q e^{G}, K e^{G_C - G} are all <= 1.
 //
 // Several M = 128 products only use 64 meaningful A rows: their descriptor
@@ -85,7 +86,7 @@ struct PrepSmem {
   static constexpr int kParts = kThreads / (DK / 8);   // token parts of the build
   // region shared by the Gram operands and, after the Gram product, the solve
   static constexpr int X = 0;                          // 128 rows [K; Q] x DK, K-major
-  static constexpr int Y = X + 128 * DK * 2;           // versions 0..3, 160 rows x DK, K-major
+  static constexpr int Y = X + 128 * DK * 2;           // versions 0..3 stacked: one 160-row K-major tile
   static constexpr int kGram = Y + 160 * DK * 2;
   static constexpr int CARRY = 0;                      // scan partials [part][DK] fp32 (before X is built)
   static_assert(kParts * DK * 4 <= 128 * DK * 2, "scan partials fit below Y");
@@ -555,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = y[i][e] * f[e];
-            st8(sbase + L::Y + yoff_rows(J) * DK * 2 + sw128(part * TPP + i, col, yrows(J)), x);
+            st8(sbase + L::Y + sw128(yoff_rows(J) + part * TPP + i, col, 160), x);
           }
         }
         // K_end = y 2^{bnd[4] - bnd[blk]} (record, token rows)
@@ -575,16 +576,14 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
       fence_before_sync();
       __syncthreads();
 
-      // ================= Gram: row block I against column version I =================
+      // ================= Gram: all 128 rows [K; Q] against the four column versions =================
+      // (one N = 160 product; row block I later reads only version I's columns)
       if (tid == 0) {
         fence_after_sync();
 #pragma unroll
-        for (int I = 0; I < 4; ++I)
-#pragma unroll
-          for (int ks = 0; ks < DK / 16; ++ks)
-            mma_bf16(tmem + yoff_rows(I), desc_kmajor(sbase + L::X, 128, ks),
-                     desc_kmajor(sbase + L::Y + yoff_rows(I) * DK * 2, yrows(I), ks),
-                     idesc_bf16(128, yrows(I), false, false), ks > 0);
+        for (int ks = 0; ks < DK / 16; ++ks)
+          mma_bf16(tmem, desc_kmajor(sbase + L::X, 128, ks), desc_kmajor(sbase + L::Y, 160, ks),
+                   idesc_bf16(128, 160, false, false), ks > 0);
         mma_commit(ctx.mbar);
       }
       // the k/q registers are free: start loading the next item while the MMAs run
