@@ -329,14 +329,15 @@ def bench_prefill(kda, idx, steps, warmup, flush, stream, clk=None, world=1, gat
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
+    # timed steps: events only around each whole call, so nothing sits between
+    # the library's own launches (its kernels may overlap one another)
     with (clk or contextlib.nullcontext()), torch.cuda.stream(stream):
-        for (e0, e1), ke in zip(evs, kev):
+        for e0, e1 in evs:
             flush.zero_()
             # keep the GPU busy while the host enqueues the step, so no host-side
             # gap falls between the events
             torch.cuda._sleep(SLEEP_CYCLES)
             e0.record(stream)
-            kda.kda_set_launch_events(ke)
             step()
             launches += kda.kda_last_launch_count()
             e1.record(stream)
@@ -346,6 +347,15 @@ def bench_prefill(kda, idx, steps, warmup, flush, stream, clk=None, world=1, gat
     wall = time.perf_counter() - wall0
     kda.kda_get_device_error(stream)
     ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    # the same steps again with the library recording an event between its
+    # kernels: the per-kernel split (these events serialise the kernels)
+    with torch.cuda.stream(stream):
+        for ke in kev:
+            flush.zero_()
+            torch.cuda._sleep(SLEEP_CYCLES)
+            kda.kda_set_launch_events(ke)
+            step()
+        stream.synchronize()
     if launches != steps * len(names):
         raise RuntimeError(f"expected {len(names)} kernels per step, counted {launches / steps}")
     kernel_ms = {}

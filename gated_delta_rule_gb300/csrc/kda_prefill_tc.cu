@@ -315,6 +315,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
   fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::TSLOT);
   Ctx ctx{sbase + L::MBAR, 0u, sFlag, a.err};
+  // the serial kernel may be launched now (it waits for this grid before it reads
+  // any record), so its CTAs set up on SMs this grid leaves early
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int oct = tid % OCT;
   const int part = tid / OCT;
@@ -967,6 +970,9 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
 
   if (warp == 5) {
     // ======================= producer warp =======================
+    // the records come from the previous grid (launched with programmatic
+    // serialization): wait until it has completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int ci = 0; ci < nch; ++ci) {
       const int b = ci & 1;
       if (ci >= 2) wait(mbar_free0 + 8 * b, (uint32_t)(((ci - 2) >> 1) & 1));  // chunk ci - 2 is done
@@ -1415,12 +1421,25 @@ cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
     prep<<<grid, kThreads, PrepSmem<DK>::kAlloc, s>>>(a, sp);
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   }
-  // pass 0: every sequence's first segment, and the tail segments' (S~ | M)
+  // pass 0: every sequence's first segment, and the tail segments' (S~ | M).
+  // Programmatic serialization lets its CTAs start while prep finishes.
   const int64_t nfirst = (int64_t)a.N * a.H * (DV / W);
   const int64_t ntail_ctas = (int64_t)pl.ntail * a.H * ((DV + DK + W - 1) / W);
-  launch_begin(s);
-  ser<<<dim3((unsigned)(nfirst + ntail_ctas)), kSerialThreads, ser_smem, s>>>(a, sp, sg, 0);
-  if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(nfirst + ntail_ctas));
+    cfg.blockDim = dim3(kSerialThreads);
+    cfg.dynamicSmemBytes = (size_t)ser_smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = grid > 0 ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    launch_begin(s);
+    if ((e = cudaLaunchKernelEx(&cfg, ser, a, sp, sg, 0)) != cudaSuccess || (e = launch_end(s)) != cudaSuccess)
+      return e;
+  }
   if (pl.ntail == 0) return cudaSuccess;
   // states entering the tail segments (only sequences of three or more segments need it)
   if (a.cu_seqlens ? pl.ntail >= 2 : pl.tps >= 2) {
