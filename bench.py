@@ -532,6 +532,44 @@ def bench_decode_fused(kda, steps_total, warmup, stream, clk=None):
     return dict(ms=ms, N=N, H=H, bytes=N * H * per_head, launches=launches, steps=steps_total)
 
 
+def bench_backward(kda, steps, warmup, stream):
+    """kda_backward on the headline prefill workload (B=2, H=16, T=4096): gradients of
+    every input given random output and final-state gradients."""
+    d = ki.workload_inputs(PREFILL_W)
+    dev = torch.device("cuda")
+    t = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in d.items()}
+    B, T, H, dk = t["q"].shape
+    dv = t["v"].shape[-1]
+    gen = torch.Generator().manual_seed(1)
+    do = torch.randn(B, T, H, dv, generator=gen).to(torch.bfloat16).to(dev)
+    dST = torch.randn(B, H, dk, dv, generator=gen).to(dev)
+
+    def step():
+        kda.kda_backward(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"], t["scale"], do, dST,
+                         stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(SLEEP_CYCLES)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+            launches += kda.kda_last_launch_count()
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    th = B * T * H
+    # inputs (q, k, v, d_out bf16; g fp32; beta) and fp32 gradients, plus the states
+    per = 2 * (2 * dk + 2 * dv) + 4 * dk + 4 + 4 * (3 * dk + dv) + 4
+    nbytes = th * per + 4 * dk * dv * B * H * 4
+    return dict(ms=ms, tokens=B * T, bytes=nbytes, launches=launches, name=ki.WORKLOADS[PREFILL_W]["name"])
+
+
 def oracle_prefill_rate(idx, max_problems=None):
     """CPU oracle on (a sample of) the workload: returns (tokens/s, threads, sample text)."""
     import oracle
@@ -723,6 +761,13 @@ def main():
         "tokens_per_s": world * gp["tokens"] / (gms * 1e-3),
         "hbm_frac": gp["bytes"] / (gms * 1e-3) / 1e9 / pk["hbm"], "gpu_launches": gp["launches"]}
     del gp
+    bw = bench_backward(kda, max(3, args.steps // 4), 3, stream)
+    bms = max_over_ranks(bw["ms"], world)
+    extra["backward"] = {
+        "workload": bw["name"] + "_backward", "ms_per_call": bms,
+        "tokens_per_s": world * bw["tokens"] / (bms * 1e-3),
+        "hbm_frac": bw["bytes"] / (bms * 1e-3) / 1e9 / pk["hbm"], "gpu_launches": bw["launches"]}
+    del bw
     if not args.no_varlen:
         clk_vl = ClockSampler(local)
         vl = bench_prefill(kda, VARLEN_W, 3, 3, flush, stream, clk_vl, world)

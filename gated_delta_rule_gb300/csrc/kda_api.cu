@@ -571,6 +571,144 @@ kda_status kda_recurrent_step(kda_tensor* state, const kda_tensor* q, const kda_
   return KDA_OK;
 }
 
+kda_status kda_backward(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                        const kda_tensor* g, const kda_tensor* beta, const kda_tensor* initial_state,
+                        float scale, const kda_tensor* cu, const kda_tensor* d_out,
+                        const kda_tensor* d_final_state, kda_tensor* dq, kda_tensor* dk, kda_tensor* dv,
+                        kda_tensor* dg, kda_tensor* dbeta, kda_tensor* d_initial_state, void* stream) {
+  LaunchScope scope;
+  g_msg.clear();
+  KDA_TRY(check_desc(q, "q", 4, 16));
+  const int32_t dt = q->dtype;
+  if (dt != KDA_DTYPE_BF16 && dt != KDA_DTYPE_F32)
+    return fail(KDA_ERR_INVALID_ARG, "q: dtype must be bf16 or f32");
+  const int64_t B = q->shape[0], T = q->shape[1], H = q->shape[2], dk_ = q->shape[3];
+  KDA_TRY(check_desc(v, "v", 4, 16));
+  const int64_t dv_ = v->shape[3];
+  KDA_TRY(check_head_dims(dk_, dv_));
+  const int64_t wq[4] = {B, T, H, dk_}, wv[4] = {B, T, H, dv_}, wb[3] = {B, T, H};
+  KDA_TRY(check_desc(k, "k", 4, 16));
+  KDA_TRY(check_shape(k, "k", 4, wq, dt));
+  KDA_TRY(check_shape(v, "v", 4, wv, dt));
+  KDA_TRY(check_desc(g, "g", 4, 16));
+  KDA_TRY(check_shape(g, "g", 4, wq, KDA_DTYPE_F32));
+  KDA_TRY(check_desc(beta, "beta", 3, 4));
+  KDA_TRY(check_shape(beta, "beta", 3, wb, KDA_DTYPE_F32));
+  KDA_TRY(check_desc(d_out, "d_out", 4, 16));
+  KDA_TRY(check_shape(d_out, "d_out", 4, wv, dt));
+  kda_tensor* gq[4] = {dq, dk, dv, dg};
+  const char* gn[4] = {"dq", "dk", "dv", "dg"};
+  for (int i = 0; i < 4; ++i) {
+    KDA_TRY(check_desc(gq[i], gn[i], 4, 16));
+    KDA_TRY(check_shape(gq[i], gn[i], 4, i == 2 ? wv : wq, KDA_DTYPE_F32));
+  }
+  KDA_TRY(check_desc(dbeta, "dbeta", 3, 4));
+  KDA_TRY(check_shape(dbeta, "dbeta", 3, wb, KDA_DTYPE_F32));
+  if (!isfinite(scale)) return fail(KDA_ERR_INVALID_ARG, "scale must be finite");
+  if (T > INT32_MAX || B > INT32_MAX || H > 65535)
+    return fail(KDA_ERR_UNSUPPORTED, "sizes too large (T, B < 2^31, H < 65536)");
+  int64_t N = B;
+  if (cu) {
+    KDA_TRY(check_desc(cu, "cu_seqlens", 1, 4));
+    if (cu->dtype != KDA_DTYPE_I32) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens: dtype must be i32");
+    if (cu->shape[0] < 1) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens: needs N+1 >= 1 entries");
+    if (B != 1) return fail(KDA_ERR_INVALID_ARG, "varlen (cu_seqlens) requires B == 1, got %lld", (long long)B);
+    N = cu->shape[0] - 1;
+  }
+  if (N * H > INT32_MAX / 8) return fail(KDA_ERR_UNSUPPORTED, "too many (sequence, head) pairs");
+  if (initial_state) KDA_TRY(check_state(initial_state, "initial_state", N, H, dk_, dv_));
+  if (d_final_state) KDA_TRY(check_state(d_final_state, "d_final_state", N, H, dk_, dv_));
+  if (d_initial_state) KDA_TRY(check_state(d_initial_state, "d_initial_state", N, H, dk_, dv_));
+  const kda_tensor* ins[] = {q, k, v, g, beta, initial_state, cu, d_out, d_final_state};
+  const char* in_names[] = {"q", "k", "v", "g", "beta", "initial_state", "cu_seqlens", "d_out", "d_final_state"};
+  kda_tensor* outs[] = {dq, dk, dv, dg, dbeta, d_initial_state};
+  const char* out_names[] = {"dq", "dk", "dv", "dg", "dbeta", "d_initial_state"};
+  for (int o = 0; o < 6; ++o) {
+    if (!outs[o]) continue;
+    for (int i = 0; i < 9; ++i)
+      if (ins[i] && overlap(outs[o], ins[i]))
+        return fail(KDA_ERR_INVALID_ARG, "%s overlaps %s", out_names[o], in_names[i]);
+    for (int p = o + 1; p < 6; ++p)
+      if (outs[p] && overlap(outs[o], outs[p]))
+        return fail(KDA_ERR_INVALID_ARG, "%s overlaps %s", out_names[o], out_names[p]);
+  }
+  if (N * H == 0) return KDA_OK;
+
+  kda::BackwardArgs ba;
+  memset(&ba, 0, sizeof(ba));
+  kda::PrefillArgs& a = ba.f;
+  a.q = act(q);
+  a.k = act(k);
+  a.v = act(v);
+  a.g = act(g);
+  a.beta = static_cast<const float*>(beta->data);
+  a.beta_sb = beta->stride[0];
+  a.beta_st = beta->stride[1];
+  a.beta_sh = beta->stride[2];
+  if (initial_state) {
+    a.s0 = static_cast<const float*>(initial_state->data);
+    a.s0_sn = initial_state->stride[0];
+    a.s0_sh = initial_state->stride[1];
+  }
+  a.cu_seqlens = cu ? static_cast<const int32_t*>(cu->data) : nullptr;
+  a.B = (int)B;
+  a.T = (int)T;
+  a.H = (int)H;
+  a.N = (int)N;
+  a.dk = (int)dk_;
+  a.dv = (int)dv_;
+  a.bf16 = dt == KDA_DTYPE_BF16;
+  a.scale = scale;
+  ba.dout = act(d_out);
+  if (d_final_state) {
+    ba.dsT = static_cast<const float*>(d_final_state->data);
+    ba.dsT_sn = d_final_state->stride[0];
+    ba.dsT_sh = d_final_state->stride[1];
+  }
+  auto gact = [](kda_tensor* t) {
+    kda::GradAct x;
+    x.ptr = static_cast<float*>(t->data);
+    x.sb = t->stride[0];
+    x.st = t->stride[1];
+    x.sh = t->stride[2];
+    return x;
+  };
+  ba.dq = gact(dq);
+  ba.dk = gact(dk);
+  ba.dv = gact(dv);
+  ba.dg = gact(dg);
+  ba.dbeta = static_cast<float*>(dbeta->data);
+  ba.db_sb = dbeta->stride[0];
+  ba.db_st = dbeta->stride[1];
+  ba.db_sh = dbeta->stride[2];
+  if (d_initial_state) {
+    ba.ds0 = static_cast<float*>(d_initial_state->data);
+    ba.ds0_sn = d_initial_state->stride[0];
+    ba.ds0_sh = d_initial_state->stride[1];
+  }
+  ba.nblk = (int)((T + kda::kBwdBlock - 1) / kda::kBwdBlock);
+  KDA_TRY(device_error_ptr(&a.err));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (cu) {
+    e = kda::launch_check_seqlens(a.cu_seqlens, a.N, a.T, a.err, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cu_seqlens check launch");
+  }
+  const size_t ws_bytes = kda::backward_workspace_bytes(a.N, a.H, a.T, a.dk, a.dv);
+  void* ws = nullptr;
+  if (ws_bytes) {
+    e = kda::scratch_alloc(&ws, ws_bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "backward workspace allocation");
+  }
+  ba.ck = static_cast<float*>(ws);
+  ba.scr = ba.ck + (int64_t)a.N * a.H * ba.nblk * a.dk * a.dv;
+  e = kda::launch_backward(ba, st);
+  const cudaError_t ef = ws ? kda::scratch_free(ws, st) : cudaSuccess;
+  if (e == cudaSuccess) e = ef;
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return KDA_OK;
+}
+
 kda_status kda_decode_step_fused(kda_tensor* state, kda_tensor* conv_q, kda_tensor* conv_k,
                                  kda_tensor* conv_v, const kda_tensor* q, const kda_tensor* k,
                                  const kda_tensor* v, const kda_tensor* w_q, const kda_tensor* w_k,

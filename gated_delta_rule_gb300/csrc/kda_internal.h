@@ -81,6 +81,30 @@ struct FusedDecodeArgs {
   float eps;                // RMSNorm epsilon
 };
 
+// Backward of the KDA core (kda_recurrent.cu): gradients with respect to q, k, v,
+// g, beta and the initial state, all fp32.
+struct GradAct {
+  float* ptr;
+  int64_t sb, st, sh;
+};
+struct BackwardArgs {
+  PrefillArgs f;   // forward inputs (out, sT, err unused)
+  Act dout;        // gradient of out, q's dtype
+  const float* dsT;  // gradient of the final state [N, H, dk, dv] or null
+  int64_t dsT_sn, dsT_sh;
+  GradAct dq, dk, dv, dg;  // [B, T, H, d] fp32
+  float* dbeta;            // [B, T, H] fp32
+  int64_t db_sb, db_st, db_sh;
+  float* ds0;              // [N, H, dk, dv] fp32 or null
+  int64_t ds0_sn, ds0_sh;
+  float* ck;   // workspace: states every kBwdBlock tokens, [N * H][nblk][dk][dv]
+  float* scr;  // workspace: the states entering each token of one block, [N * H][kBwdBlock][dk][dv]
+  int nblk;    // ceil(T / kBwdBlock)
+};
+constexpr int kBwdBlock = 32;
+size_t backward_workspace_bytes(int N, int H, int T, int dk, int dv);
+cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
+
 // SIMT kernels (kda_recurrent.cu)
 cudaError_t launch_decode_fused(const FusedDecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);

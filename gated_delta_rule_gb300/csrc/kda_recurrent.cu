@@ -305,6 +305,264 @@ __global__ void __launch_bounds__(kThreads, 2) kda_decode_fused_kernel(FusedDeco
 }
 
 // ---------------------------------------------------------------------------
+// backward: one CTA per (sequence, head), all d_v columns (the gradients of q, k
+// and g sum over them).  Reverse-mode derivative of the token step
+//   Sb = Diag(alpha) S_prev;  delta = v - Sb^T k;  S = Sb + beta k delta^T;
+//   o = scale S^T q
+// run backwards with the running gradient dS (of the state after the token):
+//   dS += scale q do^T;  dq = scale S do;  c = dS^T k;  ddelta = beta c;  dv = ddelta;
+//   dbeta = delta . c;  dk = beta dS delta - Sb ddelta;  dSb = dS - k ddelta^T;
+//   dalpha = rowsum(dSb * S_prev);  dg = dalpha * alpha;  dS <- Diag(alpha) dSb.
+// The states entering each token are recomputed: a forward pass stores every
+// kBwdBlock-th state, and each block is replayed into a scratch area before its
+// tokens are differentiated in reverse.
+
+// Sum of x over the TPR threads of a row group (all of them get the sum).
+template <int TPR>
+__device__ __forceinline__ float row_sum(float x) {
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off, TPR);
+  return x;
+}
+
+// One CTA per (sequence, head, DV value columns): with two column halves the row
+// sums (dq, dk, dg, dbeta) are added atomically into outputs zeroed beforehand;
+// two fp32 adds onto zero give the same bits in either order.
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs ba) {
+  using L = Layout<DK, DV>;
+  const PrefillArgs& a = ba.f;
+  __shared__ float s_q[2][DK], s_k[2][DK], s_a[2][DK];
+  __shared__ float4 red0[L::RPP][DV / 4];
+  __shared__ float4 red1[L::RPP][DV / 4];
+  const int nsl = a.dv / DV;
+  const bool split = nsl > 1;
+  const int col0 = (blockIdx.x % nsl) * DV;
+  const int nh = blockIdx.x / nsl;
+  const int n = nh / a.H;
+  const int h = nh - n * a.H;
+  const int64_t ld = a.dv;  // row stride of the state and its gradients
+  const int tid = threadIdx.x;
+  const int col4 = tid % L::TPR;
+  const int trow = tid / L::TPR;
+  const int64_t blk_stride = (int64_t)DK * DV;  // workspace states hold this CTA's columns only
+
+  int64_t b = n, t0 = 0, t1 = a.T;
+  if (a.cu_seqlens) {
+    b = 0;
+    t0 = min(max(__ldg(a.cu_seqlens + n), 0), a.T);
+    t1 = min(max(__ldg(a.cu_seqlens + n + 1), (int)t0), a.T);
+  }
+  const T* qb = static_cast<const T*>(a.q.ptr) + b * a.q.sb + h * a.q.sh;
+  const T* kb = static_cast<const T*>(a.k.ptr) + b * a.k.sb + h * a.k.sh;
+  const float* gb = static_cast<const float*>(a.g.ptr) + b * a.g.sb + h * a.g.sh;
+  const T* vb = static_cast<const T*>(a.v.ptr) + b * a.v.sb + h * a.v.sh + col0;
+  const float* bb = a.beta + b * a.beta_sb + h * a.beta_sh;
+  const T* dob = static_cast<const T*>(ba.dout.ptr) + b * ba.dout.sb + h * ba.dout.sh + col0;
+  float* ck = ba.ck + (int64_t)blockIdx.x * ba.nblk * blk_stride;
+  float* scr = ba.scr + (int64_t)blockIdx.x * kBwdBlock * blk_stride;
+
+  auto store_state = [&](float* dst, const float4 (&x)[L::R]) {
+#pragma unroll
+    for (int r = 0; r < L::R; ++r)
+      *reinterpret_cast<float4*>(dst + (trow + L::RPP * r) * DV + 4 * col4) = x[r];
+  };
+  auto load_state = [&](const float* src, float4 (&x)[L::R]) {
+#pragma unroll
+    for (int r = 0; r < L::R; ++r)
+      x[r] = *reinterpret_cast<const float4*>(src + (trow + L::RPP * r) * DV + 4 * col4);
+  };
+  // token t's q, k, alpha into buffer buf (threads < DK); one barrier follows
+  auto stage = [&](int64_t t, int buf) {
+    if (tid < DK) {
+      s_q[buf][tid] = to_f(qb[t * a.q.st + tid]);
+      s_k[buf][tid] = to_f(kb[t * a.k.st + tid]);
+      s_a[buf][tid] = expf(__ldg(gb + t * a.g.st + tid));
+    }
+  };
+  // one forward step of the state in registers (no read-out)
+  auto forward = [&](float4 (&x)[L::R], int64_t t, int buf) {
+    const float4 v4 = load4<T>(vb + t * a.v.st + 4 * col4);
+    const float beta = __ldg(bb + t * a.beta_st);
+    float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < L::R; ++r) {
+      const int i = trow + L::RPP * r;
+      const float al = s_a[buf][i];
+      x[r].x *= al;
+      x[r].y *= al;
+      x[r].z *= al;
+      x[r].w *= al;
+      fma4(part, s_k[buf][i], x[r]);
+    }
+    const float4 kS = column_reduce<DK, DV>(part, red0, trow, col4);
+#pragma unroll
+    for (int r = 0; r < L::R; ++r) x[r] = delta_write(x[r], beta * s_k[buf][trow + L::RPP * r], kS, v4);
+  };
+
+  // ---- pass 1: the state entering every kBwdBlock-th token ----
+  float4 S[L::R];
+  if (a.s0) {
+    const float* S0 = a.s0 + n * a.s0_sn + h * a.s0_sh + col0;
+#pragma unroll
+    for (int r = 0; r < L::R; ++r)
+      S[r] = *reinterpret_cast<const float4*>(S0 + (trow + L::RPP * r) * ld + 4 * col4);
+  } else {
+#pragma unroll
+    for (int r = 0; r < L::R; ++r) S[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  int pbuf = 0;
+  for (int64_t t = t0; t < t1; ++t) {
+    if ((t - t0) % kBwdBlock == 0) store_state(ck + ((t - t0) / kBwdBlock) * blk_stride, S);
+    stage(t, pbuf);
+    __syncthreads();
+    forward(S, t, pbuf);
+    pbuf ^= 1;
+  }
+
+  // ---- pass 2: blocks in reverse ----
+  float4 dS[L::R];
+  if (ba.dsT) {
+    const float* D = ba.dsT + n * ba.dsT_sn + h * ba.dsT_sh + col0;
+#pragma unroll
+    for (int r = 0; r < L::R; ++r)
+      dS[r] = *reinterpret_cast<const float4*>(D + (trow + L::RPP * r) * ld + 4 * col4);
+  } else {
+#pragma unroll
+    for (int r = 0; r < L::R; ++r) dS[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int64_t nb = (t1 - t0 + kBwdBlock - 1) / kBwdBlock;
+  for (int64_t blk = nb - 1; blk >= 0; --blk) {
+    const int64_t ta = t0 + blk * kBwdBlock, tb = min(ta + kBwdBlock, t1);
+    // replay the block: scratch[t - ta] = state entering token t (each thread reads
+    // back only the elements it wrote)
+    load_state(ck + blk * blk_stride, S);
+    for (int64_t t = ta; t < tb; ++t) {
+      store_state(scr + (t - ta) * blk_stride, S);
+      stage(t, pbuf);
+      __syncthreads();
+      forward(S, t, pbuf);
+      pbuf ^= 1;
+    }
+    for (int64_t t = tb - 1; t >= ta; --t) {
+      stage(t, pbuf);
+      const float4 v4 = load4<T>(vb + t * a.v.st + 4 * col4);
+      const float4 do4 = load4<T>(dob + t * ba.dout.st + 4 * col4);
+      const float beta = __ldg(bb + t * a.beta_st);
+      float4 Sp[L::R];
+      load_state(scr + (t - ta) * blk_stride, Sp);
+      __syncthreads();
+      const int buf = pbuf;
+      pbuf ^= 1;
+      // Sb = Diag(alpha) S_prev; delta = v - Sb^T k
+      float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < L::R; ++r) {
+        const int i = trow + L::RPP * r;
+        const float al = s_a[buf][i];
+        float4 sb = Sp[r];
+        sb.x *= al;
+        sb.y *= al;
+        sb.z *= al;
+        sb.w *= al;
+        fma4(part, s_k[buf][i], sb);
+      }
+      const float4 kS = column_reduce<DK, DV>(part, red0, trow, col4);
+      const float4 dl = make_float4(v4.x - kS.x, v4.y - kS.y, v4.z - kS.z, v4.w - kS.w);
+      // dS += scale q do^T; dq = scale S do (S = Sb + beta k delta^T); c = dS^T k
+      float dqr[L::R];
+      float4 cp = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < L::R; ++r) {
+        const int i = trow + L::RPP * r;
+        const float al = s_a[buf][i], ki = s_k[buf][i], qi = s_q[buf][i];
+        const float bk = beta * ki;
+        const float4 st = make_float4(fmaf(bk, dl.x, al * Sp[r].x), fmaf(bk, dl.y, al * Sp[r].y),
+                                      fmaf(bk, dl.z, al * Sp[r].z), fmaf(bk, dl.w, al * Sp[r].w));
+        dqr[r] = st.x * do4.x + st.y * do4.y + st.z * do4.z + st.w * do4.w;
+        const float sq = a.scale * qi;
+        dS[r].x = fmaf(sq, do4.x, dS[r].x);
+        dS[r].y = fmaf(sq, do4.y, dS[r].y);
+        dS[r].z = fmaf(sq, do4.z, dS[r].z);
+        dS[r].w = fmaf(sq, do4.w, dS[r].w);
+        fma4(cp, ki, dS[r]);
+      }
+      const float4 c = column_reduce<DK, DV>(cp, red1, trow, col4);
+      const float4 dd = make_float4(beta * c.x, beta * c.y, beta * c.z, beta * c.w);
+      // dk = beta dS delta - Sb ddelta; dSb = dS - k ddelta^T; dalpha = rowsum(dSb * S_prev)
+      float dkr[L::R], dar[L::R];
+#pragma unroll
+      for (int r = 0; r < L::R; ++r) {
+        const int i = trow + L::RPP * r;
+        const float al = s_a[buf][i], ki = s_k[buf][i];
+        dkr[r] = beta * (dS[r].x * dl.x + dS[r].y * dl.y + dS[r].z * dl.z + dS[r].w * dl.w) -
+                 al * (Sp[r].x * dd.x + Sp[r].y * dd.y + Sp[r].z * dd.z + Sp[r].w * dd.w);
+        float4 dsb = make_float4(fmaf(-ki, dd.x, dS[r].x), fmaf(-ki, dd.y, dS[r].y), fmaf(-ki, dd.z, dS[r].z),
+                                 fmaf(-ki, dd.w, dS[r].w));
+        dar[r] = dsb.x * Sp[r].x + dsb.y * Sp[r].y + dsb.z * Sp[r].z + dsb.w * Sp[r].w;
+        dS[r] = make_float4(al * dsb.x, al * dsb.y, al * dsb.z, al * dsb.w);
+      }
+      // row sums over the d_v columns; lane j of a row group writes row trow + RPP * j
+#pragma unroll
+      for (int r = 0; r < L::R; ++r) {
+        const float q_s = row_sum<L::TPR>(dqr[r]);
+        const float k_s = row_sum<L::TPR>(dkr[r]);
+        const float a_s = row_sum<L::TPR>(dar[r]);
+        if (col4 == r % L::TPR) {
+          const int i = trow + L::RPP * r;
+          float* pq = ba.dq.ptr + b * ba.dq.sb + t * ba.dq.st + h * ba.dq.sh + i;
+          float* pk = ba.dk.ptr + b * ba.dk.sb + t * ba.dk.st + h * ba.dk.sh + i;
+          float* pg = ba.dg.ptr + b * ba.dg.sb + t * ba.dg.st + h * ba.dg.sh + i;
+          if (split) {
+            atomicAdd(pq, a.scale * q_s);
+            atomicAdd(pk, k_s);
+            atomicAdd(pg, a_s * s_a[buf][i]);
+          } else {
+            *pq = a.scale * q_s;
+            *pk = k_s;
+            *pg = a_s * s_a[buf][i];
+          }
+        }
+      }
+      // dbeta = delta . c over the d_v columns: every row group holds the same columns,
+      // so every group forms the same sum (all lanes take part in the shuffles)
+      const float db = row_sum<L::TPR>(dl.x * c.x + dl.y * c.y + dl.z * c.z + dl.w * c.w);
+      if (trow == 0) {
+        *reinterpret_cast<float4*>(ba.dv.ptr + b * ba.dv.sb + t * ba.dv.st + h * ba.dv.sh + col0 + 4 * col4) = dd;
+        if (col4 == 0) {
+          float* pb = ba.dbeta + b * ba.db_sb + t * ba.db_st + h * ba.db_sh;
+          if (split)
+            atomicAdd(pb, db);
+          else
+            *pb = db;
+        }
+      }
+    }
+  }
+  if (ba.ds0) {
+    float* D = ba.ds0 + n * ba.ds0_sn + h * ba.ds0_sh + col0;
+#pragma unroll
+    for (int r = 0; r < L::R; ++r)
+      *reinterpret_cast<float4*>(D + (trow + L::RPP * r) * ld + 4 * col4) = dS[r];
+  }
+}
+
+// Zero the row-sum gradients (dq, dk, dg over d_k, dbeta) of every token, strided views.
+__global__ void kda_backward_zero_kernel(BackwardArgs ba) {
+  const PrefillArgs& a = ba.f;
+  const int64_t rows = (int64_t)a.B * a.T * a.H;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const int64_t h = r % a.H, bt = r / a.H, t = bt % a.T, b = bt / a.T;
+    for (int i = threadIdx.x; i < a.dk; i += blockDim.x) {
+      ba.dq.ptr[b * ba.dq.sb + t * ba.dq.st + h * ba.dq.sh + i] = 0.f;
+      ba.dk.ptr[b * ba.dk.sb + t * ba.dk.st + h * ba.dk.sh + i] = 0.f;
+      ba.dg.ptr[b * ba.dg.sb + t * ba.dg.st + h * ba.dg.sh + i] = 0.f;
+    }
+    if (threadIdx.x == 0) ba.dbeta[b * ba.db_sb + t * ba.db_st + h * ba.db_sh] = 0.f;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // token-by-token prefill: one CTA per (sequence, head, DV value columns), state in
 // registers.  The state's columns evolve independently, so a (sequence, head)
 // may be spread over a.dv / DV CTAs.
@@ -519,6 +777,31 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs& fa, cudaStream_t s) {
   launch_begin(s);
   fn<<<dim3((unsigned)(a.N * a.H)), kThreads, 0, s>>>(fa);
   const cudaError_t e = cudaGetLastError();
+  return e != cudaSuccess ? e : launch_end(s);
+}
+
+size_t backward_workspace_bytes(int N, int H, int T, int dk, int dv) {
+  const int64_t nblk = ((int64_t)T + kBwdBlock - 1) / kBwdBlock;
+  return (size_t)((int64_t)N * H * (nblk + kBwdBlock) * dk * dv * 4);
+}
+
+cudaError_t launch_backward(const BackwardArgs& ba, cudaStream_t s) {
+  const PrefillArgs& a = ba.f;
+  if ((int64_t)a.N * a.H == 0) return cudaSuccess;
+  // 64 value columns per CTA: d_v = 128 spreads a (sequence, head) over two CTAs
+  void (*fn)(BackwardArgs) = nullptr;
+  if (a.dk == 128) fn = a.bf16 ? kda_backward_kernel<128, 64, __nv_bfloat16> : kda_backward_kernel<128, 64, float>;
+  if (a.dk == 64) fn = a.bf16 ? kda_backward_kernel<64, 64, __nv_bfloat16> : kda_backward_kernel<64, 64, float>;
+  if (!fn || (a.dv != 64 && a.dv != 128)) return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (a.dv > 64) {  // partial row sums are added: start from zero
+    launch_begin(s);
+    kda_backward_zero_kernel<<<1024, 128, 0, s>>>(ba);
+    if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
+  }
+  launch_begin(s);
+  fn<<<dim3((unsigned)(a.N * a.H * (a.dv / 64))), kThreads, 0, s>>>(ba);
+  e = cudaGetLastError();
   return e != cudaSuccess ? e : launch_end(s);
 }
 

@@ -229,6 +229,34 @@ kda_status kda_chunk_fwd_gated(const kda_tensor* q, const kda_tensor* k, const k
                                kda_tensor* final_state, void* stream);
 
 /*
+ * kda_backward - gradients of the KDA core: given the gradient d_out of the
+ * outputs (and d_final_state of the final state, or NULL) of the forward that
+ * kda_chunk_fwd computes from q, k, v, g, beta, initial_state, scale and
+ * cu_seqlens, writes the gradients with respect to all of those inputs.
+ *
+ * The pages give the forward only ("尝试对Kimi KDA的数学推导&算子实现分析"
+ * (hjcheng0602.cn/blog/kdd), the recurrence of "Kimi K3 核心算子拆解"
+ * (devpress.csdn.net) §2.3); this is its exact reverse-mode derivative, run
+ * token by token in reverse per (sequence, head) with the states recomputed from
+ * checkpoints every 32 tokens.
+ *
+ *   q, k, v, g, beta, initial_state, scale, cu_seqlens  as for kda_chunk_fwd
+ *   d_out            [B, T, H, d_v] in q's dtype
+ *   d_final_state    [N, H, d_k, d_v] f32, or NULL (zero)
+ *   dq, dk, dg       [B, T, H, d_k] f32;  dv [B, T, H, d_v] f32;  dbeta [B, T, H] f32
+ *   d_initial_state  [N, H, d_k, d_v] f32, or NULL (not written)
+ *
+ * Scratch comes from the stream-ordered pool: N * H * (ceil(T / 32) + 32) *
+ * d_k * d_v * 4 bytes.  Errors as for kda_chunk_fwd; no gradient may overlap an
+ * input or another gradient.
+ */
+kda_status kda_backward(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                        const kda_tensor* g, const kda_tensor* beta, const kda_tensor* initial_state,
+                        float scale, const kda_tensor* cu_seqlens, const kda_tensor* d_out,
+                        const kda_tensor* d_final_state, kda_tensor* dq, kda_tensor* dk, kda_tensor* dv,
+                        kda_tensor* dg, kda_tensor* dbeta, kda_tensor* d_initial_state, void* stream);
+
+/*
  * kda_decode_step_fused - one decode token per (request, head) with the KDA
  * layer's front and back ends fused around kda_recurrent_step.
  *

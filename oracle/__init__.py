@@ -257,3 +257,49 @@ def decode_fused(state, conv_q, conv_k, conv_v, q, k, v, w_q, w_k, w_v, g, beta,
     y = o / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps) * wn / (1.0 + np.exp(-gate))
     shift = lambda c, x: np.concatenate([c[:, 1:], x[:, None]], axis=1)
     return y, S1, shift(cq, xq), shift(ck, xk), shift(cv, xv)
+
+
+def backward(q, k, v, g, beta, initial_state, scale, d_out, d_final_state=None, cu_seqlens=None):
+    """Oracle of ``kda_backward``: gradients of the KDA core with respect to q, k, v,
+    g, beta and the initial state, given the gradients of the outputs (d_out [B, T,
+    H, dv]) and of the final state (d_final_state [N, H, dk, dv] or None).
+
+    The forward is the token recurrence in the three-step order of "Kimi K3
+    核心算子拆解" (devpress.csdn.net) §2.3 (decay, correct, write; read-out after the
+    update), written with plain torch fp64 operations on the CPU; the gradients come
+    from torch's reverse-mode differentiation of that loop ("尝试对Kimi
+    KDA的数学推导&算子实现分析" (hjcheng0602.cn/blog/kdd) gives only the forward;
+    the backward is its exact derivative).  Returns a dict of fp64 numpy arrays
+    dq, dk, dv, dg, dbeta and d_initial_state (zeros when initial_state is None).
+    """
+    import torch
+    t = lambda x: None if x is None else torch.as_tensor(_f64(x), dtype=torch.float64)
+    q, k, v, g, beta, do = (t(a).clone().requires_grad_(True) if i < 5 else t(a)
+                            for i, a in enumerate((q, k, v, g, beta, d_out)))
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    if cu_seqlens is None:
+        N = B
+        spans = [(b, 0, T) for b in range(B)]
+    else:
+        cu = _f64(cu_seqlens).astype(np.int64)
+        N = cu.shape[0] - 1
+        spans = [(0, int(cu[n]), int(cu[n + 1])) for n in range(N)]
+    S0 = torch.zeros(N, H, dk, dv, dtype=torch.float64) if initial_state is None else t(initial_state)
+    S0 = S0.clone().requires_grad_(True)
+    loss = torch.zeros((), dtype=torch.float64)
+    dS_T = None if d_final_state is None else t(d_final_state)
+    for n, (b, t0, t1) in enumerate(spans):
+        for h in range(H):
+            S = S0[n, h]
+            for s in range(t0, t1):
+                S = S * torch.exp(g[b, s, h])[:, None]
+                kS = k[b, s, h] @ S
+                S = S + beta[b, s, h] * torch.outer(k[b, s, h], v[b, s, h] - kS)
+                o = scale * (S.T @ q[b, s, h])
+                loss = loss + o @ do[b, s, h]
+            if dS_T is not None:
+                loss = loss + torch.sum(S * dS_T[n, h])
+    loss.backward()
+    grads = dict(dq=q.grad, dk=k.grad, dv=v.grad, dg=g.grad, dbeta=beta.grad, d_initial_state=S0.grad)
+    return {name: gr.detach().numpy() for name, gr in grads.items()}

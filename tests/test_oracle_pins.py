@@ -308,6 +308,36 @@ def test_decode_fused_special_cases():
     assert np.allclose(S2[0, 0], s2, rtol=0, atol=1e-12)
 
 
+def test_backward_matches_finite_differences():
+    """The backward oracle's gradients equal central finite differences of the C++
+    forward oracle's loss <o, d_out> + <S_T, d_final_state>, for every input."""
+    rng = np.random.default_rng(11)
+    B, T, H, dk, dv = 1, 5, 1, 3, 2
+    q = rng.standard_normal((B, T, H, dk)); k = rng.standard_normal((B, T, H, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, H, dv)); g = -rng.uniform(0.05, 2.0, (B, T, H, dk))
+    beta = rng.uniform(0.1, 0.9, (B, T, H)); S0 = rng.standard_normal((B, H, dk, dv))
+    do = rng.standard_normal((B, T, H, dv)); dST = rng.standard_normal((B, H, dk, dv))
+    scale = 0.7
+    gr = oracle.backward(q, k, v, g, beta, S0, scale, do, dST)
+
+    def loss(q, k, v, g, beta, S0):
+        o, ST = oracle.prefill(q, k, v, g, beta, S0, scale)
+        return float(np.sum(o * do) + np.sum(ST * dST))
+
+    args = dict(q=q, k=k, v=v, g=g, beta=beta, S0=S0)
+    names = dict(q="dq", k="dk", v="dv", g="dg", beta="dbeta", S0="d_initial_state")
+    eps = 1e-6
+    for a, arr in args.items():
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            p, m = {x: y.copy() for x, y in args.items()}, {x: y.copy() for x, y in args.items()}
+            p[a][idx] += eps
+            m[a][idx] -= eps
+            num[idx] = (loss(**p) - loss(**m)) / (2 * eps)
+        assert np.allclose(gr[names[a]], num, rtol=1e-6, atol=1e-7), a
+
+
 def test_multi_step_matches_numpy_token_loop():
     """Multi-token decode: every request's outputs are those of the numpy three-step
     loop over its n tokens, and the kept state is that loop stopped after the
