@@ -118,10 +118,13 @@ struct SerialSmem {
   // a record buffer holds [T2 | zero tile | rest of the record]: the zero tile is
   // the lower half of T2's M = 128 window
   static constexpr int kRecBuf = align1k(Rec<DK>::kBytes + 64 * 64 * 2);
+  // MN-major tiles keep 128-byte rows (the swizzle atom) when DV = 32: the 32
+  // columns occupy half of each row's 16-byte chunks, at their swizzled places
+  static constexpr int kPitch = DV < 64 ? 64 : DV;       // stored columns of a value tile
   static constexpr int REC = 0;                          // two record buffers
   static constexpr int VT = REC + 2 * kRecBuf;           // two V chunks [64][DV] MN-major (U reuses)
-  static constexpr int SB = VT + 2 * 64 * DV * 2;        // bf16 S, [DK][DV] MN-major
-  static constexpr int OSTG = SB + DK * DV * 2;          // output staging: 2 warps x 32 rows x 144 B
+  static constexpr int SB = VT + 2 * 64 * kPitch * 2;    // bf16 S, [DK][DV] MN-major
+  static constexpr int OSTG = SB + DK * kPitch * 2;      // output staging: 2 warps x 32 rows x 144 B
   static constexpr int MBAR = OSTG + 2 * 32 * 144;       // mma_a, mma_s, rec0/1, free0/1, orel0/1
   static constexpr int TSLOT = MBAR + 64;
   static constexpr int FLAG = TSLOT + 4;
@@ -991,7 +994,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
         const int t = idx / kVec, cv = idx % kVec;
         const bool ok = t < lc;
         const __nv_bfloat16* src = ok ? vg + ((int64_t)(c0 + ci) * kC + t) * a.v.st + 8 * cv : vg;
-        cp_async16(sbase + L::VT + b * 64 * DV * 2 + sw128(t, 8 * cv, 64), src, ok ? 16u : 0u);
+        cp_async16(sbase + L::VT + b * 64 * L::kPitch * 2 + sw128(t, 8 * cv, 64), src, ok ? 16u : 0u);
       }
       cp_async_mbar_arrive(mb);
     }
@@ -1004,7 +1007,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
       const uint32_t rWQ = rec + 2 * kT2 + (R::WQ - kT2);
       const uint32_t rAQ = rec + 2 * kT2 + (R::AQ - kT2);
       const uint32_t rKE = rec + 2 * kT2 + (R::KE - kT2);
-      const uint32_t vt = sbase + L::VT + b * 64 * DV * 2;
+      const uint32_t vt = sbase + L::VT + b * 64 * L::kPitch * 2;
       wait(mbar_rec0 + 8 * b, (ci >> 1) & 1);
       // U/O buffer b was last used by chunk ci - 2: its output must have been read out
       if (ci >= 2) wait(mbar_orel0 + 8 * b, (uint32_t)(((ci - 2) >> 1) & 1));
@@ -1065,34 +1068,36 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
         mbar_arrive(mbar_orel0 + 8 * (pc & 1));
       }
       const int row0 = 32 * (warp - 2);  // this warp's first token row in the chunk
+      constexpr int kPass = DV < 64 ? DV : 64;  // columns per pass through the staging rows
+      constexpr int kCh = kPass / 8;            // 16-byte chunks of a row per pass
 #pragma unroll
-      for (int half = 0; half < DV / 64; ++half) {
-        __syncwarp();  // the previous half has been read back
+      for (int half = 0; half < DV / kPass; ++half) {
+        __syncwarp();  // the previous pass has been read back
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float* f = reinterpret_cast<const float*>(r[2 * half + (u >> 2)]) + 8 * (u & 3);
+        for (int u = 0; u < kCh; ++u) {
+          const float* f = reinterpret_cast<const float*>(r[(kPass * half + 8 * u) >> 5]) + ((8 * u) & 31);
           st_shared_v4(stage + lane * 144 + 16 * u, pack_bf16(a.scale * f[0], a.scale * f[1]),
                        pack_bf16(a.scale * f[2], a.scale * f[3]), pack_bf16(a.scale * f[4], a.scale * f[5]),
                        pack_bf16(a.scale * f[6], a.scale * f[7]));
         }
         __syncwarp();
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int rr = 4 * it + (lane >> 3), ch = lane & 7;
+        for (int it = 0; it < kCh; ++it) {
+          const int rr = (32 / kCh) * it + lane / kCh, ch = lane % kCh;
           uint4 w;
           asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                        : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
                        : "r"(stage + rr * 144 + 16 * ch));
           const int t = row0 + rr;
           if (t < lc)
-            *reinterpret_cast<uint4*>(og + ((int64_t)(c0 + pc) * kC + t) * a.out_st + 64 * half + 8 * ch) = w;
+            *reinterpret_cast<uint4*>(og + ((int64_t)(c0 + pc) * kC + t) * a.out_st + kPass * half + 8 * ch) = w;
         }
       }
     };
     for (int ci = 0; ci < nch; ++ci) {
       const int b = ci & 1;
       const uint32_t rec = sbase + L::REC + b * L::kRecBuf;
-      const uint32_t vt = sbase + L::VT + b * 64 * DV * 2;
+      const uint32_t vt = sbase + L::VT + b * 64 * L::kPitch * 2;
       // (1) bf16 copy of the state entering this chunk (read once from TMEM, kept in registers)
       uint32_t r[DV / 32][32];
       if (ci > 0) wait(mbar_s, (uint32_t)((ci - 1) & 1));
@@ -1407,11 +1412,19 @@ cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   // Few chains (sequence-heads): split d_v = 128 into two 64-column CTAs so more SMs
   // carry the serial loop.  Each slice CTA reads the whole chunk record.
-  constexpr int DVS = DV == 128 ? 64 : DV;
-  const bool split = DVS != DV && (int64_t)a.N * a.H * (DV / DVS) <= sm_count();
-  const int W = split ? DVS : DV;  // columns per serial CTA
-  auto ser = split ? kda_chunk_serial_kernel<DK, DVS> : kda_chunk_serial_kernel<DK, DV>;
-  const int ser_smem = split ? SerialSmem<DK, DVS>::kAlloc : SerialSmem<DK, DV>::kAlloc;
+  // Value-column slices: with few chains (sequence-heads), d_v is split into 32- or
+  // 64-column CTAs, as finely as the SMs hold them, so that more SMs carry the
+  // serial loop and each chunk step moves less.  Every slice CTA reads the whole
+  // chunk record.
+  constexpr int DVM = DV == 128 ? 64 : DV;
+  const int64_t nh = (int64_t)a.N * a.H;
+  const int W = nh * (DV / 32) <= sm_count() ? 32 : (DVM != DV && nh * 2 <= sm_count()) ? DVM : DV;
+  auto ser = W == 32    ? kda_chunk_serial_kernel<DK, 32>
+             : W == DVM ? kda_chunk_serial_kernel<DK, DVM>
+                        : kda_chunk_serial_kernel<DK, DV>;
+  const int ser_smem = W == 32    ? SerialSmem<DK, 32>::kAlloc
+                       : W == DVM ? SerialSmem<DK, DVM>::kAlloc
+                                  : SerialSmem<DK, DV>::kAlloc;
   e = cudaFuncSetAttribute(ser, cudaFuncAttributeMaxDynamicSharedMemorySize, ser_smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)sp.total * a.H;

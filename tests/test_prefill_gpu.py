@@ -120,6 +120,53 @@ def test_varlen_boundaries_bit_exact(kda, entry):
         assert torch.equal(o2[:, a:b], out[:, a:b]) and torch.equal(s2[n], sT[n]), n
 
 
+@pytest.mark.parametrize("T", [1500, 1600])
+def test_fixed_length_equals_varlen_packing(kda, T):
+    """A fixed-length batch (chunk indices n * chunks + c) and the same sequences
+    packed with cu_seqlens (chunk offsets built on the device) give bit-identical
+    outputs, final states and per-chunk checkpoints, in place as well, and match
+    the oracle.  24 and 25 chunks (the last one partial at T = 1500)."""
+    B, H = 2, 4
+    d = ki.prefill_inputs(B, T, H, 128, 128, "bf16", seed=31, s0=True)
+    check_prefill(kda.kda_chunk_fwd, d, label=f"fixed length T={T}")
+    t = to_dev(d)
+    C = T // 64
+    out, sT, ck = kda.kda_chunk_fwd_checkpointed(t["q"], t["k"], t["v"], t["g"], t["beta"],
+                                                 t["initial_state"], t["scale"], checkpoint_tokens=64,
+                                                 num_checkpoints=C)
+    pk = lambda x: x.reshape(1, B * T, *x.shape[2:]).contiguous()
+    cu = torch.tensor([0, T, 2 * T], dtype=torch.int32, device="cuda")
+    out2, sT2, ck2 = kda.kda_chunk_fwd_checkpointed(pk(t["q"]), pk(t["k"]), pk(t["v"]), pk(t["g"]),
+                                                    pk(t["beta"]), t["initial_state"], t["scale"],
+                                                    cu_seqlens=cu, checkpoint_tokens=64, num_checkpoints=C)
+    assert torch.equal(out, out2.reshape(out.shape))
+    assert torch.equal(sT, sT2) and torch.equal(ck, ck2)
+    S = t["initial_state"].clone()
+    out3, _ = kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], S, t["scale"], final_state=S)
+    assert torch.equal(out3, out) and torch.equal(S, sT)
+
+
+@pytest.mark.parametrize("dv", [64, 128])
+@pytest.mark.parametrize("H", [4, 48, 96])
+def test_value_column_slices(kda, dv, H):
+    """The serial kernel splits d_v into 32- or 64-column CTAs when the SMs hold
+    that many (4 heads: 32 columns; 48 heads: 64, or 32 at d_v = 64; 96 heads at
+    d_v = 128: unsplit).  Every split matches the oracle, and the slices together
+    equal the unsplit result bit for bit (columns never mix)."""
+    d = ki.prefill_inputs(1, 200, H, 128, dv, "bf16", seed=40 + H + dv, s0=True)
+    check_prefill(kda.kda_chunk_fwd, d, label=f"H={H} dv={dv}")
+    if H != 96:
+        return
+    # heads of the unsplit run, one at a time (4-slice split), bitwise
+    t = to_dev(d)
+    out, sT = kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"], t["scale"])
+    for h in (0, 37, 95):
+        sl = lambda x: x[:, :, h:h + 1].contiguous()
+        o1, s1 = kda.kda_chunk_fwd(sl(t["q"]), sl(t["k"]), sl(t["v"]), sl(t["g"]), sl(t["beta"]),
+                                   t["initial_state"][:, h:h + 1].contiguous(), t["scale"])
+        assert torch.equal(o1, out[:, :, h:h + 1]) and torch.equal(s1, sT[:, h:h + 1]), h
+
+
 def test_bad_cu_seqlens_sets_device_error(kda):
     d = to_dev(ki.prefill_inputs(1, 50, 1, 64, 64, "bf16", seed=15, n_states=2))
     for bad in ([0, 30, 20], [1, 20, 50], [0, 20, 49]):
