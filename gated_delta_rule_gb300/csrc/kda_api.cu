@@ -809,7 +809,13 @@ kda_status kda_decode_step_fused(kda_tensor* state, kda_tensor* conv_q, kda_tens
   fa.gate = act(out_gate);
   fa.norm_w = norm_weight ? static_cast<const float*>(norm_weight->data) : nullptr;
   fa.eps = eps;
-  cudaError_t e = kda::launch_decode_fused(fa, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* scratch = nullptr;
+  cudaError_t e = kda::scratch_alloc(&scratch, kda::decode_fused_workspace_bytes(a.N, a.H, a.dk, a.dv), st);
+  if (e != cudaSuccess) return cuda_fail(e, "fused decode workspace allocation");
+  e = kda::launch_decode_fused(fa, scratch, st);
+  const cudaError_t ef = kda::scratch_free(scratch, st);
+  if (e == cudaSuccess) e = ef;
   if (e != cudaSuccess) return cuda_fail(e, "fused decode launch");
   return KDA_OK;
 }

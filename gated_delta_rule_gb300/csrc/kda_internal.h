@@ -106,7 +106,9 @@ size_t backward_workspace_bytes(int N, int H, int T, int dk, int dv);
 cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
 
 // SIMT kernels (kda_recurrent.cu)
-cudaError_t launch_decode_fused(const FusedDecodeArgs& a, cudaStream_t s);
+// ws: decode_fused_workspace_bytes(N, H, dk, dv) bytes of device scratch
+cudaError_t launch_decode_fused(const FusedDecodeArgs& a, void* ws, cudaStream_t s);
+size_t decode_fused_workspace_bytes(int N, int H, int dk, int dv);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s);
 // cu_seqlens validation: sets kErrBadSeqlens in *err when the offsets are invalid.

@@ -36,6 +36,12 @@ template <>
 __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
 template <typename T>
 __device__ __forceinline__ float4 load4(const T* p);
@@ -182,8 +188,11 @@ __global__ void __launch_bounds__(kThreads, 3) kda_decode_kernel(DecodeArgs a) {
 
 // ---------------------------------------------------------------------------
 // fused decode: front end (short convolutions, SiLU, L2 norm of q and k), the
-// decode step, back end (head RMSNorm, sigmoid output gate).  One CTA per
-// (request, head) with all d_v columns, since the RMS norm spans them.
+// decode step, back end (head RMSNorm, sigmoid output gate).  Three launches:
+// the step itself is the plain decode kernel on fp32 inputs, at its own
+// occupancy (three 64-column CTAs per SM); one kernel holding a whole head for
+// the RMS norm ran at two thirds of that.  The front and back ends move a few
+// hundred bytes per (request, head), the step 128 KB.
 
 // Sum of one value per thread over the first `nthr` threads (a multiple of 32),
 // returned to every thread.  `buf` holds kThreads / 32 floats; two barriers.
@@ -213,26 +222,16 @@ __device__ __forceinline__ float conv_silu_update(T* cache, int64_t slot_stride,
   return y / (1.f + expf(-y));
 }
 
+// Front end, one CTA per (request, head), channel c on thread c: the fp32 inputs
+// of the step, [q^ | k^ | v^] per (request, head) in `x`.
 template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(kThreads, 2) kda_decode_fused_kernel(FusedDecodeArgs fa) {
-  using L = Layout<DK, DV>;
+__global__ void __launch_bounds__(kThreads) kda_decode_front_kernel(FusedDecodeArgs fa, float* x) {
   const DecodeArgs& a = fa.d;
-  __shared__ float s_q[DK], s_k[DK], s_a[DK], s_v[DV], s_buf[kThreads / 32];
-  __shared__ float4 red0[L::RPP][DV / 4];
-  __shared__ float4 red1[L::RPP][DV / 4];
-  const int n = blockIdx.x / a.H;
-  const int h = blockIdx.x - n * a.H;
+  __shared__ float s_buf[kThreads / 32];
+  const int nh = blockIdx.x;
+  const int n = nh / a.H;
+  const int h = nh - n * a.H;
   const int tid = threadIdx.x;
-  const int col4 = tid % L::TPR;
-  const int trow = tid / L::TPR;
-
-  float* S = a.state + n * a.s_sn + h * a.s_sh;
-  float4 s[L::R];
-#pragma unroll
-  for (int r = 0; r < L::R; ++r)  // issued first: the front end runs while the state arrives
-    s[r] = __ldcs(reinterpret_cast<const float4*>(S + (trow + L::RPP * r) * DV + 4 * col4));
-
-  // ---- front end ----
   float qa = 0.f, ka = 0.f;
   if (tid < DK) {
     T* cq = static_cast<T*>(fa.cq) + n * fa.cq_sn + h * fa.cq_sh + tid;
@@ -241,66 +240,37 @@ __global__ void __launch_bounds__(kThreads, 2) kda_decode_fused_kernel(FusedDeco
                              fa.wq + ((int64_t)h * DK + tid) * 4);
     ka = conv_silu_update<T>(ck, fa.ck_ss, static_cast<const T*>(a.k.ptr) + n * a.k.sb + h * a.k.sh + tid,
                              fa.wk + ((int64_t)h * DK + tid) * 4);
-    s_a[tid] = expf(__ldg(static_cast<const float*>(a.g.ptr) + n * a.g.sb + h * a.g.sh + tid));
   }
+  float* xo = x + (int64_t)nh * (2 * DK + DV);
   if (tid < DV) {
     T* cv = static_cast<T*>(fa.cv) + n * fa.cv_sn + h * fa.cv_sh + tid;
-    s_v[tid] = conv_silu_update<T>(cv, fa.cv_ss, static_cast<const T*>(a.v.ptr) + n * a.v.sb + h * a.v.sh + tid,
-                                   fa.wv + ((int64_t)h * DV + tid) * 4);
+    xo[2 * DK + tid] = conv_silu_update<T>(cv, fa.cv_ss, static_cast<const T*>(a.v.ptr) + n * a.v.sb + h * a.v.sh + tid,
+                                          fa.wv + ((int64_t)h * DV + tid) * 4);
   }
   const float nq = sqrtf(block_sum(qa * qa, s_buf, DK));
   const float nk = sqrtf(block_sum(ka * ka, s_buf, DK));
   if (tid < DK) {
-    s_q[tid] = qa / fmaxf(nq, 1e-6f);
-    s_k[tid] = ka / fmaxf(nk, 1e-6f);
+    xo[tid] = qa / fmaxf(nq, 1e-6f);
+    xo[DK + tid] = ka / fmaxf(nk, 1e-6f);
   }
-  const float beta = __ldg(a.beta + n * a.beta_sn + h * a.beta_sh);
-  __syncthreads();
-  const float4 v4 = *reinterpret_cast<const float4*>(s_v + 4 * col4);
+}
 
-  // ---- the decode step ----
-  float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int r = 0; r < L::R; ++r) {
-    const int i = trow + L::RPP * r;
-    const float al = s_a[i];
-    s[r].x *= al;
-    s[r].y *= al;
-    s[r].z *= al;
-    s[r].w *= al;
-    fma4(part, s_k[i], s[r]);
-  }
-  const float4 kS = column_reduce<DK, DV>(part, red0, trow, col4);
-  float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int r = 0; r < L::R; ++r) {
-    const int i = trow + L::RPP * r;
-    s[r] = delta_write(s[r], beta * s_k[i], kS, v4);
-    __stcs(reinterpret_cast<float4*>(S + i * DV + 4 * col4), s[r]);
-    fma4(po, s_q[i], s[r]);
-  }
-  float4 o = column_reduce<DK, DV>(po, red1, trow, col4);
-
-  // ---- back end: the threads of row group 0 hold the d_v outputs ----
-  if (trow == 0) {
-    o.x *= a.scale;
-    o.y *= a.scale;
-    o.z *= a.scale;
-    o.w *= a.scale;
-    float ss = o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
-    // row group 0 is lanes 0 .. TPR-1 of warp 0: only those take part
-    constexpr unsigned kMask = L::TPR >= 32 ? 0xffffffffu : ((1u << L::TPR) - 1u);
-#pragma unroll
-    for (int off = L::TPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(kMask, ss, off, L::TPR);
-    const float inv = rsqrtf(ss / DV + fa.eps);
-    const float4 gl = load4<T>(static_cast<const T*>(fa.gate.ptr) + n * fa.gate.sb + h * fa.gate.sh + 4 * col4);
-    const float4 wn = fa.norm_w ? __ldg(reinterpret_cast<const float4*>(fa.norm_w + 4 * col4))
-                                : make_float4(1.f, 1.f, 1.f, 1.f);
-    o.x = o.x * inv * wn.x / (1.f + expf(-gl.x));
-    o.y = o.y * inv * wn.y / (1.f + expf(-gl.y));
-    o.z = o.z * inv * wn.z / (1.f + expf(-gl.z));
-    o.w = o.w * inv * wn.w / (1.f + expf(-gl.w));
-    store4<T>(static_cast<T*>(a.out) + n * a.out_sn + h * a.out_sh + 4 * col4, o);
+// Back end, one CTA per (request, head), column c on thread c: the step's output
+// o (fp32, already times scale) -> o / rms(o) * w * sigmoid(gate).
+template <int DV, typename T>
+__global__ void __launch_bounds__(kThreads) kda_decode_back_kernel(FusedDecodeArgs fa, const float* o) {
+  const DecodeArgs& a = fa.d;
+  __shared__ float s_buf[kThreads / 32];
+  const int nh = blockIdx.x;
+  const int n = nh / a.H;
+  const int h = nh - n * a.H;
+  const int tid = threadIdx.x;
+  const float y = tid < DV ? o[(int64_t)nh * DV + tid] : 0.f;
+  const float inv = rsqrtf(block_sum(y * y, s_buf, DV) / DV + fa.eps);
+  if (tid < DV) {
+    const float gl = to_f(static_cast<const T*>(fa.gate.ptr)[n * fa.gate.sb + h * fa.gate.sh + tid]);
+    const float w = fa.norm_w ? __ldg(fa.norm_w + tid) : 1.f;
+    static_cast<T*>(a.out)[n * a.out_sn + h * a.out_sh + tid] = from_f<T>(y * inv * w / (1.f + expf(-gl)));
   }
 }
 
@@ -761,23 +731,47 @@ cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s) {
   return e != cudaSuccess ? e : launch_end(s);
 }
 
-cudaError_t launch_decode_fused(const FusedDecodeArgs& fa, cudaStream_t s) {
+size_t decode_fused_workspace_bytes(int N, int H, int dk, int dv) {
+  return (size_t)((int64_t)N * H * (2 * dk + 2 * dv) * 4);
+}
+
+cudaError_t launch_decode_fused(const FusedDecodeArgs& fa, void* ws, cudaStream_t s) {
   const DecodeArgs& a = fa.d;
   if ((int64_t)a.N * a.H == 0) return cudaSuccess;
-  void (*fn)(FusedDecodeArgs) = nullptr;
-#define KDA_FCASE(DK_, DV_)                                                                     \
-  if (a.dk == DK_ && a.dv == DV_)                                                               \
-    fn = a.bf16 ? kda_decode_fused_kernel<DK_, DV_, __nv_bfloat16> : kda_decode_fused_kernel<DK_, DV_, float>;
+  void (*front)(FusedDecodeArgs, float*) = nullptr;
+  void (*back)(FusedDecodeArgs, const float*) = nullptr;
+#define KDA_FCASE(DK_, DV_)                                                                            \
+  if (a.dk == DK_ && a.dv == DV_)                                                                      \
+    front = a.bf16 ? kda_decode_front_kernel<DK_, DV_, __nv_bfloat16> : kda_decode_front_kernel<DK_, DV_, float>;
   KDA_FCASE(64, 64)
   KDA_FCASE(64, 128)
   KDA_FCASE(128, 64)
   KDA_FCASE(128, 128)
 #undef KDA_FCASE
-  if (!fn) return cudaErrorInvalidValue;
+  if (a.dv == 64) back = a.bf16 ? kda_decode_back_kernel<64, __nv_bfloat16> : kda_decode_back_kernel<64, float>;
+  if (a.dv == 128) back = a.bf16 ? kda_decode_back_kernel<128, __nv_bfloat16> : kda_decode_back_kernel<128, float>;
+  if (!front || !back) return cudaErrorInvalidValue;
+  const int64_t nh = (int64_t)a.N * a.H;
+  const int64_t xs = 2 * a.dk + a.dv;  // [q^ | k^ | v^] per (request, head)
+  float* x = static_cast<float*>(ws);
+  float* o = x + nh * xs;
+  cudaError_t e;
   launch_begin(s);
-  fn<<<dim3((unsigned)(a.N * a.H)), kThreads, 0, s>>>(fa);
-  const cudaError_t e = cudaGetLastError();
-  return e != cudaSuccess ? e : launch_end(s);
+  front<<<dim3((unsigned)nh), kThreads, 0, s>>>(fa, x);
+  if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
+  DecodeArgs d = a;  // the step on the fp32 front-end results, output to `o`
+  d.q = Act{x, a.H * xs, 0, xs};
+  d.k = Act{x + a.dk, a.H * xs, 0, xs};
+  d.v = Act{x + 2 * a.dk, a.H * xs, 0, xs};
+  d.bf16 = 0;
+  d.out = o;
+  d.out_sn = (int64_t)a.H * a.dv;
+  d.out_sh = a.dv;
+  if ((e = launch_decode(d, s)) != cudaSuccess) return e;
+  launch_begin(s);
+  back<<<dim3((unsigned)nh), kThreads, 0, s>>>(fa, o);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_end(s);
 }
 
 size_t backward_workspace_bytes(int N, int H, int T, int dk, int dv) {

@@ -283,6 +283,11 @@ kda_status kda_backward(const kda_tensor* q, const kda_tensor* k, const kda_tens
  *   scale, eps       finite; eps >= 0
  *   out              [N, H, d_v] q's dtype
  *
+ * Three kernels on `stream`: the front end writes the processed q, k, v in fp32
+ * to scratch from the library's stream-ordered pool (N * H * (2 d_k + 2 d_v) * 4
+ * bytes, released on the stream), the decode step reads them, and the back end
+ * finishes the output.
+ *
  * Errors as for kda_recurrent_step; no output may overlap another tensor.
  */
 kda_status kda_decode_step_fused(kda_tensor* state, kda_tensor* conv_q, kda_tensor* conv_k,
