@@ -222,10 +222,10 @@ __device__ __forceinline__ float conv_silu_update(T* cache, int64_t slot_stride,
   return y / (1.f + expf(-y));
 }
 
-// Front end, one CTA per (request, head), channel c on thread c: the fp32 inputs
-// of the step, [q^ | k^ | v^] per (request, head) in `x`.
+// Front end, one CTA of max(d_k, d_v) threads per (request, head), channel c on
+// thread c: the fp32 inputs of the step, [q^ | k^ | v^] per (request, head) in `x`.
 template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(kThreads) kda_decode_front_kernel(FusedDecodeArgs fa, float* x) {
+__global__ void __launch_bounds__(DK > DV ? DK : DV) kda_decode_front_kernel(FusedDecodeArgs fa, float* x) {
   const DecodeArgs& a = fa.d;
   __shared__ float s_buf[kThreads / 32];
   const int nh = blockIdx.x;
@@ -255,10 +255,10 @@ __global__ void __launch_bounds__(kThreads) kda_decode_front_kernel(FusedDecodeA
   }
 }
 
-// Back end, one CTA per (request, head), column c on thread c: the step's output
-// o (fp32, already times scale) -> o / rms(o) * w * sigmoid(gate).
+// Back end, one CTA of d_v threads per (request, head), column c on thread c: the
+// step's output o (fp32, already times scale) -> o / rms(o) * w * sigmoid(gate).
 template <int DV, typename T>
-__global__ void __launch_bounds__(kThreads) kda_decode_back_kernel(FusedDecodeArgs fa, const float* o) {
+__global__ void __launch_bounds__(DV) kda_decode_back_kernel(FusedDecodeArgs fa, const float* o) {
   const DecodeArgs& a = fa.d;
   __shared__ float s_buf[kThreads / 32];
   const int nh = blockIdx.x;
@@ -757,7 +757,7 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs& fa, void* ws, cudaStream_
   float* o = x + nh * xs;
   cudaError_t e;
   launch_begin(s);
-  front<<<dim3((unsigned)nh), kThreads, 0, s>>>(fa, x);
+  front<<<dim3((unsigned)nh), (unsigned)(a.dk > a.dv ? a.dk : a.dv), 0, s>>>(fa, x);
   if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   DecodeArgs d = a;  // the step on the fp32 front-end results, output to `o`
   d.q = Act{x, a.H * xs, 0, xs};
@@ -769,7 +769,7 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs& fa, void* ws, cudaStream_
   d.out_sh = a.dv;
   if ((e = launch_decode(d, s)) != cudaSuccess) return e;
   launch_begin(s);
-  back<<<dim3((unsigned)nh), kThreads, 0, s>>>(fa, o);
+  back<<<dim3((unsigned)nh), (unsigned)a.dv, 0, s>>>(fa, o);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_end(s);
 }
