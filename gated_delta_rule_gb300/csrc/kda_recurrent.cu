@@ -118,6 +118,32 @@ __device__ __forceinline__ float4 column_reduce(float4 part, float4 (*red)[DV / 
   return s;
 }
 
+// The same sums in the same order, formed once per column quad: the TPR threads of
+// row group 0 add the RPP partials and publish the totals in `tot` (one more
+// barrier, one sixteenth of the shared-memory reads).  For the token loops, whose
+// reductions are not hidden behind HBM traffic.
+template <int DK, int DV>
+__device__ __forceinline__ float4 column_reduce_lean(float4 part, float4 (*red)[DV / 4], float4* tot,
+                                                    int trow, int col4) {
+  using L = Layout<DK, DV>;
+  red[trow][col4] = part;
+  __syncthreads();
+  if (trow == 0) {
+    float4 s = red[0][col4];
+#pragma unroll
+    for (int r = 1; r < L::RPP; ++r) {
+      const float4 x = red[r][col4];
+      s.x += x.x;
+      s.y += x.y;
+      s.z += x.z;
+      s.w += x.w;
+    }
+    tot[col4] = s;
+  }
+  __syncthreads();
+  return tot[col4];
+}
+
 // ---------------------------------------------------------------------------
 // decode: one CTA per (request, head); every state element read once, written once
 template <int DK, int DV, typename T>
@@ -305,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs 
   __shared__ float s_q[2][DK], s_k[2][DK], s_a[2][DK];
   __shared__ float4 red0[L::RPP][DV / 4];
   __shared__ float4 red1[L::RPP][DV / 4];
+  __shared__ float4 tot0[DV / 4], tot1[DV / 4];
   const int nsl = a.dv / DV;
   const bool split = nsl > 1;
   const int col0 = (blockIdx.x % nsl) * DV;
@@ -365,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs 
       x[r].w *= al;
       fma4(part, s_k[buf][i], x[r]);
     }
-    const float4 kS = column_reduce<DK, DV>(part, red0, trow, col4);
+    const float4 kS = column_reduce_lean<DK, DV>(part, red0, tot0, trow, col4);
 #pragma unroll
     for (int r = 0; r < L::R; ++r) x[r] = delta_write(x[r], beta * s_k[buf][trow + L::RPP * r], kS, v4);
   };
@@ -437,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs 
         sb.w *= al;
         fma4(part, s_k[buf][i], sb);
       }
-      const float4 kS = column_reduce<DK, DV>(part, red0, trow, col4);
+      const float4 kS = column_reduce_lean<DK, DV>(part, red0, tot0, trow, col4);
       const float4 dl = make_float4(v4.x - kS.x, v4.y - kS.y, v4.z - kS.z, v4.w - kS.w);
       // dS += scale q do^T; dq = scale S do (S = Sb + beta k delta^T); c = dS^T k
       float dqr[L::R];
@@ -457,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs 
         dS[r].w = fmaf(sq, do4.w, dS[r].w);
         fma4(cp, ki, dS[r]);
       }
-      const float4 c = column_reduce<DK, DV>(cp, red1, trow, col4);
+      const float4 c = column_reduce_lean<DK, DV>(cp, red1, tot1, trow, col4);
       const float4 dd = make_float4(beta * c.x, beta * c.y, beta * c.z, beta * c.w);
       // dk = beta dS delta - Sb ddelta; dSb = dS - k ddelta^T; dalpha = rowsum(dSb * S_prev)
       float dkr[L::R], dar[L::R];
@@ -542,6 +569,7 @@ __global__ void __launch_bounds__(kThreads, 3) kda_recurrent_kernel(PrefillArgs 
   __shared__ float s_q[2][DK], s_k[2][DK], s_a[2][DK];
   __shared__ float4 red0[L::RPP][DV / 4];
   __shared__ float4 red1[L::RPP][DV / 4];
+  __shared__ float4 tot0[DV / 4], tot1[DV / 4];
   const int nsl = a.dv / DV;
   const int col0 = (blockIdx.x % nsl) * DV;  // first value column of this CTA
   const int nh = blockIdx.x / nsl;
@@ -633,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 3) kda_recurrent_kernel(PrefillArgs 
       s[r].w *= al;
       fma4(part, s_k[buf][i], s[r]);
     }
-    const float4 kS = column_reduce<DK, DV>(part, red0, trow, col4);
+    const float4 kS = column_reduce_lean<DK, DV>(part, red0, tot0, trow, col4);
     float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < L::R; ++r) {
@@ -653,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 3) kda_recurrent_kernel(PrefillArgs 
       for (int r = 0; r < L::R; ++r) __stcs(reinterpret_cast<float4*>(ST + (trow + L::RPP * r) * ld + 4 * col4), s[r]);
     }
     if (a.out) {
-      float4 o = column_reduce<DK, DV>(po, red1, trow, col4);
+      float4 o = column_reduce_lean<DK, DV>(po, red1, tot1, trow, col4);
       if (trow == 0) {
         o.x *= a.scale;
         o.y *= a.scale;
