@@ -21,8 +21,10 @@
 //     ready-to-use swizzled bf16 tiles -- T B_beta, [-W ; Q+], A_Q,
 //     K e^{G_C - G} -- plus e^{G_C} to a workspace.  Tiles that come out of
 //     TMEM or the solve are staged in shared memory and leave by bulk copy.
-//   * kda_chunk_serial_kernel: one CTA per (sequence, head) keeps the fp32 state
-//     in TMEM and walks the chunks in order, with warp roles: a producer warp
+//   * kda_chunk_serial_kernel: one CTA per (sequence, head, slice of 32, 64 or
+//     all d_v value columns -- the state's columns evolve independently) keeps
+//     its fp32 state columns in TMEM and walks the chunks in order, with warp
+//     roles: a producer warp
 //     (record by bulk copy, V by cp.async, one chunk ahead), an MMA warp and
 //     four TMEM <-> memory warps.  Each chunk costs three tcgen05 products:
 //     [U ; Q+ S] = [T_beta | -W ; 0 | Q+] [V ; S], then S += K_end^T U on the
@@ -72,8 +74,7 @@ struct Rec {
   static constexpr int kBytes = align1k(P + DK * 4);
 };
 
-// Gram column versions: version I has 16 (I + 1) rows.
-__host__ __device__ constexpr int yrows(int I) { return 16 * (I + 1); }
+// Gram column versions: version I has 16 (I + 1) rows, stacked in order.
 __host__ __device__ constexpr int yoff_rows(int I) { return 8 * I * (I + 1); }  // rows before version I
 
 // Decay-factor table of the prep kernel: entry (a, b), a < b <= 4, holds
@@ -1410,8 +1411,6 @@ cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
   auto prep = a.gate ? kda_chunk_prep_kernel<DK, true> : kda_chunk_prep_kernel<DK, false>;
   e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, PrepSmem<DK>::kAlloc);
   if (e != cudaSuccess) return e;
-  // Few chains (sequence-heads): split d_v = 128 into two 64-column CTAs so more SMs
-  // carry the serial loop.  Each slice CTA reads the whole chunk record.
   // Value-column slices: with few chains (sequence-heads), d_v is split into 32- or
   // 64-column CTAs, as finely as the SMs hold them, so that more SMs carry the
   // serial loop and each chunk step moves less.  Every slice CTA reads the whole
