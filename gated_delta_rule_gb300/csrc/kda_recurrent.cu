@@ -14,10 +14,12 @@
 //   S' = fma(beta k_i, v_j, fma(-beta k_i, (k^T S)_j, S_ij)),
 // so a unit key with beta = 1 reproduces v exactly in that row.
 //
-// Thread layout (256 threads per (sequence|request, head, 64 value columns)): a
-// 64-column state row slice is covered by 16 threads holding 4 consecutive
-// columns (one 16-byte vector each); 16 rows are handled side by side and each
-// thread keeps d_k/16 rows in registers.  Column sums over the key channels
+// Thread layout of the decode and token-recurrent kernels (128 threads per
+// (sequence|request, head, 64 value columns), four CTAs per SM): a 64-column
+// state row slice is covered by 16 threads holding 4 consecutive columns (one
+// 16-byte vector each); 8 rows are handled side by side and each thread keeps
+// d_k/8 rows in registers.  (The backward kernel uses 256 threads, 16 rows side
+// by side.)  Column sums over the key channels
 // (k^T S and q^T S) are reduced through shared memory in the same order in both
 // compute kernels.  A warp loads and stores two 256-byte row slices per
 // instruction.
@@ -29,6 +31,7 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kTok = 128;  // threads of the decode and token-recurrent kernels
 
 template <typename T>
 __device__ __forceinline__ float to_f(T x);
@@ -90,20 +93,20 @@ __device__ __forceinline__ float4 delta_write(float4 s, float bk, const float4& 
   return s;
 }
 
-template <int DK, int DV>
+template <int DK, int DV, int NT = kThreads>
 struct Layout {
   static constexpr int TPR = DV / 4;           // threads per state row
-  static constexpr int RPP = kThreads / TPR;   // rows side by side
+  static constexpr int RPP = NT / TPR;         // rows side by side
   static constexpr int R = DK / RPP;           // rows per thread
   static_assert(R * RPP == DK, "layout");
 };
 
 // Sum over the RPP row groups of per-thread partial column sums (the same order
 // in both compute kernels, so a token gives the same bits whichever kernel runs it).
-template <int DK, int DV>
+template <int DK, int DV, int NT = kThreads>
 __device__ __forceinline__ float4 column_reduce(float4 part, float4 (*red)[DV / 4], int trow,
                                                int col4) {
-  using L = Layout<DK, DV>;
+  using L = Layout<DK, DV, NT>;
   red[trow][col4] = part;
   __syncthreads();
   float4 s = red[0][col4];
@@ -122,10 +125,10 @@ __device__ __forceinline__ float4 column_reduce(float4 part, float4 (*red)[DV / 
 // row group 0 add the RPP partials and publish the totals in `tot` (one more
 // barrier, one sixteenth of the shared-memory reads).  For the token loops, whose
 // reductions are not hidden behind HBM traffic.
-template <int DK, int DV>
+template <int DK, int DV, int NT = kThreads>
 __device__ __forceinline__ float4 column_reduce_lean(float4 part, float4 (*red)[DV / 4], float4* tot,
                                                     int trow, int col4) {
-  using L = Layout<DK, DV>;
+  using L = Layout<DK, DV, NT>;
   red[trow][col4] = part;
   __syncthreads();
   if (trow == 0) {
@@ -147,8 +150,8 @@ __device__ __forceinline__ float4 column_reduce_lean(float4 part, float4 (*red)[
 // ---------------------------------------------------------------------------
 // decode: one CTA per (request, head); every state element read once, written once
 template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(kThreads, 3) kda_decode_kernel(DecodeArgs a) {
-  using L = Layout<DK, DV>;
+__global__ void __launch_bounds__(kTok, 4) kda_decode_kernel(DecodeArgs a) {
+  using L = Layout<DK, DV, kTok>;
   __shared__ float s_q[DK], s_k[DK], s_a[DK];
   __shared__ float4 red0[L::RPP][DV / 4];
   __shared__ float4 red1[L::RPP][DV / 4];
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 3) kda_decode_kernel(DecodeArgs a) {
     s[r].w *= al;
     fma4(part, s_k[i], s[r]);
   }
-  const float4 kS = column_reduce<DK, DV>(part, red0, trow, col4);
+  const float4 kS = column_reduce<DK, DV, kTok>(part, red0, trow, col4);
 
   float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 3) kda_decode_kernel(DecodeArgs a) {
     __stcs(reinterpret_cast<float4*>(S + i * ld + 4 * col4), s[r]);
     fma4(po, s_q[i], s[r]);
   }
-  float4 o = column_reduce<DK, DV>(po, red1, trow, col4);
+  float4 o = column_reduce<DK, DV, kTok>(po, red1, trow, col4);
   if (trow == 0) {
     o.x *= a.scale;
     o.y *= a.scale;
@@ -564,8 +567,8 @@ __global__ void kda_backward_zero_kernel(BackwardArgs ba) {
 // registers.  The state's columns evolve independently, so a (sequence, head)
 // may be spread over a.dv / DV CTAs.
 template <int DK, int DV, typename T, bool GATE>
-__global__ void __launch_bounds__(kThreads, 3) kda_recurrent_kernel(PrefillArgs a) {
-  using L = Layout<DK, DV>;
+__global__ void __launch_bounds__(kTok, 4) kda_recurrent_kernel(PrefillArgs a) {
+  using L = Layout<DK, DV, kTok>;
   __shared__ float s_q[2][DK], s_k[2][DK], s_a[2][DK];
   __shared__ float4 red0[L::RPP][DV / 4];
   __shared__ float4 red1[L::RPP][DV / 4];
@@ -661,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 3) kda_recurrent_kernel(PrefillArgs 
       s[r].w *= al;
       fma4(part, s_k[buf][i], s[r]);
     }
-    const float4 kS = column_reduce_lean<DK, DV>(part, red0, tot0, trow, col4);
+    const float4 kS = column_reduce_lean<DK, DV, kTok>(part, red0, tot0, trow, col4);
     float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < L::R; ++r) {
@@ -681,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 3) kda_recurrent_kernel(PrefillArgs 
       for (int r = 0; r < L::R; ++r) __stcs(reinterpret_cast<float4*>(ST + (trow + L::RPP * r) * ld + 4 * col4), s[r]);
     }
     if (a.out) {
-      float4 o = column_reduce_lean<DK, DV>(po, red1, tot1, trow, col4);
+      float4 o = column_reduce_lean<DK, DV, kTok>(po, red1, tot1, trow, col4);
       if (trow == 0) {
         o.x *= a.scale;
         o.y *= a.scale;
@@ -724,7 +727,7 @@ cudaError_t dispatch(const Args& a, int dk, int dv, int bf16, dim3 grid, cudaStr
 #undef KDA_CASE
   if (!fn) return cudaErrorInvalidValue;
   launch_begin(st);
-  fn<<<grid, kThreads, 0, st>>>(a);
+  fn<<<grid, kTok, 0, st>>>(a);
   const cudaError_t e = cudaGetLastError();
   return e != cudaSuccess ? e : launch_end(st);
 }
@@ -754,7 +757,7 @@ cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s) {
 #undef KDA_REC
   if (!fn || (a.dv != 64 && a.dv != 128)) return cudaErrorInvalidValue;
   launch_begin(s);
-  fn<<<dim3((unsigned)(a.N * a.H * (a.dv / 64))), kThreads, 0, s>>>(a);
+  fn<<<dim3((unsigned)(a.N * a.H * (a.dv / 64))), kTok, 0, s>>>(a);
   const cudaError_t e = cudaGetLastError();
   return e != cudaSuccess ? e : launch_end(s);
 }
