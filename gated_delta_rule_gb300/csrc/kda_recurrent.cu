@@ -15,7 +15,10 @@
 // so a unit key with beta = 1 reproduces v exactly in that row.
 //
 // Thread layout of the decode and token-recurrent kernels (128 threads per
-// (sequence|request, head, 64 value columns), four CTAs per SM): a 64-column
+// (sequence|request, head, 64 value columns); four CTAs per SM for the decode
+// step, five for the token loop, whose arithmetic per state byte is higher and
+// which gains more from the extra CTA than it loses to a few spilled
+// registers): a 64-column
 // state row slice is covered by 16 threads holding 4 consecutive columns (one
 // 16-byte vector each); 8 rows are handled side by side and each thread keeps
 // d_k/8 rows in registers.  (The backward kernel uses 256 threads, 16 rows side
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kTok, 4) kda_decode_kernel(DecodeArgs a) {
 // fused decode: front end (short convolutions, SiLU, L2 norm of q and k), the
 // decode step, back end (head RMSNorm, sigmoid output gate).  Three launches:
 // the step itself is the plain decode kernel on fp32 inputs, at its own
-// occupancy (three 64-column CTAs per SM); one kernel holding a whole head for
+// occupancy (four 64-column CTAs per SM); one kernel holding a whole head for
 // the RMS norm ran at two thirds of that.  The front and back ends move a few
 // hundred bytes per (request, head), the step 128 KB.
 
@@ -567,7 +570,7 @@ __global__ void kda_backward_zero_kernel(BackwardArgs ba) {
 // registers.  The state's columns evolve independently, so a (sequence, head)
 // may be spread over a.dv / DV CTAs.
 template <int DK, int DV, typename T, bool GATE>
-__global__ void __launch_bounds__(kTok, 4) kda_recurrent_kernel(PrefillArgs a) {
+__global__ void __launch_bounds__(kTok, 5) kda_recurrent_kernel(PrefillArgs a) {
   using L = Layout<DK, DV, kTok>;
   __shared__ float s_q[2][DK], s_k[2][DK], s_a[2][DK];
   __shared__ float4 red0[L::RPP][DV / 4];
@@ -748,7 +751,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
 
 cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s) {
   if ((int64_t)a.N * a.H == 0) return cudaSuccess;
-  // 64 value columns per CTA (three CTAs per SM): for d_v = 128 a (sequence, head)
+  // 64 value columns per CTA (four CTAs per SM): for d_v = 128 a (sequence, head)
   // spreads over two CTAs, which keeps more state traffic in flight
   void (*fn)(PrefillArgs) = nullptr;
 #define KDA_REC(DK_, G_) (a.bf16 ? kda_recurrent_kernel<DK_, 64, __nv_bfloat16, G_> : kda_recurrent_kernel<DK_, 64, float, G_>)
