@@ -4,6 +4,11 @@
 //                             registers (the fp32-input path, any sequence length),
 //                             also the multi-token decode step (requests as
 //                             sequences, the state kept after an accepted count);
+//   * kda_decode_front_kernel, kda_decode_back_kernel - the front end (short
+//                             convolutions, SiLU, L2 norms) and back end (RMS
+//                             norm, output gate) around kda_decode_kernel in the
+//                             fused decode step;
+//   * kda_backward_kernel   - reverse-mode derivative of the token recurrence;
 //   * kda_seqlens_kernel    - device-side validation of cu_seqlens.
 //
 // Both compute kernels run the single-step recurrence in the order of
