@@ -510,25 +510,55 @@ __global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs 
         dar[r] = dsb.x * Sp[r].x + dsb.y * Sp[r].y + dsb.z * Sp[r].z + dsb.w * Sp[r].w;
         dS[r] = make_float4(al * dsb.x, al * dsb.y, al * dsb.z, al * dsb.w);
       }
-      // row sums over the d_v columns; lane j of a row group writes row trow + RPP * j
+      // Row sums over the d_v columns of this thread's dq, dk and dg rows: a
+      // reduce-scatter across the TPR lanes of the row group, each exchange
+      // halving what a lane holds (the list: dq rows, dk rows, dg rows, zero
+      // padding); lane l ends with the totals of items [l NV/TPR, (l+1) NV/TPR).
+      {
+        constexpr int NV = ((3 * L::R + L::TPR - 1) / L::TPR) * L::TPR;
+        constexpr int kPer = NV / L::TPR;
+        float rs[NV];
 #pragma unroll
-      for (int r = 0; r < L::R; ++r) {
-        const float q_s = row_sum<L::TPR>(dqr[r]);
-        const float k_s = row_sum<L::TPR>(dkr[r]);
-        const float a_s = row_sum<L::TPR>(dar[r]);
-        if (col4 == r % L::TPR) {
-          const int i = trow + L::RPP * r;
-          float* pq = ba.dq.ptr + b * ba.dq.sb + t * ba.dq.st + h * ba.dq.sh + i;
-          float* pk = ba.dk.ptr + b * ba.dk.sb + t * ba.dk.st + h * ba.dk.sh + i;
-          float* pg = ba.dg.ptr + b * ba.dg.sb + t * ba.dg.st + h * ba.dg.sh + i;
-          if (split) {
-            atomicAdd(pq, a.scale * q_s);
-            atomicAdd(pk, k_s);
-            atomicAdd(pg, a_s * s_a[buf][i]);
-          } else {
-            *pq = a.scale * q_s;
-            *pk = k_s;
-            *pg = a_s * s_a[buf][i];
+        for (int r = 0; r < L::R; ++r) {
+          rs[r] = dqr[r];
+          rs[L::R + r] = dkr[r];
+          rs[2 * L::R + r] = dar[r];
+        }
+#pragma unroll
+        for (int j = 3 * L::R; j < NV; ++j) rs[j] = 0.f;
+#pragma unroll
+        for (int st = 1; (L::TPR >> st) > 0 && st <= 5; ++st) {
+          const int m = L::TPR >> st;  // partner lane offset
+          const int half = NV >> st;   // items kept after this exchange
+          const bool up = (col4 & m) != 0;
+#pragma unroll
+          for (int i = 0; i < half; ++i) {
+            const float send = up ? rs[i] : rs[i + half];
+            const float keep = up ? rs[i + half] : rs[i];
+            rs[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int j = col4 * kPer + i;
+          if (j < 3 * L::R) {
+            const int kind = j / L::R, rr = j - kind * L::R;  // 0: dq, 1: dk, 2: dg
+            const int row = trow + L::RPP * rr;
+            float* p;
+            float val = rs[i];
+            if (kind == 0) {
+              p = ba.dq.ptr + b * ba.dq.sb + t * ba.dq.st + h * ba.dq.sh + row;
+              val *= a.scale;
+            } else if (kind == 1) {
+              p = ba.dk.ptr + b * ba.dk.sb + t * ba.dk.st + h * ba.dk.sh + row;
+            } else {
+              p = ba.dg.ptr + b * ba.dg.sb + t * ba.dg.st + h * ba.dg.sh + row;
+              val *= s_a[buf][row];
+            }
+            if (split)
+              atomicAdd(p, val);
+            else
+              *p = val;
           }
         }
       }
