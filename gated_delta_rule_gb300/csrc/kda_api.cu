@@ -694,7 +694,8 @@ kda_status kda_backward(const kda_tensor* q, const kda_tensor* k, const kda_tens
     e = kda::launch_check_seqlens(a.cu_seqlens, a.N, a.T, a.err, st);
     if (e != cudaSuccess) return cuda_fail(e, "cu_seqlens check launch");
   }
-  const size_t ws_bytes = kda::backward_workspace_bytes(a.N, a.H, a.T, a.dk, a.dv);
+  const int64_t rows = (int64_t)a.B * a.T;
+  const size_t ws_bytes = kda::backward_workspace_bytes(a.N, a.H, a.T, rows, a.dk, a.dv);
   void* ws = nullptr;
   if (ws_bytes) {
     e = kda::scratch_alloc(&ws, ws_bytes, st);
@@ -702,6 +703,9 @@ kda_status kda_backward(const kda_tensor* q, const kda_tensor* k, const kda_tens
   }
   ba.ck = static_cast<float*>(ws);
   ba.scr = ba.ck + (int64_t)a.N * a.H * ba.nblk * a.dk * a.dv;
+  ba.part = kda::backward_value_slices(a.N, a.H, a.dv) == 4
+                ? ba.scr + (int64_t)a.N * a.H * kda::kBwdBlock * a.dk * a.dv
+                : nullptr;
   e = kda::launch_backward(ba, st);
   const cudaError_t ef = ws ? kda::scratch_free(ws, st) : cudaSuccess;
   if (e == cudaSuccess) e = ef;

@@ -99,10 +99,15 @@ struct BackwardArgs {
   int64_t ds0_sn, ds0_sh;
   float* ck;   // workspace: states every kBwdBlock tokens, [N * H][nblk][dk][dv]
   float* scr;  // workspace: the states entering each token of one block, [N * H][kBwdBlock][dk][dv]
+  float* part; // workspace when d_v is split four ways: the row sums of slices 2-3,
+               // [B * T * H][4][dk] (dq, dk, dg, dbeta at [3][0]); else null
   int nblk;    // ceil(T / kBwdBlock)
 };
 constexpr int kBwdBlock = 32;
-size_t backward_workspace_bytes(int N, int H, int T, int dk, int dv);
+// value-column slices per (sequence, head) of the backward kernel (1, 2 or 4)
+int backward_value_slices(int N, int H, int dv);
+// rows = B * T (the token rows of the inputs)
+size_t backward_workspace_bytes(int N, int H, int T, int64_t rows, int dk, int dv);
 cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
 
 // SIMT kernels (kda_recurrent.cu)

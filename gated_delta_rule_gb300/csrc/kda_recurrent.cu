@@ -332,9 +332,11 @@ __device__ __forceinline__ float row_sum(float x) {
   return x;
 }
 
-// One CTA per (sequence, head, DV value columns): with two column halves the row
-// sums (dq, dk, dg, dbeta) are added atomically into outputs zeroed beforehand;
-// two fp32 adds onto zero give the same bits in either order.
+// One CTA per (sequence, head, DV = 32 or 64 value columns).  With two slices the
+// row sums (dq, dk, dg, dbeta) are added atomically into outputs zeroed
+// beforehand: two fp32 adds onto zero give the same bits in either order.  With
+// four, slices 0-1 add into the outputs and slices 2-3 into a zeroed scratch
+// copy, which a last kernel adds in: the result is again independent of order.
 template <int DK, int DV, typename T>
 __global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs ba) {
   using L = Layout<DK, DV>;
@@ -347,6 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs 
   const bool split = nsl > 1;
   const int col0 = (blockIdx.x % nsl) * DV;
   const int nh = blockIdx.x / nsl;
+  // four slices: slices 2-3 add their row sums into ba.part, so that every output
+  // element gets exactly two atomic terms (the same bits in either order)
+  const bool to_part = nsl == 4 && (blockIdx.x % nsl) >= 2;
   const int n = nh / a.H;
   const int h = nh - n * a.H;
   const int64_t ld = a.dv;  // row stride of the state and its gradients
@@ -555,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs 
               p = ba.dg.ptr + b * ba.dg.sb + t * ba.dg.st + h * ba.dg.sh + row;
               val *= s_a[buf][row];
             }
+            if (to_part) p = ba.part + ((b * a.T + t) * a.H + h) * 4 * DK + kind * DK + row;
             if (split)
               atomicAdd(p, val);
             else
@@ -568,7 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs 
       if (trow == 0) {
         *reinterpret_cast<float4*>(ba.dv.ptr + b * ba.dv.sb + t * ba.dv.st + h * ba.dv.sh + col0 + 4 * col4) = dd;
         if (col4 == 0) {
-          float* pb = ba.dbeta + b * ba.db_sb + t * ba.db_st + h * ba.db_sh;
+          float* pb = to_part ? ba.part + ((b * a.T + t) * a.H + h) * 4 * DK + 3 * DK
+                              : ba.dbeta + b * ba.db_sb + t * ba.db_st + h * ba.db_sh;
           if (split)
             atomicAdd(pb, db);
           else
@@ -597,6 +604,24 @@ __global__ void kda_backward_zero_kernel(BackwardArgs ba) {
       ba.dg.ptr[b * ba.dg.sb + t * ba.dg.st + h * ba.dg.sh + i] = 0.f;
     }
     if (threadIdx.x == 0) ba.dbeta[b * ba.db_sb + t * ba.db_st + h * ba.db_sh] = 0.f;
+    if (ba.part)
+      for (int i = threadIdx.x; i < 4 * a.dk; i += blockDim.x) ba.part[r * 4 * a.dk + i] = 0.f;
+  }
+}
+
+// Four value-column slices: outputs += the row sums that slices 2-3 collected.
+__global__ void kda_backward_merge_kernel(BackwardArgs ba) {
+  const PrefillArgs& a = ba.f;
+  const int64_t rows = (int64_t)a.B * a.T * a.H;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const int64_t h = r % a.H, bt = r / a.H, t = bt % a.T, b = bt / a.T;
+    const float* pr = ba.part + r * 4 * a.dk;
+    for (int i = threadIdx.x; i < a.dk; i += blockDim.x) {
+      ba.dq.ptr[b * ba.dq.sb + t * ba.dq.st + h * ba.dq.sh + i] += pr[i];
+      ba.dk.ptr[b * ba.dk.sb + t * ba.dk.st + h * ba.dk.sh + i] += pr[a.dk + i];
+      ba.dg.ptr[b * ba.dg.sb + t * ba.dg.st + h * ba.dg.sh + i] += pr[2 * a.dk + i];
+    }
+    if (threadIdx.x == 0) ba.dbeta[b * ba.db_sb + t * ba.db_st + h * ba.db_sh] += pr[3 * a.dk];
   }
 }
 
@@ -843,29 +868,53 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs& fa, void* ws, cudaStream_
   return launch_end(s);
 }
 
-size_t backward_workspace_bytes(int N, int H, int T, int dk, int dv) {
+int backward_value_slices(int N, int H, int dv) {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  // 32 value columns per CTA while the SMs hold them all (each CTA's token loop is
+  // a latency chain: fewer columns, shorter steps), else 64
+  const int64_t nh = (int64_t)N * H;
+  return nh * (dv / 32) <= sms ? dv / 32 : (dv + 63) / 64;
+}
+
+size_t backward_workspace_bytes(int N, int H, int T, int64_t rows, int dk, int dv) {
   const int64_t nblk = ((int64_t)T + kBwdBlock - 1) / kBwdBlock;
-  return (size_t)((int64_t)N * H * (nblk + kBwdBlock) * dk * dv * 4);
+  const int64_t part = backward_value_slices(N, H, dv) == 4 ? rows * H * 4 * dk : 0;
+  return (size_t)(((int64_t)N * H * (nblk + kBwdBlock) * dk * dv + part) * 4);
 }
 
 cudaError_t launch_backward(const BackwardArgs& ba, cudaStream_t s) {
   const PrefillArgs& a = ba.f;
   if ((int64_t)a.N * a.H == 0) return cudaSuccess;
-  // 64 value columns per CTA: d_v = 128 spreads a (sequence, head) over two CTAs
+  if (a.dv != 64 && a.dv != 128) return cudaErrorInvalidValue;
+  const int nsl = backward_value_slices(a.N, a.H, a.dv);
+  const int W = a.dv / nsl;  // value columns per CTA
   void (*fn)(BackwardArgs) = nullptr;
-  if (a.dk == 128) fn = a.bf16 ? kda_backward_kernel<128, 64, __nv_bfloat16> : kda_backward_kernel<128, 64, float>;
-  if (a.dk == 64) fn = a.bf16 ? kda_backward_kernel<64, 64, __nv_bfloat16> : kda_backward_kernel<64, 64, float>;
-  if (!fn || (a.dv != 64 && a.dv != 128)) return cudaErrorInvalidValue;
+#define KDA_BWD(DK_, W_) (a.bf16 ? kda_backward_kernel<DK_, W_, __nv_bfloat16> : kda_backward_kernel<DK_, W_, float>)
+  if (a.dk == 128) fn = W == 32 ? KDA_BWD(128, 32) : KDA_BWD(128, 64);
+  if (a.dk == 64) fn = W == 32 ? KDA_BWD(64, 32) : KDA_BWD(64, 64);
+#undef KDA_BWD
+  if (!fn || (nsl == 4) != (ba.part != nullptr)) return cudaErrorInvalidValue;
   cudaError_t e;
-  if (a.dv > 64) {  // partial row sums are added: start from zero
+  if (nsl > 1) {  // partial row sums are added: start from zero
     launch_begin(s);
     kda_backward_zero_kernel<<<1024, 128, 0, s>>>(ba);
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   }
   launch_begin(s);
-  fn<<<dim3((unsigned)(a.N * a.H * (a.dv / 64))), kThreads, 0, s>>>(ba);
-  e = cudaGetLastError();
-  return e != cudaSuccess ? e : launch_end(s);
+  fn<<<dim3((unsigned)(a.N * a.H * nsl)), kThreads, 0, s>>>(ba);
+  if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
+  if (nsl == 4) {
+    launch_begin(s);
+    kda_backward_merge_kernel<<<1024, 128, 0, s>>>(ba);
+    if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_check_seqlens(const int32_t* cu, int N, int T, int* err, cudaStream_t s) {
