@@ -337,9 +337,9 @@ __device__ __forceinline__ float row_sum(float x) {
 // beforehand: two fp32 adds onto zero give the same bits in either order.  With
 // four, slices 0-1 add into the outputs and slices 2-3 into a zeroed scratch
 // copy, which a last kernel adds in: the result is again independent of order.
-template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs ba) {
-  using L = Layout<DK, DV>;
+template <int DK, int DV, typename T, int NT>
+__global__ void __launch_bounds__(NT, 1) kda_backward_kernel(BackwardArgs ba) {
+  using L = Layout<DK, DV, NT>;
   const PrefillArgs& a = ba.f;
   __shared__ float s_q[2][DK], s_k[2][DK], s_a[2][DK];
   __shared__ float4 red0[L::RPP][DV / 4];
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs 
       x[r].w *= al;
       fma4(part, s_k[buf][i], x[r]);
     }
-    const float4 kS = column_reduce_lean<DK, DV>(part, red0, tot0, trow, col4);
+    const float4 kS = column_reduce_lean<DK, DV, NT>(part, red0, tot0, trow, col4);
 #pragma unroll
     for (int r = 0; r < L::R; ++r) x[r] = delta_write(x[r], beta * s_k[buf][trow + L::RPP * r], kS, v4);
   };
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs 
         sb.w *= al;
         fma4(part, s_k[buf][i], sb);
       }
-      const float4 kS = column_reduce_lean<DK, DV>(part, red0, tot0, trow, col4);
+      const float4 kS = column_reduce_lean<DK, DV, NT>(part, red0, tot0, trow, col4);
       const float4 dl = make_float4(v4.x - kS.x, v4.y - kS.y, v4.z - kS.z, v4.w - kS.w);
       // dS += scale q do^T; dq = scale S do (S = Sb + beta k delta^T); c = dS^T k
       float dqr[L::R];
@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_backward_kernel(BackwardArgs 
         dS[r].w = fmaf(sq, do4.w, dS[r].w);
         fma4(cp, ki, dS[r]);
       }
-      const float4 c = column_reduce_lean<DK, DV>(cp, red1, tot1, trow, col4);
+      const float4 c = column_reduce_lean<DK, DV, NT>(cp, red1, tot1, trow, col4);
       const float4 dd = make_float4(beta * c.x, beta * c.y, beta * c.z, beta * c.w);
       // dk = beta dS delta - Sb ddelta; dSb = dS - k ddelta^T; dalpha = rowsum(dSb * S_prev)
       float dkr[L::R], dar[L::R];
@@ -895,10 +895,12 @@ cudaError_t launch_backward(const BackwardArgs& ba, cudaStream_t s) {
   const int nsl = backward_value_slices(a.N, a.H, a.dv);
   const int W = a.dv / nsl;  // value columns per CTA
   void (*fn)(BackwardArgs) = nullptr;
-#define KDA_BWD(DK_, W_) (a.bf16 ? kda_backward_kernel<DK_, W_, __nv_bfloat16> : kda_backward_kernel<DK_, W_, float>)
-  if (a.dk == 128) fn = W == 32 ? KDA_BWD(128, 32) : KDA_BWD(128, 64);
-  if (a.dk == 64) fn = W == 32 ? KDA_BWD(64, 32) : KDA_BWD(64, 64);
+#define KDA_BWD(DK_, W_, NT_) \
+  (a.bf16 ? kda_backward_kernel<DK_, W_, __nv_bfloat16, NT_> : kda_backward_kernel<DK_, W_, float, NT_>)
+  if (a.dk == 128) fn = W == 32 ? KDA_BWD(128, 32, kTok) : KDA_BWD(128, 64, kThreads);
+  if (a.dk == 64) fn = W == 32 ? KDA_BWD(64, 32, kTok) : KDA_BWD(64, 64, kThreads);
 #undef KDA_BWD
+  const int nt = W == 32 ? kTok : kThreads;
   if (!fn || (nsl == 4) != (ba.part != nullptr)) return cudaErrorInvalidValue;
   cudaError_t e;
   if (nsl > 1) {  // partial row sums are added: start from zero
@@ -907,7 +909,7 @@ cudaError_t launch_backward(const BackwardArgs& ba, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   }
   launch_begin(s);
-  fn<<<dim3((unsigned)(a.N * a.H * nsl)), kThreads, 0, s>>>(ba);
+  fn<<<dim3((unsigned)(a.N * a.H * nsl)), nt, 0, s>>>(ba);
   if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   if (nsl == 4) {
     launch_begin(s);
