@@ -743,11 +743,13 @@ kda_status kda_decode_step_fused(kda_tensor* state, kda_tensor* conv_q, kda_tens
   KDA_TRY(check_shape(out, "out", 3, wv3, dt));
   KDA_TRY(check_state(state, "state", N, H, dk, dv));
   const int64_t cqk[4] = {N, 3, H, dk}, cvs[4] = {N, 3, H, dv};
-  KDA_TRY(check_desc(conv_q, "conv_q", 4, 2));
+  // the kernels move channel pairs: caches aligned to two elements
+  const size_t pair = dt == KDA_DTYPE_BF16 ? 4 : 8;
+  KDA_TRY(check_desc(conv_q, "conv_q", 4, pair));
   KDA_TRY(check_shape(conv_q, "conv_q", 4, cqk, dt));
-  KDA_TRY(check_desc(conv_k, "conv_k", 4, 2));
+  KDA_TRY(check_desc(conv_k, "conv_k", 4, pair));
   KDA_TRY(check_shape(conv_k, "conv_k", 4, cqk, dt));
-  KDA_TRY(check_desc(conv_v, "conv_v", 4, 2));
+  KDA_TRY(check_desc(conv_v, "conv_v", 4, pair));
   KDA_TRY(check_shape(conv_v, "conv_v", 4, cvs, dt));
   const kda_tensor* ws[3] = {w_q, w_k, w_v};
   const char* wn[3] = {"w_q", "w_k", "w_v"};

@@ -47,12 +47,6 @@ template <>
 __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
-template <typename T>
-__device__ __forceinline__ T from_f(float x);
-template <>
-__device__ __forceinline__ float from_f<float>(float x) { return x; }
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
 template <typename T>
 __device__ __forceinline__ float4 load4(const T* p);
@@ -245,70 +239,96 @@ __device__ __forceinline__ float block_sum(float x, float* buf, int nthr) {
   return s;
 }
 
-// conv (width 4, causal, depthwise) of channel c, then SiLU; the cache slots
-// move down by one and the raw input enters the newest slot.
+// Two adjacent channels per thread in the fused decode's front and back ends (the
+// host requires the conv caches to be aligned to a channel pair).
 template <typename T>
-__device__ __forceinline__ float conv_silu_update(T* cache, int64_t slot_stride, const T* x, const float* w) {
-  const float c0 = to_f(cache[0]), c1 = to_f(cache[slot_stride]), c2 = to_f(cache[2 * slot_stride]);
-  const T raw = *x;
-  const float4 wv = __ldg(reinterpret_cast<const float4*>(w));
-  const float y = wv.x * c0 + wv.y * c1 + wv.z * c2 + wv.w * to_f(raw);
-  cache[0] = cache[slot_stride];
-  cache[slot_stride] = cache[2 * slot_stride];
-  cache[2 * slot_stride] = raw;
-  return y / (1.f + expf(-y));
+struct Pair;
+template <>
+struct Pair<float> {
+  using type = float2;
+  static __device__ __forceinline__ float2 f(float2 p) { return p; }
+  static __device__ __forceinline__ float2 make(float x, float y) { return make_float2(x, y); }
+};
+template <>
+struct Pair<__nv_bfloat16> {
+  using type = __nv_bfloat162;
+  static __device__ __forceinline__ float2 f(__nv_bfloat162 p) { return __bfloat1622float2(p); }
+  static __device__ __forceinline__ __nv_bfloat162 make(float x, float y) { return __floats2bfloat162_rn(x, y); }
+};
+
+// conv (width 4, causal, depthwise) of channels c and c + 1 over their three
+// cached raw inputs and the new one, then SiLU; the cache slots move down by one
+// and the raw inputs enter the newest slot (cache and x point at channel c)
+template <typename T>
+__device__ __forceinline__ float2 conv_silu_update2(T* cache, int64_t slot_stride, const T* x, const float* w) {
+  using P = typename Pair<T>::type;
+  P* c = reinterpret_cast<P*>(cache);
+  const P r0 = c[0], r1 = c[slot_stride / 2], r2 = c[slot_stride], raw = *reinterpret_cast<const P*>(x);
+  const float2 c0 = Pair<T>::f(r0), c1 = Pair<T>::f(r1), c2 = Pair<T>::f(r2), xv = Pair<T>::f(raw);
+  const float4 w0 = __ldg(reinterpret_cast<const float4*>(w)), w1 = __ldg(reinterpret_cast<const float4*>(w + 4));
+  const float y0 = w0.x * c0.x + w0.y * c1.x + w0.z * c2.x + w0.w * xv.x;
+  const float y1 = w1.x * c0.y + w1.y * c1.y + w1.z * c2.y + w1.w * xv.y;
+  c[0] = r1;
+  c[slot_stride / 2] = r2;
+  c[slot_stride] = raw;
+  return make_float2(y0 / (1.f + expf(-y0)), y1 / (1.f + expf(-y1)));
 }
 
-// Front end, one CTA of max(d_k, d_v) threads per (request, head), channel c on
-// thread c: the fp32 inputs of the step, [q^ | k^ | v^] per (request, head) in `x`.
+// Front end, one CTA of max(d_k, d_v) / 2 threads per (request, head), channels
+// 2t and 2t + 1 on thread t: the fp32 inputs of the step, [q^ | k^ | v^] per
+// (request, head) in `x`.
 template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(DK > DV ? DK : DV) kda_decode_front_kernel(FusedDecodeArgs fa, float* x) {
+__global__ void __launch_bounds__((DK > DV ? DK : DV) / 2) kda_decode_front_kernel(FusedDecodeArgs fa, float* x) {
   const DecodeArgs& a = fa.d;
   __shared__ float s_buf[kThreads / 32];
   const int nh = blockIdx.x;
   const int n = nh / a.H;
   const int h = nh - n * a.H;
-  const int tid = threadIdx.x;
-  float qa = 0.f, ka = 0.f;
-  if (tid < DK) {
-    T* cq = static_cast<T*>(fa.cq) + n * fa.cq_sn + h * fa.cq_sh + tid;
-    T* ck = static_cast<T*>(fa.ck) + n * fa.ck_sn + h * fa.ck_sh + tid;
-    qa = conv_silu_update<T>(cq, fa.cq_ss, static_cast<const T*>(a.q.ptr) + n * a.q.sb + h * a.q.sh + tid,
-                             fa.wq + ((int64_t)h * DK + tid) * 4);
-    ka = conv_silu_update<T>(ck, fa.ck_ss, static_cast<const T*>(a.k.ptr) + n * a.k.sb + h * a.k.sh + tid,
-                             fa.wk + ((int64_t)h * DK + tid) * 4);
+  const int c = 2 * threadIdx.x;
+  float2 qa = make_float2(0.f, 0.f), ka = make_float2(0.f, 0.f);
+  if (c < DK) {
+    T* cq = static_cast<T*>(fa.cq) + n * fa.cq_sn + h * fa.cq_sh + c;
+    T* ck = static_cast<T*>(fa.ck) + n * fa.ck_sn + h * fa.ck_sh + c;
+    qa = conv_silu_update2<T>(cq, fa.cq_ss, static_cast<const T*>(a.q.ptr) + n * a.q.sb + h * a.q.sh + c,
+                              fa.wq + ((int64_t)h * DK + c) * 4);
+    ka = conv_silu_update2<T>(ck, fa.ck_ss, static_cast<const T*>(a.k.ptr) + n * a.k.sb + h * a.k.sh + c,
+                              fa.wk + ((int64_t)h * DK + c) * 4);
   }
   float* xo = x + (int64_t)nh * (2 * DK + DV);
-  if (tid < DV) {
-    T* cv = static_cast<T*>(fa.cv) + n * fa.cv_sn + h * fa.cv_sh + tid;
-    xo[2 * DK + tid] = conv_silu_update<T>(cv, fa.cv_ss, static_cast<const T*>(a.v.ptr) + n * a.v.sb + h * a.v.sh + tid,
-                                          fa.wv + ((int64_t)h * DV + tid) * 4);
+  if (c < DV) {
+    T* cv = static_cast<T*>(fa.cv) + n * fa.cv_sn + h * fa.cv_sh + c;
+    *reinterpret_cast<float2*>(xo + 2 * DK + c) =
+        conv_silu_update2<T>(cv, fa.cv_ss, static_cast<const T*>(a.v.ptr) + n * a.v.sb + h * a.v.sh + c,
+                             fa.wv + ((int64_t)h * DV + c) * 4);
   }
-  const float nq = sqrtf(block_sum(qa * qa, s_buf, DK));
-  const float nk = sqrtf(block_sum(ka * ka, s_buf, DK));
-  if (tid < DK) {
-    xo[tid] = qa / fmaxf(nq, 1e-6f);
-    xo[DK + tid] = ka / fmaxf(nk, 1e-6f);
+  const float nq = sqrtf(block_sum(qa.x * qa.x + qa.y * qa.y, s_buf, DK / 2));
+  const float nk = sqrtf(block_sum(ka.x * ka.x + ka.y * ka.y, s_buf, DK / 2));
+  if (c < DK) {
+    const float iq = 1.f / fmaxf(nq, 1e-6f), ik = 1.f / fmaxf(nk, 1e-6f);
+    *reinterpret_cast<float2*>(xo + c) = make_float2(qa.x * iq, qa.y * iq);
+    *reinterpret_cast<float2*>(xo + DK + c) = make_float2(ka.x * ik, ka.y * ik);
   }
 }
 
-// Back end, one CTA of d_v threads per (request, head), column c on thread c: the
-// step's output o (fp32, already times scale) -> o / rms(o) * w * sigmoid(gate).
+// Back end, one CTA of d_v / 2 threads per (request, head), columns 2t and 2t + 1
+// on thread t: the step's output o (fp32, already times scale) -> o / rms(o) * w *
+// sigmoid(gate).
 template <int DV, typename T>
-__global__ void __launch_bounds__(DV) kda_decode_back_kernel(FusedDecodeArgs fa, const float* o) {
+__global__ void __launch_bounds__(DV / 2) kda_decode_back_kernel(FusedDecodeArgs fa, const float* o) {
   const DecodeArgs& a = fa.d;
   __shared__ float s_buf[kThreads / 32];
   const int nh = blockIdx.x;
   const int n = nh / a.H;
   const int h = nh - n * a.H;
-  const int tid = threadIdx.x;
-  const float y = tid < DV ? o[(int64_t)nh * DV + tid] : 0.f;
-  const float inv = rsqrtf(block_sum(y * y, s_buf, DV) / DV + fa.eps);
-  if (tid < DV) {
-    const float gl = to_f(static_cast<const T*>(fa.gate.ptr)[n * fa.gate.sb + h * fa.gate.sh + tid]);
-    const float w = fa.norm_w ? __ldg(fa.norm_w + tid) : 1.f;
-    static_cast<T*>(a.out)[n * a.out_sn + h * a.out_sh + tid] = from_f<T>(y * inv * w / (1.f + expf(-gl)));
-  }
+  const int c = 2 * threadIdx.x;
+  const float2 y = *reinterpret_cast<const float2*>(o + (int64_t)nh * DV + c);
+  const float inv = rsqrtf(block_sum(y.x * y.x + y.y * y.y, s_buf, DV / 2) / DV + fa.eps);
+  using P = typename Pair<T>::type;
+  const float2 gl = Pair<T>::f(*reinterpret_cast<const P*>(static_cast<const T*>(fa.gate.ptr) + n * fa.gate.sb +
+                                                             h * fa.gate.sh + c));
+  const float2 w = fa.norm_w ? __ldg(reinterpret_cast<const float2*>(fa.norm_w + c)) : make_float2(1.f, 1.f);
+  *reinterpret_cast<P*>(static_cast<T*>(a.out) + n * a.out_sn + h * a.out_sh + c) =
+      Pair<T>::make(y.x * inv * w.x / (1.f + expf(-gl.x)), y.y * inv * w.y / (1.f + expf(-gl.y)));
 }
 
 // ---------------------------------------------------------------------------
@@ -851,7 +871,7 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs& fa, void* ws, cudaStream_
   float* o = x + nh * xs;
   cudaError_t e;
   launch_begin(s);
-  front<<<dim3((unsigned)nh), (unsigned)(a.dk > a.dv ? a.dk : a.dv), 0, s>>>(fa, x);
+  front<<<dim3((unsigned)nh), (unsigned)((a.dk > a.dv ? a.dk : a.dv) / 2), 0, s>>>(fa, x);
   if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   DecodeArgs d = a;  // the step on the fp32 front-end results, output to `o`
   d.q = Act{x, a.H * xs, 0, xs};
@@ -863,7 +883,7 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs& fa, void* ws, cudaStream_
   d.out_sh = a.dv;
   if ((e = launch_decode(d, s)) != cudaSuccess) return e;
   launch_begin(s);
-  back<<<dim3((unsigned)nh), (unsigned)a.dv, 0, s>>>(fa, o);
+  back<<<dim3((unsigned)nh), (unsigned)(a.dv / 2), 0, s>>>(fa, o);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_end(s);
 }

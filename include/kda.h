@@ -272,7 +272,8 @@ kda_status kda_backward(const kda_tensor* q, const kda_tensor* k, const kda_tens
  *
  *   state            [N, H, d_k, d_v] f32, inner block contiguous; in/out
  *   conv_q, conv_k   [N, 3, H, d_k] in q's dtype; conv_v [N, 3, H, d_v]: the last
- *                    three raw inputs, oldest first; in/out
+ *                    three raw inputs, oldest first; in/out.  Pointer and strides
+ *                    aligned to two elements (channels move in pairs)
  *   q, k             [N, H, d_k] raw (pre-convolution) inputs, bf16 or f32
  *   v                [N, H, d_v] raw, q's dtype
  *   w_q, w_k         [H, d_k, 4] f32 contiguous; w_v [H, d_v, 4]: convolution

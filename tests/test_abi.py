@@ -124,6 +124,32 @@ def test_decode_rejects_invalid_arguments(lib):
     assert st == 1 and "out: dtype" in lib.kda_last_error_message().decode()
 
 
+def test_fused_decode_requires_channel_pair_aligned_caches(lib):
+    """The fused decode moves conv-cache channels in pairs: a cache that starts one
+    bf16 element off a 4-byte boundary is refused before any launch."""
+    r = ctypes.byref
+    N, H, d = 2, 2, 128
+    G = 1 << 30
+    state = T([N, H, d, d], 0, FAKE)
+    cq, ck, cv = (T([N, 3, H, d], 1, FAKE + i * G) for i in (1, 2, 3))
+    q, k, v = (T([N, H, d], 1, FAKE + i * G) for i in (4, 5, 6))
+    wq, wk, wv = (T([H, d, 4], 0, FAKE + i * G) for i in (7, 8, 9))
+    g = T([N, H, d], 0, FAKE + 10 * G)
+    beta = T([N, H], 0, FAKE + 11 * G)
+    gate = T([N, H, d], 1, FAKE + 12 * G)
+    out = T([N, H, d], 1, FAKE + 13 * G)
+
+    def call(conv_q):
+        return lib.kda_decode_step_fused(r(state), r(conv_q), r(ck), r(cv), r(q), r(k), r(v), r(wq), r(wk), r(wv),
+                                         r(g), r(beta), r(gate), None, ctypes.c_float(1.0), ctypes.c_float(1e-6), r(out),
+                                         None)
+
+    st = call(T([N, 3, H, d], 1, FAKE + G + 2))
+    assert st == 1 and "conv_q" in lib.kda_last_error_message().decode()
+    st = call(T([N, 3, H, d], 1, FAKE + G, stride=[3 * H * d + 1, H * d, d, 1]))
+    assert st == 1 and "conv_q" in lib.kda_last_error_message().decode()
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     import importlib
     m = importlib.import_module("gated_delta_rule_gb300")
