@@ -923,9 +923,12 @@ cudaError_t launch_backward(const BackwardArgs& ba, cudaStream_t s) {
   const int nt = W == 32 ? kTok : kThreads;
   if (!fn || (nsl == 4) != (ba.part != nullptr)) return cudaErrorInvalidValue;
   cudaError_t e;
+  // zeroing and merging: one block per token row (grid-stride past 2^20 rows)
+  const int64_t rows = (int64_t)a.B * a.T * a.H;
+  const unsigned rgrid = (unsigned)(rows < (1 << 20) ? (rows > 0 ? rows : 1) : (1 << 20));
   if (nsl > 1) {  // partial row sums are added: start from zero
     launch_begin(s);
-    kda_backward_zero_kernel<<<1024, 128, 0, s>>>(ba);
+    kda_backward_zero_kernel<<<rgrid, 128, 0, s>>>(ba);
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   }
   launch_begin(s);
@@ -933,7 +936,7 @@ cudaError_t launch_backward(const BackwardArgs& ba, cudaStream_t s) {
   if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   if (nsl == 4) {
     launch_begin(s);
-    kda_backward_merge_kernel<<<1024, 128, 0, s>>>(ba);
+    kda_backward_merge_kernel<<<rgrid, 128, 0, s>>>(ba);
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   }
   return cudaSuccess;
