@@ -247,8 +247,10 @@ kda_status kda_chunk_fwd_gated(const kda_tensor* q, const kda_tensor* k, const k
  *   d_initial_state  [N, H, d_k, d_v] f32, or NULL (not written)
  *
  * Scratch comes from the stream-ordered pool: N * H * (ceil(T / 32) + 32) *
- * d_k * d_v * 4 bytes.  Errors as for kda_chunk_fwd; no gradient may overlap an
- * input or another gradient.
+ * d_k * d_v * 4 bytes, plus B * T * H * 4 * d_k * 4 bytes when d_v = 128 is
+ * split over four 32-column CTAs per (sequence, head) (few sequence-heads).  The
+ * result does not depend on the order in which those CTAs finish.  Errors as
+ * for kda_chunk_fwd; no gradient may overlap an input or another gradient.
  */
 kda_status kda_backward(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
                         const kda_tensor* g, const kda_tensor* beta, const kda_tensor* initial_state,
