@@ -413,3 +413,27 @@ def _loop(variant):
 def test_planted_mistakes_are_caught(variant):
     assert all(pin(_loop("none")) for pin in PINS)
     assert not all(pin(_loop(variant)) for pin in PINS), variant
+
+
+@pytest.mark.parametrize("T,C,with_state", [(11, 1, True), (11, 4, True), (70, 16, False), (70, 64, True),
+                                            (64, 64, True), (1, 64, False)])
+def test_chunked_backward_matches_token_autograd(T, C, with_state):
+    """The chunk-by-chunk hand derivative of the chunked form gives the same gradients
+    as reverse-mode differentiation of the token recurrence (itself pinned to finite
+    differences), for full, partial and single-token chunks, with and without an
+    initial state and a final-state gradient."""
+    rng = np.random.default_rng(T * 100 + C)
+    B, H, dk, dv = 1, 1, 8, 5
+    q = rng.standard_normal((B, T, H, dk)); k = rng.standard_normal((B, T, H, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, H, dv)); g = -rng.uniform(0.01, 0.5, (B, T, H, dk))
+    beta = rng.uniform(0.1, 0.9, (B, T, H)); do = rng.standard_normal((B, T, H, dv))
+    S0 = rng.standard_normal((B, H, dk, dv)) if with_state else None
+    dST = rng.standard_normal((B, H, dk, dv)) if with_state else None
+    ref = oracle.backward(q, k, v, g, beta, S0, 0.6, do, dST)
+    got = kn.backward_chunked(q[0, :, 0], k[0, :, 0], v[0, :, 0], g[0, :, 0], beta[0, :, 0],
+                              None if S0 is None else S0[0, 0], 0.6, do[0, :, 0],
+                              None if dST is None else dST[0, 0], C)
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert np.allclose(got[name], ref[name][0, :, 0], rtol=1e-9, atol=1e-10), name
+    assert np.allclose(got["d_initial_state"], ref["d_initial_state"][0, 0], rtol=1e-9, atol=1e-10)
