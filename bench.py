@@ -532,9 +532,15 @@ def bench_decode_fused(kda, steps_total, warmup, stream, clk=None):
     return dict(ms=ms, N=N, H=H, bytes=N * H * per_head, launches=launches, steps=steps_total)
 
 
-def bench_backward(kda, steps, warmup, stream):
-    """kda_backward on the headline prefill workload (B=2, H=16, T=4096): gradients of
-    every input given random output and final-state gradients."""
+CHUNK_BWD_KERNELS = ["kda_bwd_prep_kernel", "kda_bwd_state_fwd_kernel", "kda_bwd_state_rev_kernel",
+                     "kda_bwd_grad_kernel"]
+
+
+def bench_backward(kda, steps, warmup, stream, entry="kda_chunk_bwd", names=None):
+    """``entry`` (kda_chunk_bwd or kda_backward) on the headline prefill workload (B=2,
+    H=16, T=4096): gradients of every input given random output and final-state
+    gradients.  With ``names`` (the call's kernels in launch order), a second set of
+    calls records an event between the kernels for the per-kernel split."""
     d = ki.workload_inputs(PREFILL_W)
     dev = torch.device("cuda")
     t = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in d.items()}
@@ -544,9 +550,10 @@ def bench_backward(kda, steps, warmup, stream):
     do = torch.randn(B, T, H, dv, generator=gen).to(torch.bfloat16).to(dev)
     dST = torch.randn(B, H, dk, dv, generator=gen).to(dev)
 
+    fn = getattr(kda, entry)
+
     def step():
-        kda.kda_backward(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"], t["scale"], do, dST,
-                         stream=stream)
+        fn(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"], t["scale"], do, dST, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -563,11 +570,29 @@ def bench_backward(kda, steps, warmup, stream):
         e1.record(stream)
         stream.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    kernel_ms = {}
+    if names:
+        kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for ke in kev:
+                for ev in ke:
+                    ev.record(stream)
+            stream.synchronize()
+            for ke in kev:
+                torch.cuda._sleep(SLEEP_CYCLES)
+                kda.kda_set_launch_events(ke)
+                step()
+            stream.synchronize()
+        if launches != steps * len(names):
+            raise RuntimeError(f"expected {len(names)} kernels per call, counted {launches / steps}")
+        for i, n in enumerate(names):
+            kernel_ms[n] = statistics.mean(ke[i].elapsed_time(ke[i + 1]) for ke in kev)
     th = B * T * H
     # inputs (q, k, v, d_out bf16; g fp32; beta) and fp32 gradients, plus the states
     per = 2 * (2 * dk + 2 * dv) + 4 * dk + 4 + 4 * (3 * dk + dv) + 4
     nbytes = th * per + 4 * dk * dv * B * H * 4
-    return dict(ms=ms, tokens=B * T, bytes=nbytes, launches=launches, name=ki.WORKLOADS[PREFILL_W]["name"])
+    return dict(ms=ms, tokens=B * T, bytes=nbytes, launches=launches, kernel_ms=kernel_ms,
+                name=ki.WORKLOADS[PREFILL_W]["name"])
 
 
 ORACLE_MIN_CPU_S = 12.0  # CPU-seconds (wall x threads) of oracle work behind each rate
@@ -773,12 +798,18 @@ def main():
         "tokens_per_s": world * gp["tokens"] / (gms * 1e-3),
         "hbm_frac": gp["bytes"] / (gms * 1e-3) / 1e9 / pk["hbm"], "gpu_launches": gp["launches"]}
     del gp
-    bw = bench_backward(kda, max(3, args.steps // 4), 3, stream)
+    bw = bench_backward(kda, max(3, args.steps // 4), 3, stream, "kda_chunk_bwd", CHUNK_BWD_KERNELS)
     bms = max_over_ranks(bw["ms"], world)
     extra["backward"] = {
-        "workload": bw["name"] + "_backward", "ms_per_call": bms,
+        "workload": bw["name"] + "_backward", "entry": "kda_chunk_bwd", "ms_per_call": bms,
+        "kernel_ms": {n: max_over_ranks(v, world) for n, v in bw["kernel_ms"].items()},
         "tokens_per_s": world * bw["tokens"] / (bms * 1e-3),
         "hbm_frac": bw["bytes"] / (bms * 1e-3) / 1e9 / pk["hbm"], "gpu_launches": bw["launches"]}
+    bw = bench_backward(kda, 3, 3, stream, "kda_backward")
+    bms = max_over_ranks(bw["ms"], world)
+    extra["backward_token_loop"] = {
+        "workload": bw["name"] + "_backward", "entry": "kda_backward", "ms_per_call": bms,
+        "tokens_per_s": world * bw["tokens"] / (bms * 1e-3), "gpu_launches": bw["launches"]}
     del bw
     if not args.no_varlen:
         clk_vl = ClockSampler(local)

@@ -16,7 +16,7 @@ from ._build import LIB, build, up_to_date  # noqa: F401
 
 __all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
            "kda_recurrent_multi_step", "kda_chunk_fwd_gated", "kda_chunk_fwd_checkpointed",
-           "kda_decode_step_fused", "kda_backward",
+           "kda_decode_step_fused", "kda_backward", "kda_chunk_bwd",
            "kda_get_device_error", "kda_set_launch_events", "kda_last_launch_count", "KdaError",
            "load_library", "build", "STATUS"]
 
@@ -26,7 +26,7 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
 
 EXPORTED = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
             "kda_recurrent_multi_step", "kda_chunk_fwd_gated", "kda_chunk_fwd_checkpointed",
-            "kda_decode_step_fused", "kda_backward",
+            "kda_decode_step_fused", "kda_backward", "kda_chunk_bwd",
             "kda_get_device_error", "kda_status_string", "kda_last_error_message",
             "kda_set_launch_events", "kda_last_launch_count"]
 
@@ -64,6 +64,8 @@ def load_library(path: str | None = None):
     lib.kda_recurrent_step.argtypes = [_P] * 6 + [ctypes.c_float, _P, ctypes.c_void_p]
     lib.kda_backward.restype = ctypes.c_int
     lib.kda_backward.argtypes = [_P] * 6 + [ctypes.c_float] + [_P] * 9 + [ctypes.c_void_p]
+    lib.kda_chunk_bwd.restype = ctypes.c_int
+    lib.kda_chunk_bwd.argtypes = [_P] * 6 + [ctypes.c_float] + [_P] * 9 + [ctypes.c_void_p]
     lib.kda_decode_step_fused.restype = ctypes.c_int
     lib.kda_decode_step_fused.argtypes = [_P] * 14 + [ctypes.c_float, ctypes.c_float, _P, ctypes.c_void_p]
     lib.kda_chunk_fwd_checkpointed.restype = ctypes.c_int
@@ -265,11 +267,8 @@ def kda_decode_step_fused(state, conv_q, conv_k, conv_v, q, k, v, w_q, w_k, w_v,
     return out
 
 
-def kda_backward(q, k, v, g, beta, initial_state, scale, d_out, d_final_state=None, cu_seqlens=None,
-                 need_initial_state_grad=True, stream=None):
-    """Gradients of the KDA core (kda_chunk_fwd's forward) given d_out [B, T, H, dv]
-    and d_final_state [N, H, dk, dv] (or None).  Returns a dict of fp32 tensors dq,
-    dk, dv, dg, dbeta and d_initial_state (None unless requested)."""
+def _backward(entry, q, k, v, g, beta, initial_state, scale, d_out, d_final_state, cu_seqlens,
+              need_initial_state_grad, stream):
     lib = load_library()
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -284,9 +283,26 @@ def kda_backward(q, k, v, g, beta, initial_state, scale, d_out, d_final_state=No
     ds = [desc(x) for x in (q, k, v, g, beta, initial_state)]
     dr = [desc(x) for x in (cu_seqlens, d_out, d_final_state, out["dq"], out["dk"], out["dv"], out["dg"],
                             out["dbeta"], out["d_initial_state"])]
-    st = lib.kda_backward(*[_ref(x) for x in ds], float(scale), *[_ref(x) for x in dr], _stream(stream))
+    st = getattr(lib, entry)(*[_ref(x) for x in ds], float(scale), *[_ref(x) for x in dr], _stream(stream))
     _check(lib, st)
     return out
+
+
+def kda_backward(q, k, v, g, beta, initial_state, scale, d_out, d_final_state=None, cu_seqlens=None,
+                 need_initial_state_grad=True, stream=None):
+    """Gradients of the KDA core (kda_chunk_fwd's forward) given d_out [B, T, H, dv]
+    and d_final_state [N, H, dk, dv] (or None), by the token loop.  Returns a dict of
+    fp32 tensors dq, dk, dv, dg, dbeta and d_initial_state (None unless requested)."""
+    return _backward("kda_backward", q, k, v, g, beta, initial_state, scale, d_out, d_final_state, cu_seqlens,
+                     need_initial_state_grad, stream)
+
+
+def kda_chunk_bwd(q, k, v, g, beta, initial_state, scale, d_out, d_final_state=None, cu_seqlens=None,
+                  need_initial_state_grad=True, stream=None):
+    """The gradients of kda_backward by the chunked form (g in [-5, 0]); same
+    arguments and result."""
+    return _backward("kda_chunk_bwd", q, k, v, g, beta, initial_state, scale, d_out, d_final_state, cu_seqlens,
+                     need_initial_state_grad, stream)
 
 
 def kda_get_device_error(stream=None) -> int:

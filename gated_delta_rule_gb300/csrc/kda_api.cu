@@ -12,6 +12,7 @@
 
 #include "kda.h"
 #include "kda_internal.h"
+#include "kda_backward_chunk.h"
 
 namespace {
 
@@ -571,11 +572,14 @@ kda_status kda_recurrent_step(kda_tensor* state, const kda_tensor* q, const kda_
   return KDA_OK;
 }
 
-kda_status kda_backward(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
-                        const kda_tensor* g, const kda_tensor* beta, const kda_tensor* initial_state,
-                        float scale, const kda_tensor* cu, const kda_tensor* d_out,
-                        const kda_tensor* d_final_state, kda_tensor* dq, kda_tensor* dk, kda_tensor* dv,
-                        kda_tensor* dg, kda_tensor* dbeta, kda_tensor* d_initial_state, void* stream) {
+namespace {
+
+// kda_backward (token loop, chunked = false) and kda_chunk_bwd (chunked form)
+kda_status backward_impl(bool chunked, const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                         const kda_tensor* g, const kda_tensor* beta, const kda_tensor* initial_state,
+                         float scale, const kda_tensor* cu, const kda_tensor* d_out,
+                         const kda_tensor* d_final_state, kda_tensor* dq, kda_tensor* dk, kda_tensor* dv,
+                         kda_tensor* dg, kda_tensor* dbeta, kda_tensor* d_initial_state, void* stream) {
   LaunchScope scope;
   g_msg.clear();
   KDA_TRY(check_desc(q, "q", 4, 16));
@@ -694,6 +698,17 @@ kda_status kda_backward(const kda_tensor* q, const kda_tensor* k, const kda_tens
     e = kda::launch_check_seqlens(a.cu_seqlens, a.N, a.T, a.err, st);
     if (e != cudaSuccess) return cuda_fail(e, "cu_seqlens check launch");
   }
+  if (chunked) {
+    const size_t cb = kda::chunk_backward_workspace_bytes(a);
+    void* cws = nullptr;
+    e = kda::scratch_alloc(&cws, cb, st);
+    if (e != cudaSuccess) return cuda_fail(e, "backward workspace allocation");
+    e = kda::launch_chunk_backward(ba, cws, st);
+    const cudaError_t ef = kda::scratch_free(cws, st);
+    if (e == cudaSuccess) e = ef;
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return KDA_OK;
+  }
   const int64_t rows = (int64_t)a.B * a.T;
   const size_t ws_bytes = kda::backward_workspace_bytes(a.N, a.H, a.T, rows, a.dk, a.dv);
   void* ws = nullptr;
@@ -711,6 +726,26 @@ kda_status kda_backward(const kda_tensor* q, const kda_tensor* k, const kda_tens
   if (e == cudaSuccess) e = ef;
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return KDA_OK;
+}
+
+}  // namespace
+
+kda_status kda_backward(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                        const kda_tensor* g, const kda_tensor* beta, const kda_tensor* initial_state,
+                        float scale, const kda_tensor* cu, const kda_tensor* d_out,
+                        const kda_tensor* d_final_state, kda_tensor* dq, kda_tensor* dk, kda_tensor* dv,
+                        kda_tensor* dg, kda_tensor* dbeta, kda_tensor* d_initial_state, void* stream) {
+  return backward_impl(false, q, k, v, g, beta, initial_state, scale, cu, d_out, d_final_state, dq, dk, dv, dg,
+                       dbeta, d_initial_state, stream);
+}
+
+kda_status kda_chunk_bwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                         const kda_tensor* g, const kda_tensor* beta, const kda_tensor* initial_state,
+                         float scale, const kda_tensor* cu, const kda_tensor* d_out,
+                         const kda_tensor* d_final_state, kda_tensor* dq, kda_tensor* dk, kda_tensor* dv,
+                         kda_tensor* dg, kda_tensor* dbeta, kda_tensor* d_initial_state, void* stream) {
+  return backward_impl(true, q, k, v, g, beta, initial_state, scale, cu, d_out, d_final_state, dq, dk, dv, dg,
+                       dbeta, d_initial_state, stream);
 }
 
 kda_status kda_decode_step_fused(kda_tensor* state, kda_tensor* conv_q, kda_tensor* conv_k,

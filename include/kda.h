@@ -259,6 +259,31 @@ kda_status kda_backward(const kda_tensor* q, const kda_tensor* k, const kda_tens
                         kda_tensor* dg, kda_tensor* dbeta, kda_tensor* d_initial_state, void* stream);
 
 /*
+ * kda_chunk_bwd - the same gradients as kda_backward (same arguments, layouts
+ * and errors), computed by the chunked form instead of the token loop.
+ *
+ * Per chunk of 64 tokens it differentiates the chunked equations of
+ * "尝试对Kimi KDA的数学推导&算子实现分析" (hjcheng0602.cn/blog/kdd) eqs. (9),
+ * (15)-(16), (36), (51)-(52), (63)-(66): a chunk-parallel kernel forms each
+ * chunk's state-independent matrices, two sequential kernels carry the state
+ * forward and its gradient backward through the chunks (per sequence, head and
+ * 32 value columns; the reverse one writes dv), and a chunk-parallel kernel
+ * forms dq, dk, dg and dbeta.  Like kda_chunk_fwd it relies on g in [-5, 0]
+ * (cumulative decays inside a 16-token sub-block above -80; outside that range
+ * use kda_backward).  The result is deterministic (no atomics).
+ *
+ * Scratch comes from the stream-ordered pool: per (chunk, head)
+ * (4*64*d_k + 2*64*d_v + d_k + d_k*d_v + 64*64 + 2*d_k*d_v + 2*64*d_v) * 4 bytes,
+ * about 475 KB at d_k = d_v = 128, over N * ceil(T / 64) chunks (ceil(T / 64) + N
+ * with cu_seqlens).
+ */
+kda_status kda_chunk_bwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                         const kda_tensor* g, const kda_tensor* beta, const kda_tensor* initial_state,
+                         float scale, const kda_tensor* cu_seqlens, const kda_tensor* d_out,
+                         const kda_tensor* d_final_state, kda_tensor* dq, kda_tensor* dk, kda_tensor* dv,
+                         kda_tensor* dg, kda_tensor* dbeta, kda_tensor* d_initial_state, void* stream);
+
+/*
  * kda_decode_step_fused - one decode token per (request, head) with the KDA
  * layer's front and back ends fused around kda_recurrent_step.
  *
