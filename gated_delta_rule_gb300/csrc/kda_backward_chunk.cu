@@ -20,13 +20,13 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_prep_kernel(ChunkBwdArgs ca) {
 }
 
 template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(128, 1) kda_bwd_state_fwd_kernel(ChunkBwdArgs ca) {
+__global__ void __launch_bounds__(bwdc::kPassThreads, 1) kda_bwd_state_fwd_kernel(ChunkBwdArgs ca) {
   extern __shared__ __align__(16) float sm[];
   bwdc::pass_body<DK, DV, T, false>(ca, sm, blockIdx.x, threadIdx.x);
 }
 
 template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(128, 1) kda_bwd_state_rev_kernel(ChunkBwdArgs ca) {
+__global__ void __launch_bounds__(bwdc::kPassThreads, 1) kda_bwd_state_rev_kernel(ChunkBwdArgs ca) {
   extern __shared__ __align__(16) float sm[];
   bwdc::pass_body<DK, DV, T, true>(ca, sm, blockIdx.x, threadIdx.x);
 }
@@ -118,11 +118,11 @@ cudaError_t run(const ChunkBwdArgs& ca, cudaStream_t s) {
     prep<<<cgrid, 256, PS::BYTES, s>>>(ca);
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
     launch_begin(s);
-    sfwd<<<pgrid, 128, SS::BYTES, s>>>(ca);
+    sfwd<<<pgrid, bwdc::kPassThreads, SS::BYTES, s>>>(ca);
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   }
   launch_begin(s);
-  srev<<<pgrid, 128, SS::BYTES, s>>>(ca);
+  srev<<<pgrid, bwdc::kPassThreads, SS::BYTES, s>>>(ca);
   if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   if (ca.total > 0) {
     launch_begin(s);

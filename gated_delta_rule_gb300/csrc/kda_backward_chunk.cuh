@@ -83,15 +83,6 @@ struct ChunkBwdArgs {
   float* st;       // [total][H][Rec::SSIZE]
 };
 
-template <typename T>
-KB_HD float ldf(const T* p);
-template <>
-KB_HD float ldf<float>(const float* p) { return *p; }
-#if defined(__CUDACC__)
-template <>
-KB_HD float ldf<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-#endif
-
 // 16-byte copy global -> shared that lands by the next cp_wait_all()
 KB_HD void cp16(float* dst, const float* src) {
 #if defined(__CUDACC__)
@@ -113,6 +104,24 @@ KB_HD void cp_wait_all() {
 }
 
 KB_HD float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// four consecutive elements as fp32 (8-byte aligned for bf16, 16-byte for fp32)
+template <typename T>
+KB_HD float4 ld4t(const T* p);
+template <>
+KB_HD float4 ld4t<float>(const float* p) { return *reinterpret_cast<const float4*>(p); }
+#if defined(__CUDACC__)
+template <>
+KB_HD float4 ld4t<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  float4 r;
+  r.x = __uint_as_float(u.x << 16);
+  r.y = __uint_as_float(u.x & 0xffff0000u);
+  r.z = __uint_as_float(u.y << 16);
+  r.w = __uint_as_float(u.y & 0xffff0000u);
+  return r;
+}
+#endif
 KB_HD void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 KB_HD void fma4(float4& acc, float s, const float4& x) {
   acc.x += s * x.x;
@@ -126,6 +135,7 @@ KB_HD float4 zero4() {
   return z;
 }
 KB_HD float& comp(float4& v, int e) { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; }
+KB_HD float comp(const float4& v, int e) { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; }
 
 // Where a chunk index falls: sequence n, chunk c of it, its first token row and
 // its number of valid rows.
@@ -182,21 +192,55 @@ KB_HD bool locate(const ChunkBwdArgs& a, int f, ChunkLoc& L) {
   return L.rows > 0;
 }
 
-// acc[r][c4] += sum_{j in [j0, j1)} lhs(r, j) * rhs[j][4 cg + 64 c4], for a thread
-// holding rows 4 rg .. 4 rg + 3 and columns {4 cg + 64 c4 .. + 3} of a [64][D] result.
-template <int D, class Lhs>
-KB_HD void mm64(float4 (&acc)[4][D / 64], const Lhs& lhs, const float* rhs, int pitch, int j0, int j1,
-                int cg) {
+// A [64][D] row tile of an input with row stride `st` (zero past `rows`), as the
+// 4-vectors idx = tid + u NT (row idx / (D / 4), columns 4 (idx % (D / 4)) ..): all
+// loads are issued before any is used.
+template <int D, int NT, typename T>
+KB_HD void load_rows(float4 (&v)[kC * D / 4 / NT], const T* base, int64_t st, int rows, int tid) {
+  static_assert((kC * D / 4) % NT == 0, "whole vectors per thread");
+#pragma unroll
+  for (int u = 0; u < kC * D / 4 / NT; ++u) {
+    const int idx = tid + u * NT, i = idx / (D / 4), p = idx - i * (D / 4);
+    v[u] = i < rows ? ld4t<T>(base + (int64_t)i * st + 4 * p) : zero4();
+  }
+}
+
+// acc[r][c4] += sum_{j in [j0, j1)} L[4 rg + r][j] * rhs[j][4 cg + 64 c4 ..], for a
+// thread holding rows 4 rg .. 4 rg + 3 and columns {4 cg + 64 c4 .. + 3} of a [64][D]
+// result; L row-major with pitch lp, j0 and j1 multiples of 4.
+template <int D>
+KB_HD void mm64_rows(float4 (&acc)[4][D / 64], const float* L, int lp, const float* rhs, int rp, int j0,
+                     int j1, int rg, int cg) {
+  for (int j = j0; j < j1; j += 4) {
+    float4 l[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) l[r] = ld4(L + (4 * rg + r) * lp + j);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      float4 bv[D / 64];
+#pragma unroll
+      for (int c4 = 0; c4 < D / 64; ++c4) bv[c4] = ld4(rhs + (j + jj) * rp + 4 * cg + 64 * c4);
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c4 = 0; c4 < D / 64; ++c4) fma4(acc[r][c4], comp(l[r], jj), bv[c4]);
+    }
+  }
+}
+
+// The same with L stored transposed: the left factor at (row 4 rg + r, j) is L[j][4 rg + r].
+template <int D>
+KB_HD void mm64_cols(float4 (&acc)[4][D / 64], const float* L, int lp, const float* rhs, int rp, int j0,
+                     int j1, int rg, int cg) {
   for (int j = j0; j < j1; ++j) {
+    const float4 l = ld4(L + j * lp + 4 * rg);
     float4 bv[D / 64];
 #pragma unroll
-    for (int c4 = 0; c4 < D / 64; ++c4) bv[c4] = ld4(rhs + (int64_t)j * pitch + 4 * cg + 64 * c4);
+    for (int c4 = 0; c4 < D / 64; ++c4) bv[c4] = ld4(rhs + j * rp + 4 * cg + 64 * c4);
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float x = lhs(r, j);
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int c4 = 0; c4 < D / 64; ++c4) fma4(acc[r][c4], x, bv[c4]);
-    }
+      for (int c4 = 0; c4 < D / 64; ++c4) fma4(acc[r][c4], comp(l, r), bv[c4]);
   }
 }
 
@@ -262,10 +306,15 @@ KB_HD void prep_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   const int rows = L.rows;
   const float scale = a.scale;
 
+  constexpr int NK = kC * DK / 4 / NT, NV = kC * DV / 4 / NT;  // 4-vectors per thread
   // 1. log-decays (zero past the last row) and beta; then per-channel cumulative sums
-  for (int idx = tid; idx < kC * DK; idx += NT) {
-    const int i = idx / DK, d = idx - i * DK;
-    B0[i * PM + d] = i < rows ? gb[(int64_t)i * a.g.st + d] : 0.f;
+  {
+    float4 gv[NK];
+    load_rows<DK, NT, float>(gv, gb, a.g.st, rows, tid);
+    for (int u = 0; u < NK; ++u) {
+      const int idx = tid + u * NT, i = idx / (DK / 4), p = idx - i * (DK / 4);
+      st4(B0 + i * PM + 4 * p, gv[u]);
+    }
   }
   for (int i = tid; i < kC; i += NT) sb[i] = i < rows ? bb[(int64_t)i * a.beta_st] : 0.f;
   KB_SYNC();
@@ -280,15 +329,24 @@ KB_HD void prep_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   }
   KB_SYNC();
   // 2. operands referred to the sub-block start: k e^{G - r}, k e^{r - G}, q e^{G - r}
-  for (int idx = tid; idx < kC * DK; idx += NT) {
-    const int i = idx / DK, d = idx - i * DK;
-    const float G = B0[i * PM + d], r = rr[(i / kSB) * DK + d];
-    const float kv = i < rows ? ldf<T>(kb + (int64_t)i * a.k.st + d) : 0.f;
-    const float qv = i < rows ? ldf<T>(qb + (int64_t)i * a.q.st + d) : 0.f;
-    const float lam = KB_EXP(G - r), mu = KB_EXP(r - G);
-    B1[i * PM + d] = kv * lam;
-    B2[i * PM + d] = kv * mu;
-    B3[i * PM + d] = qv * lam;
+  {
+    float4 kv[NK], qv[NK];
+    load_rows<DK, NT, T>(kv, kb, a.k.st, rows, tid);
+    load_rows<DK, NT, T>(qv, qb, a.q.st, rows, tid);
+    for (int u = 0; u < NK; ++u) {
+      const int idx = tid + u * NT, i = idx / (DK / 4), p = idx - i * (DK / 4);
+      const float4 G = ld4(B0 + i * PM + 4 * p), r = ld4(rr + (i / kSB) * DK + 4 * p);
+      float4 kl, km, ql;
+      for (int e = 0; e < 4; ++e) {
+        const float lam = KB_EXP(comp(G, e) - comp(r, e)), mu = KB_EXP(comp(r, e) - comp(G, e));
+        comp(kl, e) = comp(kv[u], e) * lam;
+        comp(km, e) = comp(kv[u], e) * mu;
+        comp(ql, e) = comp(qv[u], e) * lam;
+      }
+      st4(B1 + i * PM + 4 * p, kl);
+      st4(B2 + i * PM + 4 * p, km);
+      st4(B3 + i * PM + 4 * p, ql);
+    }
   }
   for (int idx = tid; idx < 10 * DK; idx += NT) {
     const int p = idx / DK, d = idx - p * DK;
@@ -340,15 +398,15 @@ KB_HD void prep_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   //    column per thread, then block rows 1..3 from T_IJ = -T_II sum_K L_IK T_KJ
   if (tid < kC) {
     const int base = (tid / kSB) * kSB, m = tid % kSB, col = base + m;
-    for (int ii = m; ii < kSB; ++ii) {
+    float tc[kSB];  // this column of the diagonal block, in registers
+#pragma unroll
+    for (int ii = 0; ii < kSB; ++ii) {
       const int i = base + ii;
-      if (ii == m) {
-        sT[i * PA + col] = 1.f;
-      } else {
-        float s = 0.f;
-        for (int jj = m; jj < ii; ++jj) s += sA[i * PA + base + jj] * sT[(base + jj) * PA + col];
-        sT[i * PA + col] = -sb[i] * s;
-      }
+      float s = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < ii; ++jj) s += sA[i * PA + base + jj] * tc[jj];
+      tc[ii] = ii < m ? 0.f : ii == m ? 1.f : -sb[i] * s;
+      sT[i * PA + col] = tc[ii];
     }
   }
   KB_SYNC();
@@ -395,15 +453,19 @@ KB_HD void prep_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   {
     float4 acc[4][DK / 64];
     zero_acc<DK>(acc);
-    mm64<DK>(acc, [&](int r, int j) { return sT[(4 * rg + r) * PA + j]; }, B3, PM, 0, 4 * rg + 4, cg);
+    mm64_rows<DK>(acc, sT, PA, B3, PM, 0, 4 * rg + 4, rg, cg);
     store64<DK>(rec + R::W, DK, acc, rg, cg);
     zero_acc<DK>(acc);
-    mm64<DK>(acc, [&](int r, int j) { return sT[j * PA + 4 * rg + r]; }, B2, PM, 4 * rg, kC, cg);
+    mm64_cols<DK>(acc, sT, PA, B2, PM, 4 * rg, kC, rg, cg);
     store64<DK>(rec + R::WY, DK, acc, rg, cg);
   }
-  for (int idx = tid; idx < kC * DV; idx += NT) {
-    const int i = idx / DV, c = idx - i * DV;
-    B1[i * PM + c] = i < rows ? ldf<T>(ob + (int64_t)i * ba.dout.st + c) : 0.f;
+  {
+    float4 ov[NV];
+    load_rows<DV, NT, T>(ov, ob, ba.dout.st, rows, tid);
+    for (int u = 0; u < NV; ++u) {
+      const int idx = tid + u * NT, i = idx / (DV / 4), p = idx - i * (DV / 4);
+      st4(B1 + i * PM + 4 * p, ov[u]);
+    }
   }
   KB_SYNC();
   // 7. Z_q = (scale Q+)^T dO; V_t = scale A_Q^T dO into B2; diag(beta) V into B3
@@ -430,7 +492,7 @@ KB_HD void prep_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   {
     float4 acc[4][DV / 64];
     zero_acc<DV>(acc);
-    mm64<DV>(acc, [&](int r, int j) { return sAQ[j * PA + 4 * rg + r]; }, B1, PM, 4 * rg, kC, cg);
+    mm64_cols<DV>(acc, sAQ, PA, B1, PM, 4 * rg, kC, rg, cg);
     for (int r = 0; r < 4; ++r)
       for (int c4 = 0; c4 < DV / 64; ++c4) {
         float4 x = acc[r][c4];
@@ -441,28 +503,40 @@ KB_HD void prep_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
         st4(B2 + (4 * rg + r) * PM + 4 * cg + 64 * c4, x);
       }
   }
-  for (int idx = tid; idx < kC * DV; idx += NT) {
-    const int i = idx / DV, c = idx - i * DV;
-    B3[i * PM + c] = i < rows ? sb[i] * ldf<T>(vb + (int64_t)i * a.v.st + c) : 0.f;
+  {
+    float4 vv[NV];
+    load_rows<DV, NT, T>(vv, vb, a.v.st, rows, tid);
+    for (int u = 0; u < NV; ++u) {
+      const int idx = tid + u * NT, i = idx / (DV / 4), p = idx - i * (DV / 4);
+      const float be = sb[i];
+      float4 x = vv[u];
+      x.x *= be;
+      x.y *= be;
+      x.z *= be;
+      x.w *= be;
+      st4(B3 + i * PM + 4 * p, x);
+    }
   }
   KB_SYNC();
   // 8. V_y = T^T V_t, U_bar = T diag(beta) V
   {
     float4 acc[4][DV / 64];
     zero_acc<DV>(acc);
-    mm64<DV>(acc, [&](int r, int j) { return sT[j * PA + 4 * rg + r]; }, B2, PM, 4 * rg, kC, cg);
+    mm64_cols<DV>(acc, sT, PA, B2, PM, 4 * rg, kC, rg, cg);
     store64<DV>(rec + R::VY, DV, acc, rg, cg);
     zero_acc<DV>(acc);
-    mm64<DV>(acc, [&](int r, int j) { return sT[(4 * rg + r) * PA + j]; }, B3, PM, 0, 4 * rg + 4, cg);
+    mm64_rows<DV>(acc, sT, PA, B3, PM, 0, 4 * rg + 4, rg, cg);
     store64<DV>(rec + R::UB, DV, acc, rg, cg);
   }
 }
 
 
 // ---------------------------------------------------------------------------
-// forward and reverse state passes: one CTA of 128 threads per (sequence, head,
+// forward and reverse state passes: one CTA of 256 threads per (sequence, head,
 // 32 value columns); the next chunk's record slice is copied in while the
 // current one is used
+constexpr int kPassThreads = 256;
+
 template <int DK>
 struct PassSmem {
   static constexpr int PK = DK + 4, PW = kW + 4;
@@ -472,13 +546,14 @@ struct PassSmem {
   static constexpr int BUF = E0 + DK;
   static constexpr int ST = 2 * BUF;      // [DK][32] state (or state gradient) slice
   static constexpr int Y = ST + DK * PW;  // [64][32] U (forward) or dY (reverse)
-  static constexpr int FLOATS = Y + kC * PW;
+  static constexpr int P = Y + kC * PW;   // [64][32] second half of the contraction over d_k
+  static constexpr int FLOATS = P + kC * PW;
   static constexpr int BYTES = FLOATS * 4;
 };
 
 template <int DK, int DV>
 KB_HD void pass_load(float* buf, const float* rec, int col0, bool reverse, int tid) {
-  constexpr int NT = 128;
+  constexpr int NT = kPassThreads;
   using P = PassSmem<DK>;
   using R = Rec<DK, DV>;
   const float* m0 = rec + (reverse ? R::WY : R::W);
@@ -505,7 +580,7 @@ KB_HD void pass_load(float* buf, const float* rec, int col0, bool reverse, int t
 // chunk (chunks in reverse), dv = diag(beta) dY and the initial-state gradient.
 template <int DK, int DV, typename T, bool reverse>
 KB_HD void pass_body(const ChunkBwdArgs& ca, float* sm, int blk, int tid) {
-  constexpr int NT = 128;
+  constexpr int NT = kPassThreads;
   using P = PassSmem<DK>;
   using R = Rec<DK, DV>;
   constexpr int PK = P::PK, PW = P::PW;
@@ -521,6 +596,7 @@ KB_HD void pass_body(const ChunkBwdArgs& ca, float* sm, int blk, int tid) {
   const int nc = num_chunks(ca, n), f0 = first_chunk(ca, n);
   float* sS = sm + P::ST;
   float* sY = sm + P::Y;
+  float* sP = sm + P::P;
   // starting state: S_0 (forward) or the final-state gradient (reverse); zero if absent
   const float* init = reverse ? (ba.dsT ? ba.dsT + n * ba.dsT_sn + h * ba.dsT_sh : nullptr)
                               : (a.s0 ? a.s0 + n * a.s0_sn + h * a.s0_sh : nullptr);
@@ -532,7 +608,9 @@ KB_HD void pass_body(const ChunkBwdArgs& ca, float* sm, int blk, int tid) {
   auto stp = [&](int c) { return ca.st + ((int64_t)(f0 + c) * a.H + h) * R::SSIZE; };
   if (nc > 0) pass_load<DK, DV>(sm, recp(reverse ? nc - 1 : 0), col0, reverse, tid);
   cp_commit();
-  const int rg = tid / 8, cg = tid % 8;  // [64][32] tiles: rows 4 rg.., columns 4 cg..
+  // first product: [64][32] tiles of 4 x 4 (rows 4 rg.., columns 4 cg..), each half
+  // of the CTA over one half of d_k
+  const int half = tid / 128, t = tid % 128, rg = t / 8, cg = t % 8;
   for (int k = 0; k < nc; ++k) {
     const int c = reverse ? nc - 1 - k : k;
     float* buf = sm + (k & 1) * P::BUF;
@@ -546,68 +624,71 @@ KB_HD void pass_body(const ChunkBwdArgs& ca, float* sm, int blk, int tid) {
       const int d = idx / (kW / 4), p = idx - d * (kW / 4);
       st4(st + (reverse ? R::X : R::S) + (int64_t)d * DV + col0 + 4 * p, ld4(sS + d * PW + 4 * p));
     }
-    // Y = V0 -/+ M0 S  (forward: U = U_bar - W S; reverse: dY = V_y + W_y X)
+    // M0 S over this half of d_k: into sY (first half) or sP (second half)
     {
       float4 acc[4];
       for (int r = 0; r < 4; ++r) acc[r] = zero4();
-      for (int d = 0; d < DK; d += 4) {
+      const int d0 = half * (DK / 2);
+      for (int d = d0; d < d0 + DK / 2; d += 4) {
         float4 s4[4];
         for (int e = 0; e < 4; ++e) s4[e] = ld4(sS + (d + e) * PW + 4 * cg);
         for (int r = 0; r < 4; ++r) {
-          float4 m = ld4(buf + P::M0 + (4 * rg + r) * PK + d);
+          const float4 m = ld4(buf + P::M0 + (4 * rg + r) * PK + d);
           for (int e = 0; e < 4; ++e) fma4(acc[r], comp(m, e), s4[e]);
         }
       }
-      for (int r = 0; r < 4; ++r) {
-        const int i = 4 * rg + r;
-        const float4 v0 = ld4(buf + P::V0 + i * PW + 4 * cg);
-        float4 y;
-        const float sg = reverse ? 1.f : -1.f;
-        y.x = v0.x + sg * acc[r].x;
-        y.y = v0.y + sg * acc[r].y;
-        y.z = v0.z + sg * acc[r].z;
-        y.w = v0.w + sg * acc[r].w;
-        st4(sY + i * PW + 4 * cg, y);
-        st4(st + (reverse ? R::DY : R::U) + (int64_t)i * DV + col0 + 4 * cg, y);
-        if (reverse && i < len - c * kC) {  // dv = beta dY on valid rows
-          const int64_t t = t0 + (int64_t)c * kC + i;
-          const float be = a.beta[b * a.beta_sb + t * a.beta_st + (int64_t)h * a.beta_sh];
-          float4 dv;
-          dv.x = be * y.x;
-          dv.y = be * y.y;
-          dv.z = be * y.z;
-          dv.w = be * y.w;
-          st4(ba.dv.ptr + b * ba.dv.sb + t * ba.dv.st + (int64_t)h * ba.dv.sh + col0 + 4 * cg, dv);
-        }
+      float* dst = half ? sP : sY;
+      for (int r = 0; r < 4; ++r) st4(dst + (4 * rg + r) * PW + 4 * cg, acc[r]);
+    }
+    KB_SYNC();
+    // Y = V0 -/+ M0 S  (forward: U = U_bar - W S; reverse: dY = V_y + W_y X)
+    for (int idx = tid; idx < kC * kW / 4; idx += NT) {
+      const int i = idx / (kW / 4), p = idx - i * (kW / 4);
+      const float4 v0 = ld4(buf + P::V0 + i * PW + 4 * p), p0 = ld4(sY + i * PW + 4 * p),
+                   p1 = ld4(sP + i * PW + 4 * p);
+      const float sg = reverse ? 1.f : -1.f;
+      float4 y;
+      y.x = v0.x + sg * (p0.x + p1.x);
+      y.y = v0.y + sg * (p0.y + p1.y);
+      y.z = v0.z + sg * (p0.z + p1.z);
+      y.w = v0.w + sg * (p0.w + p1.w);
+      st4(sY + i * PW + 4 * p, y);
+      st4(st + (reverse ? R::DY : R::U) + (int64_t)i * DV + col0 + 4 * p, y);
+      if (reverse && i < len - c * kC) {  // dv = beta dY on valid rows
+        const int64_t tok = t0 + (int64_t)c * kC + i;
+        const float be = a.beta[b * a.beta_sb + tok * a.beta_st + (int64_t)h * a.beta_sh];
+        float4 dv;
+        dv.x = be * y.x;
+        dv.y = be * y.y;
+        dv.z = be * y.z;
+        dv.w = be * y.w;
+        st4(ba.dv.ptr + b * ba.dv.sb + tok * ba.dv.st + (int64_t)h * ba.dv.sh + col0 + 4 * p, dv);
       }
     }
     KB_SYNC();
-    // state step: S <- e^{G_C} S + K_end^T U, or X <- e^{G_C} X + Z_q - (diag(beta) K+)^T dY
-    {
-      constexpr int R4 = DK / 64;
-      float4 acc[R4][4];
-      for (int r4 = 0; r4 < R4; ++r4)
-        for (int e = 0; e < 4; ++e) acc[r4][e] = zero4();
+    // state step on [DK][32] tiles of 4 x 4 (rows 4 dg.., columns 4 vg..):
+    // S <- e^{G_C} S + K_end^T U, or X <- e^{G_C} X + Z_q - (diag(beta) K+)^T dY
+    if (tid < 2 * DK) {
+      const int dg = tid / 8, vg = tid % 8;
+      float4 acc[4];
+      for (int e = 0; e < 4; ++e) acc[e] = zero4();
       for (int i = 0; i < kC; ++i) {
-        const float4 y = ld4(sY + i * PW + 4 * cg);
-        for (int r4 = 0; r4 < R4; ++r4) {
-          float4 m = ld4(buf + P::M1 + i * PK + 4 * rg + 64 * r4);
-          for (int e = 0; e < 4; ++e) fma4(acc[r4][e], comp(m, e), y);
-        }
+        const float4 y = ld4(sY + i * PW + 4 * vg);
+        const float4 m = ld4(buf + P::M1 + i * PK + 4 * dg);
+        for (int e = 0; e < 4; ++e) fma4(acc[e], comp(m, e), y);
       }
-      for (int r4 = 0; r4 < R4; ++r4)
-        for (int e = 0; e < 4; ++e) {
-          const int d = 4 * rg + 64 * r4 + e;
-          const float eg = buf[P::E0 + d];
-          float4 s = ld4(sS + d * PW + 4 * cg);
-          float4 z = reverse ? ld4(buf + P::Z0 + d * PW + 4 * cg) : zero4();
-          const float sg = reverse ? -1.f : 1.f;
-          s.x = eg * s.x + z.x + sg * acc[r4][e].x;
-          s.y = eg * s.y + z.y + sg * acc[r4][e].y;
-          s.z = eg * s.z + z.z + sg * acc[r4][e].z;
-          s.w = eg * s.w + z.w + sg * acc[r4][e].w;
-          st4(sS + d * PW + 4 * cg, s);
-        }
+      for (int e = 0; e < 4; ++e) {
+        const int d = 4 * dg + e;
+        const float eg = buf[P::E0 + d];
+        float4 sv = ld4(sS + d * PW + 4 * vg);
+        const float4 z = reverse ? ld4(buf + P::Z0 + d * PW + 4 * vg) : zero4();
+        const float sg = reverse ? -1.f : 1.f;
+        sv.x = eg * sv.x + z.x + sg * acc[e].x;
+        sv.y = eg * sv.y + z.y + sg * acc[e].y;
+        sv.z = eg * sv.z + z.z + sg * acc[e].z;
+        sv.w = eg * sv.w + z.w + sg * acc[e].w;
+        st4(sS + d * PW + 4 * vg, sv);
+      }
     }
   }
   cp_wait_all();
@@ -681,13 +762,25 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   float* sb = sm + SM::BETA;
   const int rows = L.rows;
   const float scale = a.scale;
-  auto kval = [&](int i, int d) { return i < rows ? ldf<T>(kb + (int64_t)i * a.k.st + d) : 0.f; };
-  auto qval = [&](int i, int d) { return i < rows ? ldf<T>(qb + (int64_t)i * a.q.st + d) : 0.f; };
+  constexpr int NK = kC * DK / 4 / NT;  // 4-vectors of a [64][DK] tile per thread
+  const int rg = tid / 16, cg = tid % 16;
+  // this thread's [4][DK / 64] 4-vectors (rows 4 rg.., columns 4 cg + 64 c4 ..) of k or q
+  auto own = [&](float4 (&x)[4][C4], const T* base, int64_t st) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c4 = 0; c4 < C4; ++c4)
+        x[r][c4] = 4 * rg + r < rows ? ld4t<T>(base + (int64_t)(4 * rg + r) * st + 4 * cg + 64 * c4) : zero4();
+  };
 
   // 1. log-decays, beta, A; cumulative sums and the sub-block references
-  for (int idx = tid; idx < kC * DK; idx += NT) {
-    const int i = idx / DK, d = idx - i * DK;
-    sG[i * PK + d] = i < rows ? gb[(int64_t)i * a.g.st + d] : 0.f;
+  {
+    float4 gv[NK];
+    load_rows<DK, NT, float>(gv, gb, a.g.st, rows, tid);
+    for (int u = 0; u < NK; ++u) {
+      const int idx = tid + u * NT, i = idx / (DK / 4), p = idx - i * (DK / 4);
+      st4(sG + i * PK + 4 * p, gv[u]);
+    }
   }
   for (int i = tid; i < kC; i += NT) sb[i] = i < rows ? bb[(int64_t)i * a.beta_st] : 0.f;
   for (int idx = tid; idx < kC * kC; idx += NT) {
@@ -706,12 +799,18 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   }
   KB_SYNC();
   // 2. K+ = k e^G
-  for (int idx = tid; idx < kC * DK; idx += NT) {
-    const int i = idx / DK, d = idx - i * DK;
-    sOp[i * PK + d] = kval(i, d) * KB_EXP(sG[i * PK + d]);
+  {
+    float4 kv[NK];
+    load_rows<DK, NT, T>(kv, kb, a.k.st, rows, tid);
+    for (int u = 0; u < NK; ++u) {
+      const int idx = tid + u * NT, i = idx / (DK / 4), p = idx - i * (DK / 4);
+      const float4 G = ld4(sG + i * PK + 4 * p);
+      float4 x;
+      for (int e = 0; e < 4; ++e) comp(x, e) = comp(kv[u], e) * KB_EXP(comp(G, e));
+      st4(sOp + i * PK + 4 * p, x);
+    }
   }
 
-  const int rg = tid / 16, cg = tid % 16;
   float4 Pq[4][C4], Pk[4][C4], Pe[4][C4];  // dO S^T, dY S^T, U X^T
   float4 QA[4], YA[4];                     // dO U^T, dY U^T at columns 4 cg ..
   float dbp[4] = {0.f, 0.f, 0.f, 0.f};
@@ -729,17 +828,39 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   for (int s = 0; s < DV / kW; ++s) {
     const int col0 = s * kW;
     // 3. this slice's columns, transposed: S, X [DK][32] -> [32][DK]; U, dY, dO, V [64][32] -> [32][64]
-    for (int idx = tid; idx < DK * kW; idx += NT) {
-      const int d = idx / kW, v = idx - d * kW;
-      sST[v * PK + d] = stt[R::S + (int64_t)d * DV + col0 + v];
-      sXT[v * PK + d] = stt[R::X + (int64_t)d * DV + col0 + v];
-    }
-    for (int idx = tid; idx < kC * kW; idx += NT) {
-      const int i = idx / kW, v = idx - i * kW;
-      sUT[v * PA + i] = stt[R::U + (int64_t)i * DV + col0 + v];
-      sYT[v * PA + i] = stt[R::DY + (int64_t)i * DV + col0 + v];
-      sOT[v * PA + i] = i < rows ? ldf<T>(ob + (int64_t)i * ba.dout.st + col0 + v) : 0.f;
-      sVT[v * PA + i] = i < rows ? ldf<T>(vb + (int64_t)i * a.v.st + col0 + v) : 0.f;
+    {
+      constexpr int NS = DK * kW / 4 / NT, NR = kC * kW / 4 / NT;
+      float4 sv[NS], xv[NS], uv[NR], yv[NR], ov[NR], vv[NR];
+#pragma unroll
+      for (int u = 0; u < NS; ++u) {
+        const int idx = tid + u * NT, d = idx / (kW / 4), p = idx - d * (kW / 4);
+        sv[u] = ld4(stt + R::S + (int64_t)d * DV + col0 + 4 * p);
+        xv[u] = ld4(stt + R::X + (int64_t)d * DV + col0 + 4 * p);
+      }
+#pragma unroll
+      for (int u = 0; u < NR; ++u) {
+        const int idx = tid + u * NT, i = idx / (kW / 4), p = idx - i * (kW / 4);
+        uv[u] = ld4(stt + R::U + (int64_t)i * DV + col0 + 4 * p);
+        yv[u] = ld4(stt + R::DY + (int64_t)i * DV + col0 + 4 * p);
+        ov[u] = i < rows ? ld4t<T>(ob + (int64_t)i * ba.dout.st + col0 + 4 * p) : zero4();
+        vv[u] = i < rows ? ld4t<T>(vb + (int64_t)i * a.v.st + col0 + 4 * p) : zero4();
+      }
+      for (int u = 0; u < NS; ++u) {
+        const int idx = tid + u * NT, d = idx / (kW / 4), p = idx - d * (kW / 4);
+        for (int e = 0; e < 4; ++e) {
+          sST[(4 * p + e) * PK + d] = comp(sv[u], e);
+          sXT[(4 * p + e) * PK + d] = comp(xv[u], e);
+        }
+      }
+      for (int u = 0; u < NR; ++u) {
+        const int idx = tid + u * NT, i = idx / (kW / 4), p = idx - i * (kW / 4);
+        for (int e = 0; e < 4; ++e) {
+          sUT[(4 * p + e) * PA + i] = comp(uv[u], e);
+          sYT[(4 * p + e) * PA + i] = comp(yv[u], e);
+          sOT[(4 * p + e) * PA + i] = comp(ov[u], e);
+          sVT[(4 * p + e) * PA + i] = comp(vv[u], e);
+        }
+      }
     }
     KB_SYNC();
     // 4. dbeta partials: dY (V - K+ S - A U) at rows 4 rg.., columns cg and cg + 16
@@ -808,6 +929,8 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   }
   for (int d = tid; d < DK; d += NT) sm[SM::GS + d] = gsum;
   // after this block: Pq = dq, Pk = dk, Pe = (a - e) (the dG coefficient of k)
+  float4 kown[4][C4];
+  own(kown, kb, a.k.st);
   for (int c4 = 0; c4 < C4; ++c4)
     for (int e = 0; e < 4; ++e) {
       const int d = 4 * cg + 64 * c4 + e;
@@ -822,15 +945,25 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
         comp(Pq[r][c4], e) = dq;
         comp(Pk[r][c4], e) = av + ev;
         comp(Pe[r][c4], e) = av - ev;
-        eks += ev * kval(i, d);
+        eks += ev * comp(kown[r][c4], e);
       }
       ek[rg * DK + d] = eks;
     }
-  for (int idx = tid; idx < kC * DK; idx += NT) {
-    const int i = idx / DK, d = idx - i * DK, I = i / kSB;
-    const float G = sG[i * PK + d], kv = kval(i, d);
-    sOp[i * PK + d] = kv * KB_EXP(rr[I * DK + d] - G);
-    sOp2[i * PK + d] = kv * KB_EXP(G - rr[(I + 1) * DK + d]);
+  {
+    float4 kv[NK];
+    load_rows<DK, NT, T>(kv, kb, a.k.st, rows, tid);
+    for (int u = 0; u < NK; ++u) {
+      const int idx = tid + u * NT, i = idx / (DK / 4), p = idx - i * (DK / 4), I = i / kSB;
+      const float4 G = ld4(sG + i * PK + 4 * p);
+      const float4 r0 = ld4(rr + I * DK + 4 * p), r1 = ld4(rr + (I + 1) * DK + 4 * p);
+      float4 x, y;
+      for (int e = 0; e < 4; ++e) {
+        comp(x, e) = comp(kv[u], e) * KB_EXP(comp(r0, e) - comp(G, e));
+        comp(y, e) = comp(kv[u], e) * KB_EXP(comp(G, e) - comp(r1, e));
+      }
+      st4(sOp + i * PK + 4 * p, x);
+      st4(sOp2 + i * PK + 4 * p, y);
+    }
   }
   KB_SYNC();
   // 7. row form: sum_{j in J} M_ij (k_j e^{r_J - G_j}), times e^{G_i - r_J}
@@ -840,7 +973,7 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
     for (int J = 0; J <= Ib; ++J) {
       float4 t[4][C4];
       zero_acc<DK>(t);
-      mm64<DK>(t, [&](int r, int j) { return M[(4 * rg + r) * PA + j]; }, sOp, PK, kSB * J, kSB * J + kSB, cg);
+      mm64_rows<DK>(t, M, PA, sOp, PK, kSB * J, kSB * J + kSB, rg, cg);
       for (int r = 0; r < 4; ++r)
         for (int c4 = 0; c4 < C4; ++c4)
           for (int e = 0; e < 4; ++e) {
@@ -856,17 +989,24 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
     }
   }
   KB_SYNC();
-  for (int idx = tid; idx < kC * DK; idx += NT) {
-    const int i = idx / DK, d = idx - i * DK;
-    sOp[i * PK + d] = qval(i, d) * KB_EXP(sG[i * PK + d] - rr[(i / kSB + 1) * DK + d]);
+  {
+    float4 qv[NK];
+    load_rows<DK, NT, T>(qv, qb, a.q.st, rows, tid);
+    for (int u = 0; u < NK; ++u) {
+      const int idx = tid + u * NT, i = idx / (DK / 4), p = idx - i * (DK / 4);
+      const float4 G = ld4(sG + i * PK + 4 * p), r1 = ld4(rr + (i / kSB + 1) * DK + 4 * p);
+      float4 x;
+      for (int e = 0; e < 4; ++e) comp(x, e) = comp(qv[u], e) * KB_EXP(comp(G, e) - comp(r1, e));
+      st4(sOp + i * PK + 4 * p, x);
+    }
   }
   KB_SYNC();
   // 8. column form at rows j: sum_{i in I} (M1_ij q_i + M2_ij k_i) e^{G_i - c_I}, times e^{c_I - G_j}
   for (int I = Ib; I < 4; ++I) {
     float4 t[4][C4];
     zero_acc<DK>(t);
-    mm64<DK>(t, [&](int r, int i) { return sM1[i * PA + 4 * rg + r]; }, sOp, PK, kSB * I, kSB * I + kSB, cg);
-    mm64<DK>(t, [&](int r, int i) { return sM2[i * PA + 4 * rg + r]; }, sOp2, PK, kSB * I, kSB * I + kSB, cg);
+    mm64_cols<DK>(t, sM1, PA, sOp, PK, kSB * I, kSB * I + kSB, rg, cg);
+    mm64_cols<DK>(t, sM2, PA, sOp2, PK, kSB * I, kSB * I + kSB, rg, cg);
     for (int r = 0; r < 4; ++r)
       for (int c4 = 0; c4 < C4; ++c4)
         for (int e = 0; e < 4; ++e) {
@@ -878,14 +1018,15 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   }
   KB_SYNC();
   // 9. dq, dk out; dG = (a - b - e) k + dq q into sOp
+  float4 qown[4][C4];
+  own(kown, kb, a.k.st);
+  own(qown, qb, a.q.st);
   for (int r = 0; r < 4; ++r) {
     const int i = 4 * rg + r;
     for (int c4 = 0; c4 < C4; ++c4) {
       float4 dg4;
-      for (int e = 0; e < 4; ++e) {
-        const int d = 4 * cg + 64 * c4 + e;
-        comp(dg4, e) = comp(Pe[r][c4], e) * kval(i, d) + comp(Pq[r][c4], e) * qval(i, d);
-      }
+      for (int e = 0; e < 4; ++e)
+        comp(dg4, e) = comp(Pe[r][c4], e) * comp(kown[r][c4], e) + comp(Pq[r][c4], e) * comp(qown[r][c4], e);
       st4(sOp + i * PK + 4 * cg + 64 * c4, dg4);
       if (i < rows) {
         const int64_t t = L.t + i;
