@@ -534,6 +534,33 @@ def bench_decode_fused(kda, steps_total, warmup, stream, clk=None):
 
 CHUNK_BWD_KERNELS = ["kda_bwd_prep_kernel", "kda_bwd_state_fwd_kernel", "kda_bwd_state_rev_kernel",
                      "kda_bwd_grad_kernel"]
+# FP32 FMA peak of the CUDA cores: 128 FMA per SM per clock at the 2070 MHz maximum SM
+# clock, times the SM count (the chunked backward runs fp32 arithmetic there)
+FP32_FMA_PER_SM_CLK = 128
+SM_MAX_MHZ = 2070.0
+
+
+def chunk_bwd_fmas(dk, dv):
+    """Executed FMAs per (64-token chunk, head) of each chunked-backward kernel,
+    counted from its loop bounds."""
+    return {"kda_bwd_prep_kernel": 8704 * dk + 6528 * dv + 64 * dk * dv,
+            "kda_bwd_state_fwd_kernel": 128 * dk * dv,
+            "kda_bwd_state_rev_kernel": 128 * dk * dv,
+            "kda_bwd_grad_kernel": (dv // 32) * (8224 * dk + 331776) + 10240 * dk}
+
+
+def chunk_bwd_roofline(bw, ms, kernel_ms, sms):
+    """``roofline`` of the chunked backward: bound "alu" (fp32 FMA), dominant kernel
+    kda_bwd_grad_kernel, plus the whole call's rate."""
+    peak = sms * FP32_FMA_PER_SM_CLK * 2 * SM_MAX_MHZ * 1e6 / 1e12
+    fl = {n: 2.0 * f * bw["chunk_heads"] for n, f in chunk_bwd_fmas(bw["dk"], bw["dv"]).items()}
+    k = "kda_bwd_grad_kernel"
+    achieved = fl[k] / (kernel_ms[k] * 1e-3) / 1e12
+    call = sum(fl.values()) / (ms * 1e-3) / 1e12
+    return {"bound": "alu", "kernel": k, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": None, "peak_source": "derived (SMs x 128 FMA x 2 x 2070 MHz)",
+            "flops_per_launch": fl[k], "call_tflops": call, "call_frac": call / peak,
+            "kernel_tflops": {n: fl[n] / (kernel_ms[n] * 1e-3) / 1e12 for n in fl}}
 
 
 def bench_backward(kda, steps, warmup, stream, entry="kda_chunk_bwd", names=None):
@@ -591,8 +618,8 @@ def bench_backward(kda, steps, warmup, stream, entry="kda_chunk_bwd", names=None
     # inputs (q, k, v, d_out bf16; g fp32; beta) and fp32 gradients, plus the states
     per = 2 * (2 * dk + 2 * dv) + 4 * dk + 4 + 4 * (3 * dk + dv) + 4
     nbytes = th * per + 4 * dk * dv * B * H * 4
-    return dict(ms=ms, tokens=B * T, bytes=nbytes, launches=launches, kernel_ms=kernel_ms,
-                name=ki.WORKLOADS[PREFILL_W]["name"])
+    return dict(ms=ms, tokens=B * T, bytes=nbytes, launches=launches, kernel_ms=kernel_ms, dk=dk, dv=dv,
+                chunk_heads=B * H * ((T + 63) // 64), name=ki.WORKLOADS[PREFILL_W]["name"])
 
 
 ORACLE_MIN_CPU_S = 12.0  # CPU-seconds (wall x threads) of oracle work behind each rate
@@ -805,6 +832,8 @@ def main():
         "kernel_ms": {n: max_over_ranks(v, world) for n, v in bw["kernel_ms"].items()},
         "tokens_per_s": world * bw["tokens"] / (bms * 1e-3),
         "hbm_frac": bw["bytes"] / (bms * 1e-3) / 1e9 / pk["hbm"], "gpu_launches": bw["launches"]}
+    extra["backward"]["roofline"] = chunk_bwd_roofline(
+        bw, bms, extra["backward"]["kernel_ms"], torch.cuda.get_device_properties(local).multi_processor_count)
     bw = bench_backward(kda, 3, 3, stream, "kda_backward")
     bms = max_over_ranks(bw["ms"], world)
     extra["backward_token_loop"] = {
