@@ -620,6 +620,10 @@ kda_status backward_impl(bool chunked, const kda_tensor* q, const kda_tensor* k,
     N = cu->shape[0] - 1;
   }
   if (N * H > INT32_MAX / 8) return fail(KDA_ERR_UNSUPPORTED, "too many (sequence, head) pairs");
+  if (chunked) {  // chunk indices are int in the chunked kernels
+    const int64_t nck = (T + 63) / 64;
+    if ((cu ? nck + N : nck * N) > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "too many 64-token chunks");
+  }
   if (initial_state) KDA_TRY(check_state(initial_state, "initial_state", N, H, dk_, dv_));
   if (d_final_state) KDA_TRY(check_state(d_final_state, "d_final_state", N, H, dk_, dv_));
   if (d_initial_state) KDA_TRY(check_state(d_initial_state, "d_initial_state", N, H, dk_, dv_));

@@ -76,9 +76,10 @@ __global__ void __launch_bounds__(1024) kda_bwd_offsets_kernel(PrefillArgs a, in
   }
 }
 
-int chunk_total(const PrefillArgs& a) {
+// chunk indices to allocate (an upper bound with varlen); may exceed INT32_MAX
+int64_t chunk_total(const PrefillArgs& a) {
   const int64_t nck = ((int64_t)a.T + kC - 1) / kC;
-  return (int)(a.cu_seqlens ? nck + a.N : nck * a.N);
+  return a.cu_seqlens ? nck + a.N : nck * a.N;
 }
 
 size_t rec_floats(int dk, int dv) {
@@ -136,7 +137,8 @@ cudaError_t run(const ChunkBwdArgs& ca, cudaStream_t s) {
 
 size_t chunk_backward_workspace_bytes(const PrefillArgs& a) {
   const size_t per = (size_t)a.H * (rec_floats(a.dk, a.dv) + st_floats(a.dk, a.dv)) * 4;
-  return off_bytes(a) + (size_t)chunk_total(a) * per;
+  const int64_t total = chunk_total(a);
+  return total > INT32_MAX ? 0 : off_bytes(a) + (size_t)total * per;
 }
 
 cudaError_t launch_chunk_backward(const BackwardArgs& ba, void* ws, cudaStream_t s) {
@@ -145,7 +147,9 @@ cudaError_t launch_chunk_backward(const BackwardArgs& ba, void* ws, cudaStream_t
   ChunkBwdArgs ca;
   ca.b = ba;
   ca.nck = (a.T + kC - 1) / kC;
-  ca.total = chunk_total(a);
+  const int64_t total = chunk_total(a);
+  if (total > INT32_MAX) return cudaErrorInvalidValue;  // chunk indices are int
+  ca.total = (int)total;
   char* base = static_cast<char*>(ws);
   ca.off = a.cu_seqlens ? reinterpret_cast<const int*>(base) : nullptr;
   ca.rec = reinterpret_cast<float*>(base + off_bytes(a));

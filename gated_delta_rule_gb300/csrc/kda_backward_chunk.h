@@ -8,8 +8,8 @@
 
 namespace kda {
 
-// Bytes of device scratch the chunked backward needs for these sizes (rows = B * T,
-// the token rows of the inputs; varlen when cu_seqlens is set).
+// Bytes of device scratch the chunked backward needs for these sizes (varlen when
+// cu_seqlens is set); 0 when the chunk count does not fit an int (unsupported).
 size_t chunk_backward_workspace_bytes(const PrefillArgs& a);
 
 // Gradients as kda_backward computes them, by the chunked form: ws holds

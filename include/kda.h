@@ -275,7 +275,8 @@ kda_status kda_backward(const kda_tensor* q, const kda_tensor* k, const kda_tens
  * Scratch comes from the stream-ordered pool: per (chunk, head)
  * (4*64*d_k + 2*64*d_v + d_k + d_k*d_v + 64*64 + 2*d_k*d_v + 2*64*d_v) * 4 bytes,
  * about 475 KB at d_k = d_v = 128, over N * ceil(T / 64) chunks (ceil(T / 64) + N
- * with cu_seqlens).
+ * with cu_seqlens).  A chunk count above 2^31 - 1 returns KDA_ERR_UNSUPPORTED
+ * before any launch; otherwise errors as for kda_backward.
  */
 kda_status kda_chunk_bwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
                          const kda_tensor* g, const kda_tensor* beta, const kda_tensor* initial_state,

@@ -207,3 +207,18 @@ def test_multi_step_requires_q_and_out_together(lib):
     st = lib.kda_recurrent_multi_step(r(S), r(q), r(k), r(v), r(g), r(beta), ctypes.c_float(1.0), None,
                                       None, None)
     assert st == 1 and b"both" in lib.kda_last_error_message()
+
+
+def test_chunk_bwd_rejects_more_chunks_than_an_int_indexes(lib):
+    """65536 sequences of 2^22 tokens are 2^32 chunks of 64: refused on the host
+    (KDA_ERR_UNSUPPORTED) before any launch."""
+    r = ctypes.byref
+    B, Tn, H, d = 1 << 16, 1 << 22, 1, 64
+    base = lambda i: (i + 1) << 46  # extents of up to 2^45 bytes never overlap
+    q, k, v, do = (T([B, Tn, H, d], 1, base(i)) for i in range(4))
+    g, dq, dk, dv, dg = (T([B, Tn, H, d], 0, base(4 + i)) for i in range(5))
+    beta, dbeta = T([B, Tn, H], 0, base(9)), T([B, Tn, H], 0, base(10))
+    st = lib.kda_chunk_bwd(r(q), r(k), r(v), r(g), r(beta), None, ctypes.c_float(0.125), None, r(do), None,
+                           r(dq), r(dk), r(dv), r(dg), r(dbeta), None, None)
+    assert st == 2, (st, lib.kda_last_error_message().decode())
+    assert "64-token chunks" in lib.kda_last_error_message().decode()
