@@ -453,8 +453,42 @@ def bench_decode(kda, steps_total, warmup, stream, clk=None):
         e1.record(stream)
         stream.synchronize()
     ms = e0.elapsed_time(e1) / steps_total
+    graph = decode_graph_timing(kda, S, ins, out, stream, reps=4)
     return dict(ms=ms, NH=N * H, N=N, H=H, dk=dk, dv=dv, bytes=decode_bytes(N * H, dk, dv),
-                name=w["name"], steps=steps_total, launches=launches)
+                name=w["name"], steps=steps_total, launches=launches, graph=graph)
+
+
+def decode_graph_timing(kda, S, ins, out, stream, reps):
+    """The decode steps of ``ins`` captured once in a CUDA graph and replayed ``reps``
+    times on ``stream``: ms per step and kernels per replay, or (ms = -1) the error
+    that stopped the capture or the replay."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        captured = 0
+        with torch.cuda.graph(g, stream=cap):
+            for x in ins:
+                kda.kda_recurrent_step(S, x["q"], x["k"], x["v"], x["g"], x["beta"], scale=x["scale"], out=out,
+                                       stream=cap)
+                captured += kda.kda_last_launch_count()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            stream.wait_stream(cap)
+            g.replay()  # untimed first replay
+            stream.synchronize()
+            torch.cuda._sleep(SLEEP_CYCLES)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            stream.synchronize()
+        kda.kda_get_device_error(stream)
+        return dict(ms=e0.elapsed_time(e1) / (reps * len(ins)), launches_per_replay=captured, replays=reps,
+                    steps_per_replay=len(ins), error=None)
+    except Exception as e:  # reported in the JSON line; the eager numbers stand
+        return dict(ms=-1.0, launches_per_replay=0, replays=0, steps_per_replay=len(ins),
+                    error=f"{type(e).__name__}: {e}"[:300])
 
 
 def bench_multi_step(kda, n_tok, warmup, stream, clk=None, iters=20):
@@ -775,6 +809,12 @@ def main():
                      "traffic": committed_traffic("kda_decode_kernel"),
                      "algorithmic_bytes_per_launch": dec["bytes"]},
         "clocks": clk_dec.summary(), "gpu_launches": dec["launches"]}
+    gr = dec["graph"]
+    g_ms = max_over_ranks(gr["ms"], world)  # -1 when the capture failed on every rank
+    extra["decode"]["cuda_graph"] = {
+        "ms_per_step": g_ms if g_ms > 0 else None, "steps_per_replay": gr["steps_per_replay"],
+        "replays_timed": gr["replays"], "launches_per_replay": gr["launches_per_replay"],
+        "hbm_frac": dec["bytes"] / (g_ms * 1e-3) / 1e9 / pk["hbm"] if g_ms > 0 else None, "error": gr["error"]}
     del dec
     fz = bench_decode_fused(kda, 64, args.warmup, stream)
     f_ms = max_over_ranks(fz["ms"], world)
