@@ -903,7 +903,9 @@ def main():
             "t_roof_over_t": t_roof / (ms * 1e-3),
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": e2e["h2d"],
                     "d2h_bytes_per_step": e2e["d2h"]},
-            "gpu_launches": pre["launches"], "clocks": clk.summary(), "wall_s_timed_region": wall}
+            "gpu_launches": pre["launches"], "clocks": clk.summary(), "wall_s_timed_region": wall,
+            "step_ms": {"mean": ms, "median": max_over_ranks(statistics.median(pre["ms"]), world),
+                        "best": max_over_ranks(min(pre["ms"]), world), "reps": len(pre["ms"])}}
     line.update(extra)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r, threads, sample, _ = oracle_prefill_rate(PREFILL_W)
