@@ -1,17 +1,21 @@
 """Benchmark of the KDA core on one GB300 (or N replicas under torchrun).
 
-One step = one ``kda_chunk_fwd`` prefill of the workload B=2, H=16, T=4096,
-d_k=d_v=128 (bf16 q/k/v, fp32 g/beta/states, random initial state): the
-headline prefill tokens/s.  The same JSON line also carries the decode half
-of the metric (256 requests x 96 heads x 128 x 128, fp32 state in place, 64
-consecutive ``kda_recurrent_step`` calls) and the 96-head, 32768-token prefill.
+One step = one ``kda_chunk_fwd`` prefill of the largest workload that fits one
+GPU: 1,048,576 tokens packed as 16 sequences (lengths log-uniform in [1024,
+262144]), H=8, d_k=d_v=128, bf16 q/k/v, fp32 g/beta, a random fp32 initial
+state per sequence and the final states returned: the headline prefill
+tokens/s.  The same JSON line also carries the B=2, H=16, T=4096 prefill, the
+96-head 32768-token prefill, the decode half of the metric (256 requests x 96
+heads x 128 x 128, fp32 state in place, 64 consecutive ``kda_recurrent_step``
+calls) and the other entry points.
 
 Timing: inputs are resident in HBM; every timed step is bracketed by CUDA
 events on the launching stream, and L2 is flushed (a 256 MiB write, outside
-the events) between prefill steps.  ``e2e`` repeats the prefill through the
-C ABI with the inputs in pinned host memory: host->device copies, the call
-and the device->host copy of out and the final state are inside the timed
-region.  ``--impl reference`` times the CPU oracle instead.
+the events) between prefill steps (the headline's inputs, 12.9 GB, are larger
+than L2 anyway).  ``e2e`` repeats the headline prefill through the C ABI with
+the inputs in pinned host memory: host->device copies, the call and the
+device->host copy of out and the final states are inside the timed region.
+``--impl reference`` times the CPU oracle instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -38,9 +42,9 @@ import torch  # noqa: E402
 import kda_inputs as ki  # noqa: E402
 
 METRIC = "KDA prefill tokens/s & % bf16 TC roofline; decode steps/s & % HBM BW (1×GB300)"
-PREFILL_W = 1          # headline prefill workload
+HEADLINE_W = 4         # 1M-token varlen prefill (16 sequences): the headline
+PREFILL_W = 1          # B=2 H16 T4096 prefill, reported alongside (and the backward's workload)
 K3_W = 2               # 96-head prefill, reported alongside
-VARLEN_W = 4           # 1M-token varlen prefill (16 sequences), reported alongside
 DECODE_W = 3
 L2_FLUSH_BYTES = 256 << 20
 SLEEP_CYCLES = 200_000  # about 0.1 ms at 2 GHz, spent before each timed step
@@ -57,7 +61,9 @@ def peaks():
 
 
 # ---------------------------------------------------------------------------
-# algorithmic work (per token-head, d = head dim): see the design doc
+# algorithmic work per token-head (d = head dim): FLOPs 6 d_k d_v + 2 C (d_k + d_v);
+# bytes of q, k, v, out (input dtype), g and beta (fp32), plus each state read or
+# written
 
 def prefill_flops(token_heads, dk, dv, C=64):
     return token_heads * (6 * dk * dv + 2 * C * (dk + dv))
@@ -246,6 +252,14 @@ def whole_job_rate(units_per_rank, ms_slowest, world):
     return units_per_rank * world / (ms_slowest * 1e-3)
 
 
+def graph_ms_over_ranks(ms, world):
+    """Job-wide CUDA-graph step time from each rank's ``ms`` (-1 where that rank's
+    capture or replay failed): (None, True) if any rank failed, else (the slowest
+    rank's ms, False)."""
+    failed = max_over_ranks(1.0 if ms <= 0 else 0.0, world) > 0
+    return (None, True) if failed else (max_over_ranks(ms, world), False)
+
+
 def max_over_ranks(x, world):
     if world == 1:
         return x
@@ -373,8 +387,12 @@ def bench_prefill(kda, idx, steps, warmup, flush, stream, clk=None, world=1, gat
 
 
 def kernel_roofline(r, pk, world):
-    """Roofline of the kernel that takes the most device time per step."""
+    """Roofline of the kernel that takes the most device time per step (the serial
+    kernel's time counts both of its passes when sequences are segment-split: its
+    algorithmic bytes are moved over the two)."""
     timed = {n: ms for n, ms in r["kernel_ms"].items() if n in r["kernel_bytes"]}
+    if "kda_chunk_serial_kernel_pass1" in r["kernel_ms"]:
+        timed["kda_chunk_serial_kernel"] += r["kernel_ms"]["kda_chunk_serial_kernel_pass1"]
     name = max(timed, key=timed.get)
     ms = max_over_ranks(timed[name], world)
     gbs = r["kernel_bytes"][name] / (ms * 1e-3) / 1e9
@@ -657,62 +675,102 @@ def bench_backward(kda, steps, warmup, stream, entry="kda_chunk_bwd", names=None
 
 
 ORACLE_MIN_CPU_S = 12.0  # CPU-seconds (wall x threads) of oracle work behind each rate
+ORACLE_SEQ_TOKENS = 2048  # varlen sample: this many leading tokens of every sequence
 
 
-def oracle_prefill_rate(idx, max_problems=None, min_cpu_s=ORACLE_MIN_CPU_S):
-    """CPU oracle on (a sample of) the workload, repeated until it has done about
-    ``min_cpu_s`` of CPU work: returns (tokens/s, threads, sample text, seconds)."""
+def oracle_sample(idx, d=None, threads=None):
+    """A bounded sample of workload ``idx`` for the CPU oracle, with the workload's
+    shapes and distributions: fixed-length workloads keep every token of the first
+    heads (enough heads to give every oracle thread one (sequence, head) problem);
+    the varlen workload keeps the first ORACLE_SEQ_TOKENS tokens of each sequence
+    (each from its own initial state) on the first heads.  ``d``: the workload's
+    full inputs if already generated (a subset of heads is generated otherwise).
+    Returns (inputs, description)."""
+    w = ki.WORKLOADS[idx]
+    H = w["H"]
+    nseq = w.get("nseq", w.get("B", 1))
+    nh = max(1, min(H, -(-int(threads or 1) // nseq)))
+    heads = list(range(nh))
+    if d is None:
+        d = ki.workload_inputs(idx, heads=heads)
+    sub = {x: (d[x][:, :, heads] if d[x] is not None and d[x].shape[2] != nh else d[x])
+           for x in ("q", "k", "v", "g", "beta")}
+    s0 = d["initial_state"]
+    if s0 is not None and s0.shape[1] != nh:
+        s0 = s0[:, heads]
+    if d["cu_seqlens"] is None:
+        text = f"{w['name']}: all {w.get('B', 1)}x{w['T']} tokens on {nh} of {H} heads"
+        return dict(sub, initial_state=s0, scale=d["scale"], cu_seqlens=None), text
+    import torch as _t
+    cu = d["cu_seqlens"].numpy()
+    spans = [(int(cu[n]), min(int(cu[n + 1]), int(cu[n]) + ORACLE_SEQ_TOKENS)) for n in range(len(cu) - 1)]
+    cat = {x: _t.cat([sub[x][:, a:b] for a, b in spans], dim=1).contiguous() for x in sub}
+    new_cu = _t.from_numpy(ki.cu_seqlens_from_lengths([b - a for a, b in spans]))
+    text = (f"{w['name']}: the first {ORACLE_SEQ_TOKENS} tokens of each of its {len(spans)} sequences "
+            f"({int(new_cu[-1])} tokens) on {nh} of {H} heads")
+    return dict(cat, initial_state=s0, scale=d["scale"], cu_seqlens=new_cu), text
+
+
+def oracle_prefill_rate(idx, d=None, min_cpu_s=ORACLE_MIN_CPU_S):
+    """CPU oracle on a bounded sample of workload ``idx`` (oracle_sample), repeated
+    until it has done about ``min_cpu_s`` of CPU work: returns (tokens/s, threads,
+    sample text, seconds).  Tokens/s counts whole tokens (every head of a token)."""
     import oracle
     w = ki.WORKLOADS[idx]
-    heads = None
-    H = w["H"]
-    if max_problems is not None and max_problems < w.get("B", 1) * H:
-        heads = list(range(max(1, max_problems // w.get("B", 1))))
-    d = ki.workload_inputs(idx, heads=heads)
-    Hs = d["q"].shape[2]
-    B0 = d["q"].shape[0]
-    used = min(oracle.threads(), B0 * Hs if d["cu_seqlens"] is None else (d["cu_seqlens"].shape[0] - 1) * Hs)
+    x, text = oracle_sample(idx, d, oracle.threads())
+    Hs = x["q"].shape[2]
+    nprob = Hs * (x["q"].shape[0] if x["cu_seqlens"] is None else x["cu_seqlens"].shape[0] - 1)
+    used = min(oracle.threads(), nprob)
     passes = 0
     t0 = time.perf_counter()
     while True:
-        oracle.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], d["scale"],
-                       cu_seqlens=d["cu_seqlens"])
+        oracle.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["initial_state"], x["scale"],
+                       cu_seqlens=x["cu_seqlens"])
         passes += 1
         dt = time.perf_counter() - t0
-        if dt * used >= min_cpu_s or passes >= 64:
+        if dt * used >= min_cpu_s or passes >= 256:
             break
-    B, T = d["q"].shape[0], d["q"].shape[1]
-    token_heads = B * T * Hs
-    tokens_per_s = passes * token_heads / dt / H   # whole-token rate: every token has H heads
-    sample = (f"{w['name']}: {B}x{T} tokens x {Hs} of {H} heads ({token_heads} token-heads) x {passes} "
-              f"passes, {dt:.2f} s wall on {used} threads")
+    token_heads = x["q"].shape[0] * x["q"].shape[1] * Hs
+    tokens_per_s = passes * token_heads / dt / w["H"]   # whole-token rate: every token has H heads
+    sample = f"{text} ({token_heads} token-heads) x {passes} passes, {dt:.2f} s wall on {used} threads"
     return tokens_per_s, used, sample, dt
 
 
 # ---------------------------------------------------------------------------
 
+def headline_config(world):
+    """``config`` of the JSON line: the headline workload, named by what it is."""
+    w = ki.WORKLOADS[HEADLINE_W]
+    return {"workload": w["name"], "tokens": w["T"], "sequences": w["nseq"],
+            "lengths": f"log-uniform in [{w['lo']}, {w['hi']}], rescaled to the total",
+            "H": w["H"], "d_k": w["dk"], "d_v": w["dv"], "chunk": 64,
+            "initial_state": "random fp32 per sequence", "final_state": "returned",
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs (12.9 GB) larger than L2; also flushed (256 MiB write) between timed steps, "
+                  "outside the events"}
+
+
 def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle on bounded samples of the headline workload."""
     if rank != 0:
         return
     rates, sample, threads = [], "", 1
+    w = ki.WORKLOADS[HEADLINE_W]
     import oracle
-    nprob = max(2, oracle.threads())
+    d, _ = oracle_sample(HEADLINE_W, None, oracle.threads())
     for _ in range(min(args.warmup, 1)):
-        oracle_prefill_rate(PREFILL_W, max_problems=nprob)
+        oracle_prefill_rate(HEADLINE_W, d, min_cpu_s=ORACLE_MIN_CPU_S / 4)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        r, threads, sample, _ = oracle_prefill_rate(PREFILL_W, max_problems=nprob)
+        r, threads, sample, _ = oracle_prefill_rate(HEADLINE_W, d)
         rates.append(r)
     wall = time.perf_counter() - t0
-    w = ki.WORKLOADS[PREFILL_W]
     val = statistics.median(rates)
-    tokens = w["B"] * w["T"]
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * tokens / val, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": 1e3 * w["T"] / val, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w["name"], "B": w["B"], "T": w["T"], "H": w["H"],
-                       "d_k": w["dk"], "d_v": w["dv"], "parallelism": "none (CPU oracle)"},
+            "config": dict(headline_config(world), parallelism="none (CPU oracle)"),
             "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -722,17 +780,30 @@ def run_reference(args, world, rank):
 
 
 def ncu_case(which):
-    """Two untimed launches of one workload, for profiler captures."""
+    """Two untimed launches of one workload, for profiler captures: ``prefill`` (B2
+    H16 T4096), ``prefill96`` (96 heads x 32768), ``varlen`` (the 1M-token headline),
+    ``bwd`` (kda_chunk_bwd on B2 H16 T4096), ``decode32`` / ``decode`` (32 or 256
+    requests x 96 heads)."""
     import gated_delta_rule_gb300 as kda
     kda.build()
     kda.load_library()
     dev = torch.device("cuda")
-    if which.startswith("prefill"):
-        d = ki.workload_inputs(PREFILL_W if which == "prefill" else K3_W)
+    if which.startswith("prefill") or which in ("varlen", "bwd"):
+        idx = {"prefill": PREFILL_W, "prefill96": K3_W, "varlen": HEADLINE_W, "bwd": PREFILL_W}[which]
+        d = ki.workload_inputs(idx)
         t = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in d.items()}
+        if which == "bwd":
+            B, T, H, dk = t["q"].shape
+            gen = torch.Generator().manual_seed(1)
+            do = torch.randn(B, T, H, t["v"].shape[-1], generator=gen).to(torch.bfloat16).to(dev)
+            dST = torch.randn(B, H, dk, t["v"].shape[-1], generator=gen).to(dev)
         for _ in range(2):
-            kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"],
-                              t["scale"], cu_seqlens=t["cu_seqlens"])
+            if which == "bwd":
+                kda.kda_chunk_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"], t["scale"],
+                                  do, dST)
+            else:
+                kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"],
+                                  t["scale"], cu_seqlens=t["cu_seqlens"])
     else:
         w = ki.WORKLOADS[DECODE_W]
         N = 32 if which == "decode32" else w["N"]
@@ -746,6 +817,21 @@ def ncu_case(which):
     print(json.dumps({"ncu_case": which, "ok": True}))
 
 
+def prefill_summary(r, pk, world):
+    """A prefill workload's sub-key: step time, rates, per-kernel split and the
+    fractions of both peaks."""
+    ms = max_over_ranks(statistics.mean(r["ms"]), world)
+    return {"workload": r["name"], "ms_per_step": ms,
+            "kernel_ms": {n: max_over_ranks(v, world) for n, v in r["kernel_ms"].items()},
+            "kernel_hbm_frac": {n: r["kernel_bytes"][n] / (r["kernel_ms"][n] * 1e-3) / 1e9 / pk["hbm"]
+                                for n in r["kernel_bytes"] if n in r["kernel_ms"]},
+            "tokens_per_s": world * r["tokens"] / (ms * 1e-3),
+            "hbm_frac": r["bytes"] / (ms * 1e-3) / 1e9 / pk["hbm"],
+            "tc_frac": r["flops"] / (ms * 1e-3) / 1e12 / pk["bf16"],
+            "t_roof_over_t": max(r["flops"] / (pk["bf16"] * 1e12), r["bytes"] / (pk["hbm"] * 1e9)) / (ms * 1e-3),
+            "gpu_launches": r["launches"]}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -754,8 +840,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-k3", action="store_true")
-    ap.add_argument("--no-varlen", action="store_true")
-    ap.add_argument("--ncu-case", choices=["prefill", "prefill96", "decode32", "decode"],
+    ap.add_argument("--ncu-case", choices=["prefill", "prefill96", "varlen", "bwd", "decode32", "decode"],
                     help="run two untimed launches of one workload (for ncu captures) and exit")
     args = ap.parse_args()
     if args.ncu_case:
@@ -776,7 +861,7 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
 
     clk = ClockSampler(local)
-    pre = bench_prefill(kda, PREFILL_W, args.steps, args.warmup, flush, stream, clk, world)
+    pre = bench_prefill(kda, HEADLINE_W, args.steps, args.warmup, flush, stream, clk, world)
     wall = pre["wall"]
 
     ms = statistics.mean(pre["ms"])
@@ -792,11 +877,21 @@ def main():
     tc = {"achieved": ach_tf, "peak": pk["bf16"], "unit": "TFLOP/s", "frac": ach_tf / pk["bf16"],
           "algorithmic_flops_per_launch": pre["flops"]}
     t_roof = max(pre["flops"] / (pk["bf16"] * 1e12), pre["bytes"] / (pk["hbm"] * 1e9))
+    head_summary = prefill_summary(pre, pk, world)
+    step_ms = {"mean": ms, "median": max_over_ranks(statistics.median(pre["ms"]), world),
+               "best": max_over_ranks(min(pre["ms"]), world), "reps": len(pre["ms"])}
 
-    e2e = bench_prefill_e2e(kda, pre, max(3, args.steps // 2), args.warmup, stream)
+    e2e = bench_prefill_e2e(kda, pre, 3, 2, stream)
     e2e_val = tokens_all / (max_over_ranks(e2e["ms"], world) * 1e-3)
+    cpu_d = pre["d"] if rank == 0 and world == 1 and not args.no_cpu_baseline else None
+    del pre
 
     extra = {}
+    clk_p1 = ClockSampler(local)
+    p1 = bench_prefill(kda, PREFILL_W, args.steps, 3, flush, stream, clk_p1, world)
+    extra["prefill_B2_H16_T4096"] = dict(prefill_summary(p1, pk, world), roofline=kernel_roofline(p1, pk, world),
+                                         clocks=clk_p1.summary())
+    del p1
     clk_dec = ClockSampler(local)
     dec = bench_decode(kda, 64, args.warmup, stream, clk_dec)
     dms = max_over_ranks(dec["ms"], world)
@@ -810,11 +905,12 @@ def main():
                      "algorithmic_bytes_per_launch": dec["bytes"]},
         "clocks": clk_dec.summary(), "gpu_launches": dec["launches"]}
     gr = dec["graph"]
-    g_ms = max_over_ranks(gr["ms"], world)  # -1 when the capture failed on every rank
+    g_ms, g_failed = graph_ms_over_ranks(gr["ms"], world)
     extra["decode"]["cuda_graph"] = {
-        "ms_per_step": g_ms if g_ms > 0 else None, "steps_per_replay": gr["steps_per_replay"],
+        "ms_per_step": g_ms, "steps_per_replay": gr["steps_per_replay"],
         "replays_timed": gr["replays"], "launches_per_replay": gr["launches_per_replay"],
-        "hbm_frac": dec["bytes"] / (g_ms * 1e-3) / 1e9 / pk["hbm"] if g_ms > 0 else None, "error": gr["error"]}
+        "hbm_frac": dec["bytes"] / (g_ms * 1e-3) / 1e9 / pk["hbm"] if g_ms else None,
+        "error": gr["error"] or ("the capture failed on another rank" if g_failed else None)}
     del dec
     fz = bench_decode_fused(kda, 64, args.warmup, stream)
     f_ms = max_over_ranks(fz["ms"], world)
@@ -843,18 +939,7 @@ def main():
     if not args.no_k3:
         clk_k3 = ClockSampler(local)
         k3 = bench_prefill(kda, K3_W, max(3, args.steps // 4), 3, flush, stream, clk_k3, world)
-        kms = max_over_ranks(statistics.mean(k3["ms"]), world)
-        extra["prefill_96heads"] = {
-            "workload": k3["name"], "ms_per_step": kms,
-            "kernel_ms": {n: max_over_ranks(v, world) for n, v in k3["kernel_ms"].items()},
-            "kernel_hbm_frac": {n: k3["kernel_bytes"][n] / (k3["kernel_ms"][n] * 1e-3) / 1e9 / pk["hbm"]
-                                for n in k3["kernel_bytes"]},
-            "tokens_per_s": world * k3["tokens"] / (kms * 1e-3),
-            "hbm_frac": k3["bytes"] / (kms * 1e-3) / 1e9 / pk["hbm"],
-            "tc_frac": k3["flops"] / (kms * 1e-3) / 1e12 / pk["bf16"],
-            "t_roof_over_t": max(k3["flops"] / (pk["bf16"] * 1e12),
-                                 k3["bytes"] / (pk["hbm"] * 1e9)) / (kms * 1e-3),
-            "clocks": clk_k3.summary(), "gpu_launches": k3["launches"]}
+        extra["prefill_96heads"] = dict(prefill_summary(k3, pk, world), clocks=clk_k3.summary())
         del k3
 
     gp = bench_prefill(kda, PREFILL_W, args.steps, 3, flush, stream, None, world, gated=True)
@@ -880,35 +965,21 @@ def main():
         "workload": bw["name"] + "_backward", "entry": "kda_backward", "ms_per_call": bms,
         "tokens_per_s": world * bw["tokens"] / (bms * 1e-3), "gpu_launches": bw["launches"]}
     del bw
-    if not args.no_varlen:
-        clk_vl = ClockSampler(local)
-        vl = bench_prefill(kda, VARLEN_W, 3, 3, flush, stream, clk_vl, world)
-        vms = max_over_ranks(statistics.mean(vl["ms"]), world)
-        extra["prefill_varlen_1M"] = {
-            "workload": vl["name"], "ms_per_step": vms,
-            "kernel_ms": {n: max_over_ranks(v, world) for n, v in vl["kernel_ms"].items()},
-            "tokens_per_s": world * vl["tokens"] / (vms * 1e-3),
-            "hbm_frac": vl["bytes"] / (vms * 1e-3) / 1e9 / pk["hbm"],
-            "clocks": clk_vl.summary(), "gpu_launches": vl["launches"]}
-        del vl
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": pre["name"], "B": 2, "T": 4096, "H": pre["H"], "d_k": pre["dk"],
-                       "d_v": pre["dv"], "chunk": 64, "parallelism": f"replicas x{world}",
-                       "l2": "flushed (256 MiB write) between timed steps, outside the events"},
+            "data": "synthetic", "config": headline_config(world),
             "roofline": roof, "path_roofline": path_roof, "tc_roofline": tc,
             "t_roof_over_t": t_roof / (ms * 1e-3),
+            "kernel_ms": head_summary["kernel_ms"], "kernel_hbm_frac": head_summary["kernel_hbm_frac"],
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": e2e["h2d"],
                     "d2h_bytes_per_step": e2e["d2h"]},
-            "gpu_launches": pre["launches"], "clocks": clk.summary(), "wall_s_timed_region": wall,
-            "step_ms": {"mean": ms, "median": max_over_ranks(statistics.median(pre["ms"]), world),
-                        "best": max_over_ranks(min(pre["ms"]), world), "reps": len(pre["ms"])}}
+            "gpu_launches": head_summary["gpu_launches"], "clocks": clk.summary(), "wall_s_timed_region": wall,
+            "step_ms": step_ms}
     line.update(extra)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r, threads, sample, _ = oracle_prefill_rate(PREFILL_W)
+        r, threads, sample, _ = oracle_prefill_rate(HEADLINE_W, cpu_d)
         line["cpu_baseline"] = {"value": r, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                                 "sample": sample}
     if rank == 0:

@@ -17,18 +17,19 @@ from ._build import LIB, build, up_to_date  # noqa: F401
 __all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
            "kda_recurrent_multi_step", "kda_chunk_fwd_gated", "kda_chunk_fwd_checkpointed",
            "kda_decode_step_fused", "kda_backward", "kda_chunk_bwd",
-           "kda_get_device_error", "kda_set_launch_events", "kda_last_launch_count", "KdaError",
+           "kda_get_device_error", "kda_set_launch_events", "kda_last_launch_count",
+           "kda_test_stall_next_prefill", "KdaError",
            "load_library", "build", "STATUS"]
 
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
-          4: "KDA_ERR_DEVICE", 5: "KDA_ERR_TIMEOUT"}
+          4: "KDA_ERR_DEVICE", 5: "KDA_ERR_TIMEOUT", 6: "KDA_ERR_DOMAIN"}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
 
 EXPORTED = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_fused_recurrent_fwd", "kda_recurrent_step",
             "kda_recurrent_multi_step", "kda_chunk_fwd_gated", "kda_chunk_fwd_checkpointed",
             "kda_decode_step_fused", "kda_backward", "kda_chunk_bwd",
             "kda_get_device_error", "kda_status_string", "kda_last_error_message",
-            "kda_set_launch_events", "kda_last_launch_count"]
+            "kda_set_launch_events", "kda_last_launch_count", "kda_test_stall_next_prefill"]
 
 
 class KdaTensor(ctypes.Structure):
@@ -85,6 +86,8 @@ def load_library(path: str | None = None):
     lib.kda_set_launch_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
     lib.kda_last_launch_count.restype = ctypes.c_int
     lib.kda_last_launch_count.argtypes = []
+    lib.kda_test_stall_next_prefill.restype = ctypes.c_int
+    lib.kda_test_stall_next_prefill.argtypes = [ctypes.c_int]
     _lib = lib
     return lib
 
@@ -333,3 +336,10 @@ def kda_set_launch_events(events) -> None:
 def kda_last_launch_count() -> int:
     """Kernels enqueued by this thread's last compute call."""
     return load_library().kda_last_launch_count()
+
+
+def kda_test_stall_next_prefill(on: bool = True) -> None:
+    """Testing hook: this thread's next prefill call runs its serial kernel with the
+    chunk-record copies suppressed and short bounded waits, so the waits give up and
+    kda_get_device_error reports KDA_ERR_TIMEOUT (see include/kda.h)."""
+    _check(load_library(), load_library().kda_test_stall_next_prefill(1 if on else 0))

@@ -210,6 +210,57 @@ kda_status cuda_fail(cudaError_t e, const char* what) {
   return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Armed by kda_test_stall_next_prefill; consumed by the calling thread's next
+// prefill call, whatever path it takes.
+thread_local int g_test_stall = 0;
+
+// Domain checks of a prefill-shaped argument set (KDA_VALIDATE), enqueued before
+// the compute kernels.
+cudaError_t validate_prefill(const kda::PrefillArgs& a, cudaStream_t st) {
+  kda::ValidateArgs va;
+  memset(&va, 0, sizeof(va));
+  va.q = a.q;
+  va.k = a.k;
+  va.v = a.v;
+  va.g = a.g;
+  va.beta = a.beta;
+  va.beta_sb = a.beta_sb;
+  va.beta_st = a.beta_st;
+  va.beta_sh = a.beta_sh;
+  va.gate_scale = a.gate ? a.gate_scale : nullptr;
+  va.B = a.B;
+  va.T = a.T;
+  va.H = a.H;
+  va.dk = a.dk;
+  va.dv = a.dv;
+  va.bf16 = a.bf16;
+  va.gate = a.gate;
+  va.err = a.err;
+  return kda::launch_validate(va, st);
+}
+
+// The same for one decode token per request: rows are the N requests.
+cudaError_t validate_decode(const kda::DecodeArgs& d, int* err, cudaStream_t st) {
+  kda::PrefillArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = d.q;
+  a.k = d.k;
+  a.v = d.v;
+  a.g = d.g;
+  a.q.st = a.k.st = a.v.st = a.g.st = 0;
+  a.beta = d.beta;
+  a.beta_sb = d.beta_sn;
+  a.beta_sh = d.beta_sh;
+  a.B = d.N;
+  a.T = 1;
+  a.H = d.H;
+  a.dk = d.dk;
+  a.dv = d.dv;
+  a.bf16 = d.bf16;
+  a.err = err;
+  return validate_prefill(a, st);
+}
+
 enum class PrefillPath { kChunked, kRecurrent, kChunkedNoAlloc };
 
 kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
@@ -218,6 +269,8 @@ kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
                    void* stream, PrefillPath path, const kda_tensor* gate_scale = nullptr,
                    kda_tensor* ckpt = nullptr, int64_t ck_tokens = 0) {
   g_msg.clear();
+  const int stall = g_test_stall;
+  g_test_stall = 0;
   KDA_TRY(check_desc(q, "q", 4, 16));
   const int32_t dt = q->dtype;
   if (dt != KDA_DTYPE_BF16 && dt != KDA_DTYPE_F32)
@@ -354,9 +407,12 @@ kda_status prefill(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
                   "kda_chunk_fwd_noalloc holds %zu; split the batch or use kda_chunk_fwd",
                   need, (size_t)kda::kNoallocWorkspaceBytes);
   }
+  a.test_stall = stall;
   KDA_TRY(device_error_ptr(&a.err));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (kda::validate_enabled() && (e = validate_prefill(a, st)) != cudaSuccess)
+    return cuda_fail(e, "input check launch");
   void* fixed_ws = nullptr;
   if (path == PrefillPath::kChunkedNoAlloc && a.bf16) {
     e = kda::noalloc_workspace(&fixed_ws);
@@ -567,7 +623,14 @@ kda_status kda_recurrent_step(kda_tensor* state, const kda_tensor* q, const kda_
   a.dv = (int)dv;
   a.bf16 = dt == KDA_DTYPE_BF16;
   a.scale = scale;
-  cudaError_t e = kda::launch_decode(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (kda::validate_enabled()) {
+    int* err = nullptr;
+    KDA_TRY(device_error_ptr(&err));
+    if ((e = validate_decode(a, err, static_cast<cudaStream_t>(stream))) != cudaSuccess)
+      return cuda_fail(e, "input check launch");
+  }
+  e = kda::launch_decode(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return KDA_OK;
 }
@@ -698,6 +761,8 @@ kda_status backward_impl(bool chunked, const kda_tensor* q, const kda_tensor* k,
   KDA_TRY(device_error_ptr(&a.err));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (kda::validate_enabled() && (e = validate_prefill(a, st)) != cudaSuccess)
+    return cuda_fail(e, "input check launch");
   if (cu) {
     e = kda::launch_check_seqlens(a.cu_seqlens, a.N, a.T, a.err, st);
     if (e != cudaSuccess) return cuda_fail(e, "cu_seqlens check launch");
@@ -855,8 +920,14 @@ kda_status kda_decode_step_fused(kda_tensor* state, kda_tensor* conv_q, kda_tens
   fa.norm_w = norm_weight ? static_cast<const float*>(norm_weight->data) : nullptr;
   fa.eps = eps;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (kda::validate_enabled()) {  // g and beta as for the plain step; the raw q, k, v finite
+    int* err = nullptr;
+    KDA_TRY(device_error_ptr(&err));
+    if ((e = validate_decode(a, err, st)) != cudaSuccess) return cuda_fail(e, "input check launch");
+  }
   void* scratch = nullptr;
-  cudaError_t e = kda::scratch_alloc(&scratch, kda::decode_fused_workspace_bytes(a.N, a.H, a.dk, a.dv), st);
+  e = kda::scratch_alloc(&scratch, kda::decode_fused_workspace_bytes(a.N, a.H, a.dk, a.dv), st);
   if (e != cudaSuccess) return cuda_fail(e, "fused decode workspace allocation");
   e = kda::launch_decode_fused(fa, scratch, st);
   const cudaError_t ef = kda::scratch_free(scratch, st);
@@ -947,7 +1018,10 @@ kda_status kda_recurrent_multi_step(kda_tensor* state, const kda_tensor* q, cons
   a.bf16 = dt == KDA_DTYPE_BF16;
   a.scale = scale;
   KDA_TRY(device_error_ptr(&a.err));
-  cudaError_t e = kda::launch_recurrent_prefill(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (kda::validate_enabled() && (e = validate_prefill(a, static_cast<cudaStream_t>(stream))) != cudaSuccess)
+    return cuda_fail(e, "input check launch");
+  e = kda::launch_recurrent_prefill(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "multi-step decode launch");
   return KDA_OK;
 }
@@ -967,7 +1041,11 @@ kda_status kda_get_device_error(void* stream) {
   if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
   if (word & kda::kErrTimeout)
     return fail(KDA_ERR_TIMEOUT, "a bounded device-side wait gave up (word 0x%x)", word);
-  return fail(KDA_ERR_DEVICE, "cu_seqlens must start at 0, never decrease and end at T (word 0x%x)",
+  if (word & kda::kErrBadSeqlens)
+    return fail(KDA_ERR_DEVICE, "cu_seqlens must start at 0, never decrease and end at T (word 0x%x)",
+                word);
+  return fail(KDA_ERR_DOMAIN,
+              "an input is outside its domain: q, k, v finite, g in [-5, 0], beta in [0, 1] (word 0x%x)",
               word);
 }
 
@@ -985,6 +1063,8 @@ const char* kda_status_string(kda_status s) {
       return "KDA_ERR_DEVICE";
     case KDA_ERR_TIMEOUT:
       return "KDA_ERR_TIMEOUT";
+    case KDA_ERR_DOMAIN:
+      return "KDA_ERR_DOMAIN";
   }
   return "KDA_ERR_UNKNOWN";
 }
@@ -1001,5 +1081,11 @@ kda_status kda_set_launch_events(void* const* events, int count) {
 }
 
 int kda_last_launch_count(void) { return g_launch.launches; }
+
+kda_status kda_test_stall_next_prefill(int on) {
+  g_msg.clear();
+  g_test_stall = on ? 1 : 0;
+  return KDA_OK;
+}
 
 }  // extern "C"

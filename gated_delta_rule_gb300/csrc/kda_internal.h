@@ -11,6 +11,7 @@ namespace kda {
 enum : int {
   kErrBadSeqlens = 1,  // cu_seqlens not starting at 0, decreasing or not ending at T
   kErrTimeout = 2,     // a bounded wait gave up
+  kErrDomain = 4,      // (KDA_VALIDATE) an input outside its documented domain
 };
 
 // Strided view of a [B, T, H, D] (or [N, H, D]) activation; strides in elements.
@@ -48,6 +49,9 @@ struct PrefillArgs {
   int bf16;  // 1: q/k/v/out are bf16, 0: fp32
   float scale;
   int* err;  // device error word
+  // tests of the timeout path only (kda_test_stall_next_prefill): the chunked
+  // serial kernel issues no record copies, so its bounded waits give up
+  int test_stall;
 };
 
 struct DecodeArgs {
@@ -135,6 +139,25 @@ cudaError_t noalloc_workspace(void** ptr);
 // launch_end returns the error of recording an armed event, if any.
 void launch_begin(cudaStream_t s);
 cudaError_t launch_end(cudaStream_t s);
+
+// Input-domain checks (kda_validate.cu), enabled by KDA_VALIDATE in the environment:
+// q, k, v finite; g in [-5, 0] (or, with the gate, finite logits and gate scales);
+// beta in [0, 1].  Rows are (b, t, h) for b < B, t < T, h < H.
+struct ValidateArgs {
+  Act q, k, v, g;
+  const float* beta;
+  int64_t beta_sb, beta_st, beta_sh;
+  const float* gate_scale;  // [H] or null
+  int B, T, H, dk, dv;
+  int bf16;  // q, k, v (and gate logits) are bf16
+  int gate;  // g holds decay logits in q's dtype
+  int* err;
+};
+bool validate_enabled();
+cudaError_t launch_validate(const ValidateArgs& a, cudaStream_t s);
+
+// SM count of the current device, cached per device (kda_prefill_tc.cu).
+int sm_count();
 
 // Stream-ordered scratch memory from a per-device pool (kda_api.cu).
 cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s);

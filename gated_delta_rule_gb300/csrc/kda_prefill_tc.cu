@@ -48,6 +48,8 @@
 // rows are never read (or are overwritten before they are read).
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
 
@@ -106,8 +108,8 @@ struct PrepSmem {
   static constexpr int BETA = KP + 64 * DK * 2;
   static constexpr int BND = BETA + 64 * 4;   // 5 x DK fp32 (log2 units)
   static constexpr int FT = BND + 5 * DK * 4; // 10 x DK fp32 decay factors
-  static constexpr int MBAR = FT + 10 * DK * 4;
-  static constexpr int TSLOT = MBAR + 8;
+  static constexpr int MBAR = FT + 10 * DK * 4;  // MMA completion, then the exit drain
+  static constexpr int TSLOT = MBAR + 16;
   static constexpr int FLAG = TSLOT + 4;
   static constexpr int kAlloc = FLAG + 4 + 1024;
   static_assert(2 * (kAlloc + 1024) <= 233472, "two prep CTAs per SM");
@@ -126,8 +128,8 @@ struct SerialSmem {
   static constexpr int VT = REC + 2 * kRecBuf;           // two V chunks [64][DV] MN-major (U reuses)
   static constexpr int SB = VT + 2 * 64 * kPitch * 2;    // bf16 S, [DK][DV] MN-major
   static constexpr int OSTG = SB + DK * kPitch * 2;      // output staging: 2 warps x 32 rows x 144 B
-  static constexpr int MBAR = OSTG + 2 * 32 * 144;       // mma_a, mma_s, rec0/1, free0/1, orel0/1
-  static constexpr int TSLOT = MBAR + 64;
+  static constexpr int MBAR = OSTG + 2 * 32 * 144;       // mma_a, mma_s, rec0/1, free0/1, orel0/1, done
+  static constexpr int TSLOT = MBAR + 72;
   static constexpr int FLAG = TSLOT + 4;
   static constexpr int kAlloc = FLAG + 4 + 1024;
   static_assert(kAlloc <= 232448, "shared memory budget");
@@ -310,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
 
   if (tid == 0) {
     mbar_init(sbase + L::MBAR, 1);
+    mbar_init(sbase + L::MBAR + 8, 1);
     fence_mbar_init();
     *sFlag = 0;
   }
@@ -761,7 +764,13 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
     }
     cur = nxt;
   }
-  if (tid == 0) bulk_wait0();  // this CTA's record writes are complete
+  if (tid == 0) {
+    bulk_wait0();  // this CTA's record writes are complete
+    // every product this thread issued has completed before TMEM is freed (after a
+    // timed-out wait one may still be running; otherwise this returns at once)
+    mma_commit(sbase + L::MBAR + 8);
+    if (!mbar_wait(sbase + L::MBAR + 8, 0)) atomicOr(a.err, kErrTimeout);
+  }
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, L::kTmemCols);
@@ -888,7 +897,11 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
   const uint32_t mbar_rec0 = mbar_a + 16;   // record (+ V) of buffer b landed
   const uint32_t mbar_free0 = mbar_a + 32;  // buffer b's chunk has finished its last product
   const uint32_t mbar_orel0 = mbar_a + 48;  // buffer b's output has been read out of TMEM
+  const uint32_t mbar_done = mbar_a + 64;   // exit drain: every product issued has completed
   constexpr int kT2 = 64 * 64 * 2;  // T2 tile bytes; the rest of a record lands after the zero tile
+  // Bounded waits.  With a.test_stall (tests of the timeout path only) the producer
+  // issues no copies and every wait gives up after about 0.1 ms.
+  const long long wait_limit = a.test_stall ? 200000ll : 4000000000ll;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -919,6 +932,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
     mbar_init(mbar_free0 + 8, 1);
     mbar_init(mbar_orel0, 64);  // every thread of warps 2-3
     mbar_init(mbar_orel0 + 8, 64);
+    mbar_init(mbar_done, 1);
     fence_mbar_init();
     *sFlag = 0;
   }
@@ -933,9 +947,11 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::TSLOT);
   const uint32_t tS = tmem + 2 * DV;  // fp32 state (DV cols); U/O buffers at 0 and DV
   auto tX = [&](int b) { return tmem + (uint32_t)(b * DV); };
-  // bounded wait; after any timeout every later wait returns at once so all roles finish
+  // Bounded wait.  After any timeout the abort flag is up: every later wait returns
+  // at once, and no role issues further asynchronous work (products, copies), but
+  // every role still walks its loop through the named barriers, so all finish.
   auto wait = [&](uint32_t mbar, uint32_t parity) {
-    if (!*sFlag && !mbar_wait(mbar, parity)) {
+    if (!*sFlag && !mbar_wait(mbar, parity, wait_limit)) {
       atomicOr(a.err, kErrTimeout);
       *sFlag = 1;
     }
@@ -977,9 +993,13 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
     // the records come from the previous grid (launched with programmatic
     // serialization): wait until it has completed and its writes are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    int last[2] = {-1, -1};  // last chunk whose copies were issued into each buffer
     for (int ci = 0; ci < nch; ++ci) {
       const int b = ci & 1;
       if (ci >= 2) wait(mbar_free0 + 8 * b, (uint32_t)(((ci - 2) >> 1) & 1));  // chunk ci - 2 is done
+      // one decision for the whole warp: after an abort nothing more is issued
+      if (__shfl_sync(0xffffffffu, (a.test_stall || *sFlag) ? 1 : 0, 0)) continue;
+      last[b] = ci;
       const uint32_t dst = sbase + L::REC + b * L::kRecBuf;
       const uint32_t mb = mbar_rec0 + 8 * b;
       if (lane == 0) {
@@ -1000,6 +1020,12 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
       cp_async_mbar_arrive(mb);
     }
     cp_async_wait_all();
+    // the bulk copies issued last into each buffer have landed (the phase they
+    // complete is that barrier's latest), so none writes shared memory after exit
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+      if (last[b] >= 0 && !mbar_wait(mbar_rec0 + 8 * b, (uint32_t)((last[b] >> 1) & 1), wait_limit))
+        atomicOr(a.err, kErrTimeout);
   } else if (warp == 4) {
     // ======================= MMA warp =======================
     for (int ci = 0; ci < nch; ++ci) {
@@ -1014,7 +1040,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
       if (ci >= 2) wait(mbar_orel0 + 8 * b, (uint32_t)(((ci - 2) >> 1) & 1));
       // [U ; Q+ S] = [T_beta | -W ; 0 | Q+] [V ; S]; the V half needs no state, so it
       // is issued before the state's bf16 copy is ready
-      if (lane == 0) {
+      if (lane == 0 && !*sFlag) {
         fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
@@ -1023,7 +1049,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
       }
       __syncwarp();
       bar_sync(1, 160);
-      if (lane == 0) {
+      if (lane == 0 && !*sFlag) {
         fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < DK / 16; ++ks)
@@ -1034,7 +1060,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
       __syncwarp();
       bar_sync(2, 160);
       // S += K_end^T U  (the state chain), then O += A_Q U (rows 64..127 of buffer b)
-      if (lane == 0) {
+      if (lane == 0 && !*sFlag) {
         fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
@@ -1049,6 +1075,13 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
       }
       __syncwarp();
     }
+    // every product issued has completed before TMEM is freed (after an abort some
+    // may still run; otherwise they were all waited on and this returns at once)
+    if (lane == 0) {
+      mma_commit(mbar_done);
+      if (!mbar_wait(mbar_done, 0, wait_limit)) atomicOr(a.err, kErrTimeout);
+    }
+    __syncwarp();
   } else {
     // ======================= TMEM <-> memory warps =======================
     // rows 64..127 of chunk pc's U/O buffer -> out (warps 2-3).  The values are
@@ -1338,16 +1371,6 @@ __global__ void __launch_bounds__(kCombineThreads) kda_segment_combine_kernel(Pr
   }
 }
 
-int sm_count() {
-  static int count = 0;
-  if (!count) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev);
-    if (count <= 0) count = 1;
-  }
-  return count;
-}
 
 template <int DK>
 constexpr int rec_bytes() { return Rec<DK>::kBytes; }
@@ -1470,6 +1493,26 @@ cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
 }
 
 }  // namespace
+
+// SM count of the current device, looked up once per device (concurrent first
+// calls may both look it up; they store the same value).
+int sm_count() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> counts[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) cudaGetLastError();
+    return c > 0 ? c : 1;
+  }
+  int c = counts[dev].load(std::memory_order_relaxed);
+  if (c <= 0) {
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) cudaGetLastError();
+    if (c <= 0) c = 1;
+    counts[dev].store(c, std::memory_order_relaxed);
+  }
+  return c;
+}
 
 size_t chunk_prefill_workspace_bytes(const PrefillArgs& a) { return (size_t)plan(a).total(); }
 

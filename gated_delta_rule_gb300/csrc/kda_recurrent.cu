@@ -889,13 +889,7 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs& fa, void* ws, cudaStream_
 }
 
 int backward_value_slices(int N, int H, int dv) {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
-  }
+  const int sms = sm_count();
   // 32 value columns per CTA while the SMs hold them all (each CTA's token loop is
   // a latency chain: fewer columns, shorter steps), else 64
   const int64_t nh = (int64_t)N * H;

@@ -36,6 +36,14 @@
  *    starting at 0 or not ending at T) are recorded in a per-device error word
  *    read by kda_get_device_error; outputs are then unspecified.  NaN inputs
  *    propagate; nothing traps.
+ *  - Input-domain checks (optional): with KDA_VALIDATE set to a non-empty value
+ *    other than "0" in the environment (read at every call), every compute
+ *    entry point first enqueues one extra kernel that reads q, k, v, g (or the
+ *    gate logits) and beta once and records KDA_ERR_DOMAIN in the device error
+ *    word if a value is not finite, a g is outside [-5, 0] or a beta outside
+ *    [0, 1] (the bounded decay of "Kimi K3 技术报告解读" (marsggbo.github.io)
+ *    §3.5, which the chunked kernels rely on for exponent safety).  The check
+ *    changes no result; it costs one extra read of the inputs.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -52,7 +60,8 @@ typedef enum kda_status {
   KDA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. d_k = 96) */
   KDA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
   KDA_ERR_DEVICE = 4,      /* the device reported bad cu_seqlens (kda_get_device_error) */
-  KDA_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (kda_get_device_error) */
+  KDA_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (kda_get_device_error) */
+  KDA_ERR_DOMAIN = 6       /* KDA_VALIDATE found an input outside its domain (kda_get_device_error) */
 } kda_status;
 
 typedef enum kda_dtype {
@@ -367,9 +376,11 @@ kda_status kda_recurrent_multi_step(kda_tensor* state, const kda_tensor* q, cons
 
 /*
  * kda_get_device_error - synchronises `stream`, then returns and clears the
- * current device's error word: KDA_OK, KDA_ERR_DEVICE (bad cu_seqlens) or
- * KDA_ERR_TIMEOUT; KDA_ERR_CUDA if the synchronisation itself failed.  The
- * message of a non-OK result is available from kda_last_error_message().
+ * current device's error word: KDA_OK, KDA_ERR_TIMEOUT (a bounded wait gave up;
+ * reported first when several bits are set), KDA_ERR_DEVICE (bad cu_seqlens) or
+ * KDA_ERR_DOMAIN (KDA_VALIDATE); KDA_ERR_CUDA if the synchronisation itself
+ * failed.  The message of a non-OK result is available from
+ * kda_last_error_message().
  */
 kda_status kda_get_device_error(void* stream);
 
@@ -402,6 +413,19 @@ kda_status kda_set_launch_events(void* const* events, int count);
 /* Number of kernels the calling thread's last compute call enqueued (0 when it
  * returned before launching any). */
 int kda_last_launch_count(void);
+
+/*
+ * kda_test_stall_next_prefill - a testing hook with no counterpart on the pages:
+ * it exercises the timeout path of the device-side waits without faulting or
+ * hanging the GPU.  With on != 0 the calling host thread's next prefill call
+ * (any kda_chunk_fwd* entry point; consumed by that call whatever it does) runs
+ * its chunked serial kernel with the chunk-record copies suppressed and every
+ * bounded wait cut to about 0.1 ms: the waits give up, the kernel stops issuing
+ * work, drains what it issued, frees its tensor memory and returns, and
+ * kda_get_device_error then reports KDA_ERR_TIMEOUT.  That call's outputs are
+ * unspecified; later calls are unaffected.  on == 0 disarms.  Always KDA_OK.
+ */
+kda_status kda_test_stall_next_prefill(int on);
 
 #ifdef __cplusplus
 }

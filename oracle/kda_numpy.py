@@ -28,10 +28,12 @@ import numpy as np
 
 
 def _f64(x):
+    """Exact fp64 copy of a numpy array or a torch tensor of any float dtype (bf16
+    and fp32 widen exactly; fp64 stays as it is)."""
     if x is None:
         return None
     if hasattr(x, "detach"):
-        x = x.detach().float().cpu().numpy()
+        x = x.detach().cpu().double().numpy()
     return np.asarray(x, dtype=np.float64)
 
 

@@ -29,7 +29,7 @@ def _step(kda, S, C, d, x, norm=True):
 
 
 @pytest.mark.parametrize("dk,dv", [(128, 128), (64, 128), (128, 64), (64, 64)])
-@pytest.mark.parametrize("dtype,tol_o,tol_s", [("bf16", 3e-2, 1e-2), ("f32", 1e-4, 1e-4)])
+@pytest.mark.parametrize("dtype,tol_o,tol_s", [("bf16", 2e-2, 1e-2), ("f32", 1e-4, 1e-4)])
 def test_fused_steps_match_oracle(kda, dk, dv, dtype, tol_o, tol_s):
     N, H, steps = 5, 3, 6
     seed = 90 + dk + dv
@@ -95,5 +95,5 @@ def test_fused_decode_sized_batch(kda):
             x["w_q"][heads], x["w_k"][heads], x["w_v"][heads], sub(d["g"]), sub(d["beta"]),
             sub(x["out_gate"]), x["norm_weight"], d["scale"], EPS)
         c_ref = {"q": cq, "k": ck, "v": cv}
-        assert max_abs(y[:, heads], y_ref) <= 3e-2
+        assert max_abs(y[:, heads], y_ref) <= 2e-2
     assert rel_fro(Sd[:, heads], S_ref) <= 1e-2

@@ -437,3 +437,18 @@ def test_chunked_backward_matches_token_autograd(T, C, with_state):
     for name in ("dq", "dk", "dv", "dg", "dbeta"):
         assert np.allclose(got[name], ref[name][0, :, 0], rtol=1e-9, atol=1e-10), name
     assert np.allclose(got["d_initial_state"], ref["d_initial_state"][0, 0], rtol=1e-9, atol=1e-10)
+
+
+def test_numpy_oracle_keeps_fp64_torch_inputs_exact():
+    """fp64 torch tensors reach the numpy oracle unrounded: the result equals the one
+    from the same numbers as numpy arrays bit for bit, and differs from the result on
+    the fp32-rounded numbers (so a silent fp32 round trip would be caught)."""
+    import torch
+    p = problem(9, 6, 5, 11)
+    o_np, S_np = kn.recurrence_three_step(*p, 0.5)
+    tp = [None if a is None else torch.from_numpy(np.array(a)) for a in p]
+    o_t, S_t = kn.recurrence_three_step(*tp, 0.5)
+    assert np.array_equal(o_t, o_np) and np.array_equal(S_t, S_np)
+    rounded = [None if a is None else np.asarray(a, dtype=np.float32).astype(np.float64) for a in p]
+    o_r, _ = kn.recurrence_three_step(*rounded, 0.5)
+    assert not np.array_equal(o_r, o_np)

@@ -204,7 +204,10 @@ def test_workload2_sampled_heads(kda):
 
 def test_workload4_sampled_sequences(kda):
     """1M-token varlen packing (16 sequences x 8 heads) on the GPU; the oracle
-    recomputes the shortest and a mid-length sequence on two heads."""
+    recomputes the shortest, a mid-length and the longest sequence on two heads.
+    The longest (194893 tokens, 3046 chunks) runs the segment split over six
+    512-chunk segments: the first from its initial state, five from the chained
+    (M, S~) transitions, each rerun with outputs."""
     d = ki.workload_inputs(4)
     t = to_dev(d)
     out, sT = kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"],
@@ -213,8 +216,9 @@ def test_workload4_sampled_sequences(kda):
     cu = d["cu_seqlens"].numpy()
     lens = np.diff(cu)
     order = np.argsort(lens)
+    assert -(-int(lens[order[-1]]) // 64) > 5 * 512  # the longest sequence spans six segments
     heads = [1, 6]
-    for n in (int(order[0]), int(order[len(order) // 2])):
+    for n in (int(order[0]), int(order[len(order) // 2]), int(order[-1])):
         a, b = int(cu[n]), int(cu[n + 1])
         sub = {x: d[x][:, a:b][:, :, heads] for x in ("q", "k", "v", "g", "beta")}
         o_ref, s_ref = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"],
