@@ -509,19 +509,21 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
       if (tid == 0) bulk_wait_read0();
       __syncthreads();
 
-      // ================= build: operand tiles =================
-      // Rows use the reference G at the start of sub-block blk: X = k e^{G - bnd[blk]},
-      // and K+ = X 2^{bnd[blk]}.  Column version J >= blk uses the reference at the
-      // start of sub-block J: k e^{bnd[J] - G}.  K_end = k e^{G_C - G}.
-      {
-        float fbl[8];
-        if (blk > 0) {
-          ld8(sFt + ft_index(0, blk) * DK + col, fbl);
-        } else {
+      // ================= build: the Gram operands =================
+      // Rows use the reference G at the start of sub-block blk: X = k e^{G - bnd[blk]}
+      // (and q).  Column version J >= blk uses the reference at the start of
+      // sub-block J: k e^{bnd[J] - G}.  These feed the Gram product; Q+ = q e^{G} goes to
+      // the record on the way, and the tiles not needed until later (K+, K_end) are
+      // formed while the product runs.
+      float fbl[8];  // 2^{bnd[blk]}: from the sub-block reference to the chunk start
+      if (blk > 0) {
+        ld8(sFt + ft_index(0, blk) * DK + col, fbl);
+      } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) fbl[e] = 1.f;
-        }
-        // q rows: Gram rows 64.. and Q+ (record)
+        for (int e = 0; e < 8; ++e) fbl[e] = 1.f;
+      }
+      {
+        // q rows: Gram rows 64.., and Q+ (record)
 #pragma unroll
         for (int i = 0; i < TPP; ++i) {
           const int t = part * TPP + i;
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
           for (int e = 0; e < 8; ++e) x[e] *= fbl[e];
           *reinterpret_cast<uint4*>(rec + R::WQ + sw128(64 + t, col, 128)) = pack8(x);
         }
-        // k rows and K+; y = k e^{bnd[blk] - G} is kept for the column versions and K_end
+        // k rows; y = k e^{bnd[blk] - G} for the column versions
         float y[TPP][8];
 #pragma unroll
         for (int i = 0; i < TPP; ++i) {
@@ -544,9 +546,6 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = kv[e] * ex2(G[i][e]);
           st8(sbase + L::X + sw128(t, col, 128), x);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] *= fbl[e];
-          st8(sbase + L::KP + sw128(t, col, 64), x);
 #pragma unroll
           for (int e = 0; e < 8; ++e) y[i][e] = kv[e] * ex2(-G[i][e]);
         }
@@ -569,18 +568,6 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
             st8(sbase + L::Y + sw128(yoff_rows(J) + part * TPP + i, col, 160), x);
           }
         }
-        // K_end = y 2^{bnd[4] - bnd[blk]} (record, token rows)
-        {
-          float f[8];
-          ld8(sFt + ft_index(blk, 4) * DK + col, f);
-#pragma unroll
-          for (int i = 0; i < TPP; ++i) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = y[i][e] * f[e];
-            *reinterpret_cast<uint4*>(rec + R::KE + sw128(part * TPP + i, col, 64)) = pack8(x);
-          }
-        }
       }
       fence_async_smem();
       fence_before_sync();
@@ -595,6 +582,26 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
           mma_bf16(tmem, desc_kmajor(sbase + L::X, 128, ks), desc_kmajor(sbase + L::Y, 160, ks),
                    idesc_bf16(128, 160, false, false), ks > 0);
         mma_commit(ctx.mbar);
+      }
+      // ---- while the product runs: K_end = k e^{G_C - G} (record, token rows) and
+      // K+ = k e^{G} (shared memory, for W), from the same registers ----
+      {
+        float fend[8];
+        ld8(sFt + ft_index(blk, 4) * DK + col, fend);
+#pragma unroll
+        for (int i = 0; i < TPP; ++i) {
+          const int t = part * TPP + i;
+          float x[8], kv[8], y[8];
+          bf16x8(rk[i], kv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            x[e] = kv[e] * ex2(G[i][e]) * fbl[e];
+            y[e] = kv[e] * ex2(-G[i][e]) * fend[e];
+          }
+          st8(sbase + L::KP + sw128(t, col, 64), x);
+          *reinterpret_cast<uint4*>(rec + R::KE + sw128(t, col, 64)) = pack8(y);
+        }
+        fence_async_smem();  // K+ is read by the W product, several barriers later
       }
       // the k/q registers are free: start loading the next item while the MMAs run
       load_kq(nxt);
