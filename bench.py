@@ -585,34 +585,54 @@ def bench_decode_fused(kda, steps_total, warmup, stream, clk=None):
 
 
 CHUNK_BWD_KERNELS = ["kda_bwd_prep_kernel", "kda_bwd_state_fwd_kernel", "kda_bwd_state_rev_kernel",
-                     "kda_bwd_grad_kernel"]
+                     "kda_bwd_grad_tc_kernel"]
 # FP32 FMA peak of the CUDA cores: 128 FMA per SM per clock at the 2070 MHz maximum SM
-# clock, times the SM count (the chunked backward runs fp32 arithmetic there)
+# clock, times the SM count (the chunked backward's prep and state passes run fp32
+# arithmetic there)
 FP32_FMA_PER_SM_CLK = 128
 SM_MAX_MHZ = 2070.0
 
 
 def chunk_bwd_fmas(dk, dv):
-    """Executed FMAs per (64-token chunk, head) of each chunked-backward kernel,
-    counted from its loop bounds."""
+    """Executed FMAs per (64-token chunk, head) of the fp32 CUDA-core kernels of the
+    chunked backward, counted from their loop bounds."""
     return {"kda_bwd_prep_kernel": 8704 * dk + 6528 * dv + 64 * dk * dv,
             "kda_bwd_state_fwd_kernel": 128 * dk * dv,
-            "kda_bwd_state_rev_kernel": 128 * dk * dv,
-            "kda_bwd_grad_kernel": (dv // 32) * (8224 * dk + 331776) + 10240 * dk}
+            "kda_bwd_state_rev_kernel": 128 * dk * dv}
 
 
-def chunk_bwd_roofline(bw, ms, kernel_ms, sms):
-    """``roofline`` of the chunked backward: bound "alu" (fp32 FMA), dominant kernel
-    kda_bwd_grad_kernel, plus the whole call's rate."""
-    peak = sms * FP32_FMA_PER_SM_CLK * 2 * SM_MAX_MHZ * 1e6 / 1e12
+def chunk_bwd_grad_bytes(dk, dv, C=64):
+    """Algorithmic bytes per (chunk, head) of the tensor-core gradient kernel: it reads
+    the fp32 states S and X, the chunk's U and dY and the records' A, the bf16 q, k, v
+    and dO rows, g and beta, and writes fp32 dq, dk, dg and dbeta."""
+    rd = 4 * (2 * dk * dv + 2 * C * dv + C * C) + 2 * C * (2 * dk + 2 * dv) + 4 * C * dk + 4 * C
+    return rd + 4 * (3 * C * dk + C)
+
+
+def chunk_bwd_roofline(bw, ms, kernel_ms, sms, hbm_peak):
+    """``roofline`` of the chunked backward for its dominant kernel: bound "alu" (fp32
+    FMA) for the CUDA-core prep and state passes, "hbm" for the tensor-core gradient
+    kernel; every kernel's rate beside it."""
+    alu_peak = sms * FP32_FMA_PER_SM_CLK * 2 * SM_MAX_MHZ * 1e6 / 1e12
     fl = {n: 2.0 * f * bw["chunk_heads"] for n, f in chunk_bwd_fmas(bw["dk"], bw["dv"]).items()}
-    k = "kda_bwd_grad_kernel"
-    achieved = fl[k] / (kernel_ms[k] * 1e-3) / 1e12
-    call = sum(fl.values()) / (ms * 1e-3) / 1e12
-    return {"bound": "alu", "kernel": k, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": None, "peak_source": "derived (SMs x 128 FMA x 2 x 2070 MHz)",
-            "flops_per_launch": fl[k], "call_tflops": call, "call_frac": call / peak,
-            "kernel_tflops": {n: fl[n] / (kernel_ms[n] * 1e-3) / 1e12 for n in fl}}
+    grad = "kda_bwd_grad_tc_kernel"
+    gbytes = chunk_bwd_grad_bytes(bw["dk"], bw["dv"]) * bw["chunk_heads"]
+    rates = {n: {"achieved": fl[n] / (kernel_ms[n] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                 "frac": fl[n] / (kernel_ms[n] * 1e-3) / 1e12 / alu_peak} for n in fl if n in kernel_ms}
+    if grad in kernel_ms:
+        g = gbytes / (kernel_ms[grad] * 1e-3) / 1e9
+        rates[grad] = {"achieved": g, "unit": "GB/s", "frac": g / hbm_peak}
+    k = max(kernel_ms, key=kernel_ms.get)
+    if k == grad:
+        out = {"bound": "hbm", "kernel": k, "achieved": rates[k]["achieved"], "peak": hbm_peak, "unit": "GB/s",
+               "frac": rates[k]["frac"], "traffic": None, "peak_source": "measured (burst copy)",
+               "bytes_per_launch": gbytes}
+    else:
+        out = {"bound": "alu", "kernel": k, "achieved": rates[k]["achieved"], "peak": alu_peak,
+               "unit": "TFLOP/s", "frac": rates[k]["frac"], "traffic": None,
+               "peak_source": "derived (SMs x 128 FMA x 2 x 2070 MHz)", "flops_per_launch": fl[k]}
+    out["kernel_rates"] = rates
+    return out
 
 
 def bench_backward(kda, steps, warmup, stream, entry="kda_chunk_bwd", names=None):
@@ -958,7 +978,8 @@ def main():
         "tokens_per_s": world * bw["tokens"] / (bms * 1e-3),
         "hbm_frac": bw["bytes"] / (bms * 1e-3) / 1e9 / pk["hbm"], "gpu_launches": bw["launches"]}
     extra["backward"]["roofline"] = chunk_bwd_roofline(
-        bw, bms, extra["backward"]["kernel_ms"], torch.cuda.get_device_properties(local).multi_processor_count)
+        bw, bms, extra["backward"]["kernel_ms"], torch.cuda.get_device_properties(local).multi_processor_count,
+        pk["hbm"])
     bw = bench_backward(kda, 3, 3, stream, "kda_backward")
     bms = max_over_ranks(bw["ms"], world)
     extra["backward_token_loop"] = {

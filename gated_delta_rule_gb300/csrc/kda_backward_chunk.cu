@@ -126,6 +126,7 @@ cudaError_t run(const ChunkBwdArgs& ca, cudaStream_t s) {
   srev<<<pgrid, bwdc::kPassThreads, SS::BYTES, s>>>(ca);
   if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   if (ca.total > 0) {
+    if (chunk_grad_tc_supported(a)) return launch_chunk_grad_tc(ca, s);  // d_k = d_v = 128, bf16
     launch_begin(s);
     grad<<<cgrid, 256, GS::BYTES, s>>>(ca);
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;

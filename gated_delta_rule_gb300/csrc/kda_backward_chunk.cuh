@@ -736,6 +736,184 @@ struct GradSmem {
   static constexpr int BYTES = FLOATS * 4;
 };
 
+// Shared-memory arrays of the second half of the gradient kernels (fp32; row pitches
+// in floats).
+struct TailSmem {
+  float* G;     // [64][pg] cumulative log-decay G
+  float* rr;    // [5][DK] r_0 .. r_3 (log-decay before each sub-block), G_C
+  float* beta;  // [64]
+  float* M1;    // [64][pm] scale Tril(dO U^T)
+  float* M2;    // [64][pm] -StrictTril(diag(beta) dY U^T)
+  float* op;    // [64][po] operand buffer, then dG
+  float* op2;   // [64][po] operand buffer
+  float* ek;    // [16][DK] sums over 4 rows of e k
+  float* dbp;   // [64][pb] dbeta partials, nb per row
+  float* gs;    // [DK] rowsum(S X)
+  int pg, pm, po, pb, nb;
+};
+
+// Second half of the gradients of one chunk, from Pq = dO S^T, Pk = dY S^T and
+// Pe = U X^T (a thread's rows 4 rg .., columns 4 cg + 64 c4 ..) and M1, M2, gs and
+// the dbeta partials in shared memory: the direct terms, the row and column forms
+// inside the chunk, dq, dk, dg and dbeta.  With kp_dbeta the term
+// -rowsum(K+ * (dY S^T)) of dbeta is formed here, as partial cg of each row.
+template <int DK, int DV, typename T, bool kp_dbeta>
+KB_HD void grad_tail(const ChunkBwdArgs& ca, const ChunkLoc& L, int h, const TailSmem& s,
+                     float4 (&Pq)[4][DK / 64], float4 (&Pk)[4][DK / 64], float4 (&Pe)[4][DK / 64], int tid) {
+  constexpr int NT = 256;
+  constexpr int C4 = DK / 64;
+  constexpr int NK = kC * DK / 4 / NT;  // 4-vectors of a [64][DK] tile per thread
+  const BackwardArgs& ba = ca.b;
+  const PrefillArgs& a = ba.f;
+  const T* qb = static_cast<const T*>(a.q.ptr) + L.b * a.q.sb + L.t * a.q.st + (int64_t)h * a.q.sh;
+  const T* kb = static_cast<const T*>(a.k.ptr) + L.b * a.k.sb + L.t * a.k.st + (int64_t)h * a.k.sh;
+  const int rows = L.rows;
+  const float scale = a.scale;
+  const int rg = tid / 16, cg = tid % 16;
+  const int PG = s.pg, PA = s.pm, PO = s.po;
+  float* sG = s.G;
+  float* rr = s.rr;
+  float* sb = s.beta;
+  float* sM1 = s.M1;
+  float* sM2 = s.M2;
+  float* sOp = s.op;
+  float* sOp2 = s.op2;
+  float* ek = s.ek;
+  auto own = [&](float4 (&x)[4][C4], const T* base, int64_t st) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c4 = 0; c4 < C4; ++c4)
+        x[r][c4] = 4 * rg + r < rows ? ld4t<T>(base + (int64_t)(4 * rg + r) * st + 4 * cg + 64 * c4) : zero4();
+  };
+  // direct terms; after this block Pq = dq, Pk = dk, Pe = (a - e) (the dG coefficient of k)
+  float4 kown[4][C4];
+  own(kown, kb, a.k.st);
+  float dbk[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c4 = 0; c4 < C4; ++c4)
+    for (int e = 0; e < 4; ++e) {
+      const int d = 4 * cg + 64 * c4 + e;
+      float eks = 0.f;
+      for (int r = 0; r < 4; ++r) {
+        const int i = 4 * rg + r;
+        const float G = sG[i * PG + d];
+        const float E = KB_EXP(G), Ee = KB_EXP(rr[4 * DK + d] - G);
+        if (kp_dbeta) dbk[r] += comp(kown[r][c4], e) * E * comp(Pk[r][c4], e);
+        const float dq = scale * comp(Pq[r][c4], e) * E;
+        const float av = -sb[i] * comp(Pk[r][c4], e) * E;
+        const float ev = comp(Pe[r][c4], e) * Ee;
+        comp(Pq[r][c4], e) = dq;
+        comp(Pk[r][c4], e) = av + ev;
+        comp(Pe[r][c4], e) = av - ev;
+        eks += ev * comp(kown[r][c4], e);
+      }
+      ek[rg * DK + d] = eks;
+    }
+  if (kp_dbeta)
+    for (int r = 0; r < 4; ++r) s.dbp[(4 * rg + r) * s.pb + cg] = -dbk[r];
+  {
+    float4 kv[NK];
+    load_rows<DK, NT, T>(kv, kb, a.k.st, rows, tid);
+    for (int u = 0; u < NK; ++u) {
+      const int idx = tid + u * NT, i = idx / (DK / 4), p = idx - i * (DK / 4), I = i / kSB;
+      const float4 G = ld4(sG + i * PG + 4 * p);
+      const float4 r0 = ld4(rr + I * DK + 4 * p), r1 = ld4(rr + (I + 1) * DK + 4 * p);
+      float4 x, y;
+      for (int e = 0; e < 4; ++e) {
+        comp(x, e) = comp(kv[u], e) * KB_EXP(comp(r0, e) - comp(G, e));
+        comp(y, e) = comp(kv[u], e) * KB_EXP(comp(G, e) - comp(r1, e));
+      }
+      st4(sOp + i * PO + 4 * p, x);
+      st4(sOp2 + i * PO + 4 * p, y);
+    }
+  }
+  KB_SYNC();
+  // row form: sum_{j in J} M_ij (k_j e^{r_J - G_j}), times e^{G_i - r_J}
+  const int Ib = rg / 4;  // the sub-block of this thread's rows
+  for (int pass = 0; pass < 2; ++pass) {
+    const float* M = pass ? sM2 : sM1;
+    for (int J = 0; J <= Ib; ++J) {
+      float4 t[4][C4];
+      zero_acc<DK>(t);
+      mm64_rows<DK>(t, M, PA, sOp, PO, kSB * J, kSB * J + kSB, rg, cg);
+      for (int r = 0; r < 4; ++r)
+        for (int c4 = 0; c4 < C4; ++c4)
+          for (int e = 0; e < 4; ++e) {
+            const int i = 4 * rg + r, d = 4 * cg + 64 * c4 + e;
+            const float x = KB_EXP(sG[i * PG + d] - rr[J * DK + d]) * comp(t[r][c4], e);
+            if (pass == 0) {
+              comp(Pq[r][c4], e) += x;
+            } else {
+              comp(Pk[r][c4], e) += x;
+              comp(Pe[r][c4], e) += x;
+            }
+          }
+    }
+  }
+  KB_SYNC();
+  {
+    float4 qv[NK];
+    load_rows<DK, NT, T>(qv, qb, a.q.st, rows, tid);
+    for (int u = 0; u < NK; ++u) {
+      const int idx = tid + u * NT, i = idx / (DK / 4), p = idx - i * (DK / 4);
+      const float4 G = ld4(sG + i * PG + 4 * p), r1 = ld4(rr + (i / kSB + 1) * DK + 4 * p);
+      float4 x;
+      for (int e = 0; e < 4; ++e) comp(x, e) = comp(qv[u], e) * KB_EXP(comp(G, e) - comp(r1, e));
+      st4(sOp + i * PO + 4 * p, x);
+    }
+  }
+  KB_SYNC();
+  // column form at rows j: sum_{i in I} (M1_ij q_i + M2_ij k_i) e^{G_i - c_I}, times e^{c_I - G_j}
+  for (int I = Ib; I < 4; ++I) {
+    float4 t[4][C4];
+    zero_acc<DK>(t);
+    mm64_cols<DK>(t, sM1, PA, sOp, PO, kSB * I, kSB * I + kSB, rg, cg);
+    mm64_cols<DK>(t, sM2, PA, sOp2, PO, kSB * I, kSB * I + kSB, rg, cg);
+    for (int r = 0; r < 4; ++r)
+      for (int c4 = 0; c4 < C4; ++c4)
+        for (int e = 0; e < 4; ++e) {
+          const int j = 4 * rg + r, d = 4 * cg + 64 * c4 + e;
+          const float x = KB_EXP(rr[(I + 1) * DK + d] - sG[j * PG + d]) * comp(t[r][c4], e);
+          comp(Pk[r][c4], e) += x;
+          comp(Pe[r][c4], e) -= x;
+        }
+  }
+  KB_SYNC();
+  // dq, dk out; dG = (a - b - e) k + dq q into sOp
+  float4 qown[4][C4];
+  own(kown, kb, a.k.st);
+  own(qown, qb, a.q.st);
+  for (int r = 0; r < 4; ++r) {
+    const int i = 4 * rg + r;
+    for (int c4 = 0; c4 < C4; ++c4) {
+      float4 dg4;
+      for (int e = 0; e < 4; ++e)
+        comp(dg4, e) = comp(Pe[r][c4], e) * comp(kown[r][c4], e) + comp(Pq[r][c4], e) * comp(qown[r][c4], e);
+      st4(sOp + i * PO + 4 * cg + 64 * c4, dg4);
+      if (i < rows) {
+        const int64_t t = L.t + i;
+        st4(ba.dq.ptr + L.b * ba.dq.sb + t * ba.dq.st + (int64_t)h * ba.dq.sh + 4 * cg + 64 * c4, Pq[r][c4]);
+        st4(ba.dk.ptr + L.b * ba.dk.sb + t * ba.dk.st + (int64_t)h * ba.dk.sh + 4 * cg + 64 * c4, Pk[r][c4]);
+      }
+    }
+  }
+  KB_SYNC();
+  // dg: reverse cumulative sum down the chunk plus the G_C terms; dbeta
+  for (int d = tid; d < DK; d += NT) {
+    float run = KB_EXP(rr[4 * DK + d]) * s.gs[d];
+    for (int q = 0; q < 16; ++q) run += ek[q * DK + d];
+    for (int i = rows - 1; i >= 0; --i) {
+      run += sOp[i * PO + d];
+      ba.dg.ptr[L.b * ba.dg.sb + (L.t + i) * ba.dg.st + (int64_t)h * ba.dg.sh + d] = run;
+    }
+  }
+  for (int i = tid - (NT - kC); i >= 0 && i < rows; i += NT) {
+    float acc = 0.f;
+    for (int q = 0; q < s.nb; ++q) acc += s.dbp[i * s.pb + q];
+    ba.dbeta[L.b * ba.db_sb + (L.t + i) * ba.db_st + (int64_t)h * ba.db_sh] = acc;
+  }
+}
+
 template <int DK, int DV, typename T>
 KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   constexpr int NT = 256;
@@ -749,7 +927,6 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   if (!locate(ca, f, L)) return;  // uniform across the CTA
   const float* rec = ca.rec + ((int64_t)f * a.H + h) * R::SIZE;
   const float* stt = ca.st + ((int64_t)f * a.H + h) * R::SSIZE;
-  const T* qb = static_cast<const T*>(a.q.ptr) + L.b * a.q.sb + L.t * a.q.st + (int64_t)h * a.q.sh;
   const T* kb = static_cast<const T*>(a.k.ptr) + L.b * a.k.sb + L.t * a.k.st + (int64_t)h * a.k.sh;
   const T* vb = static_cast<const T*>(a.v.ptr) + L.b * a.v.sb + L.t * a.v.st + (int64_t)h * a.v.sh;
   const T* ob = static_cast<const T*>(ba.dout.ptr) + L.b * ba.dout.sb + L.t * ba.dout.st + (int64_t)h * ba.dout.sh;
@@ -764,14 +941,6 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   const float scale = a.scale;
   constexpr int NK = kC * DK / 4 / NT;  // 4-vectors of a [64][DK] tile per thread
   const int rg = tid / 16, cg = tid % 16;
-  // this thread's [4][DK / 64] 4-vectors (rows 4 rg.., columns 4 cg + 64 c4 ..) of k or q
-  auto own = [&](float4 (&x)[4][C4], const T* base, int64_t st) {
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-      for (int c4 = 0; c4 < C4; ++c4)
-        x[r][c4] = 4 * rg + r < rows ? ld4t<T>(base + (int64_t)(4 * rg + r) * st + 4 * cg + 64 * c4) : zero4();
-  };
 
   // 1. log-decays, beta, A; cumulative sums and the sub-block references
   {
@@ -912,12 +1081,10 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
       for (int v = 0; v < kW; ++v) gsum += sST[v * PK + d] * sXT[v * PK + d];
     KB_SYNC();
   }
-  // 6. M1 = scale Tril(dO U^T), M2 = -StrictTril(diag(beta) dY U^T); the direct
-  //    terms of dq, dk and dG; operands k e^{r - G} and k e^{G - c}
+  // 6. M1 = scale Tril(dO U^T), M2 = -StrictTril(diag(beta) dY U^T), the dbeta
+  //    partials and rowsum(S X); then the second half shared with the tensor-core kernel
   float* sM1 = sm + SM::M1;
   float* sM2 = sm + SM::M2;
-  float* sOp2 = sm + SM::OP2;
-  float* ek = sm + SM::EK;
   for (int r = 0; r < 4; ++r) {
     const int i = 4 * rg + r;
     sm[SM::DBP + i * SM::PB + cg] = dbp[r];
@@ -928,129 +1095,30 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
     }
   }
   for (int d = tid; d < DK; d += NT) sm[SM::GS + d] = gsum;
-  // after this block: Pq = dq, Pk = dk, Pe = (a - e) (the dG coefficient of k)
-  float4 kown[4][C4];
-  own(kown, kb, a.k.st);
-  for (int c4 = 0; c4 < C4; ++c4)
-    for (int e = 0; e < 4; ++e) {
-      const int d = 4 * cg + 64 * c4 + e;
-      float eks = 0.f;
-      for (int r = 0; r < 4; ++r) {
-        const int i = 4 * rg + r;
-        const float G = sG[i * PK + d];
-        const float E = KB_EXP(G), Ee = KB_EXP(rr[4 * DK + d] - G);
-        const float dq = scale * comp(Pq[r][c4], e) * E;
-        const float av = -sb[i] * comp(Pk[r][c4], e) * E;
-        const float ev = comp(Pe[r][c4], e) * Ee;
-        comp(Pq[r][c4], e) = dq;
-        comp(Pk[r][c4], e) = av + ev;
-        comp(Pe[r][c4], e) = av - ev;
-        eks += ev * comp(kown[r][c4], e);
-      }
-      ek[rg * DK + d] = eks;
-    }
-  {
-    float4 kv[NK];
-    load_rows<DK, NT, T>(kv, kb, a.k.st, rows, tid);
-    for (int u = 0; u < NK; ++u) {
-      const int idx = tid + u * NT, i = idx / (DK / 4), p = idx - i * (DK / 4), I = i / kSB;
-      const float4 G = ld4(sG + i * PK + 4 * p);
-      const float4 r0 = ld4(rr + I * DK + 4 * p), r1 = ld4(rr + (I + 1) * DK + 4 * p);
-      float4 x, y;
-      for (int e = 0; e < 4; ++e) {
-        comp(x, e) = comp(kv[u], e) * KB_EXP(comp(r0, e) - comp(G, e));
-        comp(y, e) = comp(kv[u], e) * KB_EXP(comp(G, e) - comp(r1, e));
-      }
-      st4(sOp + i * PK + 4 * p, x);
-      st4(sOp2 + i * PK + 4 * p, y);
-    }
-  }
-  KB_SYNC();
-  // 7. row form: sum_{j in J} M_ij (k_j e^{r_J - G_j}), times e^{G_i - r_J}
-  const int Ib = rg / 4;  // the sub-block of this thread's rows
-  for (int pass = 0; pass < 2; ++pass) {
-    const float* M = pass ? sM2 : sM1;
-    for (int J = 0; J <= Ib; ++J) {
-      float4 t[4][C4];
-      zero_acc<DK>(t);
-      mm64_rows<DK>(t, M, PA, sOp, PK, kSB * J, kSB * J + kSB, rg, cg);
-      for (int r = 0; r < 4; ++r)
-        for (int c4 = 0; c4 < C4; ++c4)
-          for (int e = 0; e < 4; ++e) {
-            const int i = 4 * rg + r, d = 4 * cg + 64 * c4 + e;
-            const float x = KB_EXP(sG[i * PK + d] - rr[J * DK + d]) * comp(t[r][c4], e);
-            if (pass == 0) {
-              comp(Pq[r][c4], e) += x;
-            } else {
-              comp(Pk[r][c4], e) += x;
-              comp(Pe[r][c4], e) += x;
-            }
-          }
-    }
-  }
-  KB_SYNC();
-  {
-    float4 qv[NK];
-    load_rows<DK, NT, T>(qv, qb, a.q.st, rows, tid);
-    for (int u = 0; u < NK; ++u) {
-      const int idx = tid + u * NT, i = idx / (DK / 4), p = idx - i * (DK / 4);
-      const float4 G = ld4(sG + i * PK + 4 * p), r1 = ld4(rr + (i / kSB + 1) * DK + 4 * p);
-      float4 x;
-      for (int e = 0; e < 4; ++e) comp(x, e) = comp(qv[u], e) * KB_EXP(comp(G, e) - comp(r1, e));
-      st4(sOp + i * PK + 4 * p, x);
-    }
-  }
-  KB_SYNC();
-  // 8. column form at rows j: sum_{i in I} (M1_ij q_i + M2_ij k_i) e^{G_i - c_I}, times e^{c_I - G_j}
-  for (int I = Ib; I < 4; ++I) {
-    float4 t[4][C4];
-    zero_acc<DK>(t);
-    mm64_cols<DK>(t, sM1, PA, sOp, PK, kSB * I, kSB * I + kSB, rg, cg);
-    mm64_cols<DK>(t, sM2, PA, sOp2, PK, kSB * I, kSB * I + kSB, rg, cg);
-    for (int r = 0; r < 4; ++r)
-      for (int c4 = 0; c4 < C4; ++c4)
-        for (int e = 0; e < 4; ++e) {
-          const int j = 4 * rg + r, d = 4 * cg + 64 * c4 + e;
-          const float x = KB_EXP(rr[(I + 1) * DK + d] - sG[j * PK + d]) * comp(t[r][c4], e);
-          comp(Pk[r][c4], e) += x;
-          comp(Pe[r][c4], e) -= x;
-        }
-  }
-  KB_SYNC();
-  // 9. dq, dk out; dG = (a - b - e) k + dq q into sOp
-  float4 qown[4][C4];
-  own(kown, kb, a.k.st);
-  own(qown, qb, a.q.st);
-  for (int r = 0; r < 4; ++r) {
-    const int i = 4 * rg + r;
-    for (int c4 = 0; c4 < C4; ++c4) {
-      float4 dg4;
-      for (int e = 0; e < 4; ++e)
-        comp(dg4, e) = comp(Pe[r][c4], e) * comp(kown[r][c4], e) + comp(Pq[r][c4], e) * comp(qown[r][c4], e);
-      st4(sOp + i * PK + 4 * cg + 64 * c4, dg4);
-      if (i < rows) {
-        const int64_t t = L.t + i;
-        st4(ba.dq.ptr + L.b * ba.dq.sb + t * ba.dq.st + (int64_t)h * ba.dq.sh + 4 * cg + 64 * c4, Pq[r][c4]);
-        st4(ba.dk.ptr + L.b * ba.dk.sb + t * ba.dk.st + (int64_t)h * ba.dk.sh + 4 * cg + 64 * c4, Pk[r][c4]);
-      }
-    }
-  }
-  KB_SYNC();
-  // 10. dg: reverse cumulative sum down the chunk plus the G_C terms; dbeta
-  for (int d = tid; d < DK; d += NT) {
-    float run = KB_EXP(rr[4 * DK + d]) * sm[SM::GS + d];
-    for (int q = 0; q < 16; ++q) run += ek[q * DK + d];
-    for (int i = rows - 1; i >= 0; --i) {
-      run += sOp[i * PK + d];
-      ba.dg.ptr[L.b * ba.dg.sb + (L.t + i) * ba.dg.st + (int64_t)h * ba.dg.sh + d] = run;
-    }
-  }
-  for (int i = tid - (NT - kC); i >= 0 && i < rows; i += NT) {
-    float s = 0.f;
-    for (int q = 0; q < 16; ++q) s += sm[SM::DBP + i * SM::PB + q];
-    ba.dbeta[L.b * ba.db_sb + (L.t + i) * ba.db_st + (int64_t)h * ba.db_sh] = s;
-  }
+  TailSmem ts;
+  ts.G = sG;
+  ts.rr = rr;
+  ts.beta = sb;
+  ts.M1 = sM1;
+  ts.M2 = sM2;
+  ts.op = sOp;
+  ts.op2 = sm + SM::OP2;
+  ts.ek = sm + SM::EK;
+  ts.dbp = sm + SM::DBP;
+  ts.gs = sm + SM::GS;
+  ts.pg = PK;
+  ts.pm = PA;
+  ts.po = PK;
+  ts.pb = SM::PB;
+  ts.nb = 16;
+  grad_tail<DK, DV, T, false>(ca, L, h, ts, Pq, Pk, Pe, tid);
 }
 
 }  // namespace bwdc
+
+// The gradient kernel with its dense products on the tensor cores
+// (kda_backward_tc.cu): d_k = d_v = 128 with bf16 inputs.
+bool chunk_grad_tc_supported(const PrefillArgs& a);
+cudaError_t launch_chunk_grad_tc(const bwdc::ChunkBwdArgs& ca, cudaStream_t s);
+
 }  // namespace kda

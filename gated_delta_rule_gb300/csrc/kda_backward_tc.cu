@@ -1,0 +1,600 @@
+// Chunked backward of the KDA core: the gradient kernel on the tensor cores
+// (d_k = d_v = 128, bf16 inputs).
+//
+// Per (chunk, head) the kernel follows the derivation in kda_backward_chunk.cuh.
+// Every contraction runs as tcgen05.mma with fp32 accumulators in tensor memory:
+//
+//   D1 = S [dO; dY]^T     lanes d, columns (i of dO | i of dY): (dO S^T)^T, (dY S^T)^T
+//   D2 = X U^T            lanes d, columns i: (U X^T)^T
+//   D3 = [dO; dY] U^T     lanes (i of dO | i of dY), columns j: dO U^T, dY U^T
+//   R1, R2                lanes d, columns i: the row forms inside the chunk,
+//                         sum_{j <= i} M_ij k_j e^{G_i - G_j} for M = M1, M2
+//   CF_I                  lanes d, columns j: the column form of sub-block I,
+//                         sum_{i in I} (M1_ij q_i + M2_ij k_i) e^{G_i - c_I}
+//
+// with M1 = scale Tril(dO U^T), M2 = -StrictTril(diag(beta) dY U^T).  With the
+// key channel d on the 128 lanes all products have M = 128.  The exponent
+// references of the intra-chunk forms are those of 16-token sub-blocks (g in
+// [-5, 0] keeps every factor within e^{+-80}): the row form of rows in sub-block I
+// uses k_j e^{r_I - G_j} for j < 16 (I + 1) (one operand version per I, at most 1 for
+// earlier sub-blocks), the column form refers row i to the end c_I of its own
+// sub-block, and one factor per output element restores the exponent.
+//
+// S, X, U, dY, M1, M2 and the exponent-scaled q and k are fp32, so each operand is
+// split into bf16 halves x = x_hi + x_lo (x_hi = bf16(x), x_lo = bf16(x - x_hi)) and
+// a product is taken as a_hi b_hi + a_lo b_hi + a_hi b_lo: three bf16 MMAs with a
+// relative error near 2^-16.  q, k, v and dO are bf16 already.
+//
+// dbeta needs no product of its own:
+//   dbeta_i = sum_v dY (V - K+ S - A U) = rowdot(dY, V) - rowdot(K+, dY S^T) - rowdot(A, dY U^T).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kda_backward_chunk.cuh"
+#include "kda_sm100.cuh"
+
+namespace kda {
+namespace {
+
+using namespace sm100;
+using bwdc::ChunkBwdArgs;
+using bwdc::kC;
+using bwdc::kSB;
+using bwdc::ld4;
+using bwdc::ld4t;
+using bwdc::st4;
+using bwdc::zero4;
+
+constexpr int kTcThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+// tensor-memory columns: D3 is read before R1 is written over it
+constexpr uint32_t kD1 = 0, kD2 = 128, kD3 = 192, kR1 = 192, kR2 = 256, kCF = 320;
+// first column of CF_I (16 (I + 1) columns each)
+__device__ __forceinline__ uint32_t cf_col(int I) { return kCF + 8u * (uint32_t)(I * (I + 1)); }
+
+// Byte offsets in the 1024-byte aligned dynamic shared memory.
+struct GradTcSmem {
+  // first products: bf16 tiles, 128-byte swizzle, 128 rows x K = 128 (two 16 KB panels)
+  static constexpr uint32_t TS = 0;         // S hi, then X hi
+  static constexpr uint32_t TS_LO = 32768;  // S lo, then X lo
+  static constexpr uint32_t TB = 65536;     // [dO; dY hi]
+  static constexpr uint32_t TL = 98304;     // [0; dY lo]
+  static constexpr uint32_t TU = 131072;    // [U hi; U lo]
+  static constexpr uint32_t OPS = 163840;
+  // intra-chunk forms
+  static constexpr uint32_t M1_HI = TL, M1_LO = TL + 8192;  // 64 x 64 bf16 (rows i, columns j)
+  static constexpr uint32_t M2_HI = TL + 16384, M2_LO = TL + 24576;
+  // k e^{r_I - G}: version I, 16 (I + 1) rows x 128 (kr_hi / kr_lo)
+  static constexpr uint32_t QC_HI = 0, QC_LO = 16384, KC_HI = 32768, KC_LO = 49152;  // 64 rows x 128
+  static constexpr uint32_t KRAW = TB, QRAW = TB + 16384;  // k, q of the chunk: [64][128] bf16 rows
+  static constexpr uint32_t DG = 0;  // [64][128] fp32 dG
+  // kept throughout
+  static constexpr uint32_t G = OPS;                  // [64][128] fp32 cumulative log-decay
+  static constexpr uint32_t RR = G + 64 * 128 * 4;    // [5][128] r_0..r_3, G_C (c_I = r_{I+1})
+  static constexpr uint32_t BETA = RR + 5 * 128 * 4;  // [64]
+  static constexpr uint32_t GS = BETA + 64 * 4;       // [128] rowsum(S X)
+  static constexpr int PB = 8;                        // dbeta partials per row (7 used)
+  static constexpr uint32_t DBP = GS + 128 * 4;       // [64][PB]
+  static constexpr uint32_t EKP = DBP + 64 * PB * 4;  // [2][128] sums of e k over half the rows
+  static constexpr uint32_t MBAR = EKP + 2 * 128 * 4; // four mbarriers
+  static constexpr uint32_t SLOT = MBAR + 32;         // tensor-memory base address
+  static constexpr uint32_t FLAG = SLOT + 4;          // a bounded wait gave up
+  static constexpr uint32_t BYTES = SLOT + 16;
+};
+// Version I of k e^{r_I - G} (4096 (I + 1) bytes per half): the high halves fill
+// [0, 40960), the low halves of versions 0..2 [40960, 65536) and that of version 3
+// the U tile.  All are written after D2 has read the X and U tiles.
+__device__ __forceinline__ uint32_t kr_hi(int I) { return 2048u * (uint32_t)(I * (I + 1)); }
+__device__ __forceinline__ uint32_t kr_lo(int I) { return I < 3 ? 40960u + kr_hi(I) : GradTcSmem::TU; }
+static_assert(GradTcSmem::KRAW >= 65536 && GradTcSmem::QRAW + 16384 <= GradTcSmem::M1_HI, "raw k, q between");
+// dbeta partials of a row: [0, 4) -rowdot(K+, dY S^T) by lane quarter, [4, 6)
+// -rowdot(A, dY U^T) by column half, [6] rowdot(dY, V)
+constexpr int kDbAY = 4, kDbYV = 6, kDbCount = 7;
+
+__device__ __forceinline__ uint32_t bf2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float bflo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bfhi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// x = hi + lo for a pair: returns hi, sets lo
+__device__ __forceinline__ uint32_t split2(float a, float b, uint32_t& lo) {
+  const uint32_t h = bf2(a, b);
+  lo = bf2(a - bflo(h), b - bfhi(h));
+  return h;
+}
+
+// hi and lo quadruples of x, stored 8 bytes each
+__device__ __forceinline__ void store_split4(uint32_t hi_addr, uint32_t lo_addr, float4 x) {
+  uint32_t l0, l1;
+  const uint32_t h0 = split2(x.x, x.y, l0), h1 = split2(x.z, x.w, l1);
+  asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(hi_addr), "r"(h0), "r"(h1) : "memory");
+  asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(lo_addr), "r"(l0), "r"(l1) : "memory");
+}
+
+// the four values hi + lo stored by store_split4 at these addresses
+__device__ __forceinline__ float4 load_split4(uint32_t hi_addr, uint32_t lo_addr) {
+  uint32_t h0, h1, l0, l1;
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(h0), "=r"(h1) : "r"(hi_addr) : "memory");
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(l0), "=r"(l1) : "r"(lo_addr) : "memory");
+  float4 r;
+  r.x = bflo(h0) + bflo(l0);
+  r.y = bfhi(h0) + bfhi(l0);
+  r.z = bflo(h1) + bflo(l1);
+  r.w = bfhi(h1) + bfhi(l1);
+  return r;
+}
+
+// eight bf16 at a 16-byte aligned shared address, as fp32
+__device__ __forceinline__ void bf8(uint32_t addr, float (&x)[8]) {
+  uint32_t u0, u1, u2, u3;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(u0), "=r"(u1), "=r"(u2), "=r"(u3) : "r"(addr) : "memory");
+  x[0] = bflo(u0), x[1] = bfhi(u0), x[2] = bflo(u1), x[3] = bfhi(u1);
+  x[4] = bflo(u2), x[5] = bfhi(u2), x[6] = bflo(u3), x[7] = bfhi(u3);
+}
+
+// 8-byte global -> shared copy, zero-filled when src_bytes == 0
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// Sums v[r] over the 32 lanes for eight r at once (a transposing butterfly, nine
+// shuffles); returns the sum for r = 4 bit4 + 2 bit3 + bit2 of the lane index.
+__device__ __forceinline__ float reduce8(const float (&v)[8], int lane) {
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float w4[4], w2[2];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    w4[k] = (b4 ? v[k + 4] : v[k]) + __shfl_xor_sync(0xffffffffu, b4 ? v[k] : v[k + 4], 16);
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+    w2[k] = (b3 ? w4[k + 2] : w4[k]) + __shfl_xor_sync(0xffffffffu, b3 ? w4[k] : w4[k + 2], 8);
+  float w = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+  w += __shfl_xor_sync(0xffffffffu, w, 2);
+  w += __shfl_xor_sync(0xffffffffu, w, 1);
+  return w;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// K = 128 (eight 16-deep steps) of one K-major product into the accumulator at d_tmem
+__device__ __forceinline__ void mma_k128(uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile, int b_row0,
+                                         uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks)
+    mma_bf16(d_tmem, desc_kmajor(a_tile, 128, ks), desc_kmajor(b_tile, 128, ks, b_row0), idesc,
+             (accumulate || ks > 0) ? 1u : 0u);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_grad_tc_kernel(ChunkBwdArgs ca) {
+  constexpr int DK = 128, DV = 128, NT = kTcThreads;
+  using SM = GradTcSmem;
+  using R = bwdc::Rec<DK, DV>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s0 = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int f = blockIdx.x, h = blockIdx.y;
+  const BackwardArgs& ba = ca.b;
+  const PrefillArgs& a = ba.f;
+  bwdc::ChunkLoc L;
+  if (!bwdc::locate(ca, f, L)) return;  // uniform across the CTA
+  const int rows = L.rows;
+  const float* rec = ca.rec + ((int64_t)f * a.H + h) * R::SIZE;
+  const float* stt = ca.st + ((int64_t)f * a.H + h) * R::SSIZE;
+  const T* ob = static_cast<const T*>(ba.dout.ptr) + L.b * ba.dout.sb + L.t * ba.dout.st + (int64_t)h * ba.dout.sh;
+  const T* vb = static_cast<const T*>(a.v.ptr) + L.b * a.v.sb + L.t * a.v.st + (int64_t)h * a.v.sh;
+  const T* qb = static_cast<const T*>(a.q.ptr) + L.b * a.q.sb + L.t * a.q.st + (int64_t)h * a.q.sh;
+  const T* kb = static_cast<const T*>(a.k.ptr) + L.b * a.k.sb + L.t * a.k.st + (int64_t)h * a.k.sh;
+  const float* gb = static_cast<const float*>(a.g.ptr) + L.b * a.g.sb + L.t * a.g.st + (int64_t)h * a.g.sh;
+  const float* bb = a.beta + L.b * a.beta_sb + L.t * a.beta_st + (int64_t)h * a.beta_sh;
+  float* sG = reinterpret_cast<float*>(smem + SM::G);
+  float* rr = reinterpret_cast<float*>(smem + SM::RR);
+  float* sb = reinterpret_cast<float*>(smem + SM::BETA);
+  float* gs = reinterpret_cast<float*>(smem + SM::GS);
+  float* dbp = reinterpret_cast<float*>(smem + SM::DBP);
+  float* ekp = reinterpret_cast<float*>(smem + SM::EKP);
+  volatile int* sFlag = reinterpret_cast<volatile int*>(smem + SM::FLAG);
+  const uint32_t mbar1 = s0 + SM::MBAR, mbar2 = mbar1 + 8, mbar3 = mbar1 + 16, mbar4 = mbar1 + 24;
+  const int q4 = warp & 3, half = warp >> 2;  // lane quarter and column (or row) half of this warp
+  const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+
+  if (warp == 0) tmem_alloc(s0 + SM::SLOT, kTmemCols);
+  if (tid == 0) {
+    mbar_init(mbar1, 1);
+    mbar_init(mbar2, 1);
+    mbar_init(mbar3, 1);
+    mbar_init(mbar4, 1);
+    *sFlag = 0;
+    fence_mbar_init();
+  }
+
+  // ---- operand tiles of the first products ----
+  // S -> TS (hi), TS_LO (lo): row d = warp + 8 u, columns 4 lane ..
+  {
+    float4 x[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) x[u] = ld4(stt + R::S + (int64_t)(warp + 8 * u) * DV + 4 * lane);
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const uint32_t o = sw128(warp + 8 * u, 4 * lane, 128);
+      store_split4(s0 + SM::TS + o, s0 + SM::TS_LO + o, x[u]);
+    }
+  }
+  // dY -> TB rows 64.. (hi), TL rows 64.. (lo); U -> TU rows 0.. (hi), 64.. (lo);
+  // rowdot(dY, V); dO -> TB rows 0..; zeros in TL rows 0..63
+  {
+    float4 y[8], uu[8], vv[8];
+    uint2 o2[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = warp + 8 * u;
+      y[u] = ld4(stt + R::DY + (int64_t)i * DV + 4 * lane);
+      uu[u] = ld4(stt + R::U + (int64_t)i * DV + 4 * lane);
+      vv[u] = i < rows ? ld4t<T>(vb + (int64_t)i * a.v.st + 4 * lane) : zero4();
+      o2[u] = i < rows ? *reinterpret_cast<const uint2*>(ob + (int64_t)i * ba.dout.st + 4 * lane) : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = warp + 8 * u;
+      store_split4(s0 + SM::TB + sw128(64 + i, 4 * lane, 128), s0 + SM::TL + sw128(64 + i, 4 * lane, 128), y[u]);
+      store_split4(s0 + SM::TU + sw128(i, 4 * lane, 128), s0 + SM::TU + sw128(64 + i, 4 * lane, 128), uu[u]);
+      asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(s0 + SM::TB + sw128(i, 4 * lane, 128)), "r"(o2[u].x),
+                   "r"(o2[u].y)
+                   : "memory");
+      const float yv = warp_sum(y[u].x * vv[u].x + y[u].y * vv[u].y + y[u].z * vv[u].z + y[u].w * vv[u].w);
+      if (lane == 0) dbp[i * SM::PB + kDbYV] = yv;
+    }
+    for (int idx = tid; idx < 1024; idx += NT)  // rows 0..63 of both panels
+      st_shared_v4(s0 + SM::TL + (uint32_t)(idx >> 9) * 16384u + (uint32_t)(idx & 511) * 16u, 0u, 0u, 0u, 0u);
+  }
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM::SLOT);
+  if (tid == 0) {
+    const uint32_t i128 = idesc_bf16(128, 128, false, false), i64 = idesc_bf16(128, 64, false, false);
+    // D1 = S [dO; dY]^T;  D3 = [dO; dY] U^T
+    mma_k128(tmem + kD1, s0 + SM::TS, s0 + SM::TB, 0, i128, false);
+    mma_k128(tmem + kD1, s0 + SM::TS_LO, s0 + SM::TB, 0, i128, true);
+    mma_k128(tmem + kD1 + 64, s0 + SM::TS, s0 + SM::TL, 64, i64, true);
+    mma_k128(tmem + kD3, s0 + SM::TB, s0 + SM::TU, 0, i64, false);
+    mma_k128(tmem + kD3, s0 + SM::TB, s0 + SM::TU, 64, i64, true);
+    mma_k128(tmem + kD3, s0 + SM::TL, s0 + SM::TU, 0, i64, true);
+    mma_commit(mbar1);
+  }
+
+  // ---- while they run: log-decays, beta, the sub-block references; X ----
+  {
+    constexpr int NK = kC * DK / 4 / NT;
+    float4 gv[NK];
+    bwdc::load_rows<DK, NT, float>(gv, gb, a.g.st, rows, tid);
+#pragma unroll
+    for (int u = 0; u < NK; ++u) {
+      const int idx = tid + u * NT, i = idx / (DK / 4), p = idx - i * (DK / 4);
+      st4(sG + i * DK + 4 * p, gv[u]);
+    }
+  }
+  if (tid < kC) sb[tid] = tid < rows ? bb[(int64_t)tid * a.beta_st] : 0.f;
+  float4 x[16];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) x[u] = ld4(stt + R::X + (int64_t)(warp + 8 * u) * DV + 4 * lane);
+  __syncthreads();
+  if (tid < DK) {
+    const int d = tid;
+    float run = 0.f;
+    rr[d] = 0.f;
+    for (int i = 0; i < kC; ++i) {
+      run += sG[i * DK + d];
+      sG[i * DK + d] = run;
+      if ((i & (kSB - 1)) == kSB - 1) rr[((i + 1) / kSB) * DK + d] = run;
+    }
+  }
+  if (!mbar_wait(mbar1, 0)) *sFlag = 1;
+  __syncthreads();
+  if (*sFlag) goto fail;
+  fence_after_sync();
+  // raw k and q rows of the chunk (zero past the last row), landing while X is split
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int idx = tid + u * NT, i = idx >> 5, c = idx & 31;
+    const int ic = i < rows ? i : 0;
+    const uint32_t o = (uint32_t)(i * 256 + 8 * c), n = i < rows ? 8u : 0u;
+    cp_async8(s0 + SM::KRAW + o, kb + (int64_t)ic * a.k.st + 4 * c, n);
+    cp_async8(s0 + SM::QRAW + o, qb + (int64_t)ic * a.q.st + 4 * c, n);
+  }
+  cp_async_commit();
+
+  // ---- X -> TS, TS_LO (S is read back from its tiles for rowsum(S X) first); D2 ----
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const int d = warp + 8 * u;
+    const uint32_t o = sw128(d, 4 * lane, 128);
+    const float4 sv = load_split4(s0 + SM::TS + o, s0 + SM::TS_LO + o);
+    const float p = warp_sum(sv.x * x[u].x + sv.y * x[u].y + sv.z * x[u].z + sv.w * x[u].w);
+    if (lane == 0) gs[d] = p;
+    store_split4(s0 + SM::TS + o, s0 + SM::TS_LO + o, x[u]);
+  }
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  if (tid == 0) {
+    fence_after_sync();
+    const uint32_t i64 = idesc_bf16(128, 64, false, false);
+    // D2 = X U^T
+    mma_k128(tmem + kD2, s0 + SM::TS, s0 + SM::TU, 0, i64, false);
+    mma_k128(tmem + kD2, s0 + SM::TS_LO, s0 + SM::TU, 0, i64, true);
+    mma_k128(tmem + kD2, s0 + SM::TS, s0 + SM::TU, 64, i64, true);
+    mma_commit(mbar2);
+  }
+
+  // ---- D3 -> M1 = scale Tril(dO U^T), M2 = -StrictTril(diag(beta) dY U^T) as bf16
+  //      halves (rows i, columns j) over TL; -rowdot(A, dY U^T) ----
+  {
+    float v[32];
+    tmem_ld32(tmem + lane_base + kD3 + 32 * half, v);
+    const int ip = 32 * q4 + lane, j0 = 32 * half;
+    const bool m2 = ip >= kC;
+    const int i = m2 ? ip - kC : ip;
+    const float be = sb[i];
+    float ay = 0.f;
+    if (m2) {
+      const float* arow = rec + R::A + i * kC + j0;
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        const float4 av = ld4(arow + k);
+        ay += av.x * v[k] + av.y * v[k + 1] + av.z * v[k + 2] + av.w * v[k + 3];
+      }
+      dbp[i * SM::PB + kDbAY + half] = -ay;
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int j = j0 + k;
+      v[k] = m2 ? (j < i ? -be * v[k] : 0.f) : (j <= i ? a.scale * v[k] : 0.f);
+    }
+    const uint32_t hi = s0 + (m2 ? SM::M2_HI : SM::M1_HI), lo = s0 + (m2 ? SM::M2_LO : SM::M1_LO);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t ph[4], pl[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ph[e] = split2(v[8 * c + 2 * e], v[8 * c + 2 * e + 1], pl[e]);
+      const uint32_t o = sw128(i, j0 + 8 * c, 64);
+      st_shared_v4(hi + o, ph[0], ph[1], ph[2], ph[3]);
+      st_shared_v4(lo + o, pl[0], pl[1], pl[2], pl[3]);
+    }
+  }
+  if (!mbar_wait(mbar2, 0)) *sFlag = 1;
+  cp_async_wait_all();
+  fence_before_sync();
+  __syncthreads();
+  if (*sFlag) goto fail;
+
+  // ---- row-form operand: version I of k e^{r_I - G}, rows j < 16 (I + 1), as an
+  //      MN-major tile (K rows j, M = d) ----
+  for (int idx = tid; idx < 2560; idx += NT) {
+    const int I = idx < 256 ? 0 : idx < 768 ? 1 : idx < 1536 ? 2 : 3;
+    const int rem = idx - 128 * I * (I + 1), j = rem >> 4, d0 = 8 * (rem & 15);
+    float kv[8];
+    bf8(s0 + SM::KRAW + j * 256 + 2 * d0, kv);
+    const float4 g0 = ld4(sG + j * DK + d0), g1 = ld4(sG + j * DK + d0 + 4);
+    const float4 r0 = ld4(rr + I * DK + d0), r1 = ld4(rr + I * DK + d0 + 4);
+    const float y[8] = {kv[0] * __expf(r0.x - g0.x), kv[1] * __expf(r0.y - g0.y), kv[2] * __expf(r0.z - g0.z),
+                        kv[3] * __expf(r0.w - g0.w), kv[4] * __expf(r1.x - g1.x), kv[5] * __expf(r1.y - g1.y),
+                        kv[6] * __expf(r1.z - g1.z), kv[7] * __expf(r1.w - g1.w)};
+    uint32_t ph[4], pl[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) ph[e] = split2(y[2 * e], y[2 * e + 1], pl[e]);
+    const uint32_t o = sw128(j, d0, kSB * (I + 1));
+    st_shared_v4(s0 + kr_hi(I) + o, ph[0], ph[1], ph[2], ph[3]);
+    st_shared_v4(s0 + kr_lo(I) + o, pl[0], pl[1], pl[2], pl[3]);
+  }
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  if (tid == 0) {
+    fence_after_sync();
+    // R1, R2 at rows (columns) of sub-block I: sum over j < 16 (I + 1)
+    const uint32_t idesc = idesc_bf16(128, 16, true, false);
+    for (int I = 0; I < 4; ++I) {
+      const int kr = kSB * (I + 1);
+      for (int m = 0; m < 2; ++m) {
+        const uint32_t d = tmem + (m ? kR2 : kR1) + kSB * I;
+        const uint32_t bh = s0 + (m ? SM::M2_HI : SM::M1_HI), bl = s0 + (m ? SM::M2_LO : SM::M1_LO);
+        for (int ks = 0; ks <= I; ++ks) {
+          const uint64_t ah = desc_mnmajor(s0 + kr_hi(I), kr, ks);
+          const uint64_t al = desc_mnmajor(s0 + kr_lo(I), kr, ks);
+          const uint64_t bhd = desc_kmajor(bh, 64, ks, kSB * I), bld = desc_kmajor(bl, 64, ks, kSB * I);
+          mma_bf16(d, ah, bhd, idesc, ks > 0 ? 1u : 0u);
+          mma_bf16(d, al, bhd, idesc, 1u);
+          mma_bf16(d, ah, bld, idesc, 1u);
+        }
+      }
+    }
+    mma_commit(mbar3);
+  }
+
+  // ---- column-form operands q e^{G - c_I}, k e^{G - c_I} (row i in sub-block I),
+  //      formed while the row forms run and stored once they are done ----
+  {
+    uint32_t qh[4][4], ql[4][4], kh[4][4], kl[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = tid + u * NT, i = idx >> 4, d0 = 8 * (idx & 15), I = i / kSB;
+      float qv[8], kv[8];
+      bf8(s0 + SM::QRAW + i * 256 + 2 * d0, qv);
+      bf8(s0 + SM::KRAW + i * 256 + 2 * d0, kv);
+      const float4 g0 = ld4(sG + i * DK + d0), g1 = ld4(sG + i * DK + d0 + 4);
+      const float4 c0 = ld4(rr + (I + 1) * DK + d0), c1 = ld4(rr + (I + 1) * DK + d0 + 4);
+      const float ex[8] = {__expf(g0.x - c0.x), __expf(g0.y - c0.y), __expf(g0.z - c0.z), __expf(g0.w - c0.w),
+                           __expf(g1.x - c1.x), __expf(g1.y - c1.y), __expf(g1.z - c1.z), __expf(g1.w - c1.w)};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        qh[u][e] = split2(qv[2 * e] * ex[2 * e], qv[2 * e + 1] * ex[2 * e + 1], ql[u][e]);
+        kh[u][e] = split2(kv[2 * e] * ex[2 * e], kv[2 * e + 1] * ex[2 * e + 1], kl[u][e]);
+      }
+    }
+    if (!mbar_wait(mbar3, 0)) *sFlag = 1;
+    __syncthreads();
+    if (*sFlag) goto fail;
+    fence_after_sync();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = tid + u * NT, i = idx >> 4, d0 = 8 * (idx & 15);
+      const uint32_t o = sw128(i, d0, kC);
+      st_shared_v4(s0 + SM::QC_HI + o, qh[u][0], qh[u][1], qh[u][2], qh[u][3]);
+      st_shared_v4(s0 + SM::QC_LO + o, ql[u][0], ql[u][1], ql[u][2], ql[u][3]);
+      st_shared_v4(s0 + SM::KC_HI + o, kh[u][0], kh[u][1], kh[u][2], kh[u][3]);
+      st_shared_v4(s0 + SM::KC_LO + o, kl[u][0], kl[u][1], kl[u][2], kl[u][3]);
+    }
+  }
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  if (tid == 0) {
+    fence_after_sync();
+    // CF_I: columns j < 16 (I + 1), sum over i in sub-block I
+    for (int I = 0; I < 4; ++I) {
+      const uint32_t idesc = idesc_bf16(128, kSB * (I + 1), true, true);
+      const uint32_t d = tmem + cf_col(I);
+      const uint64_t qhd = desc_mnmajor(s0 + SM::QC_HI, kC, I), qld = desc_mnmajor(s0 + SM::QC_LO, kC, I);
+      const uint64_t khd = desc_mnmajor(s0 + SM::KC_HI, kC, I), kld = desc_mnmajor(s0 + SM::KC_LO, kC, I);
+      const uint64_t m1h = desc_mnmajor(s0 + SM::M1_HI, kC, I), m1l = desc_mnmajor(s0 + SM::M1_LO, kC, I);
+      const uint64_t m2h = desc_mnmajor(s0 + SM::M2_HI, kC, I), m2l = desc_mnmajor(s0 + SM::M2_LO, kC, I);
+      mma_bf16(d, qhd, m1h, idesc, 0u);
+      mma_bf16(d, qld, m1h, idesc, 1u);
+      mma_bf16(d, qhd, m1l, idesc, 1u);
+      mma_bf16(d, khd, m2h, idesc, 1u);
+      mma_bf16(d, kld, m2h, idesc, 1u);
+      mma_bf16(d, khd, m2l, idesc, 1u);
+    }
+    mma_commit(mbar4);
+  }
+  if (!mbar_wait(mbar4, 0)) *sFlag = 1;
+  __syncthreads();
+  if (*sFlag) goto fail;
+  fence_after_sync();
+
+  // ---- per (i, d): dq, dk and dG (lanes d, rows of this warp's half) ----
+  //   E = e^{G} = e^{G - r_J} e^{r_J},  e^{G_C - G} = e^{c_J - G} e^{G_C - c_J},
+  //   e^{c_I - G} = e^{c_J - G} e^{c_I - c_J}: two exponentials per element
+  {
+    const int d = 32 * q4 + lane;
+    const __nv_bfloat16* sk = reinterpret_cast<const __nv_bfloat16*>(smem + SM::KRAW);
+    const __nv_bfloat16* sq = reinterpret_cast<const __nv_bfloat16*>(smem + SM::QRAW);
+    float* sDG = reinterpret_cast<float*>(smem + SM::DG);
+    float ek = 0.f;
+#pragma unroll 1
+    for (int g8 = 0; g8 < 4; ++g8) {
+      const int i0 = 32 * half + 8 * g8, J = i0 / kSB;
+      const float rJ = rr[J * DK + d], cJ = rr[(J + 1) * DK + d];
+      const float eR = __expf(rJ);
+      float rho[4];  // e^{c_I - c_J}, zero for I < J
+#pragma unroll
+      for (int I = 0; I < 4; ++I) rho[I] = I >= J ? __expf(rr[(I + 1) * DK + d] - cJ) : 0.f;
+      uint32_t pq[8], pk[8], pe[8], r1[8], r2[8], cf[4][8];
+      tmem_ld8_async(tmem + lane_base + kD1 + i0, pq);
+      tmem_ld8_async(tmem + lane_base + kD1 + 64 + i0, pk);
+      tmem_ld8_async(tmem + lane_base + kD2 + i0, pe);
+      tmem_ld8_async(tmem + lane_base + kR1 + i0, r1);
+      tmem_ld8_async(tmem + lane_base + kR2 + i0, r2);
+#pragma unroll
+      for (int I = 0; I < 4; ++I) tmem_ld8_async(tmem + lane_base + cf_col(I) + i0, cf[I]);
+      tmem_wait_ld();
+      float kp[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = i0 + e;
+        const float G = sG[i * DK + d];
+        const float fr = __expf(G - rJ), fc = __expf(cJ - G);
+        const float E = fr * eR, Ee = fc * rho[3];
+        float cs = 0.f;
+#pragma unroll
+        for (int I = 0; I < 4; ++I) cs += rho[I] * __uint_as_float(cf[I][e]);
+        const float b = fc * cs;
+        const float kv = __bfloat162float(sk[i * DK + d]), qv = __bfloat162float(sq[i * DK + d]);
+        const float pkv = __uint_as_float(pk[e]);
+        const float dq = a.scale * __uint_as_float(pq[e]) * E + fr * __uint_as_float(r1[e]);
+        const float av = -sb[i] * pkv * E + fr * __uint_as_float(r2[e]);
+        const float ev = __uint_as_float(pe[e]) * Ee;
+        sDG[i * DK + d] = (av - b - ev) * kv + dq * qv;
+        ek += ev * kv;
+        kp[e] = kv * E * pkv;
+        if (i < rows) {
+          const int64_t t = L.t + i;
+          ba.dq.ptr[L.b * ba.dq.sb + t * ba.dq.st + (int64_t)h * ba.dq.sh + d] = dq;
+          ba.dk.ptr[L.b * ba.dk.sb + t * ba.dk.st + (int64_t)h * ba.dk.sh + d] = av + b + ev;
+        }
+      }
+      const float w = reduce8(kp, lane);
+      if ((lane & 3) == 0) dbp[(i0 + (lane >> 2)) * SM::PB + q4] = -w;
+    }
+    ekp[half * DK + d] = ek;
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  // ---- dg: reverse cumulative sum down the chunk plus the G_C terms; dbeta ----
+  if (tid < DK) {
+    const int d = tid;
+    const float* sDG = reinterpret_cast<const float*>(smem + SM::DG);
+    float run = __expf(rr[4 * DK + d]) * gs[d] + ekp[d] + ekp[DK + d];
+    for (int i = rows - 1; i >= 0; --i) {
+      run += sDG[i * DK + d];
+      ba.dg.ptr[L.b * ba.dg.sb + (L.t + i) * ba.dg.st + (int64_t)h * ba.dg.sh + d] = run;
+    }
+  } else if (tid - DK < rows) {
+    const int i = tid - DK;
+    float acc = 0.f;
+#pragma unroll
+    for (int q = 0; q < kDbCount; ++q) acc += dbp[i * SM::PB + q];
+    ba.dbeta[L.b * ba.db_sb + (L.t + i) * ba.db_st + (int64_t)h * ba.db_sh] = acc;
+  }
+  return;
+
+fail:
+  // a product did not complete in time: report it, give the tensor core a bounded
+  // second wait for what was issued, free the tensor memory and leave
+  if (tid == 0) {
+    atomicOr(a.err, kErrTimeout);
+    mbar_wait(mbar1, 0);
+    mbar_wait(mbar2, 0);
+    mbar_wait(mbar3, 0);
+    mbar_wait(mbar4, 0);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool chunk_grad_tc_supported(const PrefillArgs& a) { return a.dk == 128 && a.dv == 128 && a.bf16; }
+
+cudaError_t launch_chunk_grad_tc(const bwdc::ChunkBwdArgs& ca, cudaStream_t s) {
+  const PrefillArgs& a = ca.b.f;
+  if (!chunk_grad_tc_supported(a)) return cudaErrorInvalidValue;
+  auto* k = kda_bwd_grad_tc_kernel<__nv_bfloat16>;
+  constexpr int bytes = (int)GradTcSmem::BYTES + 1024;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  launch_begin(s);
+  k<<<dim3((unsigned)ca.total, (unsigned)a.H), kTcThreads, bytes, s>>>(ca);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_end(s);
+}
+
+}  // namespace kda

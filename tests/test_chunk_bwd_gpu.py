@@ -66,6 +66,28 @@ def test_chunk_bwd_head_dims(kda, dk, dv, dtype):
     _check(kda, d, _do(1, 140, 2, dv, dtype, 5), dST, f"{dk}x{dv} {dtype}")
 
 
+@pytest.mark.parametrize("T", [1, 17, 64, 65, 200])
+def test_chunk_bwd_tensor_core_lengths(kda, T):
+    """d_k = d_v = 128 with bf16 inputs (the tensor-core gradient kernel) at ragged
+    lengths: partial last chunks, a single token, exact multiples of the chunk."""
+    d = ki.prefill_inputs(2, T, 2, 128, 128, "bf16", seed=220 + T, s0=True)
+    g = torch.Generator().manual_seed(T + 1)
+    dST = torch.randn(2, 2, 128, 128, generator=g)
+    _check(kda, d, _do(2, T, 2, 128, "bf16", T + 2), dST, f"tc T={T}")
+
+
+def test_chunk_bwd_tensor_core_varlen_and_strongest_decay(kda):
+    lens = [0, 40, 1, 70, 0, 129, 64]
+    cu = ki.cu_seqlens_from_lengths(lens)
+    T = int(cu[-1])
+    d = ki.prefill_inputs(1, T, 2, 128, 128, "bf16", seed=226, s0=True, n_states=len(lens))
+    d["cu_seqlens"] = torch.from_numpy(cu)
+    d["g"][..., 64:] = -5.0
+    g = torch.Generator().manual_seed(17)
+    dST = torch.randn(len(lens), 2, 128, 128, generator=g)
+    _check(kda, d, _do(1, T, 2, 128, "bf16", 18), dST, "tc varlen, g=-5")
+
+
 def test_chunk_bwd_without_states(kda):
     d = ki.prefill_inputs(1, 100, 1, 128, 128, "bf16", seed=211, s0=False)
     _check(kda, d, _do(1, 100, 1, 128, "bf16", 6), None, "no s0", need_s0=False)
