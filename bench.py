@@ -584,49 +584,52 @@ def bench_decode_fused(kda, steps_total, warmup, stream, clk=None):
     return dict(ms=ms, N=N, H=H, bytes=N * H * per_head, launches=launches, steps=steps_total)
 
 
-CHUNK_BWD_KERNELS = ["kda_bwd_prep_kernel", "kda_bwd_state_fwd_kernel", "kda_bwd_state_rev_kernel",
+CHUNK_BWD_KERNELS = ["kda_bwd_prep_tc_kernel", "kda_bwd_state_fwd_kernel", "kda_bwd_state_rev_kernel",
                      "kda_bwd_grad_tc_kernel"]
 # FP32 FMA peak of the CUDA cores: 128 FMA per SM per clock at the 2070 MHz maximum SM
-# clock, times the SM count (the chunked backward's prep and state passes run fp32
-# arithmetic there)
+# clock, times the SM count (the chunked backward's state passes run fp32 arithmetic there)
 FP32_FMA_PER_SM_CLK = 128
 SM_MAX_MHZ = 2070.0
 
 
 def chunk_bwd_fmas(dk, dv):
-    """Executed FMAs per (64-token chunk, head) of the fp32 CUDA-core kernels of the
-    chunked backward, counted from their loop bounds."""
-    return {"kda_bwd_prep_kernel": 8704 * dk + 6528 * dv + 64 * dk * dv,
-            "kda_bwd_state_fwd_kernel": 128 * dk * dv,
-            "kda_bwd_state_rev_kernel": 128 * dk * dv}
+    """Executed FMAs per (64-token chunk, head) of the fp32 CUDA-core state passes of
+    the chunked backward, counted from their loop bounds."""
+    return {"kda_bwd_state_fwd_kernel": 128 * dk * dv, "kda_bwd_state_rev_kernel": 128 * dk * dv}
 
 
-def chunk_bwd_grad_bytes(dk, dv, C=64):
-    """Algorithmic bytes per (chunk, head) of the tensor-core gradient kernel: it reads
-    the fp32 states S and X, the chunk's U and dY and the records' A, the bf16 q, k, v
-    and dO rows, g and beta, and writes fp32 dq, dk, dg and dbeta."""
-    rd = 4 * (2 * dk * dv + 2 * C * dv + C * C) + 2 * C * (2 * dk + 2 * dv) + 4 * C * dk + 4 * C
-    return rd + 4 * (3 * C * dk + C)
+def chunk_bwd_tc_bytes(dk, dv, C=64):
+    """Algorithmic bytes per (chunk, head) of the two tensor-core kernels of the chunked
+    backward.  Prep: reads the bf16 q, k, v and dO rows, g and beta; writes the fp32
+    record (4 [C][dk] and 2 [C][dv] matrices, e^{G_C}, the [dk][dv] Z_q, the [C][C] A).
+    Gradient kernel: reads the fp32 states S and X, the chunk's U and dY and the
+    record's A, the bf16 q, k, v and dO rows, g and beta; writes fp32 dq, dk, dg, dbeta."""
+    inputs = 2 * C * (2 * dk + 2 * dv) + 4 * C * dk + 4 * C
+    rec = 4 * (4 * C * dk + 2 * C * dv + dk + dk * dv + C * C)
+    grad = inputs + 4 * (2 * dk * dv + 2 * C * dv + C * C) + 4 * (3 * C * dk + C)
+    return {"kda_bwd_prep_tc_kernel": inputs + rec, "kda_bwd_grad_tc_kernel": grad}
 
 
 def chunk_bwd_roofline(bw, ms, kernel_ms, sms, hbm_peak):
-    """``roofline`` of the chunked backward for its dominant kernel: bound "alu" (fp32
-    FMA) for the CUDA-core prep and state passes, "hbm" for the tensor-core gradient
-    kernel; every kernel's rate beside it."""
+    """``roofline`` of the chunked backward for its dominant kernel: bound "hbm" for the
+    tensor-core prep and gradient kernels (algorithmic bytes), "alu" (fp32 FMA) for the
+    CUDA-core state passes; every kernel's rate beside it."""
     alu_peak = sms * FP32_FMA_PER_SM_CLK * 2 * SM_MAX_MHZ * 1e6 / 1e12
     fl = {n: 2.0 * f * bw["chunk_heads"] for n, f in chunk_bwd_fmas(bw["dk"], bw["dv"]).items()}
-    grad = "kda_bwd_grad_tc_kernel"
-    gbytes = chunk_bwd_grad_bytes(bw["dk"], bw["dv"]) * bw["chunk_heads"]
-    rates = {n: {"achieved": fl[n] / (kernel_ms[n] * 1e-3) / 1e12, "unit": "TFLOP/s",
-                 "frac": fl[n] / (kernel_ms[n] * 1e-3) / 1e12 / alu_peak} for n in fl if n in kernel_ms}
-    if grad in kernel_ms:
-        g = gbytes / (kernel_ms[grad] * 1e-3) / 1e9
-        rates[grad] = {"achieved": g, "unit": "GB/s", "frac": g / hbm_peak}
+    by = {n: b * bw["chunk_heads"] for n, b in chunk_bwd_tc_bytes(bw["dk"], bw["dv"]).items()}
+    rates = {}
+    for n, t in kernel_ms.items():
+        if n in fl:
+            x = fl[n] / (t * 1e-3) / 1e12
+            rates[n] = {"achieved": x, "unit": "TFLOP/s", "frac": x / alu_peak}
+        elif n in by:
+            x = by[n] / (t * 1e-3) / 1e9
+            rates[n] = {"achieved": x, "unit": "GB/s", "frac": x / hbm_peak}
     k = max(kernel_ms, key=kernel_ms.get)
-    if k == grad:
+    if k in by:
         out = {"bound": "hbm", "kernel": k, "achieved": rates[k]["achieved"], "peak": hbm_peak, "unit": "GB/s",
                "frac": rates[k]["frac"], "traffic": None, "peak_source": "measured (burst copy)",
-               "bytes_per_launch": gbytes}
+               "bytes_per_launch": by[k]}
     else:
         out = {"bound": "alu", "kernel": k, "achieved": rates[k]["achieved"], "peak": alu_peak,
                "unit": "TFLOP/s", "frac": rates[k]["frac"], "traffic": None,

@@ -115,9 +115,13 @@ cudaError_t run(const ChunkBwdArgs& ca, cudaStream_t s) {
   // with no chunks at all only the reverse pass runs (it copies d_final_state to
   // d_initial_state)
   if (ca.total > 0) {
-    launch_begin(s);
-    prep<<<cgrid, 256, PS::BYTES, s>>>(ca);
-    if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
+    if (chunk_grad_tc_supported(a)) {
+      if ((e = launch_chunk_prep_tc(ca, s)) != cudaSuccess) return e;
+    } else {
+      launch_begin(s);
+      prep<<<cgrid, 256, PS::BYTES, s>>>(ca);
+      if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
+    }
     launch_begin(s);
     sfwd<<<pgrid, bwdc::kPassThreads, SS::BYTES, s>>>(ca);
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;

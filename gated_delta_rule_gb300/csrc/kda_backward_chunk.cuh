@@ -276,6 +276,61 @@ struct PrepSmem {
   static constexpr int BYTES = FLOATS * 4;
 };
 
+// T = (I + diag(beta) A)^-1 for a strictly lower triangular [64][64] A (row pitch pa):
+// the diagonal 16 x 16 blocks by substitution, one column per thread, then block rows
+// 1..3 from T_IJ = -T_II sum_K L_IK T_KJ with L = diag(beta) A.  sT (pitch pa) must be
+// zero above the diagonal blocks on entry; B0 is a [16][pb] scratch.
+template <int NT>
+KB_HD void invert_lower(const float* sA, float* sT, const float* sb, float* B0, int pa, int pb, int tid) {
+  if (tid < kC) {
+    // right-looking substitution down column m of its diagonal block: s[ii] gathers
+    // sum_{jj < ii} A[i][base + jj] t[jj] as the t[jj] become known
+    const int base = (tid / kSB) * kSB, m = tid % kSB, col = base + m;
+    float sacc[kSB], tc[kSB];
+#pragma unroll
+    for (int ii = 0; ii < kSB; ++ii) sacc[ii] = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < kSB; ++jj) {
+      tc[jj] = jj < m ? 0.f : jj == m ? 1.f : -sb[base + jj] * sacc[jj];
+      sT[(base + jj) * pa + col] = tc[jj];
+#pragma unroll
+      for (int ii = jj + 1; ii < kSB; ++ii) sacc[ii] += sA[(base + ii) * pa + base + jj] * tc[jj];
+    }
+  }
+  KB_SYNC();
+  for (int I = 1; I < 4; ++I) {
+    const int w = kSB * I;  // columns left of the diagonal block
+    // (L T)[i][m] = beta_i sum_{kk in [16 (m / 16), w)} A[i][kk] T[kk][m]: the range is
+    // a multiple of 16 long, summed in four interleaved parts
+    for (int idx = tid; idx < kSB * w; idx += NT) {
+      const int ii = idx / w, m = idx - ii * w, i = w + ii;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      for (int kk = (m / kSB) * kSB; kk < w; kk += 4) {
+        s0 += sA[i * pa + kk] * sT[kk * pa + m];
+        s1 += sA[i * pa + kk + 1] * sT[(kk + 1) * pa + m];
+        s2 += sA[i * pa + kk + 2] * sT[(kk + 2) * pa + m];
+        s3 += sA[i * pa + kk + 3] * sT[(kk + 3) * pa + m];
+      }
+      B0[ii * pb + m] = sb[i] * ((s0 + s1) + (s2 + s3));
+    }
+    KB_SYNC();
+    // T[i][m] = -sum_kk T_II[ii][kk] (L T)[kk][m]; T_II is zero above its diagonal
+    for (int idx = tid; idx < kSB * w; idx += NT) {
+      const int ii = idx / w, m = idx - ii * w, i = w + ii;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < kSB; kk += 4) {
+        s0 += sT[i * pa + w + kk] * B0[kk * pb + m];
+        s1 += sT[i * pa + w + kk + 1] * B0[(kk + 1) * pb + m];
+        s2 += sT[i * pa + w + kk + 2] * B0[(kk + 2) * pb + m];
+        s3 += sT[i * pa + w + kk + 3] * B0[(kk + 3) * pb + m];
+      }
+      sT[i * pa + m] = -((s0 + s1) + (s2 + s3));
+    }
+    KB_SYNC();
+  }
+}
+
 template <int DK, int DV, typename T>
 KB_HD void prep_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
   constexpr int NT = 256;
@@ -394,39 +449,8 @@ KB_HD void prep_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
       }
   }
   KB_SYNC();
-  // 4. T = (I + diag(beta) A)^-1: diagonal 16 x 16 blocks by substitution, one
-  //    column per thread, then block rows 1..3 from T_IJ = -T_II sum_K L_IK T_KJ
-  if (tid < kC) {
-    const int base = (tid / kSB) * kSB, m = tid % kSB, col = base + m;
-    float tc[kSB];  // this column of the diagonal block, in registers
-#pragma unroll
-    for (int ii = 0; ii < kSB; ++ii) {
-      const int i = base + ii;
-      float s = 0.f;
-#pragma unroll
-      for (int jj = 0; jj < ii; ++jj) s += sA[i * PA + base + jj] * tc[jj];
-      tc[ii] = ii < m ? 0.f : ii == m ? 1.f : -sb[i] * s;
-      sT[i * PA + col] = tc[ii];
-    }
-  }
-  KB_SYNC();
-  for (int I = 1; I < 4; ++I) {
-    const int w = kSB * I;  // columns left of the diagonal block
-    for (int idx = tid; idx < kSB * w; idx += NT) {
-      const int ii = idx / w, m = idx - ii * w, i = w + ii;
-      float s = 0.f;
-      for (int kk = (m / kSB) * kSB; kk < w; ++kk) s += sA[i * PA + kk] * sT[kk * PA + m];
-      B0[ii * PM + m] = sb[i] * s;  // (L T)[i][m]
-    }
-    KB_SYNC();
-    for (int idx = tid; idx < kSB * w; idx += NT) {
-      const int ii = idx / w, m = idx - ii * w, i = w + ii;
-      float s = 0.f;
-      for (int kk = 0; kk <= ii; ++kk) s += sT[i * PA + w + kk] * B0[kk * PM + m];
-      sT[i * PA + m] = -s;
-    }
-    KB_SYNC();
-  }
+  // 4. T = (I + diag(beta) A)^-1
+  invert_lower<NT>(sA, sT, sb, B0, PA, PM, tid);
   // 5. elementwise: B3 <- diag(beta) K+, B2 <- K_end, B0 <- scale Q+; records
   //    K_end, diag(beta) K+, e^{G_C} and A
   for (int idx = tid; idx < kC * DK; idx += NT) {
@@ -1116,9 +1140,10 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
 
 }  // namespace bwdc
 
-// The gradient kernel with its dense products on the tensor cores
+// The prep and gradient kernels with their products on the tensor cores
 // (kda_backward_tc.cu): d_k = d_v = 128 with bf16 inputs.
 bool chunk_grad_tc_supported(const PrefillArgs& a);
+cudaError_t launch_chunk_prep_tc(const bwdc::ChunkBwdArgs& ca, cudaStream_t s);
 cudaError_t launch_chunk_grad_tc(const bwdc::ChunkBwdArgs& ca, cudaStream_t s);
 
 }  // namespace kda

@@ -76,7 +76,8 @@ struct GradTcSmem {
   static constexpr int PB = 8;                        // dbeta partials per row (7 used)
   static constexpr uint32_t DBP = GS + 128 * 4;       // [64][PB]
   static constexpr uint32_t EKP = DBP + 64 * PB * 4;  // [2][128] sums of e k over half the rows
-  static constexpr uint32_t MBAR = EKP + 2 * 128 * 4; // four mbarriers
+  static constexpr uint32_t PART = EKP + 2 * 128 * 4; // [128] scratch of the cumulative sum
+  static constexpr uint32_t MBAR = PART + 128 * 4;    // four mbarriers
   static constexpr uint32_t SLOT = MBAR + 32;         // tensor-memory base address
   static constexpr uint32_t FLAG = SLOT + 4;          // a bounded wait gave up
   static constexpr uint32_t BYTES = SLOT + 16;
@@ -160,6 +161,36 @@ __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
+}
+
+// G, the cumulative sum of g down the chunk (g zero past `rows`), into sG [64][128],
+// and the sub-block references r_0 .. r_3 and G_C into rr [5][128]: two threads per
+// channel, 32 rows each summed in registers; part is a [128] scratch.  All threads of
+// the CTA call it; sG and rr are complete after the caller's next barrier.
+__device__ __forceinline__ void chunk_cumsum(const float* gb, int64_t gst, int rows, float* sG, float* rr,
+                                             float* part, int tid) {
+  const int d = tid & 127, hf = tid >> 7;
+  float g[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int r = 32 * hf + i;
+    g[i] = r < rows ? gb[(int64_t)r * gst + d] : 0.f;
+  }
+#pragma unroll
+  for (int i = 1; i < 32; ++i) g[i] += g[i - 1];
+  if (hf == 0) part[d] = g[31];
+  __syncthreads();
+  const float off = hf ? part[d] : 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) sG[(32 * hf + i) * 128 + d] = g[i] + off;
+  if (hf == 0) {
+    rr[d] = 0.f;
+    rr[128 + d] = g[15];
+    rr[256 + d] = g[31];
+  } else {
+    rr[384 + d] = g[15] + off;
+    rr[512 + d] = g[31] + off;
+  }
 }
 
 // K = 128 (eight 16-deep steps) of one K-major product into the accumulator at d_tmem
@@ -273,31 +304,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_grad_tc_kernel(ChunkBwd
   }
 
   // ---- while they run: log-decays, beta, the sub-block references; X ----
-  {
-    constexpr int NK = kC * DK / 4 / NT;
-    float4 gv[NK];
-    bwdc::load_rows<DK, NT, float>(gv, gb, a.g.st, rows, tid);
-#pragma unroll
-    for (int u = 0; u < NK; ++u) {
-      const int idx = tid + u * NT, i = idx / (DK / 4), p = idx - i * (DK / 4);
-      st4(sG + i * DK + 4 * p, gv[u]);
-    }
-  }
-  if (tid < kC) sb[tid] = tid < rows ? bb[(int64_t)tid * a.beta_st] : 0.f;
   float4 x[16];
 #pragma unroll
   for (int u = 0; u < 16; ++u) x[u] = ld4(stt + R::X + (int64_t)(warp + 8 * u) * DV + 4 * lane);
-  __syncthreads();
-  if (tid < DK) {
-    const int d = tid;
-    float run = 0.f;
-    rr[d] = 0.f;
-    for (int i = 0; i < kC; ++i) {
-      run += sG[i * DK + d];
-      sG[i * DK + d] = run;
-      if ((i & (kSB - 1)) == kSB - 1) rr[((i + 1) / kSB) * DK + d] = run;
-    }
-  }
+  if (tid < kC) sb[tid] = tid < rows ? bb[(int64_t)tid * a.beta_st] : 0.f;
+  chunk_cumsum(gb, a.g.st, rows, sG, rr, reinterpret_cast<float*>(smem + SM::PART), tid);
   if (!mbar_wait(mbar1, 0)) *sFlag = 1;
   __syncthreads();
   if (*sFlag) goto fail;
@@ -580,6 +591,417 @@ fail:
   }
 }
 
+// ---------------------------------------------------------------------------
+// prep on the tensor cores: the state-independent chunk matrices of one (chunk,
+// head), d_k = d_v = 128, bf16 inputs.  Records and their meaning are those of
+// the fp32 prep (bwdc::Rec): W = T diag(beta) K+, K_end, U_bar = T diag(beta) V,
+// e^{G_C}, W_y = T^T K_end, diag(beta) K+, V_y = scale T^T A_Q^T dO,
+// Z_q = scale Q+^T dO, A = StrictTril(K+ K-^T).
+//
+//   Gram  D_G = [k e^{G - r_I}; q e^{G - r_I}] Y^T with the column versions
+//         Y = [k e^{r_0 - G} (rows < 16); ...; k e^{r_3 - G} (rows < 64)]: lanes
+//         (i of k | i of q), 160 columns; row i of sub-block I reads version I,
+//         giving A = K+ K-^T and A_Q = Q+ K-^T with every factor within e^{+-80}
+//   D_ZQ  = dO^T (scale Q+)     lanes v, columns d      (Z_q^T)
+//   D_VT  = dO^T (scale A_Q)    lanes v, columns j      (V_t^T, V_t = scale A_Q^T dO)
+//   D_W   = (diag(beta) K+)^T T^T   lanes d, columns i  (W^T)
+//   D_WY  = K_end^T T               lanes d, columns i  (W_y^T)
+//   D_UB  = (diag(beta) V)^T T^T    lanes v, columns i  (U_bar^T)
+//   D_VY  = V_t^T T                 lanes v, columns i  (V_y^T)
+//
+// T = (I + diag(beta) A)^-1 is formed on the CUDA cores (invert_lower) while
+// D_ZQ and D_VT run.  fp32 operands are split into bf16 halves as in the gradient
+// kernel; dO is bf16 already.
+struct PrepTcSmem {
+  // Gram operands (bf16 halves, K = 128): X 128 rows, Y 160 rows
+  static constexpr uint32_t XH = 0, XL = 32768, YH = 65536, YL = 106496;  // ends 147456
+  // after the Gram
+  static constexpr uint32_t AQH = 0, AQL = 8192;       // scale A_Q: 64 x 64, rows i
+  static constexpr uint32_t DOT = 16384;               // dO: K rows i x 128 v (MN-major)
+  static constexpr uint32_t QPH = 32768, QPL = 49152;  // scale Q+: K rows i x 128 d (MN-major)
+  static constexpr int PA = 68;                        // row pitch of the fp32 matrices
+  static constexpr uint32_t SA = 65536, SAQ = SA + 64 * PA * 4, STT = SAQ + 64 * PA * 4;  // fp32 A, A_Q, T
+  static constexpr uint32_t B0 = STT + 64 * PA * 4;    // fp32 [16][64] scratch of the inverse
+  static constexpr uint32_t TH = 147456, TL = 155648;  // T: 64 x 64, rows i
+  // after D_ZQ, D_VT and the inverse
+  static constexpr uint32_t BKH = 0, BKL = 16384;      // diag(beta) K+: K rows j x 128 d
+  static constexpr uint32_t KEH = 32768, KEL = 49152;  // K_end: K rows j x 128 d
+  static constexpr uint32_t BVH = 65536, BVL = 81920;  // diag(beta) V: K rows j x 128 v
+  static constexpr uint32_t VTH = 98304, VTL = 114688; // V_t^T: 128 rows v x K = 64 j (K-major)
+  static constexpr uint32_t OPS = 163840;
+  static_assert(B0 + 16 * 64 * 4 <= TH && VTL + 16384 <= TH, "fp32 scratch and tiles stay below T");
+  // kept throughout
+  static constexpr uint32_t G = OPS;                  // [64][128] fp32 cumulative log-decay
+  static constexpr uint32_t RR = G + 64 * 128 * 4;    // [5][128] r_0..r_3, G_C
+  static constexpr uint32_t BETA = RR + 5 * 128 * 4;  // [64]
+  static constexpr uint32_t PART = BETA + 64 * 4;     // [128] scratch of the cumulative sum
+  static constexpr uint32_t MBAR = PART + 128 * 4;    // three mbarriers
+  static constexpr uint32_t SLOT = MBAR + 24;
+  static constexpr uint32_t FLAG = SLOT + 4;
+  static constexpr uint32_t BYTES = SLOT + 16;
+};
+// tensor-memory columns (D_UB and D_VY reuse the Gram's after it has been read)
+constexpr uint32_t kPG = 0, kPZQ = 160, kPVT = 288, kPW = 352, kPWY = 416, kPUB = 0, kPVY = 64;
+
+// eight fp32 of shared memory at a 16-byte aligned address
+__device__ __forceinline__ void lds8(const float* p, float (&x)[8]) {
+  const float4 a = ld4(p), b = ld4(p + 4);
+  x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+}
+// eight values as bf16 halves into two tiles at byte offset o
+__device__ __forceinline__ void store_split8(uint32_t hi, uint32_t lo, uint32_t o, const float (&x)[8]) {
+  uint32_t ph[4], pl[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) ph[e] = split2(x[2 * e], x[2 * e + 1], pl[e]);
+  st_shared_v4(hi + o, ph[0], ph[1], ph[2], ph[3]);
+  st_shared_v4(lo + o, pl[0], pl[1], pl[2], pl[3]);
+}
+// eight bf16 of row i (zero past `rows`) at 8-byte aligned p
+template <typename T>
+__device__ __forceinline__ void row8(const T* base, int64_t st, int i, int rows, int d0, float (&x)[8]) {
+  if (i < rows) {
+    const float4 a = ld4t<T>(base + (int64_t)i * st + d0), b = ld4t<T>(base + (int64_t)i * st + d0 + 4);
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = 0.f;
+  }
+}
+
+// eight bf16 of row i (zero past `rows`) as a raw uint4
+template <typename T>
+__device__ __forceinline__ uint4 raw8(const T* base, int64_t st, int i, int rows, int d0) {
+  if (i >= rows) return make_uint4(0u, 0u, 0u, 0u);
+  const uint2 a = *reinterpret_cast<const uint2*>(base + (int64_t)i * st + d0);
+  const uint2 b = *reinterpret_cast<const uint2*>(base + (int64_t)i * st + d0 + 4);
+  return make_uint4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void unpack8(uint4 u, float (&x)[8]) {
+  x[0] = bflo(u.x), x[1] = bfhi(u.x), x[2] = bflo(u.y), x[3] = bfhi(u.y);
+  x[4] = bflo(u.z), x[5] = bfhi(u.z), x[6] = bflo(u.w), x[7] = bfhi(u.w);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_prep_tc_kernel(ChunkBwdArgs ca) {
+  constexpr int DK = 128, DV = 128, NT = kTcThreads;
+  using SM = PrepTcSmem;
+  using R = bwdc::Rec<DK, DV>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s0 = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int f = blockIdx.x, h = blockIdx.y;
+  const BackwardArgs& ba = ca.b;
+  const PrefillArgs& a = ba.f;
+  bwdc::ChunkLoc L;
+  if (!bwdc::locate(ca, f, L)) return;  // uniform across the CTA
+  const int rows = L.rows;
+  float* rec = ca.rec + ((int64_t)f * a.H + h) * R::SIZE;
+  const T* qb = static_cast<const T*>(a.q.ptr) + L.b * a.q.sb + L.t * a.q.st + (int64_t)h * a.q.sh;
+  const T* kb = static_cast<const T*>(a.k.ptr) + L.b * a.k.sb + L.t * a.k.st + (int64_t)h * a.k.sh;
+  const T* vb = static_cast<const T*>(a.v.ptr) + L.b * a.v.sb + L.t * a.v.st + (int64_t)h * a.v.sh;
+  const T* ob = static_cast<const T*>(ba.dout.ptr) + L.b * ba.dout.sb + L.t * ba.dout.st + (int64_t)h * ba.dout.sh;
+  const float* gb = static_cast<const float*>(a.g.ptr) + L.b * a.g.sb + L.t * a.g.st + (int64_t)h * a.g.sh;
+  const float* bb = a.beta + L.b * a.beta_sb + L.t * a.beta_st + (int64_t)h * a.beta_sh;
+  float* sG = reinterpret_cast<float*>(smem + SM::G);
+  float* rr = reinterpret_cast<float*>(smem + SM::RR);
+  float* sb = reinterpret_cast<float*>(smem + SM::BETA);
+  float* sA = reinterpret_cast<float*>(smem + SM::SA);
+  float* sAQ = reinterpret_cast<float*>(smem + SM::SAQ);
+  float* sT = reinterpret_cast<float*>(smem + SM::STT);
+  volatile int* sFlag = reinterpret_cast<volatile int*>(smem + SM::FLAG);
+  const uint32_t mbarG = s0 + SM::MBAR, mbar2 = mbarG + 8, mbar1 = mbarG + 16;
+  const int q4 = warp & 3, half = warp >> 2;
+  const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+  const float scale = a.scale;
+
+  if (warp == 0) tmem_alloc(s0 + SM::SLOT, kTmemCols);
+  if (tid == 0) {
+    mbar_init(mbarG, 1);
+    mbar_init(mbar2, 1);
+    mbar_init(mbar1, 1);
+    *sFlag = 0;
+    fence_mbar_init();
+  }
+  // This thread's rows (tid >> 4) + 16 u (one in each sub-block u) and channels
+  // d0 .. d0 + 7 of k, q, v and dO, loaded once; every elementwise step below uses
+  // this mapping.
+  const int r0 = tid >> 4, d0 = 8 * (tid & 15);
+  uint4 kr[4], qr[4], vr[4], orw[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    kr[u] = raw8<T>(kb, a.k.st, r0 + 16 * u, rows, d0);
+    qr[u] = raw8<T>(qb, a.q.st, r0 + 16 * u, rows, d0);
+    vr[u] = raw8<T>(vb, a.v.st, r0 + 16 * u, rows, d0);
+    orw[u] = raw8<T>(ob, ba.dout.st, r0 + 16 * u, rows, d0);
+  }
+  // ---- log-decays, beta; cumulative sums and the sub-block references ----
+  if (tid < kC) sb[tid] = tid < rows ? bb[(int64_t)tid * a.beta_st] : 0.f;
+  chunk_cumsum(gb, a.g.st, rows, sG, rr, reinterpret_cast<float*>(smem + SM::PART), tid);
+  __syncthreads();
+  // ---- Gram operands: X rows (k then q) referred to their sub-block start, and the
+  //      column versions of k (row j of sub-block u appears in versions u .. 3) ----
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = r0 + 16 * u;
+    float k8[8], q8[8], g[8], rv[8];
+    unpack8(kr[u], k8);
+    unpack8(qr[u], q8);
+    lds8(sG + i * DK + d0, g);
+    lds8(rr + u * DK + d0, rv);
+    float x[8], y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float f = __expf(g[e] - rv[e]);
+      x[e] = k8[e] * f;
+      y[e] = q8[e] * f;
+    }
+    store_split8(s0 + SM::XH, s0 + SM::XL, sw128(i, d0, 128), x);
+    store_split8(s0 + SM::XH, s0 + SM::XL, sw128(64 + i, d0, 128), y);
+#pragma unroll
+    for (int I = u; I < 4; ++I) {
+      lds8(rr + I * DK + d0, rv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = k8[e] * __expf(rv[e] - g[e]);
+      store_split8(s0 + SM::YH, s0 + SM::YL, sw128(8 * I * (I + 1) + i, d0, 160), y);
+    }
+  }
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM::SLOT);
+  if (tid == 0) {
+    const uint32_t idg = idesc_bf16(128, 160, false, false);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint64_t xh = desc_kmajor(s0 + SM::XH, 128, ks), xl = desc_kmajor(s0 + SM::XL, 128, ks);
+      const uint64_t yh = desc_kmajor(s0 + SM::YH, 160, ks), yl = desc_kmajor(s0 + SM::YL, 160, ks);
+      mma_bf16(tmem + kPG, xh, yh, idg, ks > 0 ? 1u : 0u);
+      mma_bf16(tmem + kPG, xl, yh, idg, 1u);
+      mma_bf16(tmem + kPG, xh, yl, idg, 1u);
+    }
+    mma_commit(mbarG);
+  }
+  // ---- while the Gram runs: the elementwise records K_end, diag(beta) K+, e^{G_C} ----
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = r0 + 16 * u;
+    float k8[8], g[8], gc[8], ke[8], kp[8];
+    unpack8(kr[u], k8);
+    lds8(sG + i * DK + d0, g);
+    lds8(rr + 4 * DK + d0, gc);
+    const float be = sb[i];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      ke[e] = k8[e] * __expf(gc[e] - g[e]);
+      kp[e] = be * k8[e] * __expf(g[e]);
+    }
+    st4(rec + R::KE + i * DK + d0, make_float4(ke[0], ke[1], ke[2], ke[3]));
+    st4(rec + R::KE + i * DK + d0 + 4, make_float4(ke[4], ke[5], ke[6], ke[7]));
+    st4(rec + R::KB + i * DK + d0, make_float4(kp[0], kp[1], kp[2], kp[3]));
+    st4(rec + R::KB + i * DK + d0 + 4, make_float4(kp[4], kp[5], kp[6], kp[7]));
+  }
+  if (tid < DK) rec[R::EGC + tid] = __expf(rr[4 * DK + tid]);
+  if (!mbar_wait(mbarG, 0)) *sFlag = 1;
+  __syncthreads();
+  if (*sFlag) goto fail;
+  fence_after_sync();
+
+  // ---- D_G -> A (strict) and A_Q (inclusive), fp32 ----
+  for (int idx = tid; idx < 64 * SM::PA / 4; idx += NT) st4(sT + 4 * idx, zero4());  // T starts at zero
+  {
+    // warp quarter q4 holds rows 32 (q4 & 1) .. + 31 of k (q4 < 2) or q: sub-blocks
+    // Ia (lanes 0-15) and Ia + 1 (lanes 16-31), whose versions are adjacent columns
+    const int Ia = 2 * (q4 & 1), ca0 = 8 * Ia * (Ia + 1), na = kSB * (Ia + 1), nab = na + kSB * (Ia + 2);
+    const int nchunk = nab / 16, c_lo = half ? (nchunk + 1) / 2 : 0, c_hi = half ? nchunk : (nchunk + 1) / 2;
+    const int i = 32 * (q4 & 1) + lane;
+    const bool qrow = q4 >= 2;
+    float* dst = (qrow ? sAQ : sA) + i * SM::PA;
+    for (int c = c_lo; c < c_hi; ++c) {
+      float v[16];
+      tmem_ld16(tmem + lane_base + kPG + ca0 + 16 * c, v);
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const int col = 16 * c + t;
+        const int j = lane < 16 ? col : col - na;
+        const bool mine = lane < 16 ? col < na : col >= na;
+        if (mine) dst[j] = (qrow ? j <= i : j < i) ? v[t] : 0.f;
+      }
+    }
+    // columns past this row's version (j >= 16 (I + 1) > i) are zero
+    if (half) {
+      const int jz = kSB * (i / kSB + 1);
+      for (int j = jz; j < kC; j += 4) st4(dst + j, zero4());
+    }
+  }
+  __syncthreads();
+  // ---- record A; the operands of D_ZQ and D_VT ----
+  for (int idx = tid; idx < kC * kC / 4; idx += NT) {
+    const int i = idx >> 4, j4 = 4 * (idx & 15);
+    st4(rec + R::A + i * kC + j4, ld4(sA + i * SM::PA + j4));
+  }
+  for (int idx = tid; idx < 512; idx += NT) {  // scale A_Q: rows i, octets of j
+    const int i = idx >> 3, j0 = 8 * (idx & 7);
+    float x[8];
+    lds8(sAQ + i * SM::PA + j0, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] *= scale;
+    store_split8(s0 + SM::AQH, s0 + SM::AQL, sw128(i, j0, 64), x);
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {  // dO rows (exact) and scale Q+ rows
+    const int i = r0 + 16 * u;
+    const uint32_t o = sw128(i, d0, 64);
+    st_shared_v4(s0 + SM::DOT + o, orw[u].x, orw[u].y, orw[u].z, orw[u].w);
+    float x[8], g[8];
+    unpack8(qr[u], x);
+    lds8(sG + i * DK + d0, g);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] *= scale * __expf(g[e]);
+    store_split8(s0 + SM::QPH, s0 + SM::QPL, o, x);
+  }
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  if (tid == 0) {
+    fence_after_sync();
+    const uint32_t izq = idesc_bf16(128, 128, true, true), ivt = idesc_bf16(128, 64, true, true);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint64_t ad = desc_mnmajor(s0 + SM::DOT, kC, ks);
+      mma_bf16(tmem + kPZQ, ad, desc_mnmajor(s0 + SM::QPH, kC, ks), izq, ks > 0 ? 1u : 0u);
+      mma_bf16(tmem + kPZQ, ad, desc_mnmajor(s0 + SM::QPL, kC, ks), izq, 1u);
+      mma_bf16(tmem + kPVT, ad, desc_mnmajor(s0 + SM::AQH, kC, ks), ivt, ks > 0 ? 1u : 0u);
+      mma_bf16(tmem + kPVT, ad, desc_mnmajor(s0 + SM::AQL, kC, ks), ivt, 1u);
+    }
+    mma_commit(mbar2);
+  }
+  // ---- T = (I + diag(beta) A)^-1 on the CUDA cores meanwhile; its bf16 halves ----
+  bwdc::invert_lower<NT>(sA, sT, sb, reinterpret_cast<float*>(smem + SM::B0), SM::PA, 64, tid);
+  for (int idx = tid; idx < 512; idx += NT) {
+    const int i = idx >> 3, j0 = 8 * (idx & 7);
+    float x[8];
+    lds8(sT + i * SM::PA + j0, x);
+    store_split8(s0 + SM::TH, s0 + SM::TL, sw128(i, j0, 64), x);
+  }
+  if (!mbar_wait(mbar2, 0)) *sFlag = 1;
+  __syncthreads();
+  if (*sFlag) goto fail;
+  fence_after_sync();
+  // ---- D_VT -> V_t^T halves (rows v, K = j); D_ZQ -> record Z_q [d][v] ----
+  {
+    const int v = 32 * q4 + lane;
+    float x[32];
+    tmem_ld32(tmem + lane_base + kPVT + 32 * half, x);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = x[8 * c + e];
+      store_split8(s0 + SM::VTH, s0 + SM::VTL, sw128(v, 32 * half + 8 * c, 128), y);
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      tmem_ld32(tmem + lane_base + kPZQ + 64 * half + 32 * c, x);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) rec[R::ZQ + (64 * half + 32 * c + k) * DV + v] = x[k];
+    }
+  }
+  // ---- operands of the T products: diag(beta) K+, K_end, diag(beta) V (rows j) ----
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int j = r0 + 16 * u;
+    const uint32_t o = sw128(j, d0, 64);
+    float x[8], g[8], gc[8], y[8];
+    unpack8(kr[u], x);
+    lds8(sG + j * DK + d0, g);
+    lds8(rr + 4 * DK + d0, gc);
+    const float be = sb[j];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      y[e] = be * x[e] * __expf(g[e]);
+      x[e] *= __expf(gc[e] - g[e]);
+    }
+    store_split8(s0 + SM::BKH, s0 + SM::BKL, o, y);
+    store_split8(s0 + SM::KEH, s0 + SM::KEL, o, x);
+    unpack8(vr[u], x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] *= be;
+    store_split8(s0 + SM::BVH, s0 + SM::BVL, o, x);
+  }
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  if (tid == 0) {
+    fence_after_sync();
+    const uint32_t ik = idesc_bf16(128, 64, true, false), im = idesc_bf16(128, 64, true, true);
+    const uint32_t iv = idesc_bf16(128, 64, false, true);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint64_t tkh = desc_kmajor(s0 + SM::TH, 64, ks), tkl = desc_kmajor(s0 + SM::TL, 64, ks);
+      const uint64_t tmh = desc_mnmajor(s0 + SM::TH, kC, ks), tml = desc_mnmajor(s0 + SM::TL, kC, ks);
+      const uint64_t bkh = desc_mnmajor(s0 + SM::BKH, kC, ks), bkl = desc_mnmajor(s0 + SM::BKL, kC, ks);
+      const uint64_t keh = desc_mnmajor(s0 + SM::KEH, kC, ks), kel = desc_mnmajor(s0 + SM::KEL, kC, ks);
+      const uint64_t bvh = desc_mnmajor(s0 + SM::BVH, kC, ks), bvl = desc_mnmajor(s0 + SM::BVL, kC, ks);
+      const uint64_t vth = desc_kmajor(s0 + SM::VTH, 128, ks), vtl = desc_kmajor(s0 + SM::VTL, 128, ks);
+      const uint32_t acc = ks > 0 ? 1u : 0u;
+      mma_bf16(tmem + kPW, bkh, tkh, ik, acc);
+      mma_bf16(tmem + kPW, bkl, tkh, ik, 1u);
+      mma_bf16(tmem + kPW, bkh, tkl, ik, 1u);
+      mma_bf16(tmem + kPWY, keh, tmh, im, acc);
+      mma_bf16(tmem + kPWY, kel, tmh, im, 1u);
+      mma_bf16(tmem + kPWY, keh, tml, im, 1u);
+      mma_bf16(tmem + kPUB, bvh, tkh, ik, acc);
+      mma_bf16(tmem + kPUB, bvl, tkh, ik, 1u);
+      mma_bf16(tmem + kPUB, bvh, tkl, ik, 1u);
+      mma_bf16(tmem + kPVY, vth, tmh, iv, acc);
+      mma_bf16(tmem + kPVY, vtl, tmh, iv, 1u);
+      mma_bf16(tmem + kPVY, vth, tml, iv, 1u);
+    }
+    mma_commit(mbar1);
+  }
+  if (!mbar_wait(mbar1, 0)) *sFlag = 1;
+  __syncthreads();
+  if (*sFlag) goto fail;
+  fence_after_sync();
+  // ---- records W, W_y (lanes d) and U_bar, V_y (lanes v): [i][lane] ----
+  {
+    const int c = 32 * q4 + lane;
+    const uint32_t cols[4] = {kPW, kPWY, kPUB, kPVY};
+    const int64_t offs[4] = {R::W, R::WY, R::UB, R::VY};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      float x[32];
+      tmem_ld32(tmem + lane_base + cols[m] + 32 * half, x);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) rec[offs[m] + (32 * half + k) * DK + c] = x[k];
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  return;
+
+fail:
+  if (tid == 0) {
+    atomicOr(a.err, kErrTimeout);
+    mbar_wait(mbarG, 0);
+    mbar_wait(mbar2, 0);
+    mbar_wait(mbar1, 0);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 }  // namespace
 
 bool chunk_grad_tc_supported(const PrefillArgs& a) { return a.dk == 128 && a.dv == 128 && a.bf16; }
@@ -589,6 +1011,19 @@ cudaError_t launch_chunk_grad_tc(const bwdc::ChunkBwdArgs& ca, cudaStream_t s) {
   if (!chunk_grad_tc_supported(a)) return cudaErrorInvalidValue;
   auto* k = kda_bwd_grad_tc_kernel<__nv_bfloat16>;
   constexpr int bytes = (int)GradTcSmem::BYTES + 1024;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  launch_begin(s);
+  k<<<dim3((unsigned)ca.total, (unsigned)a.H), kTcThreads, bytes, s>>>(ca);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_end(s);
+}
+
+cudaError_t launch_chunk_prep_tc(const bwdc::ChunkBwdArgs& ca, cudaStream_t s) {
+  const PrefillArgs& a = ca.b.f;
+  if (!chunk_grad_tc_supported(a)) return cudaErrorInvalidValue;
+  auto* k = kda_bwd_prep_tc_kernel<__nv_bfloat16>;
+  constexpr int bytes = (int)PrepTcSmem::BYTES + 1024;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   launch_begin(s);
