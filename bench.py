@@ -586,56 +586,39 @@ def bench_decode_fused(kda, steps_total, warmup, stream, clk=None):
 
 CHUNK_BWD_KERNELS = ["kda_bwd_prep_tc_kernel", "kda_bwd_state_fwd_kernel", "kda_bwd_state_rev_kernel",
                      "kda_bwd_grad_tc_kernel"]
-# FP32 FMA peak of the CUDA cores: 128 FMA per SM per clock at the 2070 MHz maximum SM
-# clock, times the SM count (the chunked backward's state passes run fp32 arithmetic there)
-FP32_FMA_PER_SM_CLK = 128
-SM_MAX_MHZ = 2070.0
-
-
-def chunk_bwd_fmas(dk, dv):
-    """Executed FMAs per (64-token chunk, head) of the fp32 CUDA-core state passes of
-    the chunked backward, counted from their loop bounds."""
-    return {"kda_bwd_state_fwd_kernel": 128 * dk * dv, "kda_bwd_state_rev_kernel": 128 * dk * dv}
-
-
-def chunk_bwd_tc_bytes(dk, dv, C=64):
-    """Algorithmic bytes per (chunk, head) of the two tensor-core kernels of the chunked
-    backward.  Prep: reads the bf16 q, k, v and dO rows, g and beta; writes the fp32
-    record (4 [C][dk] and 2 [C][dv] matrices, e^{G_C}, the [dk][dv] Z_q, the [C][C] A).
-    Gradient kernel: reads the fp32 states S and X, the chunk's U and dY and the
-    record's A, the bf16 q, k, v and dO rows, g and beta; writes fp32 dq, dk, dg, dbeta."""
+def chunk_bwd_bytes(dk, dv, C=64):
+    """Algorithmic bytes per (chunk, head) of the four tensor-core kernels of the
+    chunked backward (each tensor counted once per chunk and head).
+    Prep: reads the bf16 q, k, v and dO rows, g and beta; writes the record (four
+    [C][d_k] and two [C][d_v] matrices, e^{G_C}, the [d_k][d_v] Z_q, the [C][C] A).
+    Forward pass: reads W, K_end, U_bar, e^{G_C}; writes the state S and U.
+    Reverse pass: reads W_y, diag(beta) K+, V_y, Z_q, e^{G_C}, beta; writes X, dY, dv.
+    Gradient kernel: reads S, X, U, dY, A, the bf16 q, k, v, dO rows, g and beta; writes
+    fp32 dq, dk, dg and dbeta."""
     inputs = 2 * C * (2 * dk + 2 * dv) + 4 * C * dk + 4 * C
     rec = 4 * (4 * C * dk + 2 * C * dv + dk + dk * dv + C * C)
-    grad = inputs + 4 * (2 * dk * dv + 2 * C * dv + C * C) + 4 * (3 * C * dk + C)
-    return {"kda_bwd_prep_tc_kernel": inputs + rec, "kda_bwd_grad_tc_kernel": grad}
+    state = 4 * (dk * dv + C * dv)
+    fwd = 4 * (2 * C * dk + C * dv + dk) + state
+    rev = 4 * (2 * C * dk + C * dv + dk * dv + dk + C) + state + 4 * C * dv
+    grad = inputs + 2 * state + 4 * C * C + 4 * (3 * C * dk + C)
+    return {"kda_bwd_prep_tc_kernel": inputs + rec, "kda_bwd_state_fwd_kernel": fwd,
+            "kda_bwd_state_rev_kernel": rev, "kda_bwd_grad_tc_kernel": grad}
 
 
-def chunk_bwd_roofline(bw, ms, kernel_ms, sms, hbm_peak):
-    """``roofline`` of the chunked backward for its dominant kernel: bound "hbm" for the
-    tensor-core prep and gradient kernels (algorithmic bytes), "alu" (fp32 FMA) for the
-    CUDA-core state passes; every kernel's rate beside it."""
-    alu_peak = sms * FP32_FMA_PER_SM_CLK * 2 * SM_MAX_MHZ * 1e6 / 1e12
-    fl = {n: 2.0 * f * bw["chunk_heads"] for n, f in chunk_bwd_fmas(bw["dk"], bw["dv"]).items()}
-    by = {n: b * bw["chunk_heads"] for n, b in chunk_bwd_tc_bytes(bw["dk"], bw["dv"]).items()}
+def chunk_bwd_roofline(bw, ms, kernel_ms, hbm_peak):
+    """``roofline`` of the chunked backward for its dominant kernel (bound "hbm",
+    algorithmic bytes over the kernel's event time), every kernel's rate beside it."""
+    by = {n: b * bw["chunk_heads"] for n, b in chunk_bwd_bytes(bw["dk"], bw["dv"]).items()}
     rates = {}
     for n, t in kernel_ms.items():
-        if n in fl:
-            x = fl[n] / (t * 1e-3) / 1e12
-            rates[n] = {"achieved": x, "unit": "TFLOP/s", "frac": x / alu_peak}
-        elif n in by:
+        if n in by:
             x = by[n] / (t * 1e-3) / 1e9
             rates[n] = {"achieved": x, "unit": "GB/s", "frac": x / hbm_peak}
     k = max(kernel_ms, key=kernel_ms.get)
-    if k in by:
-        out = {"bound": "hbm", "kernel": k, "achieved": rates[k]["achieved"], "peak": hbm_peak, "unit": "GB/s",
-               "frac": rates[k]["frac"], "traffic": None, "peak_source": "measured (burst copy)",
-               "bytes_per_launch": by[k]}
-    else:
-        out = {"bound": "alu", "kernel": k, "achieved": rates[k]["achieved"], "peak": alu_peak,
-               "unit": "TFLOP/s", "frac": rates[k]["frac"], "traffic": None,
-               "peak_source": "derived (SMs x 128 FMA x 2 x 2070 MHz)", "flops_per_launch": fl[k]}
-    out["kernel_rates"] = rates
-    return out
+    call = sum(by.values()) / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": k, "achieved": rates[k]["achieved"], "peak": hbm_peak, "unit": "GB/s",
+            "frac": rates[k]["frac"], "traffic": None, "peak_source": "measured (burst copy)",
+            "bytes_per_launch": by[k], "call_gbs": call, "call_frac": call / hbm_peak, "kernel_rates": rates}
 
 
 def bench_backward(kda, steps, warmup, stream, entry="kda_chunk_bwd", names=None):
@@ -980,9 +963,7 @@ def main():
         "kernel_ms": {n: max_over_ranks(v, world) for n, v in bw["kernel_ms"].items()},
         "tokens_per_s": world * bw["tokens"] / (bms * 1e-3),
         "hbm_frac": bw["bytes"] / (bms * 1e-3) / 1e9 / pk["hbm"], "gpu_launches": bw["launches"]}
-    extra["backward"]["roofline"] = chunk_bwd_roofline(
-        bw, bms, extra["backward"]["kernel_ms"], torch.cuda.get_device_properties(local).multi_processor_count,
-        pk["hbm"])
+    extra["backward"]["roofline"] = chunk_bwd_roofline(bw, bms, extra["backward"]["kernel_ms"], pk["hbm"])
     bw = bench_backward(kda, 3, 3, stream, "kda_backward")
     bms = max_over_ranks(bw["ms"], world)
     extra["backward_token_loop"] = {

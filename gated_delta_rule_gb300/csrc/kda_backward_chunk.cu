@@ -122,13 +122,21 @@ cudaError_t run(const ChunkBwdArgs& ca, cudaStream_t s) {
       prep<<<cgrid, 256, PS::BYTES, s>>>(ca);
       if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
     }
+    if (chunk_grad_tc_supported(a)) {
+      if ((e = launch_chunk_pass_tc(ca, false, s)) != cudaSuccess) return e;
+    } else {
+      launch_begin(s);
+      sfwd<<<pgrid, bwdc::kPassThreads, SS::BYTES, s>>>(ca);
+      if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
+    }
+  }
+  if (chunk_grad_tc_supported(a)) {
+    if ((e = launch_chunk_pass_tc(ca, true, s)) != cudaSuccess) return e;
+  } else {
     launch_begin(s);
-    sfwd<<<pgrid, bwdc::kPassThreads, SS::BYTES, s>>>(ca);
+    srev<<<pgrid, bwdc::kPassThreads, SS::BYTES, s>>>(ca);
     if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   }
-  launch_begin(s);
-  srev<<<pgrid, bwdc::kPassThreads, SS::BYTES, s>>>(ca);
-  if ((e = cudaGetLastError()) != cudaSuccess || (e = launch_end(s)) != cudaSuccess) return e;
   if (ca.total > 0) {
     if (chunk_grad_tc_supported(a)) return launch_chunk_grad_tc(ca, s);  // d_k = d_v = 128, bf16
     launch_begin(s);

@@ -1140,10 +1140,11 @@ KB_HD void grad_body(const ChunkBwdArgs& ca, float* sm, int f, int h, int tid) {
 
 }  // namespace bwdc
 
-// The prep and gradient kernels with their products on the tensor cores
+// The prep, state-pass and gradient kernels with their products on the tensor cores
 // (kda_backward_tc.cu): d_k = d_v = 128 with bf16 inputs.
 bool chunk_grad_tc_supported(const PrefillArgs& a);
 cudaError_t launch_chunk_prep_tc(const bwdc::ChunkBwdArgs& ca, cudaStream_t s);
+cudaError_t launch_chunk_pass_tc(const bwdc::ChunkBwdArgs& ca, bool reverse, cudaStream_t s);
 cudaError_t launch_chunk_grad_tc(const bwdc::ChunkBwdArgs& ca, cudaStream_t s);
 
 }  // namespace kda

@@ -612,6 +612,12 @@ fail:
 // T = (I + diag(beta) A)^-1 is formed on the CUDA cores (invert_lower) while
 // D_ZQ and D_VT run.  fp32 operands are split into bf16 halves as in the gradient
 // kernel; dO is bf16 already.
+//
+// The record keeps the fp32 layout's offsets and sizes but holds what the
+// tensor-core state passes load (RecTc): W and W_y as [hi; lo] bf16 tiles of 128
+// rows x K = 128 (K-major), K_end and -diag(beta) K+ as hi and lo MN-major tiles
+// (K rows j x 128 channels), U_bar, V_y and Z_q slice-major ([d_v / 32] slices of
+// 32 columns), e^{G_C} and A as before.
 struct PrepTcSmem {
   // Gram operands (bf16 halves, K = 128): X 128 rows, Y 160 rows
   static constexpr uint32_t XH = 0, XL = 32768, YH = 65536, YL = 106496;  // ends 147456
@@ -666,6 +672,15 @@ __device__ __forceinline__ void row8(const T* base, int64_t st, int i, int rows,
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] = 0.f;
   }
+}
+
+// eight values as bf16 halves into a pair of 16 KB global tiles (hi, then lo) at byte offset o
+__device__ __forceinline__ void rec_split8(unsigned char* tile, uint32_t o, const float (&x)[8]) {
+  uint32_t ph[4], pl[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) ph[e] = split2(x[2 * e], x[2 * e + 1], pl[e]);
+  *reinterpret_cast<uint4*>(tile + o) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+  *reinterpret_cast<uint4*>(tile + 16384 + o) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
 }
 
 // eight bf16 of row i (zero past `rows`) as a raw uint4
@@ -784,7 +799,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_prep_tc_kernel(ChunkBwd
     }
     mma_commit(mbarG);
   }
-  // ---- while the Gram runs: the elementwise records K_end, diag(beta) K+, e^{G_C} ----
+  // ---- while the Gram runs: the elementwise records K_end, -diag(beta) K+ (as tiles), e^{G_C} ----
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     const int i = r0 + 16 * u;
@@ -798,10 +813,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_prep_tc_kernel(ChunkBwd
       ke[e] = k8[e] * __expf(gc[e] - g[e]);
       kp[e] = be * k8[e] * __expf(g[e]);
     }
-    st4(rec + R::KE + i * DK + d0, make_float4(ke[0], ke[1], ke[2], ke[3]));
-    st4(rec + R::KE + i * DK + d0 + 4, make_float4(ke[4], ke[5], ke[6], ke[7]));
-    st4(rec + R::KB + i * DK + d0, make_float4(kp[0], kp[1], kp[2], kp[3]));
-    st4(rec + R::KB + i * DK + d0 + 4, make_float4(kp[4], kp[5], kp[6], kp[7]));
+#pragma unroll
+    for (int e = 0; e < 8; ++e) kp[e] = -kp[e];
+    const uint32_t o = sw128(i, d0, 64);
+    rec_split8(reinterpret_cast<unsigned char*>(rec + R::KE), o, ke);
+    rec_split8(reinterpret_cast<unsigned char*>(rec + R::KB), o, kp);
   }
   if (tid < DK) rec[R::EGC + tid] = __expf(rr[4 * DK + tid]);
   if (!mbar_wait(mbarG, 0)) *sFlag = 1;
@@ -906,7 +922,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_prep_tc_kernel(ChunkBwd
     for (int c = 0; c < 2; ++c) {
       tmem_ld32(tmem + lane_base + kPZQ + 64 * half + 32 * c, x);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) rec[R::ZQ + (64 * half + 32 * c + k) * DV + v] = x[k];
+      for (int k = 0; k < 32; ++k) rec[R::ZQ + (v >> 5) * (DK * 32) + (64 * half + 32 * c + k) * 32 + (v & 31)] = x[k];
     }
   }
   // ---- operands of the T products: diag(beta) K+, K_end, diag(beta) V (rows j) ----
@@ -966,17 +982,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_prep_tc_kernel(ChunkBwd
   __syncthreads();
   if (*sFlag) goto fail;
   fence_after_sync();
-  // ---- records W, W_y (lanes d) and U_bar, V_y (lanes v): [i][lane] ----
+  // ---- records W, W_y (lanes d: [hi; lo] tiles) and U_bar, V_y (lanes v: slice-major) ----
   {
     const int c = 32 * q4 + lane;
-    const uint32_t cols[4] = {kPW, kPWY, kPUB, kPVY};
-    const int64_t offs[4] = {R::W, R::WY, R::UB, R::VY};
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
+    for (int m = 0; m < 2; ++m) {
       float x[32];
-      tmem_ld32(tmem + lane_base + cols[m] + 32 * half, x);
+      tmem_ld32(tmem + lane_base + (m ? kPWY : kPW) + 32 * half, x);
+      unsigned char* t = reinterpret_cast<unsigned char*>(rec + (m ? R::WY : R::W));
 #pragma unroll
-      for (int k = 0; k < 32; ++k) rec[offs[m] + (32 * half + k) * DK + c] = x[k];
+      for (int k = 0; k < 32; ++k) {
+        const int i = 32 * half + k;
+        uint32_t lo;
+        const uint32_t hi = split2(x[k], 0.f, lo);
+        *reinterpret_cast<uint16_t*>(t + sw128(i, c, 128)) = (uint16_t)hi;
+        *reinterpret_cast<uint16_t*>(t + sw128(kC + i, c, 128)) = (uint16_t)lo;
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      float x[32];
+      tmem_ld32(tmem + lane_base + (m ? kPVY : kPUB) + 32 * half, x);
+      float* dst = rec + (m ? R::VY : R::UB) + (c >> 5) * (kC * 32) + (c & 31);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) dst[(32 * half + k) * 32] = x[k];
     }
   }
   fence_before_sync();
@@ -1002,6 +1031,271 @@ fail:
   }
 }
 
+// ---------------------------------------------------------------------------
+// forward and reverse state passes on the tensor cores (d_k = d_v = 128, bf16
+// inputs, records as the tensor-core prep writes them).  One CTA per (sequence,
+// head, 32 value columns); the 32-column slice of the state lives in tensor memory
+// (lanes d) and every chunk takes two products:
+//   forward   D_U = [W_hi; W_lo] S              U   = U_bar - (D_U[i] + D_U[64 + i])
+//             S  <- e^{G_C} S + K_end^T U
+//   reverse   D_U = [W_y,hi; W_y,lo] X          dY  = V_y + (D_U[i] + D_U[64 + i])
+//             X  <- e^{G_C} X + Z_q + (-diag(beta) K+)^T dY,  dv = diag(beta) dY
+// with S (or X) and U (or dY) split into bf16 halves for the B operands.  The two
+// record tiles of the next chunk (64 KB) arrive by one bulk copy into the other
+// buffer while this chunk runs; the chunk's U_bar / V_y rows, e^{G_C}, Z_q rows and
+// beta are loaded into registers one chunk ahead.
+struct PassTcSmem {
+  static constexpr uint32_t BUF = 65536;     // two buffers: [W; W_lo] tile, then K_end hi, lo tiles
+  static constexpr uint32_t M1 = 32768;      // offset of the second matrix in a buffer
+  static constexpr uint32_t SH = 2 * BUF;    // state halves: K rows d (128) x 32 columns, MN-major
+  static constexpr uint32_t SL = SH + 16384;
+  static constexpr uint32_t UH = SL + 16384; // U (or dY) halves: K rows i (64) x 32 columns
+  static constexpr uint32_t UL = UH + 8192;
+  static constexpr int PX = 33;              // exchange rows: D_U of the low halves, [64][33] fp32
+  static constexpr uint32_t XCH = UL + 8192;
+  static constexpr uint32_t MBAR = XCH + 64 * PX * 4;  // rec0, rec1, u, s, done
+  static constexpr uint32_t SLOT = MBAR + 40;
+  static constexpr uint32_t FLAG = SLOT + 4;
+  static constexpr uint32_t BYTES = SLOT + 16;
+};
+constexpr uint32_t kPassTmemCols = 64;  // D_S at 0, D_U at 32
+
+template <bool REV>
+__global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_pass_tc_kernel(ChunkBwdArgs ca) {
+  constexpr int DK = 128, DV = 128, NSL = DV / 32;
+  using SM = PassTcSmem;
+  using R = bwdc::Rec<DK, DV>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s0 = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3, half = warp >> 2;
+  const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+  const BackwardArgs& ba = ca.b;
+  const PrefillArgs& a = ba.f;
+  const int sl = blockIdx.x % NSL, nh = blockIdx.x / NSL;
+  const int n = nh / a.H, h = nh - n * a.H, col0 = 32 * sl;
+  int64_t bq, t0;
+  int len;
+  bwdc::seq_span(a, n, bq, t0, len);
+  const int nc = bwdc::num_chunks(ca, n), f0 = bwdc::first_chunk(ca, n);
+  auto recp = [&](int c) { return ca.rec + ((int64_t)(f0 + c) * a.H + h) * R::SIZE; };
+  auto stp = [&](int c) { return ca.st + ((int64_t)(f0 + c) * a.H + h) * R::SSIZE; };
+  auto chunk = [&](int k) { return REV ? nc - 1 - k : k; };
+  volatile int* sFlag = reinterpret_cast<volatile int*>(smem + SM::FLAG);
+  float* xch = reinterpret_cast<float*>(smem + SM::XCH);
+  const uint32_t mrec = s0 + SM::MBAR, mu = mrec + 16, ms = mrec + 24, mdone = mrec + 32;
+  const int64_t m0off = REV ? R::WY : R::W;     // [hi; lo] tile, then the K_end / -beta K+ halves
+  const int64_t voff = REV ? R::VY : R::UB;     // slice-major [64][32] rows
+
+  if (warp == 0) tmem_alloc(s0 + SM::SLOT, kPassTmemCols);
+  if (tid == 0) {
+    mbar_init(mrec, 1);
+    mbar_init(mrec + 8, 1);
+    mbar_init(mu, 1);
+    mbar_init(ms, 1);
+    mbar_init(mdone, 1);
+    *sFlag = 0;
+    fence_mbar_init();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM::SLOT);
+  const uint32_t tS = tmem, tU = tmem + 32;
+  const int d = 32 * q4 + lane;          // state row of warps 0-3
+  const int ir = 32 * (q4 & 1) + lane;   // chunk row of warps with q4 < 2
+  // the starting state: S_0 (forward) or the final-state gradient (reverse); zero if absent
+  if (warp < 4) {
+    const float* init = REV ? (ba.dsT ? ba.dsT + n * ba.dsT_sn + h * ba.dsT_sh : nullptr)
+                            : (a.s0 ? a.s0 + n * a.s0_sn + h * a.s0_sh : nullptr);
+    float v[32];
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) {
+      const float4 x = init ? ld4(init + (int64_t)d * DV + col0 + c) : zero4();
+      v[c] = x.x, v[c + 1] = x.y, v[c + 2] = x.z, v[c + 3] = x.w;
+    }
+    tmem_st32(tS + lane_base, v);
+  }
+  // per-chunk vectors, one chunk ahead
+  float eg = 0.f, zq[32], vrow[16], be = 0.f;
+  auto fetch = [&](int c) {
+    const float* rc = recp(c);
+    if (warp < 4) {
+      eg = rc[R::EGC + d];
+      if (REV)
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+          const float4 x = ld4(rc + R::ZQ + sl * (DK * 32) + d * 32 + k);
+          zq[k] = x.x, zq[k + 1] = x.y, zq[k + 2] = x.z, zq[k + 3] = x.w;
+        }
+    }
+    if (q4 < 2) {
+#pragma unroll
+      for (int k = 0; k < 16; k += 4) {
+        const float4 x = ld4(rc + voff + sl * (kC * 32) + ir * 32 + 16 * half + k);
+        vrow[k] = x.x, vrow[k + 1] = x.y, vrow[k + 2] = x.z, vrow[k + 3] = x.w;
+      }
+      if (REV) {
+        const int tok = c * kC + ir;
+        be = tok < len ? a.beta[bq * a.beta_sb + (t0 + tok) * a.beta_st + (int64_t)h * a.beta_sh] : 0.f;
+      }
+    }
+  };
+  auto issue = [&](int k) {  // thread 0: chunk k's two tiles into buffer k & 1
+    const uint32_t mb = mrec + 8 * (k & 1);
+    mbar_arrive_expect_tx(mb, 65536u);
+    bulk_g2s(s0 + (uint32_t)(k & 1) * SM::BUF, recp(chunk(k)) + m0off, 65536u, mb);
+  };
+  int issued = 0;  // bulk copies issued (chunks 0 .. issued - 1)
+  if (tid == 0 && nc > 0) {
+    issue(0);
+    issued = 1;
+  }
+  if (nc > 0) fetch(chunk(0));
+  fence_before_sync();
+  __syncthreads();
+  for (int k = 0; k < nc; ++k) {
+    const int c = chunk(k), b = k & 1;
+    if (tid == 0 && k + 1 < nc) {  // buffer b ^ 1 last served chunk k - 1, whose products are done
+      issue(k + 1);
+      issued = k + 2;
+    }
+    const float eg_c = eg, be_c = be;
+    float zq_c[32], v_c[16];
+#pragma unroll
+    for (int t = 0; t < 32; ++t) zq_c[t] = REV ? zq[t] : 0.f;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) v_c[t] = vrow[t];
+    if (k + 1 < nc) fetch(chunk(k + 1));
+    float* st = stp(c);
+    // (1) the state entering this step: record, bf16 halves (B of D_U), then decayed in place
+    if (warp < 4) {
+      float v[32];
+      tmem_ld32(tS + lane_base, v);
+      float* dst = st + (REV ? R::X : R::S) + (int64_t)d * DV + col0;
+#pragma unroll
+      for (int t = 0; t < 32; t += 4) st4(dst + t, make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]));
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = v[8 * cc + e];
+        store_split8(s0 + SM::SH, s0 + SM::SL, sw128(d, 8 * cc, 128), y);
+      }
+#pragma unroll
+      for (int t = 0; t < 32; ++t) v[t] = eg_c * v[t] + zq_c[t];
+      tmem_st32(tS + lane_base, v);
+    }
+    fence_async_smem();
+    if (!mbar_wait(mrec + 8 * b, (uint32_t)((k >> 1) & 1))) *sFlag = 1;
+    fence_before_sync();
+    __syncthreads();
+    if (*sFlag) goto fail;
+    if (tid == 0) {
+      fence_after_sync();
+      const uint32_t idu = idesc_bf16(128, 32, false, true);
+      const uint32_t buf = s0 + (uint32_t)b * SM::BUF;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t ad = desc_kmajor(buf, 128, ks);
+        mma_bf16(tU, ad, desc_mnmajor(s0 + SM::SH, 128, ks), idu, ks > 0 ? 1u : 0u);
+        mma_bf16(tU, ad, desc_mnmajor(s0 + SM::SL, 128, ks), idu, 1u);
+      }
+      mma_commit(mu);
+    }
+    if (!mbar_wait(mu, (uint32_t)(k & 1))) *sFlag = 1;
+    fence_after_sync();
+    // (2) U (or dY) rows: the high-half rows add the low-half rows through shared memory
+    {
+      float u[16];
+      tmem_ld16(tU + lane_base + 16 * half, u);
+      if (q4 >= 2)
+#pragma unroll
+        for (int t = 0; t < 16; ++t) xch[ir * SM::PX + 16 * half + t] = u[t];
+      __syncthreads();
+      if (*sFlag) goto fail;
+      if (q4 < 2) {
+        float y[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float p = u[t] + xch[ir * SM::PX + 16 * half + t];
+          y[t] = REV ? v_c[t] + p : v_c[t] - p;
+        }
+        float* dst = st + (REV ? R::DY : R::U) + (int64_t)ir * DV + col0 + 16 * half;
+#pragma unroll
+        for (int t = 0; t < 16; t += 4) st4(dst + t, make_float4(y[t], y[t + 1], y[t + 2], y[t + 3]));
+        const int tok = c * kC + ir;
+        if (REV && tok < len) {
+          float* dv = ba.dv.ptr + bq * ba.dv.sb + (t0 + tok) * ba.dv.st + (int64_t)h * ba.dv.sh + col0 + 16 * half;
+#pragma unroll
+          for (int t = 0; t < 16; t += 4)
+            st4(dv + t, make_float4(be_c * y[t], be_c * y[t + 1], be_c * y[t + 2], be_c * y[t + 3]));
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          float z[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) z[e] = y[8 * cc + e];
+          store_split8(s0 + SM::UH, s0 + SM::UL, sw128(ir, 16 * half + 8 * cc, 64), z);
+        }
+      }
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      fence_after_sync();
+      const uint32_t ids = idesc_bf16(128, 32, true, true);
+      const uint32_t m1 = s0 + (uint32_t)b * SM::BUF + SM::M1;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint64_t ah = desc_mnmajor(m1, kC, ks), al = desc_mnmajor(m1 + 16384, kC, ks);
+        const uint64_t uh = desc_mnmajor(s0 + SM::UH, kC, ks), ul = desc_mnmajor(s0 + SM::UL, kC, ks);
+        mma_bf16(tS, ah, uh, ids, 1u);
+        mma_bf16(tS, al, uh, ids, 1u);
+        mma_bf16(tS, ah, ul, ids, 1u);
+      }
+      mma_commit(ms);
+    }
+    if (!mbar_wait(ms, (uint32_t)(k & 1))) *sFlag = 1;
+    fence_after_sync();
+    __syncthreads();
+    if (*sFlag) goto fail;
+  }
+  // reverse: the initial-state gradient is the last X
+  if (REV && ba.ds0 && warp < 4) {
+    float v[32];
+    tmem_ld32(tS + lane_base, v);
+    float* dst = ba.ds0 + n * ba.ds0_sn + h * ba.ds0_sh + (int64_t)d * DV + col0;
+#pragma unroll
+    for (int t = 0; t < 32; t += 4) st4(dst + t, make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]));
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after_sync();
+    tmem_dealloc(tmem, kPassTmemCols);
+  }
+  return;
+
+fail:
+  // a wait gave up: report it, let what was issued finish (bounded), free the tensor memory
+  if (tid == 0) {
+    atomicOr(a.err, kErrTimeout);
+    mma_commit(mdone);
+    mbar_wait(mdone, 0);
+    for (int k = (issued > 2 ? issued - 2 : 0); k < issued; ++k) mbar_wait(mrec + 8 * (k & 1), (uint32_t)((k >> 1) & 1));
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after_sync();
+    tmem_dealloc(tmem, kPassTmemCols);
+  }
+}
+
 }  // namespace
 
 bool chunk_grad_tc_supported(const PrefillArgs& a) { return a.dk == 128 && a.dv == 128 && a.bf16; }
@@ -1015,6 +1309,20 @@ cudaError_t launch_chunk_grad_tc(const bwdc::ChunkBwdArgs& ca, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   launch_begin(s);
   k<<<dim3((unsigned)ca.total, (unsigned)a.H), kTcThreads, bytes, s>>>(ca);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_end(s);
+}
+
+cudaError_t launch_chunk_pass_tc(const bwdc::ChunkBwdArgs& ca, bool reverse, cudaStream_t s) {
+  const PrefillArgs& a = ca.b.f;
+  if (!chunk_grad_tc_supported(a)) return cudaErrorInvalidValue;
+  auto* k = reverse ? kda_bwd_pass_tc_kernel<true> : kda_bwd_pass_tc_kernel<false>;
+  constexpr int bytes = (int)PassTcSmem::BYTES + 1024;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)((int64_t)a.N * a.H * (a.dv / 32));
+  launch_begin(s);
+  k<<<grid, kTcThreads, bytes, s>>>(ca);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_end(s);
 }
