@@ -617,7 +617,7 @@ fail:
 // tensor-core state passes load (RecTc): W and W_y as [hi; lo] bf16 tiles of 128
 // rows x K = 128 (K-major), K_end and -diag(beta) K+ as hi and lo MN-major tiles
 // (K rows j x 128 channels), U_bar, V_y and Z_q slice-major ([d_v / 32] slices of
-// 32 columns), e^{G_C} and A as before.
+// 32 columns; Z_q's 16-byte chunks of row d rotated by d), e^{G_C} and A as before.
 struct PrepTcSmem {
   // Gram operands (bf16 halves, K = 128): X 128 rows, Y 160 rows
   static constexpr uint32_t XH = 0, XL = 32768, YH = 65536, YL = 106496;  // ends 147456
@@ -922,7 +922,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_prep_tc_kernel(ChunkBwd
     for (int c = 0; c < 2; ++c) {
       tmem_ld32(tmem + lane_base + kPZQ + 64 * half + 32 * c, x);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) rec[R::ZQ + (v >> 5) * (DK * 32) + (64 * half + 32 * c + k) * 32 + (v & 31)] = x[k];
+      for (int k = 0; k < 32; ++k) {
+        const int dd = 64 * half + 32 * c + k;  // row d of slice v / 32; chunk (v % 32) / 4 rotated by d
+        rec[R::ZQ + (v >> 5) * (DK * 32) + dd * 32 + ((((v & 31) >> 2) + dd) & 7) * 4 + (v & 3)] = x[k];
+      }
     }
   }
   // ---- operands of the T products: diag(beta) K+, K_end, diag(beta) V (rows j) ----
@@ -1036,29 +1039,32 @@ fail:
 // inputs, records as the tensor-core prep writes them).  One CTA per (sequence,
 // head, 32 value columns); the 32-column slice of the state lives in tensor memory
 // (lanes d) and every chunk takes two products:
-//   forward   D_U = [W_hi; W_lo] S              U   = U_bar - (D_U[i] + D_U[64 + i])
+//   forward   D_U = [W_hi; W_lo] [S_hi | S_lo]   U  = U_bar - (sum of the four quarters)
 //             S  <- e^{G_C} S + K_end^T U
-//   reverse   D_U = [W_y,hi; W_y,lo] X          dY  = V_y + (D_U[i] + D_U[64 + i])
+//   reverse   D_U = [W_y,hi; W_y,lo] [X_hi | X_lo]  dY = V_y + (sum of the four quarters)
 //             X  <- e^{G_C} X + Z_q + (-diag(beta) K+)^T dY,  dv = diag(beta) dY
-// with S (or X) and U (or dY) split into bf16 halves for the B operands.  The two
-// record tiles of the next chunk (64 KB) arrive by one bulk copy into the other
-// buffer while this chunk runs; the chunk's U_bar / V_y rows, e^{G_C}, Z_q rows and
+// The bf16 halves of S (or X) and of U (or dY) sit side by side along N (N = 64), so a
+// product of split operands takes one chain of N = 64 MMAs plus, for the state
+// update, one chain of N = 32 (K_end,lo U_hi): 16 MMAs per chunk.  The state update's
+// N = 64 chain leaves K_end,hi U_lo in columns 32..63 of the state accumulator,
+// which are added in when the state is next read and then cleared.  The next
+// chunk's record tiles (64 KB, and the reverse pass's 16 KB Z_q slice) arrive by bulk
+// copy into the other buffer while this chunk runs; U_bar / V_y rows, e^{G_C} and
 // beta are loaded into registers one chunk ahead.
 struct PassTcSmem {
-  static constexpr uint32_t BUF = 65536;     // two buffers: [W; W_lo] tile, then K_end hi, lo tiles
+  static constexpr uint32_t BUF = 65536;     // two buffers: [W_hi; W_lo] tile, then K_end hi, lo tiles
   static constexpr uint32_t M1 = 32768;      // offset of the second matrix in a buffer
-  static constexpr uint32_t SH = 2 * BUF;    // state halves: K rows d (128) x 32 columns, MN-major
-  static constexpr uint32_t SL = SH + 16384;
-  static constexpr uint32_t UH = SL + 16384; // U (or dY) halves: K rows i (64) x 32 columns
-  static constexpr uint32_t UL = UH + 8192;
-  static constexpr int PX = 33;              // exchange rows: D_U of the low halves, [64][33] fp32
-  static constexpr uint32_t XCH = UL + 8192;
+  static constexpr uint32_t ZQB = 2 * BUF;   // reverse: two Z_q slices, [128][32] fp32 (rotated chunks)
+  static constexpr uint32_t SB = ZQB + 32768;  // state halves: K rows d (128) x [hi 32 | lo 32], MN-major
+  static constexpr uint32_t UB = SB + 16384;   // U (or dY) halves: K rows i (64) x [hi 32 | lo 32]
+  static constexpr int PX = 33;                // exchange rows: the low-half rows of D_U, [64][33] fp32
+  static constexpr uint32_t XCH = UB + 8192;
   static constexpr uint32_t MBAR = XCH + 64 * PX * 4;  // rec0, rec1, u, s, done
   static constexpr uint32_t SLOT = MBAR + 40;
   static constexpr uint32_t FLAG = SLOT + 4;
   static constexpr uint32_t BYTES = SLOT + 16;
 };
-constexpr uint32_t kPassTmemCols = 64;  // D_S at 0, D_U at 32
+constexpr uint32_t kPassTmemCols = 128;  // state accumulator at 0 (64 columns), D_U at 64
 
 template <bool REV>
 __global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_pass_tc_kernel(ChunkBwdArgs ca) {
@@ -1086,8 +1092,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_pass_tc_kernel(ChunkBwd
   volatile int* sFlag = reinterpret_cast<volatile int*>(smem + SM::FLAG);
   float* xch = reinterpret_cast<float*>(smem + SM::XCH);
   const uint32_t mrec = s0 + SM::MBAR, mu = mrec + 16, ms = mrec + 24, mdone = mrec + 32;
-  const int64_t m0off = REV ? R::WY : R::W;     // [hi; lo] tile, then the K_end / -beta K+ halves
-  const int64_t voff = REV ? R::VY : R::UB;     // slice-major [64][32] rows
+  const int64_t m0off = REV ? R::WY : R::W;  // [hi; lo] tile, then the K_end / -beta K+ halves
+  const int64_t voff = REV ? R::VY : R::UB;  // slice-major [64][32] rows
+  constexpr uint32_t kRecBytes = REV ? 65536u + 16384u : 65536u;
 
   if (warp == 0) tmem_alloc(s0 + SM::SLOT, kPassTmemCols);
   if (tid == 0) {
@@ -1103,38 +1110,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_pass_tc_kernel(ChunkBwd
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM::SLOT);
-  const uint32_t tS = tmem, tU = tmem + 32;
-  const int d = 32 * q4 + lane;          // state row of warps 0-3
+  const uint32_t tS = tmem, tU = tmem + 64;
+  const int d = 32 * q4 + lane;          // state row
   const int ir = 32 * (q4 & 1) + lane;   // chunk row of warps with q4 < 2
+  const int cv = 16 * half;              // this thread's first state column
   // the starting state: S_0 (forward) or the final-state gradient (reverse); zero if absent
-  if (warp < 4) {
+  {
     const float* init = REV ? (ba.dsT ? ba.dsT + n * ba.dsT_sn + h * ba.dsT_sh : nullptr)
                             : (a.s0 ? a.s0 + n * a.s0_sn + h * a.s0_sh : nullptr);
-    float v[32];
+    uint32_t r[16], z[16];
 #pragma unroll
-    for (int c = 0; c < 32; c += 4) {
-      const float4 x = init ? ld4(init + (int64_t)d * DV + col0 + c) : zero4();
-      v[c] = x.x, v[c + 1] = x.y, v[c + 2] = x.z, v[c + 3] = x.w;
+    for (int t = 0; t < 16; t += 4) {
+      const float4 x = init ? ld4(init + (int64_t)d * DV + col0 + cv + t) : zero4();
+      r[t] = __float_as_uint(x.x), r[t + 1] = __float_as_uint(x.y), r[t + 2] = __float_as_uint(x.z),
+      r[t + 3] = __float_as_uint(x.w);
     }
-    tmem_st32(tS + lane_base, v);
+#pragma unroll
+    for (int t = 0; t < 16; ++t) z[t] = 0u;
+    tmem_st16_async(tS + lane_base + cv, r);
+    tmem_st16_async(tS + lane_base + 32 + cv, z);
+    tmem_wait_st();
   }
   // per-chunk vectors, one chunk ahead
-  float eg = 0.f, zq[32], vrow[16], be = 0.f;
+  float eg = 0.f, vrow[16], be = 0.f;
   auto fetch = [&](int c) {
     const float* rc = recp(c);
-    if (warp < 4) {
-      eg = rc[R::EGC + d];
-      if (REV)
-#pragma unroll
-        for (int k = 0; k < 32; k += 4) {
-          const float4 x = ld4(rc + R::ZQ + sl * (DK * 32) + d * 32 + k);
-          zq[k] = x.x, zq[k + 1] = x.y, zq[k + 2] = x.z, zq[k + 3] = x.w;
-        }
-    }
+    eg = rc[R::EGC + d];
     if (q4 < 2) {
 #pragma unroll
       for (int k = 0; k < 16; k += 4) {
-        const float4 x = ld4(rc + voff + sl * (kC * 32) + ir * 32 + 16 * half + k);
+        const float4 x = ld4(rc + voff + sl * (kC * 32) + ir * 32 + cv + k);
         vrow[k] = x.x, vrow[k + 1] = x.y, vrow[k + 2] = x.z, vrow[k + 3] = x.w;
       }
       if (REV) {
@@ -1143,11 +1148,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_pass_tc_kernel(ChunkBwd
       }
     }
   };
-  auto issue = [&](int k) {  // thread 0: chunk k's two tiles into buffer k & 1
+  auto issue = [&](int k) {  // thread 0: chunk k's tiles (and Z_q slice) into buffer k & 1
     const uint32_t mb = mrec + 8 * (k & 1);
-    mbar_arrive_expect_tx(mb, 65536u);
-    bulk_g2s(s0 + (uint32_t)(k & 1) * SM::BUF, recp(chunk(k)) + m0off, 65536u, mb);
+    const float* rc = recp(chunk(k));
+    mbar_arrive_expect_tx(mb, kRecBytes);
+    bulk_g2s(s0 + (uint32_t)(k & 1) * SM::BUF, rc + m0off, 65536u, mb);
+    if (REV) bulk_g2s(s0 + SM::ZQB + (uint32_t)(k & 1) * 16384u, rc + R::ZQ + sl * (DK * 32), 16384u, mb);
   };
+  // operand descriptors; a k-step adds a constant (in 16-byte units) to the address field
+  const uint64_t dW0 = desc_kmajor(s0, 128, 0), dW1 = desc_kmajor(s0 + SM::BUF, 128, 0);
+  const uint64_t dM0 = desc_mnmajor(s0 + SM::M1, kC, 0), dM1 = desc_mnmajor(s0 + SM::BUF + SM::M1, kC, 0);
+  const uint64_t dSB = desc_mnmajor(s0 + SM::SB, 128, 0), dUB = desc_mnmajor(s0 + SM::UB, kC, 0);
   int issued = 0;  // bulk copies issued (chunks 0 .. issued - 1)
   if (tid == 0 && nc > 0) {
     issue(0);
@@ -1163,82 +1174,100 @@ __global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_pass_tc_kernel(ChunkBwd
       issued = k + 2;
     }
     const float eg_c = eg, be_c = be;
-    float zq_c[32], v_c[16];
-#pragma unroll
-    for (int t = 0; t < 32; ++t) zq_c[t] = REV ? zq[t] : 0.f;
+    float v_c[16];
 #pragma unroll
     for (int t = 0; t < 16; ++t) v_c[t] = vrow[t];
     if (k + 1 < nc) fetch(chunk(k + 1));
     float* st = stp(c);
-    // (1) the state entering this step: record, bf16 halves (B of D_U), then decayed in place
-    if (warp < 4) {
-      float v[32];
-      tmem_ld32(tS + lane_base, v);
-      float* dst = st + (REV ? R::X : R::S) + (int64_t)d * DV + col0;
+    // (1) the state entering this step (both accumulator halves): its bf16 halves (B of
+    //     D_U), then decayed (plus Z_q) in place, the second half cleared
+    float sv[16];
+    {
+      uint32_t ra[16], rb[16];
+      tmem_ld16_async(tS + lane_base + cv, ra);
+      tmem_ld16_async(tS + lane_base + 32 + cv, rb);
+      tmem_wait_ld();
 #pragma unroll
-      for (int t = 0; t < 32; t += 4) st4(dst + t, make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]));
+      for (int t = 0; t < 16; ++t) sv[t] = __uint_as_float(ra[t]) + __uint_as_float(rb[t]);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         float y[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = v[8 * cc + e];
-        store_split8(s0 + SM::SH, s0 + SM::SL, sw128(d, 8 * cc, 128), y);
+        for (int e = 0; e < 8; ++e) y[e] = sv[8 * cc + e];
+        store_split8(s0 + SM::SB + sw128(d, cv + 8 * cc, 128), s0 + SM::SB + sw128(d, 32 + cv + 8 * cc, 128), 0u, y);
       }
-#pragma unroll
-      for (int t = 0; t < 32; ++t) v[t] = eg_c * v[t] + zq_c[t];
-      tmem_st32(tS + lane_base, v);
     }
     fence_async_smem();
     if (!mbar_wait(mrec + 8 * b, (uint32_t)((k >> 1) & 1))) *sFlag = 1;
+    {
+      float zq[16];
+      if (REV) {  // Z_q row d, 16-byte chunks rotated by d
+        const float* zr = reinterpret_cast<const float*>(smem + SM::ZQB + b * 16384) + d * 32;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 x = ld4(zr + 4 * ((4 * half + j + d) & 7));
+          zq[4 * j] = x.x, zq[4 * j + 1] = x.y, zq[4 * j + 2] = x.z, zq[4 * j + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) zq[t] = 0.f;
+      }
+      uint32_t r[16], z[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        r[t] = __float_as_uint(eg_c * sv[t] + zq[t]);
+        z[t] = 0u;
+      }
+      tmem_st16_async(tS + lane_base + cv, r);
+      tmem_st16_async(tS + lane_base + 32 + cv, z);
+      tmem_wait_st();
+    }
     fence_before_sync();
     __syncthreads();
     if (*sFlag) goto fail;
     if (tid == 0) {
       fence_after_sync();
-      const uint32_t idu = idesc_bf16(128, 32, false, true);
-      const uint32_t buf = s0 + (uint32_t)b * SM::BUF;
+      const uint32_t idu = idesc_bf16(128, 64, false, true);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t ad = desc_kmajor(buf, 128, ks);
-        mma_bf16(tU, ad, desc_mnmajor(s0 + SM::SH, 128, ks), idu, ks > 0 ? 1u : 0u);
-        mma_bf16(tU, ad, desc_mnmajor(s0 + SM::SL, 128, ks), idu, 1u);
-      }
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(tU, (b ? dW1 : dW0) + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), dSB + (uint64_t)(ks * 128),
+                 idu, ks > 0 ? 1u : 0u);
       mma_commit(mu);
+    }
+    {  // the state record, while D_U runs
+      float* dst = st + (REV ? R::X : R::S) + (int64_t)d * DV + col0 + cv;
+#pragma unroll
+      for (int t = 0; t < 16; t += 4) st4(dst + t, make_float4(sv[t], sv[t + 1], sv[t + 2], sv[t + 3]));
     }
     if (!mbar_wait(mu, (uint32_t)(k & 1))) *sFlag = 1;
     fence_after_sync();
     // (2) U (or dY) rows: the high-half rows add the low-half rows through shared memory
+    float y[16];
     {
-      float u[16];
-      tmem_ld16(tU + lane_base + 16 * half, u);
+      uint32_t ra[16], rb[16];
+      tmem_ld16_async(tU + lane_base + cv, ra);
+      tmem_ld16_async(tU + lane_base + 32 + cv, rb);
+      tmem_wait_ld();
+      float p[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) p[t] = __uint_as_float(ra[t]) + __uint_as_float(rb[t]);
       if (q4 >= 2)
 #pragma unroll
-        for (int t = 0; t < 16; ++t) xch[ir * SM::PX + 16 * half + t] = u[t];
+        for (int t = 0; t < 16; ++t) xch[ir * SM::PX + cv + t] = p[t];
       __syncthreads();
       if (*sFlag) goto fail;
       if (q4 < 2) {
-        float y[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-          const float p = u[t] + xch[ir * SM::PX + 16 * half + t];
-          y[t] = REV ? v_c[t] + p : v_c[t] - p;
-        }
-        float* dst = st + (REV ? R::DY : R::U) + (int64_t)ir * DV + col0 + 16 * half;
-#pragma unroll
-        for (int t = 0; t < 16; t += 4) st4(dst + t, make_float4(y[t], y[t + 1], y[t + 2], y[t + 3]));
-        const int tok = c * kC + ir;
-        if (REV && tok < len) {
-          float* dv = ba.dv.ptr + bq * ba.dv.sb + (t0 + tok) * ba.dv.st + (int64_t)h * ba.dv.sh + col0 + 16 * half;
-#pragma unroll
-          for (int t = 0; t < 16; t += 4)
-            st4(dv + t, make_float4(be_c * y[t], be_c * y[t + 1], be_c * y[t + 2], be_c * y[t + 3]));
+          const float q = p[t] + xch[ir * SM::PX + cv + t];
+          y[t] = REV ? v_c[t] + q : v_c[t] - q;
         }
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           float z[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) z[e] = y[8 * cc + e];
-          store_split8(s0 + SM::UH, s0 + SM::UL, sw128(ir, 16 * half + 8 * cc, 64), z);
+          store_split8(s0 + SM::UB + sw128(ir, cv + 8 * cc, 64), s0 + SM::UB + sw128(ir, 32 + cv + 8 * cc, 64), 0u, z);
         }
       }
     }
@@ -1247,17 +1276,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_pass_tc_kernel(ChunkBwd
     __syncthreads();
     if (tid == 0) {
       fence_after_sync();
-      const uint32_t ids = idesc_bf16(128, 32, true, true);
-      const uint32_t m1 = s0 + (uint32_t)b * SM::BUF + SM::M1;
+      const uint32_t i64 = idesc_bf16(128, 64, true, true), i32 = idesc_bf16(128, 32, true, true);
+      const uint64_t am = b ? dM1 : dM0;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        const uint64_t ah = desc_mnmajor(m1, kC, ks), al = desc_mnmajor(m1 + 16384, kC, ks);
-        const uint64_t uh = desc_mnmajor(s0 + SM::UH, kC, ks), ul = desc_mnmajor(s0 + SM::UL, kC, ks);
-        mma_bf16(tS, ah, uh, ids, 1u);
-        mma_bf16(tS, al, uh, ids, 1u);
-        mma_bf16(tS, ah, ul, ids, 1u);
+        mma_bf16(tS, am + (uint64_t)(ks * 128), dUB + (uint64_t)(ks * 128), i64, 1u);          // K_hi [U_hi | U_lo]
+        mma_bf16(tS, am + (uint64_t)(ks * 128 + 1024), dUB + (uint64_t)(ks * 128), i32, 1u);   // K_lo U_hi
       }
       mma_commit(ms);
+    }
+    if (q4 < 2) {  // the U (or dY) record and dv, while the state update runs
+      float* dst = st + (REV ? R::DY : R::U) + (int64_t)ir * DV + col0 + cv;
+#pragma unroll
+      for (int t = 0; t < 16; t += 4) st4(dst + t, make_float4(y[t], y[t + 1], y[t + 2], y[t + 3]));
+      const int tok = c * kC + ir;
+      if (REV && tok < len) {
+        float* dv = ba.dv.ptr + bq * ba.dv.sb + (t0 + tok) * ba.dv.st + (int64_t)h * ba.dv.sh + col0 + cv;
+#pragma unroll
+        for (int t = 0; t < 16; t += 4)
+          st4(dv + t, make_float4(be_c * y[t], be_c * y[t + 1], be_c * y[t + 2], be_c * y[t + 3]));
+      }
     }
     if (!mbar_wait(ms, (uint32_t)(k & 1))) *sFlag = 1;
     fence_after_sync();
@@ -1265,12 +1303,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) kda_bwd_pass_tc_kernel(ChunkBwd
     if (*sFlag) goto fail;
   }
   // reverse: the initial-state gradient is the last X
-  if (REV && ba.ds0 && warp < 4) {
-    float v[32];
-    tmem_ld32(tS + lane_base, v);
-    float* dst = ba.ds0 + n * ba.ds0_sn + h * ba.ds0_sh + (int64_t)d * DV + col0;
+  if (REV && ba.ds0) {
+    uint32_t ra[16], rb[16];
+    tmem_ld16_async(tS + lane_base + cv, ra);
+    tmem_ld16_async(tS + lane_base + 32 + cv, rb);
+    tmem_wait_ld();
+    float* dst = ba.ds0 + n * ba.ds0_sn + h * ba.ds0_sh + (int64_t)d * DV + col0 + cv;
 #pragma unroll
-    for (int t = 0; t < 32; t += 4) st4(dst + t, make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]));
+    for (int t = 0; t < 16; t += 4)
+      st4(dst + t, make_float4(__uint_as_float(ra[t]) + __uint_as_float(rb[t]),
+                               __uint_as_float(ra[t + 1]) + __uint_as_float(rb[t + 1]),
+                               __uint_as_float(ra[t + 2]) + __uint_as_float(rb[t + 2]),
+                               __uint_as_float(ra[t + 3]) + __uint_as_float(rb[t + 3])));
   }
   fence_before_sync();
   __syncthreads();
