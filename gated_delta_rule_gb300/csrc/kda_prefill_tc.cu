@@ -1011,18 +1011,33 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
       const uint32_t mb = mbar_rec0 + 8 * b;
       if (lane == 0) {
         const unsigned char* src = sp.rec + (rec0 + (int64_t)(c0 + ci) * a.H) * R::kBytes;
-        mbar_arrive_expect_tx(mb, R::kBytes);
-        bulk_g2s(dst, src, kT2, mb);
-        bulk_g2s(dst + 2 * kT2, src + kT2, R::kBytes - kT2, mb);
+        if (outs) {
+          mbar_arrive_expect_tx(mb, R::kBytes);
+          bulk_g2s(dst, src, kT2, mb);
+          bulk_g2s(dst + 2 * kT2, src + kT2, R::kBytes - kT2, mb);
+        } else {
+          // no outputs: A_Q and the Q+ rows of [-W ; Q+] are not needed, nor T_beta
+          // without values.  -W is rows 0-63 of each 128-row panel of that tile.
+          constexpr uint32_t kHalfPanel = 64 * 128, kPanel = 2 * kHalfPanel;
+          constexpr uint32_t kTail = R::kBytes - R::KE;  // K_end and e^{G_C}
+          const uint32_t rw = dst + 2 * kT2 + (R::WQ - kT2);
+          mbar_arrive_expect_tx(mb, (vzero ? 0u : (uint32_t)kT2) + 2 * kHalfPanel + kTail);
+          if (!vzero) bulk_g2s(dst, src, kT2, mb);
+          bulk_g2s(rw, src + R::WQ, kHalfPanel, mb);
+          bulk_g2s(rw + kPanel, src + R::WQ + kPanel, kHalfPanel, mb);
+          bulk_g2s(dst + 2 * kT2 + (R::KE - kT2), src + R::KE, kTail, mb);
+        }
       }
-      const int lc = vzero ? 0 : min(kC, rg.len - (c0 + ci) * kC);  // no values: zero fill
-      constexpr int kVec = DV / 8;
+      if (!vzero) {
+        const int lc = min(kC, rg.len - (c0 + ci) * kC);
+        constexpr int kVec = DV / 8;
 #pragma unroll 4
-      for (int idx = lane; idx < 64 * kVec; idx += 32) {
-        const int t = idx / kVec, cv = idx % kVec;
-        const bool ok = t < lc;
-        const __nv_bfloat16* src = ok ? vg + ((int64_t)(c0 + ci) * kC + t) * a.v.st + 8 * cv : vg;
-        cp_async16(sbase + L::VT + b * 64 * L::kPitch * 2 + sw128(t, 8 * cv, 64), src, ok ? 16u : 0u);
+        for (int idx = lane; idx < 64 * kVec; idx += 32) {
+          const int t = idx / kVec, cv = idx % kVec;
+          const bool ok = t < lc;
+          const __nv_bfloat16* src = ok ? vg + ((int64_t)(c0 + ci) * kC + t) * a.v.st + 8 * cv : vg;
+          cp_async16(sbase + L::VT + b * 64 * L::kPitch * 2 + sw128(t, 8 * cv, 64), src, ok ? 16u : 0u);
+        }
       }
       cp_async_mbar_arrive(mb);
     }
@@ -1047,7 +1062,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
       if (ci >= 2) wait(mbar_orel0 + 8 * b, (uint32_t)(((ci - 2) >> 1) & 1));
       // [U ; Q+ S] = [T_beta | -W ; 0 | Q+] [V ; S]; the V half needs no state, so it
       // is issued before the state's bf16 copy is ready
-      if (lane == 0 && !*sFlag) {
+      if (lane == 0 && !*sFlag && !vzero) {
         fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
@@ -1058,10 +1073,12 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
       bar_sync(1, 160);
       if (lane == 0 && !*sFlag) {
         fence_after_sync();
+        // without values the state product starts the accumulator (rows 64..127,
+        // Q+ S, are only read for outputs)
 #pragma unroll
         for (int ks = 0; ks < DK / 16; ++ks)
           mma_bf16(tX(b), desc_kmajor(rWQ, 128, ks), desc_mnmajor(sbase + L::SB, DK, ks),
-                   idesc_bf16(128, DV, false, true), 1u);
+                   idesc_bf16(128, DV, false, true), (vzero && ks == 0) ? 0u : 1u);
         mma_commit(mbar_a);
       }
       __syncwarp();
@@ -1074,10 +1091,11 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
           mma_bf16(tS, desc_mnmajor(rKE, 64, ks), desc_mnmajor(vt, 64, ks),
                    idesc_bf16(128, DV, true, true), 1u);
         mma_commit(mbar_s);
+        if (outs)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tX(b), desc_kmajor(rAQ - 64 * 128, 64, ks), desc_mnmajor(vt, 64, ks),
-                   idesc_bf16(128, DV, false, true), 1u);
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tX(b), desc_kmajor(rAQ - 64 * 128, 64, ks), desc_mnmajor(vt, 64, ks),
+                     idesc_bf16(128, DV, false, true), 1u);
         mma_commit(mbar_free0 + 8 * b);  // chunk ci's output is ready; its buffers are free
       }
       __syncwarp();
