@@ -271,10 +271,15 @@ def max_over_ranks(x, world):
 
 
 # source files each kernel is compiled from (their hash dates a traffic record)
+_BWD_TC = ["kda_backward_tc.cu", "kda_backward_chunk.cuh", "kda_sm100.cuh", "kda_internal.h"]
 KERNEL_SOURCES = {
     "kda_chunk_prep_kernel": ["kda_prefill_tc.cu", "kda_sm100.cuh", "kda_internal.h"],
     "kda_chunk_serial_kernel": ["kda_prefill_tc.cu", "kda_sm100.cuh", "kda_internal.h"],
     "kda_decode_kernel": ["kda_recurrent.cu", "kda_internal.h"],
+    "kda_bwd_prep_tc_kernel": _BWD_TC,
+    "kda_bwd_pass_tc_kernel<0>": _BWD_TC,
+    "kda_bwd_pass_tc_kernel<1>": _BWD_TC,
+    "kda_bwd_grad_tc_kernel": _BWD_TC,
 }
 
 
@@ -286,14 +291,14 @@ def source_sha(kernel):
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel):
-    """DRAM bytes (read + write) per launch from the committed ncu summary
-    (profiles/traffic.json), if it was taken on the kernel's current sources;
-    else None."""
+def committed_traffic(kernel, workload):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from the
+    committed ncu summary (profiles/traffic.json), if it was taken on the kernel's
+    current sources; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p) or kernel not in KERNEL_SOURCES:
         return None
-    d = json.load(open(p)).get(kernel)
+    d = json.load(open(p)).get(kernel, {}).get(workload)
     if not d or d.get("source_sha") != source_sha(kernel):
         return None
     return d.get("bytes_per_launch")
@@ -397,7 +402,7 @@ def kernel_roofline(r, pk, world):
     ms = max_over_ranks(timed[name], world)
     gbs = r["kernel_bytes"][name] / (ms * 1e-3) / 1e9
     return {"bound": "hbm", "kernel": name, "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
-            "frac": gbs / pk["hbm"], "traffic": committed_traffic(name),
+            "frac": gbs / pk["hbm"], "traffic": committed_traffic(name, r["name"]),
             "peak_source": pk["src"] + " (burst copy)",
             "algorithmic_bytes_per_launch": r["kernel_bytes"][name],
             "launch_ms": ms,
@@ -584,15 +589,15 @@ def bench_decode_fused(kda, steps_total, warmup, stream, clk=None):
     return dict(ms=ms, N=N, H=H, bytes=N * H * per_head, launches=launches, steps=steps_total)
 
 
-CHUNK_BWD_KERNELS = ["kda_bwd_prep_tc_kernel", "kda_bwd_state_fwd_kernel", "kda_bwd_state_rev_kernel",
+CHUNK_BWD_KERNELS = ["kda_bwd_prep_tc_kernel", "kda_bwd_pass_tc_kernel<0>", "kda_bwd_pass_tc_kernel<1>",
                      "kda_bwd_grad_tc_kernel"]
 def chunk_bwd_bytes(dk, dv, C=64):
     """Algorithmic bytes per (chunk, head) of the four tensor-core kernels of the
     chunked backward (each tensor counted once per chunk and head).
     Prep: reads the bf16 q, k, v and dO rows, g and beta; writes the record (four
     [C][d_k] and two [C][d_v] matrices, e^{G_C}, the [d_k][d_v] Z_q, the [C][C] A).
-    Forward pass: reads W, K_end, U_bar, e^{G_C}; writes the state S and U.
-    Reverse pass: reads W_y, diag(beta) K+, V_y, Z_q, e^{G_C}, beta; writes X, dY, dv.
+    Forward pass (kda_bwd_pass_tc_kernel<0>): reads W, K_end, U_bar, e^{G_C}; writes S and U.
+    Reverse pass (<1>): reads W_y, diag(beta) K+, V_y, Z_q, e^{G_C}, beta; writes X, dY, dv.
     Gradient kernel: reads S, X, U, dY, A, the bf16 q, k, v, dO rows, g and beta; writes
     fp32 dq, dk, dg and dbeta."""
     inputs = 2 * C * (2 * dk + 2 * dv) + 4 * C * dk + 4 * C
@@ -601,11 +606,11 @@ def chunk_bwd_bytes(dk, dv, C=64):
     fwd = 4 * (2 * C * dk + C * dv + dk) + state
     rev = 4 * (2 * C * dk + C * dv + dk * dv + dk + C) + state + 4 * C * dv
     grad = inputs + 2 * state + 4 * C * C + 4 * (3 * C * dk + C)
-    return {"kda_bwd_prep_tc_kernel": inputs + rec, "kda_bwd_state_fwd_kernel": fwd,
-            "kda_bwd_state_rev_kernel": rev, "kda_bwd_grad_tc_kernel": grad}
+    return {"kda_bwd_prep_tc_kernel": inputs + rec, "kda_bwd_pass_tc_kernel<0>": fwd,
+            "kda_bwd_pass_tc_kernel<1>": rev, "kda_bwd_grad_tc_kernel": grad}
 
 
-def chunk_bwd_roofline(bw, ms, kernel_ms, hbm_peak):
+def chunk_bwd_roofline(bw, ms, kernel_ms, hbm_peak, workload):
     """``roofline`` of the chunked backward for its dominant kernel (bound "hbm",
     algorithmic bytes over the kernel's event time), every kernel's rate beside it."""
     by = {n: b * bw["chunk_heads"] for n, b in chunk_bwd_bytes(bw["dk"], bw["dv"]).items()}
@@ -617,7 +622,7 @@ def chunk_bwd_roofline(bw, ms, kernel_ms, hbm_peak):
     k = max(kernel_ms, key=kernel_ms.get)
     call = sum(by.values()) / (ms * 1e-3) / 1e9
     return {"bound": "hbm", "kernel": k, "achieved": rates[k]["achieved"], "peak": hbm_peak, "unit": "GB/s",
-            "frac": rates[k]["frac"], "traffic": None, "peak_source": "measured (burst copy)",
+            "frac": rates[k]["frac"], "traffic": committed_traffic(k, workload), "peak_source": "measured (burst copy)",
             "bytes_per_launch": by[k], "call_gbs": call, "call_frac": call / hbm_peak, "kernel_rates": rates}
 
 
@@ -907,7 +912,7 @@ def main():
         "steps_per_s": world * 1e3 / dms, "tokens_per_s": world * dec["N"] * 1e3 / dms,
         "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": d_gbs,
                      "peak": pk["hbm"], "unit": "GB/s", "frac": d_gbs / pk["hbm"],
-                     "traffic": committed_traffic("kda_decode_kernel"),
+                     "traffic": committed_traffic("kda_decode_kernel", dec["name"]),
                      "algorithmic_bytes_per_launch": dec["bytes"]},
         "clocks": clk_dec.summary(), "gpu_launches": dec["launches"]}
     gr = dec["graph"]
@@ -963,7 +968,8 @@ def main():
         "kernel_ms": {n: max_over_ranks(v, world) for n, v in bw["kernel_ms"].items()},
         "tokens_per_s": world * bw["tokens"] / (bms * 1e-3),
         "hbm_frac": bw["bytes"] / (bms * 1e-3) / 1e9 / pk["hbm"], "gpu_launches": bw["launches"]}
-    extra["backward"]["roofline"] = chunk_bwd_roofline(bw, bms, extra["backward"]["kernel_ms"], pk["hbm"])
+    extra["backward"]["roofline"] = chunk_bwd_roofline(bw, bms, extra["backward"]["kernel_ms"], pk["hbm"],
+                                                       extra["backward"]["workload"])
     bw = bench_backward(kda, 3, 3, stream, "kda_backward")
     bms = max_over_ranks(bw["ms"], world)
     extra["backward_token_loop"] = {
