@@ -89,3 +89,25 @@ def test_checkpoint_at_sequence_end(kda):
     d = ki.prefill_inputs(1, 512, 2, 64, 64, "bf16", seed=84, s0=True)
     out, sT, cks = _run(kda, d, 256, 2)
     assert torch.equal(cks[1], sT[0])  # the last checkpoint is the final state
+
+
+def test_checkpoints_with_full_width_slices(kda):
+    """96 heads at d_v = 128: the serial kernel runs one 128-column CTA per head
+    (eight TMEM warps, each holding half of a state row), while one head alone runs
+    as four 32-column CTAs.  Checkpoints, outputs and final states of the two
+    agree bit for bit (columns never mix), and a head matches the oracle."""
+    d = ki.prefill_inputs(1, 640 + 37, 96, 128, 128, "bf16", seed=85, s0=True)
+    ck, C = 128, 5
+    out, sT, cks = _run(kda, d, ck, C)
+    for h in (0, 47, 95):
+        one = {k: (v[:, :, h:h + 1].contiguous() if k in ("q", "k", "v", "g") else v) for k, v in d.items()}
+        one["beta"] = d["beta"][:, :, h:h + 1].contiguous()
+        one["initial_state"] = d["initial_state"][:, h:h + 1].contiguous()
+        o1, s1, c1 = _run(kda, one, ck, C)
+        assert torch.equal(o1, out[:, :, h:h + 1]) and torch.equal(s1, sT[:, h:h + 1]), h
+        assert torch.equal(c1, cks[:, h:h + 1]), h
+    h = 47
+    ref = oracle.prefill_checkpoints(d["q"][:, :, h:h + 1], d["k"][:, :, h:h + 1], d["v"][:, :, h:h + 1],
+                                     d["g"][:, :, h:h + 1], d["beta"][:, :, h:h + 1],
+                                     d["initial_state"][:, h:h + 1], d["scale"], ck, C)
+    _compare(cks[:, h:h + 1], ref, 1e-2)
