@@ -88,6 +88,38 @@ def test_chunk_bwd_tensor_core_varlen_and_strongest_decay(kda):
     _check(kda, d, _do(1, T, 2, 128, "bf16", 18), dST, "tc varlen, g=-5")
 
 
+def test_chunk_bwd_tensor_core_strided_views(kda):
+    """q, k, v as head slices of a fused projection and d_out inside a wider buffer
+    (non-contiguous head and token strides), on the tensor-core kernels."""
+    B, T, H, D = 1, 150, 3, 128
+    d = ki.prefill_inputs(B, T, H, D, D, "bf16", seed=230, s0=True)
+    fused = torch.empty(B, T, H, 3 * D, dtype=torch.bfloat16, device="cuda")
+    fused[..., :D] = d["q"].cuda()
+    fused[..., D:2 * D] = d["k"].cuda()
+    fused[..., 2 * D:] = d["v"].cuda()
+    q, k, v = fused[..., :D], fused[..., D:2 * D], fused[..., 2 * D:]
+    do = _do(B, T, H, D, "bf16", 231)
+    wide = torch.zeros(B, T, H, D + 64, dtype=torch.bfloat16, device="cuda")
+    wide[..., :D] = do.cuda()
+    dST = torch.randn(B, H, D, D, generator=torch.Generator().manual_seed(232))
+    got = kda.kda_chunk_bwd(q, k, v, d["g"].cuda(), d["beta"].cuda(), d["initial_state"].cuda(), d["scale"],
+                            wide[..., :D], dST.cuda())
+    ref = oracle.backward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], d["scale"], do, dST)
+    for name in NAMES + ("d_initial_state",):
+        err = rel_fro(got[name], ref[name])
+        assert err <= TOL, f"{name}: {err:.3g}"
+
+
+@pytest.mark.parametrize("beta_value", [0.0, 1.0])
+def test_chunk_bwd_tensor_core_extreme_beta(kda, beta_value):
+    """beta = 0 (no writes: T = I, the state only decays) and beta = 1 (full
+    delta-rule overwrite) on the tensor-core kernels."""
+    d = ki.prefill_inputs(1, 130, 2, 128, 128, "bf16", seed=233, s0=True)
+    d["beta"] = torch.full_like(d["beta"], beta_value)
+    dST = torch.randn(1, 2, 128, 128, generator=torch.Generator().manual_seed(234))
+    _check(kda, d, _do(1, 130, 2, 128, "bf16", 235), dST, f"beta={beta_value}")
+
+
 def test_chunk_bwd_without_states(kda):
     d = ki.prefill_inputs(1, 100, 1, 128, 128, "bf16", seed=211, s0=False)
     _check(kda, d, _do(1, 100, 1, 128, "bf16", 6), None, "no s0", need_s0=False)
