@@ -794,7 +794,8 @@ def ncu_case(which):
     """Two untimed launches of one workload, for profiler captures: ``prefill`` (B2
     H16 T4096), ``prefill96`` (96 heads x 32768), ``varlen`` (the 1M-token headline),
     ``bwd`` (kda_chunk_bwd on B2 H16 T4096), ``decode32`` / ``decode`` (32 or 256
-    requests x 96 heads)."""
+    requests x 96 heads), ``multi32`` / ``multi`` (4-token multi-step decode on 32 or
+    256 requests x 96 heads)."""
     import gated_delta_rule_gb300 as kda
     kda.build()
     kda.load_library()
@@ -821,8 +822,14 @@ def ncu_case(which):
         S = ki.decode_state(N, w["H"], w["dk"], w["dv"], seed=1).to(dev)
         x = ki.decode_inputs(N, w["H"], w["dk"], w["dv"], "bf16", seed=1, step=0)
         x = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+        if which.startswith("multi"):
+            x = ki.prefill_inputs(N, 4, w["H"], w["dk"], w["dv"], "bf16", seed=2)
+            x = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
         for _ in range(2):
-            kda.kda_recurrent_step(S, x["q"], x["k"], x["v"], x["g"], x["beta"], scale=x["scale"])
+            if which.startswith("multi"):
+                kda.kda_recurrent_multi_step(S, x["q"], x["k"], x["v"], x["g"], x["beta"], scale=x["scale"])
+            else:
+                kda.kda_recurrent_step(S, x["q"], x["k"], x["v"], x["g"], x["beta"], scale=x["scale"])
     torch.cuda.synchronize()
     kda.kda_get_device_error()
     print(json.dumps({"ncu_case": which, "ok": True}))
@@ -851,7 +858,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-k3", action="store_true")
-    ap.add_argument("--ncu-case", choices=["prefill", "prefill96", "varlen", "bwd", "decode32", "decode"],
+    ap.add_argument("--ncu-case", choices=["prefill", "prefill96", "varlen", "bwd", "decode32", "decode", "multi32", "multi"],
                     help="run two untimed launches of one workload (for ncu captures) and exit")
     args = ap.parse_args()
     if args.ncu_case:

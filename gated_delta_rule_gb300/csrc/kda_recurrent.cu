@@ -1,9 +1,10 @@
 // SIMT kernels of the KDA core:
 //   * kda_decode_kernel     - one decode token per (request, head), state in place;
-//   * kda_recurrent_kernel  - token-by-token prefill with the state held in
-//                             registers (the fp32-input path, any sequence length),
-//                             also the multi-token decode step (requests as
-//                             sequences, the state kept after an accepted count);
+//   * kda_recurrent_kernel  - token-recurrent prefill with the state held in
+//                             registers, four tokens per pass over the state (the
+//                             fp32-input path, any sequence length), also the
+//                             multi-token decode step (requests as sequences, the
+//                             state kept after an accepted count);
 //   * kda_decode_front_kernel, kda_decode_back_kernel - the front end (short
 //                             convolutions, SiLU, L2 norms) and back end (RMS
 //                             norm, output gate) around kda_decode_kernel in the
@@ -11,26 +12,25 @@
 //   * kda_backward_kernel   - reverse-mode derivative of the token recurrence;
 //   * kda_seqlens_kernel    - device-side validation of cu_seqlens.
 //
-// Both compute kernels run the single-step recurrence in the order of
+// The decode kernel runs the single-step recurrence in the order of
 // "Kimi K3 核心算子拆解" (devpress.csdn.net) §2.3: decay every key-channel row by
 // alpha_i = exp(g_i), subtract beta k (k^T S), add beta k v^T, then read out
 // o = scale * S^T q ("Kimi K3 技术报告解读" (marsggbo.github.io) §3.2).  The
 // correction and the write are two fused multiply-adds per element,
 //   S' = fma(beta k_i, v_j, fma(-beta k_i, (k^T S)_j, S_ij)),
-// so a unit key with beta = 1 reproduces v exactly in that row.
+// so a unit key with beta = 1 reproduces v exactly in that row.  The
+// token-recurrent kernel takes the same recurrence four tokens at a time in its
+// unrolled form (derived above that kernel): the same values up to fp32
+// rounding, with the state read twice and written once per four tokens.
 //
 // Thread layout of the decode and token-recurrent kernels (128 threads per
 // (sequence|request, head, 64 value columns); four CTAs per SM for the decode
-// step, five for the token loop, whose arithmetic per state byte is higher and
-// which gains more from the extra CTA than it loses to a few spilled
-// registers): a 64-column
+// step, five for the token-recurrent kernel): a 64-column
 // state row slice is covered by 16 threads holding 4 consecutive columns (one
 // 16-byte vector each); 8 rows are handled side by side and each thread keeps
 // d_k/8 rows in registers.  (The backward kernel uses 256 threads, 16 rows side
-// by side.)  Column sums over the key channels
-// (k^T S and q^T S) are reduced through shared memory in the same order in both
-// compute kernels.  A warp loads and stores two 256-byte row slices per
-// instruction.
+// by side.)  Column sums over the key channels are reduced through shared
+// memory.  A warp loads and stores two 256-byte row slices per instruction.
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -47,6 +47,13 @@ template <>
 __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
 template <typename T>
 __device__ __forceinline__ float4 load4(const T* p);
@@ -85,6 +92,21 @@ __device__ __forceinline__ void fma4(float4& acc, float s, const float4& x) {
   acc.z = fmaf(s, x.z, acc.z);
   acc.w = fmaf(s, x.w, acc.w);
 }
+
+// asynchronous global -> shared copies (the token-recurrent kernel's inputs)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // S' = fma(bk, v, fma(-bk, kS, S)) element-wise
 __device__ __forceinline__ float4 delta_write(float4 s, float bk, const float4& kS, const float4& v) {
@@ -646,16 +668,69 @@ __global__ void kda_backward_merge_kernel(BackwardArgs ba) {
 }
 
 // ---------------------------------------------------------------------------
-// token-by-token prefill: one CTA per (sequence, head, DV value columns), state in
-// registers.  The state's columns evolve independently, so a (sequence, head)
-// may be spread over a.dv / DV CTAs.
+// token-recurrent prefill and multi-token decode: one CTA per (sequence, head, DV
+// value columns), state in registers, tokens taken kNB at a time.  The state's
+// columns evolve independently, so a (sequence, head) may be spread over
+// a.dv / DV CTAs.
+//
+// A block of tokens 0 .. l (l < kNB) entering with state S is the single-step
+// recurrence unrolled.  With G_t the in-block sum of g up to and including t,
+//   delta_t = v_t - S^T (e^{G_t} k_t) - sum_{s<t} L_ts delta_s,
+//   o_t     = scale (S^T (e^{G_t} q_t) + sum_{s<=t} M_ts delta_s),
+//   S'      = e^{G_l} S + sum_s (beta_s e^{G_l - G_s} k_s) delta_s^T,
+// L_ts = beta_s sum_i k_ti k_si e^{G_ti - G_si}, M_ts = beta_s sum_i q_ti k_si
+// e^{G_ti - G_si} (every exponent a difference G_t - G_s with s <= t, or G_t
+// itself: none exceeds 0 for g <= 0).  So the state is read twice (the 2 kNB
+// column sums, one reduction) and written once per block, against three passes
+// and two reductions per token one at a time.  Blocks start at the sequence start
+// and end where the accepted tokens end, so the kept state is a block's result.
+constexpr int kNB = 4;  // tokens per block of the token-recurrent kernel
+
+// the pair terms of a block: index of L_ts (s < t) and of M_ts (s <= t)
+__host__ __device__ constexpr int l_index(int t, int s) { return t * (t - 1) / 2 + s; }
+__host__ __device__ constexpr int m_index(int t, int s) { return kNB * (kNB - 1) / 2 + t * (t + 1) / 2 + s; }
+constexpr int kPairs = kNB * (kNB - 1) / 2 + kNB * (kNB + 1) / 2;  // 16
+static_assert(kPairs == 16, "the pair reduction below handles 16 values");
+
+// Warp sum of 16 values per lane, one value per lane pair out: at each level half
+// of the values go to the partner lane, so lane bits 4..1 select the value index
+// (8 b4 + 4 b3 + 2 b2 + b1) and both lanes of a pair return its full warp sum.
+__device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
+  float w8[8], w4[4], w2[2];
+  const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    w8[j] = (h16 ? v[8 + j] : v[j]) + __shfl_xor_sync(0xffffffffu, h16 ? v[j] : v[8 + j], 16);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    w4[j] = (h8 ? w8[4 + j] : w8[j]) + __shfl_xor_sync(0xffffffffu, h8 ? w8[j] : w8[4 + j], 8);
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+    w2[j] = (h4 ? w4[2 + j] : w4[j]) + __shfl_xor_sync(0xffffffffu, h4 ? w4[j] : w4[2 + j], 4);
+  float w = (h2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, h2 ? w2[0] : w2[1], 2);
+  return w + __shfl_xor_sync(0xffffffffu, w, 1);
+}
+
 template <int DK, int DV, typename T, bool GATE>
 __global__ void __launch_bounds__(kTok, 5) kda_recurrent_kernel(PrefillArgs a) {
   using L = Layout<DK, DV, kTok>;
-  __shared__ float s_q[2][DK], s_k[2][DK], s_a[2][DK];
-  __shared__ float4 red0[L::RPP][DV / 4];
-  __shared__ float4 red1[L::RPP][DV / 4];
-  __shared__ float4 tot0[DV / 4], tot1[DV / 4];
+  // a block's inputs as stored, [q | k | g or z | v] and beta per token, brought
+  // in by 16-byte asynchronous copies one block ahead
+  constexpr int kQB = DK * (int)sizeof(T);               // bytes of q, and of k
+  constexpr int kGB = DK * (GATE ? (int)sizeof(T) : 4);  // bytes of g (or z)
+  constexpr int kVB = DV * (int)sizeof(T);               // bytes of this CTA's v columns
+  constexpr int kC = (2 * kQB + kGB + kVB) / 16;         // 16-byte pieces of a token's rows
+  constexpr int kSlot = 16 * kC + 16;                    // + beta
+  constexpr int kW = kTok / 32;
+  __shared__ __align__(16) unsigned char raw[2][kNB][kSlot];
+  __shared__ __align__(16) float kq[DK][2 * kNB];  // per channel: e^{G_t} k_t, then e^{G_t} q_t
+  __shared__ __align__(16) float ke[DK][kNB];      // per channel: beta_t e^{G_l - G_t} k_t
+  __shared__ float dec[DK];                        // e^{G_l}
+  __shared__ float pair_w[kW][kPairs];             // per-warp channel sums of the pair terms
+  __shared__ float lm[kPairs];                     // L and M, beta applied
+  __shared__ __align__(16) float4 redp[kW][2][kNB][DV / 4];  // column sums per warp
+  __shared__ __align__(16) float tot[2][kNB][DV];            // S^T (e^G k), S^T (e^G q)
+  __shared__ __align__(16) float dl[kNB][DV];                // delta
   const int nsl = a.dv / DV;
   const int col0 = (blockIdx.x % nsl) * DV;  // first value column of this CTA
   const int nh = blockIdx.x / nsl;
@@ -663,6 +738,7 @@ __global__ void __launch_bounds__(kTok, 5) kda_recurrent_kernel(PrefillArgs a) {
   const int h = nh - n * a.H;
   const int64_t ld = a.dv;                   // state row stride
   const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   const int col4 = tid % L::TPR;
   const int trow = tid / L::TPR;
 
@@ -688,96 +764,229 @@ __global__ void __launch_bounds__(kTok, 5) kda_recurrent_kernel(PrefillArgs a) {
   // tokens whose update is kept (the rest still produce outputs)
   const int64_t keep = a.accepted ? min(max((int64_t)__ldg(a.accepted + n), (int64_t)0), t1 - t0) : t1 - t0;
   if (!a.out) t1 = t0 + keep;  // nothing to read out past the kept tokens
+  const int64_t tk = t0 + keep;
   const bool has_q = a.q.ptr != nullptr;
+  const bool outs = a.out != nullptr;
 
   const T* qb = has_q ? static_cast<const T*>(a.q.ptr) + b * a.q.sb + h * a.q.sh : nullptr;
   const T* kb = static_cast<const T*>(a.k.ptr) + b * a.k.sb + h * a.k.sh;
-  // per-token decay factors alpha = e^g: g given (fp32), or g = -5 sigmoid(A_h z)
-  // from decay logits z in the input dtype
-  const float* gb = static_cast<const float*>(a.g.ptr) + b * a.g.sb + h * a.g.sh;
-  const T* zb = static_cast<const T*>(a.g.ptr) + b * a.g.sb + h * a.g.sh;
+  // g given (fp32), or decay logits z in the input dtype with g = -5 sigmoid(A_h z)
+  const unsigned char* gbase = static_cast<const unsigned char*>(a.g.ptr) +
+                               (b * a.g.sb + h * a.g.sh) * (GATE ? (int64_t)sizeof(T) : (int64_t)4);
+  const int64_t g_st = a.g.st * (GATE ? (int64_t)sizeof(T) : (int64_t)4);  // token stride, bytes
   const float gsc = GATE ? __ldg(a.gate_scale + h) : 0.f;
-  auto alpha = [&](int64_t t) {
-    if constexpr (GATE) return expf(-5.f / (1.f + expf(-gsc * to_f(zb[t * a.g.st + tid]))));
-    else return expf(__ldg(gb + t * a.g.st + tid));
-  };
   const T* vb = static_cast<const T*>(a.v.ptr) + b * a.v.sb + h * a.v.sh + col0;
   const float* bb = a.beta + b * a.beta_sb + h * a.beta_sh;
-  T* ob = a.out ? static_cast<T*>(a.out) + b * a.out_sb + h * a.out_sh + col0 : nullptr;
+  T* ob = outs ? static_cast<T*>(a.out) + b * a.out_sb + h * a.out_sh + col0 : nullptr;
 
-  // stage token t0 into buffer 0
-  float pq = 0.f, pk = 0.f, pa = 0.f, pb = 0.f;
-  float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (t0 < t1) {
-    if (tid < DK) {
-      pq = has_q ? to_f(qb[t0 * a.q.st + tid]) : 0.f;
-      pk = to_f(kb[t0 * a.k.st + tid]);
-      pa = alpha(t0);
-    }
-    pv = load4<T>(vb + t0 * a.v.st + 4 * col4);
-    pb = __ldg(bb + t0 * a.beta_st);
-  }
-  for (int64_t t = t0; t < t1; ++t) {
-    const int buf = (int)((t - t0) & 1);
-    if (tid < DK) {
-      s_q[buf][tid] = pq;
-      s_k[buf][tid] = pk;
-      s_a[buf][tid] = pa;
-    }
-    const float4 v4 = pv;
-    const float beta = pb;
-    if (t + 1 < t1) {  // prefetch the next token while this one computes
-      if (tid < DK) {
-        pq = has_q ? to_f(qb[(t + 1) * a.q.st + tid]) : 0.f;
-        pk = to_f(kb[(t + 1) * a.k.st + tid]);
-        pa = alpha(t + 1);
+  // blocks of kNB tokens over [t0, tk), then over [tk, t1)
+  auto block_len = [&](int64_t tb) { return (int)min((int64_t)kNB, (tb < tk ? tk : t1) - tb); };
+  auto fetch = [&](int64_t tb, int nb, int buf) {  // one 16-byte piece per thread and step
+    for (int p = tid; p < nb * (kC + 1); p += kTok) {
+      const int j = p / (kC + 1), c = p - j * (kC + 1);
+      const int64_t t = tb + j;
+      unsigned char* slot = raw[buf][j];
+      if (c < kQB / 16) {
+        if (has_q) cp_async16(slot + 16 * c, reinterpret_cast<const unsigned char*>(qb + t * a.q.st) + 16 * c);
+      } else if (c < 2 * kQB / 16) {
+        cp_async16(slot + 16 * c, reinterpret_cast<const unsigned char*>(kb + t * a.k.st) + 16 * c - kQB);
+      } else if (c < (2 * kQB + kGB) / 16) {
+        cp_async16(slot + 16 * c, gbase + t * g_st + 16 * c - 2 * kQB);
+      } else if (c < kC) {
+        cp_async16(slot + 16 * c, reinterpret_cast<const unsigned char*>(vb + t * a.v.st) + 16 * c - 2 * kQB - kGB);
+      } else {
+        cp_async4(slot + 16 * kC, bb + t * a.beta_st);
       }
-      pv = load4<T>(vb + (t + 1) * a.v.st + 4 * col4);
-      pb = __ldg(bb + (t + 1) * a.beta_st);
     }
-    __syncthreads();
-    float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+    cp_async_commit();
+  };
+
+  int64_t tb = t0;
+  int nb = tb < t1 ? block_len(tb) : 0;
+  int buf = 0;
+  if (nb) fetch(tb, nb, 0);
+  while (tb < t1) {
+    const int64_t tn = tb + nb;
+    const int nn = tn < t1 ? block_len(tn) : 0;
+    cp_async_wait<0>();  // this thread's pieces of the block
+    __syncthreads();     // (1) the block's inputs have landed; the previous block is done
+    if (nn) fetch(tn, nn, buf ^ 1);
+
+    // (2) per key channel: decay factors, scaled keys and queries, pair terms
+    if (tid < DK) {
+      const int i = tid;
+      float kk[kNB], qq[kNB], G[kNB], bt[kNB];
+      float gacc = 0.f;
 #pragma unroll
-    for (int r = 0; r < L::R; ++r) {
-      const int i = trow + L::RPP * r;
-      const float al = s_a[buf][i];
-      s[r].x *= al;
-      s[r].y *= al;
-      s[r].z *= al;
-      s[r].w *= al;
-      fma4(part, s_k[buf][i], s[r]);
-    }
-    const float4 kS = column_reduce_lean<DK, DV, kTok>(part, red0, tot0, trow, col4);
-    float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < kNB; ++j) {
+        kk[j] = qq[j] = bt[j] = 0.f;
+        if (j < nb) {
+          const unsigned char* slot = raw[buf][j];
+          kk[j] = to_f(reinterpret_cast<const T*>(slot + kQB)[i]);
+          if (has_q) qq[j] = to_f(reinterpret_cast<const T*>(slot)[i]);
+          if constexpr (GATE)
+            gacc += -5.f / (1.f + expf(-gsc * to_f(reinterpret_cast<const T*>(slot + 2 * kQB)[i])));
+          else
+            gacc += reinterpret_cast<const float*>(slot + 2 * kQB)[i];
+          bt[j] = *reinterpret_cast<const float*>(slot + 16 * kC);
+        }
+        G[j] = gacc;
+      }
+      float4 kp, qp, kd;
+      float* kpv = &kp.x;
+      float* qpv = &qp.x;
+      float* kdv = &kd.x;
 #pragma unroll
-    for (int r = 0; r < L::R; ++r) {
-      const int i = trow + L::RPP * r;
-      s[r] = delta_write(s[r], beta * s_k[buf][i], kS, v4);
-      fma4(po, s_q[buf][i], s[r]);
+      for (int j = 0; j < kNB; ++j) {
+        const float e = expf(G[j]);
+        kpv[j] = kk[j] * e;
+        qpv[j] = qq[j] * e;
+        kdv[j] = bt[j] * kk[j] * expf(gacc - G[j]);
+      }
+      *reinterpret_cast<float4*>(&kq[i][0]) = kp;
+      *reinterpret_cast<float4*>(&kq[i][kNB]) = qp;
+      *reinterpret_cast<float4*>(&ke[i][0]) = kd;
+      dec[i] = expf(gacc);
+      float pv[kPairs];
+#pragma unroll
+      for (int t = 0; t < kNB; ++t) {
+        pv[m_index(t, t)] = qq[t] * kk[t];
+#pragma unroll
+        for (int u = 0; u < t; ++u) {
+          const float e = expf(G[t] - G[u]);
+          pv[l_index(t, u)] = kk[t] * kk[u] * e;
+          pv[m_index(t, u)] = qq[t] * kk[u] * e;
+        }
+      }
+      const float w = warp_sum16(pv, lane);
+      if (!(lane & 1)) pair_w[warp][lane >> 1] = w;  // value index of lane pair lane/2
+    } else if (lane < kPairs) {
+      pair_w[warp][lane] = 0.f;  // warps beyond d_k channels
     }
-    if (a.ckpt && ((t - t0 + 1) % a.ck_tokens) == 0 && (t - t0 + 1) / a.ck_tokens <= a.ck_count) {
-      // prefix-cache checkpoint: the state after (t - t0 + 1) tokens of the sequence
-      float* C = a.ckpt + ((int64_t)n * a.ck_count + (t - t0 + 1) / a.ck_tokens - 1) * a.ck_sr + h * a.ck_sh + col0;
+    __syncthreads();  // (2)
+
+    // (3) the block's column sums: S^T (e^{G_t} k_t), then S^T (e^{G_t} q_t); the two
+    // row groups of a warp are added by one exchange
+#pragma unroll
+    for (int kind = 0; kind < 2; ++kind) {
+      if (kind == 1 && !outs) break;
+      float4 acc[kNB];
+#pragma unroll
+      for (int j = 0; j < kNB; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < L::R; ++r) {
+        const float4 wv = *reinterpret_cast<const float4*>(&kq[trow + L::RPP * r][kind * kNB]);
+        fma4(acc[0], wv.x, s[r]);
+        fma4(acc[1], wv.y, s[r]);
+        fma4(acc[2], wv.z, s[r]);
+        fma4(acc[3], wv.w, s[r]);
+      }
+#pragma unroll
+      for (int j = 0; j < kNB; ++j) {
+        acc[j].x += __shfl_xor_sync(0xffffffffu, acc[j].x, 16);
+        acc[j].y += __shfl_xor_sync(0xffffffffu, acc[j].y, 16);
+        acc[j].z += __shfl_xor_sync(0xffffffffu, acc[j].z, 16);
+        acc[j].w += __shfl_xor_sync(0xffffffffu, acc[j].w, 16);
+        if ((lane >> 4) == kind) redp[warp][kind][j][col4] = acc[j];
+      }
+    }
+    __syncthreads();  // (3)
+
+    // (4) totals over the warps, in warp order; the pair terms times beta_s
+    {
+      const int kind = tid / (kNB * DV / 4), j = (tid / (DV / 4)) % kNB, c4 = tid % (DV / 4);
+      static_assert(2 * kNB * (DV / 4) == kTok, "one column quad of one sum per thread");
+      if (kind == 0 || outs) {
+        float4 x = redp[0][kind][j][c4];
+#pragma unroll
+        for (int w = 1; w < kW; ++w) {
+          const float4 y = redp[w][kind][j][c4];
+          x.x += y.x;
+          x.y += y.y;
+          x.z += y.z;
+          x.w += y.w;
+        }
+        *reinterpret_cast<float4*>(&tot[kind][j][4 * c4]) = x;
+      }
+      if (tid < kPairs) {
+        // the pair's s: L entries first (t = 1.., s < t), then M (s <= t)
+        int u = 0;
+#pragma unroll
+        for (int t = 0; t < kNB; ++t)
+#pragma unroll
+          for (int v = 0; v <= t; ++v) {
+            if (v < t && l_index(t, v) == tid) u = v;
+            if (m_index(t, v) == tid) u = v;
+          }
+        float p = pair_w[0][tid];
+#pragma unroll
+        for (int w = 1; w < kW; ++w) p += pair_w[w][tid];
+        lm[tid] = u < nb ? p * *reinterpret_cast<const float*>(raw[buf][u] + 16 * kC) : 0.f;
+      }
+    }
+    __syncthreads();  // (4)
+
+    // (5) per value column: the deltas in token order, and the outputs
+    if (tid < DV) {
+      const int c = tid;
+      float d[kNB];
+#pragma unroll
+      for (int t = 0; t < kNB; ++t) {
+        d[t] = 0.f;
+        if (t < nb) {
+          float x = to_f(reinterpret_cast<const T*>(raw[buf][t] + 2 * kQB + kGB)[c]) - tot[0][t][c];
+#pragma unroll
+          for (int u = 0; u < t; ++u) x = fmaf(-lm[l_index(t, u)], d[u], x);
+          d[t] = x;
+          if (outs) {
+            float o = tot[1][t][c];
+#pragma unroll
+            for (int u = 0; u <= t; ++u) o = fmaf(lm[m_index(t, u)], d[u], o);
+            ob[(tb + t) * a.out_st + c] = from_f<T>(a.scale * o);
+          }
+        }
+        dl[t][c] = d[t];
+      }
+    }
+    __syncthreads();  // (5)
+
+    // (6) S' = e^{G_l} S + sum_t (beta_t e^{G_l - G_t} k_t) delta_t^T
+    {
+      float4 d4[kNB];
+#pragma unroll
+      for (int j = 0; j < kNB; ++j) d4[j] = *reinterpret_cast<const float4*>(&dl[j][4 * col4]);
+#pragma unroll
+      for (int r = 0; r < L::R; ++r) {
+        const int i = trow + L::RPP * r;
+        const float4 e = *reinterpret_cast<const float4*>(&ke[i][0]);
+        const float de = dec[i];
+        float4 x = s[r];
+        x.x *= de;
+        x.y *= de;
+        x.z *= de;
+        x.w *= de;
+        fma4(x, e.x, d4[0]);
+        fma4(x, e.y, d4[1]);
+        fma4(x, e.z, d4[2]);
+        fma4(x, e.w, d4[3]);
+        s[r] = x;
+      }
+    }
+    const int64_t te = tn;  // tokens done: te - t0
+    if (a.ckpt && ((te - t0) % a.ck_tokens) == 0 && (te - t0) / a.ck_tokens <= a.ck_count) {
+      // prefix-cache checkpoint: the state after (te - t0) tokens of the sequence
+      float* C = a.ckpt + ((int64_t)n * a.ck_count + (te - t0) / a.ck_tokens - 1) * a.ck_sr + h * a.ck_sh + col0;
 #pragma unroll
       for (int r = 0; r < L::R; ++r) *reinterpret_cast<float4*>(C + (trow + L::RPP * r) * ld + 4 * col4) = s[r];
     }
-    if (a.accepted && a.sT && t == t0 + keep - 1) {  // the kept state: written once
+    if (a.accepted && a.sT && te == tk) {  // the kept state: written once
       float* ST = a.sT + n * a.sT_sn + h * a.sT_sh + col0;
 #pragma unroll
       for (int r = 0; r < L::R; ++r) __stcs(reinterpret_cast<float4*>(ST + (trow + L::RPP * r) * ld + 4 * col4), s[r]);
     }
-    if (a.out) {
-      float4 o = column_reduce_lean<DK, DV, kTok>(po, red1, tot1, trow, col4);
-      if (trow == 0) {
-        o.x *= a.scale;
-        o.y *= a.scale;
-        o.z *= a.scale;
-        o.w *= a.scale;
-        store4<T>(ob + t * a.out_st + 4 * col4, o);
-      }
-    }
-    // red0/red1 are rewritten next token only after that token's first barrier,
-    // which every thread reaches after finishing its reads of this token.
+    tb = tn;
+    nb = nn;
+    buf ^= 1;
   }
   if (a.sT && !a.accepted) {
     float* ST = a.sT + n * a.sT_sn + h * a.sT_sh + col0;

@@ -1,6 +1,6 @@
 """Parity of kda_recurrent_multi_step (n decode tokens per request, state kept after
 an accepted count, read once and written once) with the CPU oracle, and its
-equivalence with n calls of kda_recurrent_step."""
+agreement with n calls of kda_recurrent_step."""
 import numpy as np
 import pytest
 import torch
@@ -43,8 +43,11 @@ def test_multi_step_matches_oracle(kda, n, dk, dv, dtype):
     assert torch.equal(Sd.cpu()[0], S[0]) and torch.equal(Sd.cpu()[4], S[4])  # nothing accepted
 
 
-def test_all_accepted_equals_single_steps_bitwise(kda):
-    """With every token accepted, one call equals n calls of kda_recurrent_step, bit for bit."""
+def test_all_accepted_equals_single_steps(kda):
+    """With every token accepted, one call equals n calls of kda_recurrent_step up to
+    fp32 rounding (the multi-token kernel takes four tokens per pass over the state,
+    the single step one): states within 1e-5 of their scale, outputs within one bf16
+    rounding step of theirs."""
     N, n, H, dk, dv = 4, 5, 2, 128, 128
     S, d = _inputs(N, n, H, dk, dv, "bf16", seed=60)
     t = to_dev(d)
@@ -54,8 +57,9 @@ def test_all_accepted_equals_single_steps_bitwise(kda):
     outs = [kda.kda_recurrent_step(S2, t["q"][:, j].contiguous(), t["k"][:, j].contiguous(),
                                    t["v"][:, j].contiguous(), t["g"][:, j].contiguous(),
                                    t["beta"][:, j].contiguous(), scale=d["scale"]) for j in range(n)]
-    assert torch.equal(S1, S2)
-    assert torch.equal(out1, torch.stack(outs, dim=1))
+    assert (S1 - S2).abs().max().item() <= 1e-5 * S2.abs().max().item()
+    o2 = torch.stack(outs, dim=1).float()
+    assert ((out1.float() - o2).abs() <= 2 ** -7 * o2.abs() + 1e-5).all()
 
 
 def test_verify_then_commit(kda):
