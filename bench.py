@@ -818,7 +818,7 @@ def ncu_case(which):
                                   t["scale"], cu_seqlens=t["cu_seqlens"])
     else:
         w = ki.WORKLOADS[DECODE_W]
-        N = 32 if which == "decode32" else w["N"]
+        N = 32 if which in ("decode32", "multi32") else w["N"]
         S = ki.decode_state(N, w["H"], w["dk"], w["dv"], seed=1).to(dev)
         x = ki.decode_inputs(N, w["H"], w["dk"], w["dv"], "bf16", seed=1, step=0)
         x = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
