@@ -48,6 +48,7 @@
 // rows are never read (or are overwritten before they are read).
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "kda_internal.h"
@@ -168,16 +169,21 @@ __device__ __forceinline__ int num_chunks(const Split& sp, int n) {
   return sp.off ? __ldg(sp.off + n + 1) - __ldg(sp.off + n) : sp.nck;
 }
 
-// Segment split of long sequences.  A sequence of more than kSegChunks chunks is
-// cut into segments of kSegChunks chunks counted from its start (so the cut
-// depends on the sequence alone).  Segment 0 runs from the initial state.  Each
-// later ("tail") segment s first runs from zero on the augmented state
-// [S~ | M], which starts as [0 | I] with values [V | 0]: M then equals the
-// product of the chunk transitions Diag(e^{G_C}) - K_end^T W over the segment
-// and S~ the segment's result from a zero state.  The states entering the tail
-// segments follow in order, S_in(s + 1) = M_s S_in(s) + S~_s, and a second
-// pass reruns the tail segments from them, writing their outputs.
-constexpr int kSegChunks = 512;
+// Segment split of long sequences.  A sequence of more than kFirstSeg chunks is
+// cut into a first segment of kFirstSeg chunks and tail segments of kTailSeg
+// chunks, counted from its start (so the cut depends on the sequence alone).
+// Segment 0 runs from the initial state.  Each tail segment s first runs from
+// zero on the augmented state [S~ | M], which starts as [0 | I] with values
+// [V | 0]: M then equals the product of the chunk transitions
+// Diag(e^{G_C}) - K_end^T W over the segment and S~ the segment's result from a
+// zero state.  The states entering the tail segments follow in order,
+// S_in(s + 1) = M_s S_in(s) + S~_s, and a second pass reruns the tail segments
+// from them, writing their outputs.  Every chunk past the first segment is run
+// twice, however the tail is cut; short tail segments give both passes more,
+// shorter units to spread over the SMs.
+constexpr int kFirstSeg = 1152;
+constexpr int kTailSeg = 128;
+static_assert(kTailSeg <= kFirstSeg, "the tail-unit bound of the workspace plan");
 
 struct Seg {
   float* tr;        // [tail unit][H][DK][dv + DK] fp32: (S~ | M) of each tail segment
@@ -188,7 +194,7 @@ struct Seg {
 };
 
 __host__ __device__ __forceinline__ int num_segments(int nc) {
-  return nc > kSegChunks ? (nc + kSegChunks - 1) / kSegChunks : 1;
+  return nc > kFirstSeg ? 1 + (nc - kFirstSeg + kTailSeg - 1) / kTailSeg : 1;
 }
 __device__ __forceinline__ int tail_first(const Seg& sg, int n) { return sg.soff ? __ldg(sg.soff + n) : n * sg.tps; }
 __device__ __forceinline__ int tail_count(const Seg& sg, int N) {
@@ -832,7 +838,7 @@ __device__ __forceinline__ bool serial_unit(const PrefillArgs& a, const Split& s
     const Range rg = seq_range(a, u.n);
     const int nc = min(num_chunks(sp, u.n), (rg.len + kC - 1) / kC);
     u.c0 = 0;
-    u.c1 = min(nc, kSegChunks);
+    u.c1 = min(nc, kFirstSeg);
     u.kind = 0;
     u.col = sl * DV;
     u.m0 = 0;
@@ -858,8 +864,8 @@ __device__ __forceinline__ bool serial_unit(const PrefillArgs& a, const Split& s
   const Range rg = seq_range(a, u.n);
   const int nc = min(num_chunks(sp, u.n), (rg.len + kC - 1) / kC);
   const int sgi = ut - tail_first(sg, u.n) + 1;  // segment index (>= 1)
-  u.c0 = sgi * kSegChunks;
-  u.c1 = min(nc, u.c0 + kSegChunks);
+  u.c0 = kFirstSeg + (sgi - 1) * kTailSeg;
+  u.c1 = min(nc, u.c0 + kTailSeg);
   u.m0 = 0;
   if (pass == 0) {
     const int x0 = xs * DV;
@@ -1419,8 +1425,10 @@ Plan plan(const PrefillArgs& a) {
   p.off_bytes = a.cu_seqlens ? (((int64_t)(a.N + 1) * 4 + 1023) & ~int64_t(1023)) : 0;
   p.rec_bytes = total * a.H * (a.dk == 128 ? Rec<128>::kBytes : Rec<64>::kBytes);
   if (a.cu_seqlens) {
-    // sum over sequences of (segments - 1) <= (sum of chunks) / kSegChunks
-    p.ntail = (int)(total / kSegChunks);
+    // sum over sequences of (segments - 1) <= (sum of chunks) / kTailSeg: a
+    // sequence of nc > kFirstSeg chunks has ceil((nc - kFirstSeg) / kTailSeg)
+    // tail segments, at most nc / kTailSeg as kTailSeg <= kFirstSeg
+    p.ntail = (int)(total / kTailSeg);
     p.tps = 0;
     p.soff_bytes = p.ntail ? (((int64_t)(a.N + 1) * 4 + 1023) & ~int64_t(1023)) : 0;
   } else {
@@ -1459,13 +1467,18 @@ cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
   auto prep = a.gate ? kda_chunk_prep_kernel<DK, true> : kda_chunk_prep_kernel<DK, false>;
   e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, PrepSmem<DK>::kAlloc);
   if (e != cudaSuccess) return e;
-  // Value-column slices: with few chains (sequence-heads), d_v is split into 32- or
-  // 64-column CTAs, as finely as the SMs hold them, so that more SMs carry the
+  // Value-column slices: d_v is split into 32- or 64-column CTAs, as finely as the
+  // first pass's CTAs then still fit on the SMs at once, so that more SMs carry the
   // serial loop and each chunk step moves less.  Every slice CTA reads the whole
-  // chunk record.
+  // chunk record.  The first pass holds every sequence's first segment and, per tail
+  // segment and head, the DV + DK augmented columns; the tail count is exact for
+  // fixed-length batches and, with cu_seqlens, a lower bound from the total chunks.
   constexpr int DVM = DV == 128 ? 64 : DV;
   const int64_t nh = (int64_t)a.N * a.H;
-  const int W = nh * (DV / 32) <= sm_count() ? 32 : (DVM != DV && nh * 2 <= sm_count()) ? DVM : DV;
+  const int64_t tails = a.cu_seqlens ? std::max<int64_t>(0, (int64_t)sp.total - (int64_t)a.N * kFirstSeg) / kTailSeg
+                                     : (int64_t)a.N * pl.tps;
+  auto first_pass_ctas = [&](int w) { return nh * (DV / w) + tails * a.H * ((DV + DK + w - 1) / w); };
+  const int W = first_pass_ctas(32) <= sm_count() ? 32 : (DVM != DV && first_pass_ctas(DVM) <= sm_count()) ? DVM : DV;
   auto ser = W == 32    ? kda_chunk_serial_kernel<DK, 32>
              : W == DVM ? kda_chunk_serial_kernel<DK, DVM>
                         : kda_chunk_serial_kernel<DK, DV>;

@@ -147,9 +147,10 @@ kda_status kda_fused_recurrent_fwd(const kda_tensor* q, const kda_tensor* k,
  *    at d_k = 128 and 41984 at d_k = 64, over B * ceil(T / 64) chunks (with
  *    cu_seqlens: ceil(T / 64) + N, plus a small offset table), so at most
  *    1008 (chunk, head) pairs at d_k = 128, e.g. B=1, H=15, T=4096.  A
- *    sequence longer than 512 chunks (32768 tokens) also needs, per head and
- *    per 512-chunk segment after its first, d_k * (2 d_v + d_k) * 4 bytes
- *    (192 KiB at d_k = d_v = 128) of segment states.
+ *    sequence longer than 1152 chunks (73728 tokens) also needs, per head and
+ *    per 128-chunk segment after its first, d_k * (2 d_v + d_k) * 4 bytes
+ *    (192 KiB at d_k = d_v = 128) of segment states; with cu_seqlens that room
+ *    is set aside for every 128 chunks of the call.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any stream
  *    capture.
@@ -198,7 +199,7 @@ kda_status kda_recurrent_step(kda_tensor* state, const kda_tensor* q, const kda_
  * (j + 1) * checkpoint_tokens tokens of that sequence, exactly the state the
  * chunked recurrence holds there, so a prefill resumed from it (initial_state =
  * the checkpoint, inputs = the rest of the sequence) continues the original
- * run; without the segment split (sequences of at most 32768 tokens) the resumed
+ * run; without the segment split (sequences of at most 73728 tokens) the resumed
  * outputs and final state are bit-identical.
  *
  *   checkpoint_tokens  positive multiple of 64 (the chunk length)

@@ -75,10 +75,12 @@ def test_resume_from_checkpoint_is_bit_exact(kda):
 
 
 def test_checkpoint_on_segment_boundary(kda):
-    """A checkpoint at 32768 tokens falls where the segment split cuts the sequence."""
-    T = 32768 + 200
+    """Checkpoints every 8192 tokens, two of them where the segment split cuts the
+    sequence (after the 1152-chunk first segment and after the first 128-chunk
+    tail segment)."""
+    T = (1152 + 128) * 64 + 200
     d = ki.prefill_inputs(1, T, 1, 128, 128, "bf16", seed=83, s0=True)
-    ck, C = 16384, 2
+    ck, C = 8192, 10
     out, sT, cks = _run(kda, d, ck, C)
     ref = oracle.prefill_checkpoints(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"],
                                      d["scale"], ck, C)

@@ -182,7 +182,7 @@ def test_outputs_stay_inside_their_views(kda, case):
         d = ki.prefill_inputs(1, sum(lens), 2, 128, 64, "bf16", seed=511, s0=True, n_states=len(lens))
         d["cu_seqlens"] = torch.from_numpy(ki.cu_seqlens_from_lengths(lens))
     else:  # a sequence long enough for the segment split, next to a short one
-        lens = [512 * 64 + 333, 90]
+        lens = [(1152 + 128) * 64 + 333, 90]  # a first segment and two tail segments
         d = ki.prefill_inputs(1, sum(lens), 2, 128, 128, "bf16", seed=512, s0=True, n_states=len(lens))
         d["cu_seqlens"] = torch.from_numpy(ki.cu_seqlens_from_lengths(lens))
     t = to_dev(d)

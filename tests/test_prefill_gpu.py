@@ -205,9 +205,9 @@ def test_workload2_sampled_heads(kda):
 def test_workload4_sampled_sequences(kda):
     """1M-token varlen packing (16 sequences x 8 heads) on the GPU; the oracle
     recomputes the shortest, a mid-length and the longest sequence on two heads.
-    The longest (194893 tokens, 3046 chunks) runs the segment split over six
-    512-chunk segments: the first from its initial state, five from the chained
-    (M, S~) transitions, each rerun with outputs."""
+    The longest (194893 tokens, 3046 chunks) runs the segment split: a first
+    segment of 1152 chunks from its initial state, then fifteen tail segments of
+    128 chunks from the chained (M, S~) transitions, each rerun with outputs."""
     d = ki.workload_inputs(4)
     t = to_dev(d)
     out, sT = kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"],
@@ -216,7 +216,7 @@ def test_workload4_sampled_sequences(kda):
     cu = d["cu_seqlens"].numpy()
     lens = np.diff(cu)
     order = np.argsort(lens)
-    assert -(-int(lens[order[-1]]) // 64) > 5 * 512  # the longest sequence spans six segments
+    assert -(-int(lens[order[-1]]) // 64) > 1152 + 14 * 128  # the longest spans sixteen segments
     heads = [1, 6]
     for n in (int(order[0]), int(order[len(order) // 2]), int(order[-1])):
         a, b = int(cu[n]), int(cu[n + 1])
@@ -228,13 +228,14 @@ def test_workload4_sampled_sequences(kda):
     assert torch.isfinite(sT).all()
 
 
-# ---- segment split: sequences longer than 512 chunks (32768 tokens) ----
+# ---- segment split: sequences longer than 1152 chunks (73728 tokens) ----
 
-SEG = 512 * 64  # tokens per segment
+SEG = 1152 * 64   # tokens of a sequence's first segment
+TAIL = 128 * 64   # tokens of each later segment
 
 
-@pytest.mark.parametrize("B,T,H", [(1, SEG + 100, 2),          # two segments, the second of 2 chunks
-                                   (2, 3 * SEG + 200, 1)])     # four segments per sequence
+@pytest.mark.parametrize("B,T,H", [(1, SEG + 100, 2),             # two segments, the second of 2 chunks
+                                   (2, SEG + 2 * TAIL + 200, 1)])  # four segments per sequence
 def test_segment_split_matches_oracle(kda, B, T, H):
     d = ki.prefill_inputs(B, T, H, 128, 128, "bf16", seed=40 + B, s0=True)
     check_prefill(kda.kda_chunk_fwd, d, label=f"segments B{B} T{T}")
@@ -242,14 +243,14 @@ def test_segment_split_matches_oracle(kda, B, T, H):
 
 @pytest.mark.parametrize("dk,dv", [(64, 128), (128, 64), (64, 64)])
 def test_segment_split_head_dims(kda, dk, dv):
-    d = ki.prefill_inputs(1, 2 * SEG + 64 * 7 + 5, 1, dk, dv, "bf16", seed=43, s0=True)
+    d = ki.prefill_inputs(1, SEG + TAIL + 64 * 7 + 5, 1, dk, dv, "bf16", seed=43, s0=True)
     check_prefill(kda.kda_chunk_fwd, d, label=f"segments {dk}x{dv}")
 
 
 def test_segment_split_varlen_bit_exact(kda):
     """Packed long and short sequences: each matches the oracle, and equals the same
     sequence run alone bit for bit (segments are cut from each sequence start)."""
-    lens = [100, SEG + 6000, 0, 2 * SEG + 4000, SEG + 200]
+    lens = [100, SEG + 6000, 0, SEG + 3 * TAIL + 4000, SEG + 200]
     cu = ki.cu_seqlens_from_lengths(lens)
     d = ki.prefill_inputs(1, int(cu[-1]), 1, 128, 128, "bf16", seed=44, s0=True, n_states=len(lens))
     d["cu_seqlens"] = torch.from_numpy(cu)
@@ -258,6 +259,33 @@ def test_segment_split_varlen_bit_exact(kda):
     out, sT = kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"], t["scale"],
                                 cu_seqlens=t["cu_seqlens"])
     for n in (1, 3, 4):
+        a, b = int(cu[n]), int(cu[n + 1])
+        sl = lambda x: x[:, a:b].contiguous()
+        o1, s1 = kda.kda_chunk_fwd(sl(t["q"]), sl(t["k"]), sl(t["v"]), sl(t["g"]), sl(t["beta"]),
+                                   t["initial_state"][n:n + 1].contiguous(), t["scale"])
+        assert torch.equal(out[:, a:b], o1) and torch.equal(sT[n:n + 1], s1), n
+
+
+def test_segment_split_full_width_units(kda):
+    """80 sequence-heads at d = 128: one 128-column CTA per serial unit, and the
+    tail segment's S~ and M halves as two CTAs.  The long sequence matches the
+    oracle and equals the same sequence run alone (one head pair, 32-column CTAs)
+    bit for bit; so do two short ones."""
+    lens = [SEG + 3000] + [300 + 7 * i for i in range(39)]
+    cu = ki.cu_seqlens_from_lengths(lens)
+    d = ki.prefill_inputs(1, int(cu[-1]), 2, 128, 128, "bf16", seed=45, s0=True, n_states=len(lens))
+    d["cu_seqlens"] = torch.from_numpy(cu)
+    t = to_dev(d)
+    out, sT = kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"], t["scale"],
+                                cu_seqlens=t["cu_seqlens"])
+    kda.kda_get_device_error()
+    a, b = int(cu[0]), int(cu[1])
+    sub = {x: d[x][:, a:b] for x in ("q", "k", "v", "g", "beta")}
+    o_ref, s_ref = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"],
+                                  d["initial_state"][0:1], d["scale"])
+    assert max_abs(out[:, a:b], o_ref) <= 2e-2
+    assert rel_fro(sT[0:1], s_ref) <= 1e-2
+    for n in (0, 5, 39):
         a, b = int(cu[n]), int(cu[n + 1])
         sl = lambda x: x[:, a:b].contiguous()
         o1, s1 = kda.kda_chunk_fwd(sl(t["q"]), sl(t["k"]), sl(t["v"]), sl(t["g"]), sl(t["beta"]),
