@@ -276,6 +276,7 @@ KERNEL_SOURCES = {
     "kda_chunk_prep_kernel": ["kda_prefill_tc.cu", "kda_sm100.cuh", "kda_internal.h"],
     "kda_chunk_serial_kernel": ["kda_prefill_tc.cu", "kda_sm100.cuh", "kda_internal.h"],
     "kda_decode_kernel": ["kda_recurrent.cu", "kda_internal.h"],
+    "kda_recurrent_kernel": ["kda_recurrent.cu", "kda_internal.h"],
     "kda_bwd_prep_tc_kernel": _BWD_TC,
     "kda_bwd_pass_tc_kernel<0>": _BWD_TC,
     "kda_bwd_pass_tc_kernel<1>": _BWD_TC,
@@ -946,11 +947,13 @@ def main():
     ms4 = bench_multi_step(kda, 4, args.warmup, stream, clk_ms)
     m_ms = max_over_ranks(ms4["ms"], world)
     m_gbs = ms4["bytes"] / (m_ms * 1e-3) / 1e9
+    m_wl = f"kda_multi_step_N{ms4['N']}_H{ms4['H']}_n{ms4['n']}_d128"
     extra["decode_multi_token"] = {
-        "workload": f"kda_multi_step_N{ms4['N']}_H{ms4['H']}_n{ms4['n']}_d128", "ms_per_call": m_ms,
+        "workload": m_wl, "ms_per_call": m_ms,
         "tokens_per_s": world * ms4["N"] * ms4["n"] * 1e3 / m_ms,
         "roofline": {"bound": "hbm", "kernel": "kda_recurrent_kernel", "achieved": m_gbs,
                      "peak": pk["hbm"], "unit": "GB/s", "frac": m_gbs / pk["hbm"],
+                     "traffic": committed_traffic("kda_recurrent_kernel", m_wl),
                      "algorithmic_bytes_per_launch": ms4["bytes"]},
         "clocks": clk_ms.summary(), "gpu_launches": ms4["launches"]}
     del ms4
