@@ -266,6 +266,28 @@ def test_segment_split_varlen_bit_exact(kda):
         assert torch.equal(out[:, a:b], o1) and torch.equal(sT[n:n + 1], s1), n
 
 
+def test_segment_split_64_column_units(kda):
+    """20 heads of one 73828-token sequence: with its tail segment the first pass
+    holds 60 units, so the serial kernel runs 64-column slices (120 CTAs).  Two
+    heads match the oracle, and a head run alone (32-column slices) equals its
+    slice of the batch bit for bit."""
+    d = ki.prefill_inputs(1, SEG + 100, 20, 128, 128, "bf16", seed=46, s0=True)
+    t = to_dev(d)
+    out, sT = kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["initial_state"], t["scale"])
+    kda.kda_get_device_error()
+    for h in (3, 17):
+        sub = {x: d[x][:, :, h:h + 1] for x in ("q", "k", "v", "g", "beta")}
+        o_ref, s_ref = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"],
+                                      d["initial_state"][:, h:h + 1], d["scale"])
+        assert max_abs(out[:, :, h:h + 1], o_ref) <= 2e-2, h
+        assert rel_fro(sT[:, h:h + 1], s_ref) <= 1e-2, h
+    h = 17
+    sl = lambda x: x[:, :, h:h + 1].contiguous()
+    o1, s1 = kda.kda_chunk_fwd(sl(t["q"]), sl(t["k"]), sl(t["v"]), sl(t["g"]), sl(t["beta"]),
+                               t["initial_state"][:, h:h + 1].contiguous(), t["scale"])
+    assert torch.equal(o1, out[:, :, h:h + 1]) and torch.equal(s1, sT[:, h:h + 1])
+
+
 def test_segment_split_full_width_units(kda):
     """80 sequence-heads at d = 128: one 128-column CTA per serial unit, and the
     tail segment's S~ and M halves as two CTAs.  The long sequence matches the
