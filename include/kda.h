@@ -117,8 +117,9 @@ kda_status kda_chunk_fwd(const kda_tensor* q, const kda_tensor* k, const kda_ten
 
 /*
  * kda_fused_recurrent_fwd - the same operation and contract as kda_chunk_fwd,
- * computed token by token with each (sequence, head) state held on chip in
- * fp32 ("把注意力换成一块「会遗忘的内存」" (jokeuncle.github.io), section on
+ * computed by the recurrence itself with each (sequence, head) state held on
+ * chip in fp32, four tokens per pass over the state (the single step unrolled
+ * over four tokens: the same values up to fp32 rounding) ("把注意力换成一块「会遗忘的内存」" (jokeuncle.github.io), section on
  * the layer's two execution paths: short sequences use the fused recurrent
  * kernel).  Meant for short sequences and as an independent device-side
  * cross-check of the chunked path; kda_chunk_fwd uses it for fp32 inputs.
@@ -367,8 +368,12 @@ kda_status kda_decode_step_fused(kda_tensor* state, kda_tensor* conv_q, kda_tens
  *   stream       cudaStream_t as void*
  *
  * Errors as for kda_recurrent_step; q and out must both be given or both be
- * NULL.  n = 0 is a no-op.  Tokens are processed one after another inside the
- * kernel, so n is meant to be small (draft lengths of a few tokens); any n works.
+ * NULL.  n = 0 is a no-op.  The kernel takes the tokens four at a time (the
+ * single step unrolled over each block of four, one pass over the state to
+ * read and one to write per block, a block also ending where the accepted
+ * tokens end), so the results equal n calls of kda_recurrent_step up to fp32
+ * rounding.  n is meant to be small (draft lengths of a few tokens); any n
+ * works.
  */
 kda_status kda_recurrent_multi_step(kda_tensor* state, const kda_tensor* q, const kda_tensor* k,
                                     const kda_tensor* v, const kda_tensor* g, const kda_tensor* beta,
