@@ -1479,13 +1479,22 @@ cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
                                      : (int64_t)a.N * pl.tps;
   auto first_pass_ctas = [&](int w) { return nh * (DV / w) + tails * a.H * ((DV + DK + w - 1) / w); };
   const int W = first_pass_ctas(32) <= sm_count() ? 32 : (DVM != DV && first_pass_ctas(DVM) <= sm_count()) ? DVM : DV;
-  auto ser = W == 32    ? kda_chunk_serial_kernel<DK, 32>
-             : W == DVM ? kda_chunk_serial_kernel<DK, DVM>
-                        : kda_chunk_serial_kernel<DK, DV>;
-  const int ser_smem = W == 32    ? SerialSmem<DK, 32>::kAlloc
-                       : W == DVM ? SerialSmem<DK, DVM>::kAlloc
-                                  : SerialSmem<DK, DV>::kAlloc;
+  // the second pass runs the tail segments alone: its own slice width (from the
+  // workspace's tail-unit bound, which is exact for fixed-length batches)
+  auto second_pass_ctas = [&](int w) { return (int64_t)pl.ntail * a.H * (DV / w); };
+  const int W1 = second_pass_ctas(32) <= sm_count() ? 32 : (DVM != DV && second_pass_ctas(DVM) <= sm_count()) ? DVM : DV;
+  using SerFn = void (*)(PrefillArgs, Split, Seg, int);
+  auto ser_fn = [&](int w) -> SerFn {
+    return w == 32 ? kda_chunk_serial_kernel<DK, 32> : w == DVM ? kda_chunk_serial_kernel<DK, DVM> : kda_chunk_serial_kernel<DK, DV>;
+  };
+  auto ser_bytes = [&](int w) {
+    return w == 32 ? SerialSmem<DK, 32>::kAlloc : w == DVM ? SerialSmem<DK, DVM>::kAlloc : SerialSmem<DK, DV>::kAlloc;
+  };
+  const SerFn ser = ser_fn(W), ser1 = ser_fn(W1);
+  const int ser_smem = ser_bytes(W), ser1_smem = ser_bytes(W1);
   e = cudaFuncSetAttribute(ser, cudaFuncAttributeMaxDynamicSharedMemorySize, ser_smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ser1, cudaFuncAttributeMaxDynamicSharedMemorySize, ser1_smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)sp.total * a.H;
   const int grid = (int)(items < 2 * sm_count() ? items : 2 * sm_count());
@@ -1525,7 +1534,7 @@ cudaError_t launch(const PrefillArgs& a, void* ws, cudaStream_t s) {
   }
   // pass 1: the tail segments from their input states, with outputs
   launch_begin(s);
-  ser<<<dim3((unsigned)((int64_t)pl.ntail * a.H * (DV / W))), kSerialThreads, ser_smem, s>>>(a, sp, sg, 1);
+  ser1<<<dim3((unsigned)second_pass_ctas(W1)), kSerialThreads, ser1_smem, s>>>(a, sp, sg, 1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_end(s);
 }
