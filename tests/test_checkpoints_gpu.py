@@ -58,11 +58,14 @@ def test_checkpoints_varlen_and_short_buffer(kda):
     _compare(cks, ref, 1e-2)
 
 
-def test_resume_from_checkpoint_is_bit_exact(kda):
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_resume_from_checkpoint_is_bit_exact(kda, dtype):
     """A prefill resumed from checkpoint j on the rest of the sequence gives the
-    original outputs and final state bit for bit."""
-    B, T, H, ck = 2, 640, 2, 256
-    d = ki.prefill_inputs(B, T, H, 128, 128, "bf16", seed=82, s0=True)
+    original outputs and final state bit for bit (bf16: the chunked kernels; fp32:
+    the token-recurrent kernel, whose four-token blocks start at the sequence start
+    and so at every checkpoint)."""
+    B, T, H, ck = 2, 640 + 3, 2, 256
+    d = ki.prefill_inputs(B, T, H, 128, 128, dtype, seed=82, s0=True)
     out, sT, cks = _run(kda, d, ck, 2)
     t = to_dev(d)
     j = 1
