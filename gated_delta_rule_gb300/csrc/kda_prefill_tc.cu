@@ -713,6 +713,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
         warp_tile_store(acc, sT + (32 + 16 * mt) * L::kTd + 8 * nt, L::kTd, -1.f, lane);
       }
       __syncthreads();
+      // the next item's decay rows: issued here, a few phases before its scan reads
+      // them (issued later they arrive too late; earlier, the registers they hold
+      // push the inverse's live values into local memory)
+      load_g(nxt);
       // T_beta = T Diag(beta) -> bf16 K-major [i][j] in shared memory (and the record, by bulk copy)
       {
         const int i = tid >> 2, j0 = 16 * (tid & 3);
@@ -740,7 +744,6 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
         mma_commit(ctx.mbar);
         bulk_s2g(rec + R::T2, sbase + L::T2, 64 * 64 * 2);
       }
-      load_g(nxt);
       wait_mma(ctx);
       // ---- -W (bf16, rows 0..63 of the [-W ; Q+] tile) staged over K+ (free once W is
       // done), then one bulk copy per 64-column panel.  Lane quarters 0-1; warps 4-5
