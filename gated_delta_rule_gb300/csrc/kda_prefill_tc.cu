@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
   load_g(cur);
 
   for (int w = blockIdx.x; w < nitems; w += gridDim.x) {
-    const Item nxt = item(w + gridDim.x);
+    Item nxt;  // placed while the Gram product runs, where its loads are hidden
     if (cur.valid) {
       unsigned char* rec = sp.rec + cur.rec * R::kBytes;
       const int col = 8 * oct;
@@ -610,6 +610,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
         fence_async_smem();  // K+ is read by the W product, several barriers later
       }
       // the k/q registers are free: start loading the next item while the MMAs run
+      nxt = item(w + gridDim.x);
       load_kq(nxt);
       wait_mma(ctx);
 
@@ -775,6 +776,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chunk_prep_kernel(PrefillArgs
       }
       if (*sFlag) break;
     } else {
+      nxt = item(w + gridDim.x);
       load_kq(nxt);
       load_g(nxt);
     }
