@@ -410,13 +410,54 @@ def kernel_roofline(r, pk, world):
             "kernel_ms": {n: max_over_ranks(v, world) for n, v in r["kernel_ms"].items()}}
 
 
+def gpu_local_cpus(index):
+    """The CPUs NVML names as closest to GPU ``index`` (nvmlDeviceGetCpuAffinity),
+    within this process's allowed set; None when NVML cannot say."""
+    try:
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        try:
+            h = ctypes.c_void_p()
+            ok = False
+            try:
+                uuid = "GPU-" + str(torch.cuda.get_device_properties(index).uuid)
+                ok = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+            except (AttributeError, RuntimeError):
+                ok = False
+            if not ok and lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) != 0:
+                return None
+            words = (max(os.cpu_count() or 1, max(os.sched_getaffinity(0)) + 1) + 63) // 64
+            mask = (ctypes.c_ulong * words)()
+            if lib.nvmlDeviceGetCpuAffinity(h, words, mask) != 0:
+                return None
+            cpus = {64 * i + b for i in range(words) for b in range(64) if (mask[i] >> b) & 1}
+            cpus &= os.sched_getaffinity(0)
+            return cpus or None
+        finally:
+            lib.nvmlShutdown()
+    except (OSError, AttributeError):
+        return None
+
+
 def bench_prefill_e2e(kda, r, steps, warmup, stream):
-    """Same prefill through the C ABI from pinned host buffers (H2D + call + D2H timed)."""
+    """Same prefill through the C ABI from pinned host buffers (H2D + call + D2H timed).
+    The pinned buffers are allocated (and first touched) from the CPUs closest to the
+    GPU, so that they sit in that CPU's memory; the process's CPU set is restored
+    afterwards."""
     d = r["d"]
-    host = {k: v.pin_memory() for k, v in d.items() if torch.is_tensor(v)}
+    prev = os.sched_getaffinity(0)
+    local = gpu_local_cpus(torch.cuda.current_device())
+    if local:
+        os.sched_setaffinity(0, local)
+    try:
+        host = {k: v.pin_memory() for k, v in d.items() if torch.is_tensor(v)}
+        out_h = torch.empty(r["out"].shape, dtype=r["out"].dtype).pin_memory()
+        sT_h = torch.empty(r["sT"].shape, dtype=torch.float32).pin_memory()
+    finally:
+        os.sched_setaffinity(0, prev)
     dev = r["t"]
-    out_h = torch.empty(r["out"].shape, dtype=r["out"].dtype).pin_memory()
-    sT_h = torch.empty(r["sT"].shape, dtype=torch.float32).pin_memory()
     names = [k for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens")
              if host.get(k) is not None]
     h2d = sum(host[k].numel() * host[k].element_size() for k in names)
@@ -442,7 +483,7 @@ def bench_prefill_e2e(kda, r, steps, warmup, stream):
         e1.record(stream)
     stream.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    return dict(ms=ms, h2d=h2d, d2h=d2h)
+    return dict(ms=ms, h2d=h2d, d2h=d2h, host_cpus=len(local) if local else None)
 
 
 def bench_decode(kda, steps_total, warmup, stream, clk=None):
@@ -995,7 +1036,9 @@ def main():
             "t_roof_over_t": t_roof / (ms * 1e-3),
             "kernel_ms": head_summary["kernel_ms"], "kernel_hbm_frac": head_summary["kernel_hbm_frac"],
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": e2e["h2d"],
-                    "d2h_bytes_per_step": e2e["d2h"]},
+                    "d2h_bytes_per_step": e2e["d2h"],
+                    "pinned_on": (f"memory of the {e2e['host_cpus']} CPUs NVML names closest to the GPU"
+                                  if e2e["host_cpus"] else "the allocating thread's memory node")},
             "gpu_launches": head_summary["gpu_launches"], "clocks": clk.summary(), "wall_s_timed_region": wall,
             "step_ms": step_ms}
     line.update(extra)
