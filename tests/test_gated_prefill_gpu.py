@@ -38,8 +38,9 @@ def test_gated_bf16(kda, T, dk, dv):
     _check(kda, d, label=f"gated T={T} {dk}x{dv}")
 
 
-def test_gated_f32(kda):
-    d = ki.gate_logits(ki.prefill_inputs(1, 130, 2, 64, 64, "f32", seed=71, s0=True), seed=71)
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128)])
+def test_gated_f32(kda, dk, dv):
+    d = ki.gate_logits(ki.prefill_inputs(1, 130, 2, dk, dv, "f32", seed=71, s0=True), seed=71)
     _check(kda, d, label="gated f32")
 
 
