@@ -941,7 +941,9 @@ def main():
     step_ms = {"mean": ms, "median": max_over_ranks(statistics.median(pre["ms"]), world),
                "best": max_over_ranks(min(pre["ms"]), world), "reps": len(pre["ms"])}
 
-    e2e = bench_prefill_e2e(kda, pre, 3, 2, stream)
+    # warm-up: the first device reads of freshly pinned host pages run several
+    # times slower (one or two calls), so five untimed calls precede the timed three
+    e2e = bench_prefill_e2e(kda, pre, 3, 5, stream)
     e2e_val = tokens_all / (max_over_ranks(e2e["ms"], world) * 1e-3)
     cpu_d = pre["d"] if rank == 0 and world == 1 and not args.no_cpu_baseline else None
     del pre

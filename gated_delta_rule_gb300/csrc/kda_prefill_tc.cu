@@ -1202,10 +1202,15 @@ __global__ void __launch_bounds__(kSerialThreads, 1)
       }
       fence_async_smem();
       bar_arrive(1, 160);
-      // (2) decay the TMEM state by e^{G_C} of this chunk (overlaps the first product)
+      // (2) decay the TMEM state by e^{G_C} of this chunk (overlaps the first product);
+      // the state is read from TMEM again rather than kept in registers across the
+      // record wait (217 instead of 255 registers at 128 columns, no spills)
       wait(mbar_rec0 + 8 * b, (ci >> 1) & 1);
       if (tid < DK) {
         const float pc = reinterpret_cast<const float*>(smem + (rec - sbase) + 2 * kT2 + (R::P - kT2))[tid];
+#pragma unroll
+        for (int q = 0; q < DV / 32; ++q) tmem_ld32_async(tS + lane_base + 32 * q, r[q]);
+        tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < DV / 32; ++q) {
 #pragma unroll
