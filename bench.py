@@ -942,8 +942,8 @@ def main():
                "best": max_over_ranks(min(pre["ms"]), world), "reps": len(pre["ms"])}
 
     # warm-up: the first device reads of freshly pinned host pages run several
-    # times slower (one or two calls), so five untimed calls precede the timed three
-    e2e = bench_prefill_e2e(kda, pre, 3, 5, stream)
+    # times slower (one or two calls), so eight untimed calls precede the timed five
+    e2e = bench_prefill_e2e(kda, pre, 5, 8, stream)
     e2e_val = tokens_all / (max_over_ranks(e2e["ms"], world) * 1e-3)
     cpu_d = pre["d"] if rank == 0 and world == 1 and not args.no_cpu_baseline else None
     del pre
