@@ -125,8 +125,9 @@ struct Layout {
   static_assert(R * RPP == DK, "layout");
 };
 
-// Sum over the RPP row groups of per-thread partial column sums (the same order
-// in both compute kernels, so a token gives the same bits whichever kernel runs it).
+// Sum over the RPP row groups of per-thread partial column sums, every thread
+// forming the totals of its column quad (the decode step, whose reductions hide
+// behind its HBM traffic).
 template <int DK, int DV, int NT = kThreads>
 __device__ __forceinline__ float4 column_reduce(float4 part, float4 (*red)[DV / 4], int trow,
                                                int col4) {
@@ -147,8 +148,8 @@ __device__ __forceinline__ float4 column_reduce(float4 part, float4 (*red)[DV / 
 
 // The same sums in the same order, formed once per column quad: the TPR threads of
 // row group 0 add the RPP partials and publish the totals in `tot` (one more
-// barrier, one sixteenth of the shared-memory reads).  For the token loops, whose
-// reductions are not hidden behind HBM traffic.
+// barrier, one sixteenth of the shared-memory reads).  For the backward's token
+// loop, whose reductions are not hidden behind HBM traffic.
 template <int DK, int DV, int NT = kThreads>
 __device__ __forceinline__ float4 column_reduce_lean(float4 part, float4 (*red)[DV / 4], float4* tot,
                                                     int trow, int col4) {
