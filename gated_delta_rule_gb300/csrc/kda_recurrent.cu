@@ -839,22 +839,22 @@ __global__ void __launch_bounds__(kTok, 5) kda_recurrent_kernel(PrefillArgs a) {
       float* kdv = &kd.x;
 #pragma unroll
       for (int j = 0; j < kNB; ++j) {
-        const float e = expf(G[j]);
+        const float e = __expf(G[j]);
         kpv[j] = kk[j] * e;
         qpv[j] = qq[j] * e;
-        kdv[j] = bt[j] * kk[j] * expf(gacc - G[j]);
+        kdv[j] = bt[j] * kk[j] * __expf(gacc - G[j]);
       }
       *reinterpret_cast<float4*>(&kq[i][0]) = kp;
       *reinterpret_cast<float4*>(&kq[i][kNB]) = qp;
       *reinterpret_cast<float4*>(&ke[i][0]) = kd;
-      dec[i] = expf(gacc);
+      dec[i] = __expf(gacc);
       float pv[kPairs];
 #pragma unroll
       for (int t = 0; t < kNB; ++t) {
         pv[m_index(t, t)] = qq[t] * kk[t];
 #pragma unroll
         for (int u = 0; u < t; ++u) {
-          const float e = expf(G[t] - G[u]);
+          const float e = __expf(G[t] - G[u]);
           pv[l_index(t, u)] = kk[t] * kk[u] * e;
           pv[m_index(t, u)] = qq[t] * kk[u] * e;
         }
